@@ -1,0 +1,177 @@
+/*
+ * mk.h -- C ABI of the persistent MoE decode megakernel library (libmk).
+ *
+ * One call, mk_decode_step, runs the whole batch-1..8 BF16 decode step of a
+ * mixture-of-experts transformer as ONE persistent kernel: RMSNorm, QKV
+ * projection, RoPE + KV append, paged split-K attention, router top-k,
+ * gathered expert SwiGLU, output projection, residual, final norm, LM head
+ * and greedy argmax.  The method is the one described on three pages about a
+ * decode megakernel for a 30B-total / 3.3B-active MoE model:
+ *   - "Cohere speeds up North Mini Code with new megakernel"
+ *     (latestnews.news), paragraphs 2-3: the whole forward pass in one
+ *     persistent kernel, one threadblock per SM, a host-built static
+ *     schedule, global-memory counters;
+ *   - "Cohere Packs the Entire Decoding Step Into a Single CUDA Megakernel"
+ *     (ainews.surl.tw), paragraph 2: the task table of GEMM tiles and
+ *     attention splits, dataflow start on per-dependency counters, attention
+ *     and MoE from the same normalized input; paragraph 4: BF16, batch 1-8;
+ *   - "Cohere megakernel serves 30B MoE 1.58x faster than vLLM"
+ *     (aiweekly.co), paragraphs 2-4: 32-int32 task descriptors, O(1)
+ *     counter barriers, weight prefetch ahead of dependencies.
+ *
+ * Conventions
+ *   - Every function returns mk_status (0 = MK_OK) unless stated; nothing
+ *     throws across the ABI.
+ *   - Pointers passed to mk_create are DEVICE pointers owned by the caller;
+ *     they must stay valid until mk_destroy.  The library never frees them.
+ *     Every weight / KV pointer must be 16-byte aligned.
+ *   - The library owns only its workspace (activations, partials, counters,
+ *     the device task table, device copies of page tables and lengths).
+ *   - Work is enqueued on the stream given to mk_create; calls are
+ *     asynchronous unless stated.
+ *   - Layouts: bf16 matrices are row-major W[out][in] (the input dimension is
+ *     contiguous); experts are stacked [E][F][d] (gate, up) and [E][d][F]
+ *     (down); the K and V pools of a layer are [num_pages][n_kv_heads]
+ *     [page_size][head_dim] and hold post-RoPE keys.
+ *   - Errors: argument errors are returned synchronously.  Device errors
+ *     (a counter wait that ran out of time, a corrupt task) are sticky and
+ *     surface from the next call (mk_sync reports them at once); the context
+ *     must then be destroyed.
+ */
+#ifndef MK_H
+#define MK_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t mk_status;
+enum {
+  MK_OK = 0,
+  MK_ERR_INVALID_ARG = 1,   /* null / misaligned pointer, bad dimension */
+  MK_ERR_BATCH = 2,         /* batch < 1 or > max_batch (at most 8) */
+  MK_ERR_PAGE_OOB = 3,      /* a page id outside [0, num_pages), or no page for position L_b */
+  MK_ERR_NO_SCHEDULE = 4,   /* mk_decode_step before mk_build_schedule */
+  MK_ERR_CUDA = 5,          /* a CUDA runtime call failed */
+  MK_ERR_DEVICE_TIMEOUT = 6,/* a device wait exceeded the wait limit (sticky) */
+  MK_ERR_BAD_TASK = 7,      /* the kernel met an unknown task opcode (sticky) */
+  MK_ERR_UNSUPPORTED = 8,   /* dims this build does not support (see mk_create) */
+  MK_ERR_NO_DEVICE = 9      /* no usable sm_103 device */
+};
+
+/* Model dimensions.  page_size tokens per KV page; num_pages pages in each
+ * layer's pool; max_pages_per_seq entries per page-table row. */
+typedef struct {
+  int32_t n_layers, d_model, n_q_heads, n_kv_heads, head_dim;
+  int32_t n_experts, top_k, d_ffn, vocab;
+  int32_t page_size, max_batch, num_pages, max_pages_per_seq;
+  float rope_base, rms_eps;
+} mk_model_dims;
+
+/* One layer's device pointers (all bf16 unless stated). */
+typedef struct {
+  const void *norm;                      /* [d] RMSNorm gain (one norm: parallel block) */
+  const void *wq, *wk, *wv;              /* [Hq*D][d], [Hkv*D][d], [Hkv*D][d] */
+  const void *wo;                        /* [d][Hq*D] */
+  const void *w_router;                  /* [E][d] */
+  const float *router_bias;              /* fp32 [E] added to the router logits, or NULL */
+  const void *w_gate, *w_up;             /* [E][F][d] */
+  const void *w_down;                    /* [E][d][F] */
+  void *k_cache, *v_cache;               /* [num_pages][Hkv][P][D]; the step appends rows */
+} mk_layer_ptrs;
+
+typedef struct {
+  const void *embed;                     /* [V][d] */
+  const mk_layer_ptrs *layers;           /* HOST array [n_layers], copied by mk_create */
+  const void *final_norm;                /* [d] */
+  const void *lm_head;                   /* [V][d]; may equal embed (tied) */
+} mk_weights;
+
+typedef struct mk_ctx mk_ctx;
+
+/* Validates dims and pointers, queries the device, allocates the workspace.
+ * stream: a cudaStream_t (NULL = legacy default stream).  Supported: head_dim
+ * in {32, 64, 128}; n_q_heads / n_kv_heads <= 8; top_k <= 16; n_experts <=
+ * 128; d_model, d_ffn and n_q_heads*head_dim multiples of 64; max_batch <= 8.
+ * Returns MK_ERR_INVALID_ARG / MK_ERR_UNSUPPORTED / MK_ERR_NO_DEVICE /
+ * MK_ERR_CUDA; *out is set only on MK_OK. */
+mk_status mk_create(const mk_model_dims *dims, const mk_weights *w, void *stream, mk_ctx **out);
+
+/* Builds the task table for `batch` sequences: seq_lens (HOST [batch]) =
+ * cached tokens L_b before the next step; page_tables (HOST
+ * [batch][max_pages_per_seq]) = physical page ids, -1 where unallocated.
+ * Copies both to the device, resets the counters, uploads the table.
+ * Call again whenever batch membership changes (continuous batching). */
+mk_status mk_build_schedule(mk_ctx *ctx, int32_t batch, const int32_t *seq_lens,
+                            const int32_t *page_tables);
+
+/* One decode step for the scheduled batch.  token_ids: DEVICE int32 [batch];
+ * out_logits: DEVICE fp32 [batch][vocab] or NULL; out_next_tokens: DEVICE
+ * int32 [batch] (greedy argmax, ties -> lowest id).  Token b is processed at
+ * position L_b and its K/V row is written there; L_b then advances by one
+ * (on the device and in the context).  The page covering L_b must be present
+ * in the page table (MK_ERR_PAGE_OOB otherwise).  When a sequence has grown
+ * far past the lengths the table was built for, the table is rebuilt first.
+ * Asynchronous: returns after the launch. */
+mk_status mk_decode_step(mk_ctx *ctx, const int32_t *token_ids, float *out_logits,
+                         int32_t *out_next_tokens);
+
+/* Waits for the stream and returns the sticky device status. */
+mk_status mk_sync(mk_ctx *ctx);
+
+void mk_destroy(mk_ctx *ctx);
+
+const char *mk_status_string(mk_status s);
+
+/* ---- diagnostics (tests / benchmark) ------------------------------------- */
+
+/* Device wait limit in nanoseconds (default 1e9).  Every counter / mbarrier
+ * wait in the kernel gives up after this long and reports
+ * MK_ERR_DEVICE_TIMEOUT instead of hanging. */
+mk_status mk_set_wait_limit_ns(mk_ctx *ctx, uint64_t ns);
+
+/* Routing of the last step (synchronises): ids / w HOST [n_layers][batch][top_k]
+ * in descending-logit order; either may be NULL. */
+mk_status mk_debug_routing(mk_ctx *ctx, int32_t *ids, float *w);
+
+/* Copies a workspace buffer of the last step to HOST memory (synchronises).
+ * what: 0 = residual h [n_layers+1][batch][d] bf16 (h[0] is the embedding),
+ *       1 = attention output o [n_layers][batch][Hq*D] bf16,
+ *       2 = router logits [n_layers][batch][E] fp32.
+ * bytes must equal the buffer size. */
+mk_status mk_debug_dump(mk_ctx *ctx, int32_t what, void *host_out, uint64_t bytes);
+
+/* Running totals since mk_build_schedule (synchronises). */
+typedef struct {
+  uint64_t steps;          /* decode steps launched */
+  uint64_t sum_experts;    /* sum over steps and layers of distinct experts U */
+  uint64_t rebuilds;       /* automatic table rebuilds */
+} mk_stats;
+mk_status mk_get_stats(mk_ctx *ctx, mk_stats *out);
+
+/* Test only: adds `delta` to the target of layer `layer`'s attention-done
+ * counter in the next launch, making that wait unsatisfiable so that the
+ * bounded-wait path (MK_ERR_DEVICE_TIMEOUT) can be exercised without a hang. */
+mk_status mk_debug_poison_wait(mk_ctx *ctx, int32_t layer, int32_t delta);
+
+/* Host-only schedule planning (no GPU needed): the task table that
+ * mk_build_schedule would upload for n_sm SMs.  Writes at most cap int32s of
+ * [n_cta][tasks_per_cta][32] descriptors into table (may be NULL to query)
+ * and the table geometry into info.  Returns MK_ERR_INVALID_ARG /
+ * MK_ERR_BATCH / MK_ERR_UNSUPPORTED / MK_ERR_PAGE_OOB on bad input. */
+typedef struct {
+  int32_t n_cta, tasks_per_cta;       /* table is [n_cta][tasks_per_cta][32] */
+  int32_t n_layer_tasks_max;          /* per-CTA tasks of one layer (template) */
+  int32_t n_qkv, n_router, n_attn, n_up, n_out, n_lm; /* tasks per layer (lm: per step) */
+  int32_t n_attn_slots;               /* attention partial slots per layer */
+} mk_plan_info;
+mk_status mk_plan(const mk_model_dims *dims, int32_t n_sm, int32_t batch, const int32_t *seq_lens,
+                  mk_plan_info *info, int32_t *table, int64_t cap);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MK_H */

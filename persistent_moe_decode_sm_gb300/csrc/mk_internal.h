@@ -1,0 +1,158 @@
+/*
+ * mk_internal.h -- types shared by the host schedule builder and the kernel.
+ *
+ * Task descriptors are exactly 32 int32 fields (128 bytes, one cache line),
+ * the size the aiweekly.co page gives for the megakernel's descriptors
+ * ("Cohere megakernel serves 30B MoE 1.58x faster than vLLM", paragraph 2).
+ * The per-CTA table row is: a header, the per-layer template (run once per
+ * layer, in order), then the final (LM head) tasks.
+ */
+#ifndef MK_INTERNAL_H
+#define MK_INTERNAL_H
+
+#include <stdint.h>
+
+#define MK_DESC_INTS 32
+
+/* ---- opcodes ---------------------------------------------------------------- */
+enum {
+  OP_HEADER = 100, /* [1] n_layer_tasks, [2] n_final_tasks */
+  OP_QKV = 1,      /* [1] mat (0 q, 1 k, 2 v), [2] row0, [3] nrows */
+  OP_ROUTER = 2,   /* [2] row0 (expert), [3] nrows */
+  OP_ATTN = 3,     /* [1] b, [2] kvh, [3] page0, [4] page1 (-1: up to the live length),
+                      [5] slot (partial slot), [6] slot0 of (b,kvh), [7] n_splits,
+                      [8] is_last (handles and appends the new token) */
+  OP_UP = 4,       /* [1] share, [2] n_shares */
+  OP_OUT = 5,      /* [2] row0, [3] nrows */
+  OP_LM = 6        /* [2] row0, [3] nrows, [4] lm task index */
+};
+
+/* ---- counters ----------------------------------------------------------------
+ * Every counter sits in its own 32-byte sector.  Counters are epoch based:
+ * in step e (0-based since the last table build) a counter that receives n
+ * increments per step is complete when it reaches (e + 1) * n (compared
+ * modulo 2^32), so nothing is reset between steps. */
+#define MK_CTR_STRIDE 8 /* int32s per counter */
+enum {
+  CTR_QKV_DONE = 0,
+  CTR_ROUTER_TICKET = 1,
+  CTR_ROUTED = 2,
+  CTR_ATTN_DONE = 3,
+  CTR_UP_DONE = 4,
+  CTR_OUT_DONE = 5,
+  CTR_ATTN_TICKET0 = 6 /* + b * n_kv_heads + kvh */
+};
+/* after the per-layer blocks: */
+enum { GCTR_LM_TICKET = 0, GCTR_EXIT = 1, GCTR_COUNT = 2 };
+
+static inline int mk_ctrs_per_layer(int max_batch, int n_kv_heads) {
+  return CTR_ATTN_TICKET0 + max_batch * n_kv_heads;
+}
+
+/* ---- limits ----------------------------------------------------------------- */
+#define MK_MAX_BATCH 8
+#define MK_MAX_TOPK 16
+#define MK_MAX_GROUP 8          /* q heads per kv head */
+#define MK_MAX_OUT_ROWS 64      /* rows of d per OUT task */
+#define MK_STAGE_BYTES 32768    /* one ring stage */
+#define MK_MAX_STAGES 16
+#define MK_NC_WARPS 8           /* consumer warps */
+#define MK_THREADS ((MK_NC_WARPS + 1) * 32)
+
+/* Routing result of one layer, written by the last router task. */
+typedef struct {
+  int32_t U;                               /* distinct experts chosen */
+  int32_t pad[3];
+  int32_t expert[128];                     /* slot -> expert id (ascending) */
+  float slot_w[128][MK_MAX_BATCH];         /* weight of slot u for token b (0: unused) */
+  int32_t ids[MK_MAX_BATCH][MK_MAX_TOPK];  /* per token, descending logit */
+  float w[MK_MAX_BATCH][MK_MAX_TOPK];
+} mk_routing;
+
+/* Device-side control block. */
+typedef struct {
+  uint32_t epoch;            /* steps since the last table build */
+  int32_t abort;             /* set by the first failing wait; every CTA polls it */
+  int32_t err_code;          /* first error (mk_status), 0 = none */
+  int32_t err_cta, err_task, err_op, err_layer, err_ctr;
+  int32_t err_seen, err_target;
+  unsigned long long sum_experts; /* sum of U over layers and steps */
+} mk_ctrl;
+
+/* Per-layer device pointers (a device array of n_layers of these). */
+typedef struct {
+  const uint16_t *norm, *wq, *wk, *wv, *wo, *wr;
+  const float *bias;
+  const uint16_t *wg, *wu, *wd;
+  uint16_t *kc, *vc;
+} mk_layer_dev;
+
+/* Everything the kernel needs; passed by value. */
+typedef struct {
+  /* dims */
+  int32_t L, d, Hq, Hkv, D, E, K, F, V, P, max_pages, B;
+  float eps, attn_scale;
+  /* model */
+  const mk_layer_dev *layers;
+  const uint16_t *embed, *final_norm, *lm_head;
+  /* step io */
+  const int32_t *tokens;
+  float *out_logits;          /* may be NULL */
+  int32_t *out_next;
+  /* workspace */
+  uint16_t *h;                /* [L+1][MAXB][d]  (h[0] holds the embedding rows for dumps) */
+  uint16_t *qkv;              /* [L][MAXB][(Hq+2Hkv)D] pre-RoPE q, k, v */
+  uint16_t *o;                /* [L][MAXB][Hq D] */
+  float *attn_part;           /* [L][n_slots][G][D + 2] (m, l, o) */
+  float *router_logits;       /* [L][MAXB][E] */
+  mk_routing *routing;        /* [L] */
+  uint16_t *act;              /* [L][Umax][MAXB][F] */
+  float *lm_part;             /* [n_lm][MAXB][2] (value, index as float bits) */
+  int32_t *ctr;               /* counters */
+  mk_ctrl *ctrl;
+  int32_t *seq_lens;          /* [MAXB] live lengths (advanced by the kernel) */
+  const int32_t *page_table;  /* [MAXB][max_pages] */
+  const float *rope;          /* [max_pos][D/2][2] (cos, sin) */
+  int32_t rope_max_pos;
+  const int32_t *table;       /* [n_cta][tasks_per_cta][32] */
+  int32_t tasks_per_cta;
+  int32_t n_slots, u_max;
+  /* per-step increments of each counter */
+  int32_t n_qkv, n_router, n_up, n_out, n_lm, n_attn_done;
+  int32_t ctrs_per_layer;
+  unsigned long long wait_limit_ns;
+  int32_t *err_host;          /* host-mapped mirror: [code, cta, task, op, layer, ctr, seen, target] */
+  int32_t ring_stages;        /* stages of MK_STAGE_BYTES in the shared ring */
+  int32_t xbuf_bytes;         /* shared activation buffer */
+  int32_t poison_layer, poison_delta; /* test hook: see mk_debug_poison_wait */
+} mk_kparams;
+
+#ifdef __CUDACC__
+#define MK_HD __host__ __device__
+#else
+#define MK_HD
+#endif
+
+/* Rows of row_bytes each that one ring stage carries (the producer and the
+ * consumers must agree on it). */
+static inline MK_HD int mk_rows_per_stage(int row_bytes) {
+  int r = MK_STAGE_BYTES / row_bytes;
+  return r > 64 ? 64 : r;
+}
+
+/* Gate/up row pairs per stage (a pair is one gate row and one up row of
+ * row_bytes each); at most 32 so that 2 * pairs rows fit the partial-sum
+ * buffer. */
+static inline MK_HD int mk_pairs_per_stage(int row_bytes) {
+  int r = MK_STAGE_BYTES / (2 * row_bytes);
+  return r > 32 ? 32 : r;
+}
+
+/* KV pages per stage: each page brings a K block and a V block of
+ * page_bytes each. */
+static inline MK_HD int mk_pages_per_stage(int page_bytes) {
+  int r = MK_STAGE_BYTES / (2 * page_bytes);
+  return r > 8 ? 8 : r;
+}
+
+#endif /* MK_INTERNAL_H */

@@ -1,0 +1,316 @@
+/*
+ * mk_schedule.cpp -- host-side task-table builder.
+ *
+ * The pages describe a host-built, static, fine-grained task table that
+ * assigns GEMM tiles and attention splits to the SMs, each SM running one
+ * threadblock ("Cohere Packs the Entire Decoding Step Into a Single CUDA
+ * Megakernel", ainews.surl.tw, paragraph 2; "Cohere speeds up North Mini
+ * Code with new megakernel", latestnews.news, paragraph 3).  This builder
+ * produces that table for any SM count the device reports.
+ *
+ * Shape of the table: one row per CTA = [header][per-layer template]
+ * [final tasks].  The template is executed once per layer, so the table
+ * stays small (a few hundred descriptors) for any depth.
+ *
+ * Per-layer phases, in the order every CTA runs them:
+ *   ROUTER  (a few CTAs; first, because routing heads the MoE critical path)
+ *   QKV     (the Wq/Wk/Wv rows cut into one contiguous piece per CTA)
+ *   ATTN    (split-K attention: the CTAs are shared out among the
+ *            (sequence, kv head) pairs in proportion to their pages, one
+ *            split of about equal size per CTA)
+ *   UP      (one share per CTA of the gate/up rows of the experts the
+ *            router chose; the share is resolved on the device)
+ *   OUT     (rows of d: Wo rows, then the chosen experts' down rows, then
+ *            the residual; this produces the next layer's input)
+ * then the LM head rows, one piece per CTA.
+ *
+ * Deadlock freedom: a task only waits on counters fed by tasks of an
+ * earlier phase (or an earlier layer), and every CTA runs its tasks in
+ * phase order, so by induction over phases every wait is eventually met
+ * as long as all CTAs are co-resident (the launch is cooperative).
+ */
+#include <algorithm>
+#include <array>
+#include <cstring>
+#include <numeric>
+#include <vector>
+
+#include "mk.h"
+#include "mk_internal.h"
+#include "mk_plan.h"
+
+namespace {
+
+using Desc = std::array<int32_t, MK_DESC_INTS>;
+
+Desc desc(int op) {
+  Desc d;
+  d.fill(0);
+  d[0] = op;
+  return d;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+mk_status mk_validate_dims(const mk_model_dims *dm) {
+  if (!dm) return MK_ERR_INVALID_ARG;
+  const mk_model_dims &d = *dm;
+  if (d.n_layers < 1 || d.d_model < 1 || d.n_q_heads < 1 || d.n_kv_heads < 1 || d.head_dim < 1 ||
+      d.n_experts < 1 || d.top_k < 1 || d.d_ffn < 1 || d.vocab < 1 || d.page_size < 1 ||
+      d.max_batch < 1 || d.num_pages < 1 || d.max_pages_per_seq < 1)
+    return MK_ERR_INVALID_ARG;
+  if (d.top_k > d.n_experts) return MK_ERR_INVALID_ARG;
+  if (d.n_q_heads % d.n_kv_heads != 0) return MK_ERR_INVALID_ARG;
+  if (!(d.rms_eps >= 0.0f) || !(d.rope_base > 0.0f)) return MK_ERR_INVALID_ARG;
+  if (d.max_batch > MK_MAX_BATCH) return MK_ERR_BATCH;
+  if (d.head_dim != 32 && d.head_dim != 64 && d.head_dim != 128) return MK_ERR_UNSUPPORTED;
+  if (d.n_q_heads / d.n_kv_heads > MK_MAX_GROUP) return MK_ERR_UNSUPPORTED;
+  if (d.top_k > MK_MAX_TOPK || d.n_experts > 128) return MK_ERR_UNSUPPORTED;
+  if (d.d_model % 64 || d.d_ffn % 64 || (d.n_q_heads * d.head_dim) % 64) return MK_ERR_UNSUPPORTED;
+  /* every streamed unit must fit one ring stage */
+  const int64_t row_max = std::max<int64_t>(2LL * d.d_model, (int64_t)d.n_q_heads * d.head_dim);
+  if (row_max * 2 > MK_STAGE_BYTES) return MK_ERR_UNSUPPORTED;
+  if (2LL * d.page_size * d.head_dim * 2 > MK_STAGE_BYTES) return MK_ERR_UNSUPPORTED;
+  if ((int64_t)d.page_size * d.head_dim * 2 % 16) return MK_ERR_UNSUPPORTED;
+  return MK_OK;
+}
+
+mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int32_t *seq_lens,
+                        MkPlan *out) {
+  mk_status st = mk_validate_dims(dm);
+  if (st != MK_OK) return st;
+  if (n_cta < 1 || !seq_lens || !out) return MK_ERR_INVALID_ARG;
+  if (batch < 1 || batch > dm->max_batch) return MK_ERR_BATCH;
+  const mk_model_dims &d = *dm;
+  const int64_t cap_tokens = (int64_t)d.max_pages_per_seq * d.page_size;
+  for (int b = 0; b < batch; ++b)
+    if (seq_lens[b] < 0 || seq_lens[b] + 1 > cap_tokens) return MK_ERR_PAGE_OOB;
+
+  const int Hq = d.n_q_heads, Hkv = d.n_kv_heads, D = d.head_dim, P = d.page_size;
+  std::vector<std::vector<Desc>> lt(n_cta), ft(n_cta);
+  std::vector<std::vector<Desc>> router_t(n_cta), qkv_t(n_cta), attn_t(n_cta), up_t(n_cta),
+      out_t(n_cta);
+  MkPlan &p = *out;
+  p = MkPlan();
+
+  /* ROUTER: as many rows per task as fit one stage. */
+  {
+    const int rpr = std::max(1, std::min(d.n_experts, MK_STAGE_BYTES / (2 * d.d_model)));
+    const int n = (int)ceil_div(d.n_experts, rpr);
+    for (int i = 0; i < n; ++i) {
+      Desc t = desc(OP_ROUTER);
+      t[2] = i * rpr;
+      t[3] = std::min(rpr, d.n_experts - i * rpr);
+      const int c = (int)((int64_t)i * n_cta / n);
+      router_t[c].push_back(t);
+    }
+    p.n_router = n;
+  }
+
+  /* QKV: the concatenated [q | k | v] rows cut into n_cta contiguous pieces,
+   * each split again at matrix boundaries. */
+  {
+    const int64_t rows[3] = {(int64_t)Hq * D, (int64_t)Hkv * D, (int64_t)Hkv * D};
+    const int64_t R = rows[0] + rows[1] + rows[2];
+    const int pieces = (int)std::min<int64_t>(n_cta, R);
+    int n = 0;
+    for (int c = 0; c < pieces; ++c) {
+      const int64_t a = R * c / pieces, b = R * (c + 1) / pieces;
+      int64_t base = 0;
+      for (int m = 0; m < 3; ++m) {
+        const int64_t lo = std::max(a, base), hi = std::min(b, base + rows[m]);
+        if (lo < hi) {
+          Desc t = desc(OP_QKV);
+          t[1] = m;
+          t[2] = (int32_t)(lo - base);
+          t[3] = (int32_t)(hi - lo);
+          qkv_t[c].push_back(t);
+          ++n;
+        }
+        base += rows[m];
+      }
+    }
+    p.n_qkv = n;
+  }
+
+  /* ATTN: split-K over pages. */
+  {
+    struct Split { int b, kvh, p0, p1, slot, slot0, ns, last; int64_t pages; };
+    std::vector<Split> splits;
+    int64_t T = 0;
+    std::vector<int64_t> npages(batch);
+    for (int b = 0; b < batch; ++b) {
+      npages[b] = ceil_div(seq_lens[b], P);
+      T += npages[b] * Hkv;
+    }
+    /* CTAs per (b, kvh) in proportion to its pages (largest remainder), so
+     * that every CTA gets one split of about T / n_cta pages. */
+    const int nbh = batch * Hkv;
+    std::vector<int64_t> share(nbh, 1);
+    if (nbh <= n_cta && T > 0) {
+      std::vector<double> rem(nbh);
+      int64_t used = 0;
+      for (int i = 0; i < nbh; ++i) {
+        const double q = (double)npages[i / Hkv] * n_cta / (double)T;
+        share[i] = std::max<int64_t>(1, (int64_t)q);
+        rem[i] = q - (double)share[i];
+        used += share[i];
+      }
+      while (used < n_cta) {
+        const int best = (int)(std::max_element(rem.begin(), rem.end()) - rem.begin());
+        share[best] += 1;
+        rem[best] -= 1.0;
+        ++used;
+      }
+      while (used > n_cta) {
+        int best = -1;
+        for (int i = 0; i < nbh; ++i)
+          if (share[i] > 1 && (best < 0 || rem[i] < rem[best])) best = i;
+        if (best < 0) break;
+        share[best] -= 1;
+        rem[best] += 1.0;
+        --used;
+      }
+    }
+    int slot = 0;
+    for (int b = 0; b < batch; ++b)
+      for (int h = 0; h < Hkv; ++h) {
+        const int64_t n = npages[b];
+        const int ns = (int)std::max<int64_t>(1, std::min<int64_t>(share[b * Hkv + h], n));
+        for (int i = 0; i < ns; ++i) {
+          Split s;
+          s.b = b;
+          s.kvh = h;
+          s.p0 = (int)(n * i / ns);
+          s.p1 = (int)(n * (i + 1) / ns);
+          s.slot = slot + i;
+          s.slot0 = slot;
+          s.ns = ns;
+          s.last = (i == ns - 1);
+          s.pages = s.p1 - s.p0 + (s.last ? 1 : 0);
+          splits.push_back(s);
+        }
+        slot += ns;
+      }
+    p.n_attn_slots = slot;
+    p.n_attn = (int)splits.size();
+    /* greedy: largest first onto the least-loaded CTA */
+    std::vector<int> order(splits.size());
+    std::iota(order.begin(), order.end(), 0);
+    std::stable_sort(order.begin(), order.end(),
+                     [&](int x, int y) { return splits[x].pages > splits[y].pages; });
+    std::vector<int64_t> load(n_cta, 0);
+    std::vector<std::vector<int>> mine(n_cta);
+    for (int idx : order) {
+      const int c = (int)(std::min_element(load.begin(), load.end()) - load.begin());
+      load[c] += splits[idx].pages + 1;
+      mine[c].push_back(idx);
+    }
+    for (int c = 0; c < n_cta; ++c) {
+      std::sort(mine[c].begin(), mine[c].end());
+      for (int idx : mine[c]) {
+        const Split &s = splits[idx];
+        Desc t = desc(OP_ATTN);
+        t[1] = s.b;
+        t[2] = s.kvh;
+        t[3] = s.p0;
+        t[4] = s.last ? -1 : s.p1;
+        t[5] = s.slot;
+        t[6] = s.slot0;
+        t[7] = s.ns;
+        t[8] = s.last;
+        attn_t[c].push_back(t);
+      }
+    }
+  }
+
+  /* UP: one share per CTA, resolved on the device once routing is known. */
+  for (int c = 0; c < n_cta; ++c) {
+    Desc t = desc(OP_UP);
+    t[1] = c;
+    t[2] = n_cta;
+    up_t[c].push_back(t);
+  }
+  p.n_up = n_cta;
+
+  /* OUT: rows of d. */
+  {
+    int n = std::min(n_cta, d.d_model);
+    if (ceil_div(d.d_model, n) > MK_MAX_OUT_ROWS) n = (int)ceil_div(d.d_model, MK_MAX_OUT_ROWS);
+    for (int i = 0; i < n; ++i) {
+      Desc t = desc(OP_OUT);
+      const int a = (int)((int64_t)d.d_model * i / n), b = (int)((int64_t)d.d_model * (i + 1) / n);
+      t[2] = a;
+      t[3] = b - a;
+      out_t[i % n_cta].push_back(t);
+    }
+    p.n_out = n;
+  }
+
+  /* LM head: vocab rows, one piece per CTA. */
+  {
+    const int n = std::min(n_cta, d.vocab);
+    for (int i = 0; i < n; ++i) {
+      Desc t = desc(OP_LM);
+      const int a = (int)((int64_t)d.vocab * i / n), b = (int)((int64_t)d.vocab * (i + 1) / n);
+      t[2] = a;
+      t[3] = b - a;
+      t[4] = i;
+      ft[i].push_back(t);
+    }
+    p.n_lm = n;
+  }
+
+  int width = 0, lmax = 0;
+  for (int c = 0; c < n_cta; ++c) {
+    for (auto *v : {&router_t[c], &qkv_t[c], &attn_t[c], &up_t[c], &out_t[c]})
+      lt[c].insert(lt[c].end(), v->begin(), v->end());
+    width = std::max<int>(width, 1 + (int)lt[c].size() + (int)ft[c].size());
+    lmax = std::max<int>(lmax, (int)lt[c].size());
+  }
+  p.n_cta = n_cta;
+  p.tasks_per_cta = width;
+  p.n_layer_tasks_max = lmax;
+  p.n_attn_done = batch * Hkv;
+  p.batch = batch;
+  p.table.assign((size_t)n_cta * width * MK_DESC_INTS, 0);
+  for (int c = 0; c < n_cta; ++c) {
+    int32_t *row = &p.table[(size_t)c * width * MK_DESC_INTS];
+    Desc h = desc(OP_HEADER);
+    h[1] = (int)lt[c].size();
+    h[2] = (int)ft[c].size();
+    std::memcpy(row, h.data(), sizeof(Desc));
+    int at = 1;
+    for (auto &t : lt[c]) std::memcpy(row + MK_DESC_INTS * at++, t.data(), sizeof(Desc));
+    for (auto &t : ft[c]) std::memcpy(row + MK_DESC_INTS * at++, t.data(), sizeof(Desc));
+  }
+  p.built_lens.assign(seq_lens, seq_lens + batch);
+  return MK_OK;
+}
+
+extern "C" mk_status mk_plan(const mk_model_dims *dims, int32_t n_sm, int32_t batch,
+                             const int32_t *seq_lens, mk_plan_info *info, int32_t *table,
+                             int64_t cap) {
+  MkPlan p;
+  mk_status st = mk_build_plan(dims, n_sm, batch, seq_lens, &p);
+  if (st != MK_OK) return st;
+  if (info) {
+    info->n_cta = p.n_cta;
+    info->tasks_per_cta = p.tasks_per_cta;
+    info->n_layer_tasks_max = p.n_layer_tasks_max;
+    info->n_qkv = p.n_qkv;
+    info->n_router = p.n_router;
+    info->n_attn = p.n_attn;
+    info->n_up = p.n_up;
+    info->n_out = p.n_out;
+    info->n_lm = p.n_lm;
+    info->n_attn_slots = p.n_attn_slots;
+  }
+  if (table) {
+    if (cap < (int64_t)p.table.size()) return MK_ERR_INVALID_ARG;
+    std::memcpy(table, p.table.data(), p.table.size() * sizeof(int32_t));
+  }
+  return MK_OK;
+}

@@ -324,4 +324,43 @@ def fmt_bytes(n: float) -> str:
     return f"{n:.1f} PB"
 
 
+# ------------------------------------------------------------- device-side inputs
+
+
+@dataclass
+class DeviceInputs:
+    """Every input of a workload, generated in device memory."""
+    dims: Dims
+    tensors: Dict[str, object]      # name -> torch bf16 tensor (weights and KV pools)
+    layout: PageLayout
+    biases: List[Optional[np.ndarray]]
+    bias_tensors: List[object]      # torch fp32 [E] or None per layer
+    seed: int
+
+
+def device_inputs(dims: Dims, seq_lens: Sequence[int], reserve_steps: int,
+                  zipf_s: Optional[float] = None, seed: int = 0, gen: int = 0,
+                  shuffle: bool = True, device="cuda") -> DeviceInputs:
+    import torch
+
+    layout = page_layout(dims, seq_lens, reserve_steps, seed, gen, shuffle)
+    specs = dict(weight_specs(dims))
+    specs.update(kv_specs(dims, layout.num_pages, gen))
+    tensors = {n: device_tensor(s, seed, device) for n, s in specs.items()}
+    biases = [router_bias(dims, l, zipf_s, seed) for l in range(dims.n_layers)]
+    bias_t = [None if b is None else torch.from_numpy(b).to(device) for b in biases]
+    return DeviceInputs(dims, tensors, layout, biases, bias_t, seed)
+
+
+def host_inputs(dims: Dims, layout: PageLayout, seed: int = 0, gen: int = 0,
+                materialise: bool = True) -> Dict[str, object]:
+    """The same inputs for the oracle: host arrays, or (materialise=False)
+    the TensorSpecs from which the oracle regenerates every value."""
+    specs = dict(weight_specs(dims))
+    specs.update(kv_specs(dims, layout.num_pages, gen))
+    if not materialise:
+        return specs
+    return {n: host_tensor(s, seed) for n, s in specs.items()}
+
+
 __all__ = [n for n in dir() if not n.startswith("_")]

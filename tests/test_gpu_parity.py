@@ -1,0 +1,102 @@
+"""GPU decode step vs the CPU oracle, element by element (needs a GB300).
+
+Small workloads cover several tiles, ragged tails, every batch bucket of the
+kernel (1, 2, 4, 8 tokens), pages crossed mid-run, an empty cache, an
+automatic schedule rebuild and continuous batching.  The tolerance and the
+routing / greedy-token rules are the parity bar described in harness.py.
+"""
+import numpy as np
+import pytest
+
+import harness
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def run_steps(run, n, dumps=False):
+    reps = []
+    for _ in range(n):
+        rep = run.step(dumps=dumps)
+        reps.append(rep)
+        assert run.ok(rep), rep
+    return reps
+
+
+def test_generator_device_matches_host():
+    import torch
+
+    spec = synth.weight_specs(synth.TINY)["l1.wg"]
+    t = synth.device_tensor(spec)
+    torch.cuda.synchronize()
+    dev = t.view(torch.int16).cpu().numpy().view(np.uint16).ravel()
+    host = synth.host_tensor(spec).ravel()
+    assert np.array_equal(dev, host)
+
+
+def test_tiny_one_step_plus_eight_greedy():
+    run = harness.ParityRun("tiny")
+    run_steps(run, 9, dumps=True)
+    run.close()
+
+
+def test_odd_shapes_ragged_batch():
+    run = harness.ParityRun("odd", seq_lens=[29, 3, 50], reserve_steps=4)
+    run_steps(run, 4)
+    run.close()
+
+
+@pytest.mark.parametrize("batch", [2, 3, 4, 5, 8])
+def test_tiny_batch_buckets(batch):
+    lens = [64, 17, 0, 33, 16, 47, 5, 80][:batch]
+    run = harness.ParityRun("tiny", seq_lens=lens, reserve_steps=3)
+    run_steps(run, 3)
+    run.close()
+
+
+def test_empty_cache_and_page_boundaries():
+    run = harness.ParityRun("tiny", seq_lens=[0, 15, 16], reserve_steps=20)
+    run_steps(run, 18)
+    run.close()
+
+
+def test_mid_workload():
+    run = harness.ParityRun("mid", reserve_steps=4)
+    run_steps(run, 3)
+    run.close()
+
+
+def test_automatic_rebuild_after_growth():
+    run = harness.ParityRun("tiny", seq_lens=[40], reserve_steps=70)
+    run_steps(run, 66)
+    assert run.dec.stats().rebuilds >= 1
+    run.close()
+
+
+def test_continuous_batching_rebuild():
+    """Membership change: the schedule is rebuilt over a new set of sequences
+    whose pages the GPU has not written, so the oracle regenerates them."""
+    import oracle
+
+    P = synth.TINY.page_size
+    run = harness.ParityRun("tiny", seq_lens=[30, 12], reserve_steps=100, max_batch=4)
+    steps = 3
+    run_steps(run, steps)
+    pl = run.dev.layout
+    written = {int(pl.page_tables[b, pos // P]) for b, L in enumerate([30, 12])
+               for pos in range(L, L + steps)}
+    free = [p for p in range(pl.num_pages) if p not in written]
+    new_lens = [5, 20, 9]
+    need = [-(-(L + 4) // P) for L in new_lens]
+    pt = np.full((3, pl.max_pages), -1, np.int32)
+    at = 0
+    for b, n in enumerate(need):
+        pt[b, :n] = free[at:at + n]
+        at += n
+    run.dec.build_schedule(new_lens, pt)
+    host = synth.host_inputs(run.dims, pl)
+    run.orc = oracle.Oracle(run.dims, host, new_lens, pt, run.dev.biases)
+    run.tokens = np.array([1, 2, 3], np.int32)
+    run.alloc_io(3)
+    run_steps(run, 3)
+    run.close()

@@ -1,0 +1,194 @@
+"""The host task-table builder, checked on the CPU (no GPU needed).
+
+A simulator executes each CTA's queue in order with the kernel's counter
+semantics (wait on one count, signal one increment, last-ticket merges) and
+checks that every step completes (no deadlock in randomised interleavings),
+that every counter receives exactly the per-step increments the kernel is
+told to expect, and that the tiles cover every weight row, every KV page and
+every output row exactly once.
+"""
+import numpy as np
+import pytest
+
+import persistent_moe_decode_sm_gb300 as mk
+import synth
+
+OP_QKV, OP_ROUTER, OP_ATTN, OP_UP, OP_OUT, OP_LM, OP_HEADER = 1, 2, 3, 4, 5, 6, 100
+
+
+def cdims(d, max_batch, max_pages):
+    return mk.make_dims(d.n_layers, d.d_model, d.n_q_heads, d.n_kv_heads, d.head_dim, d.n_experts,
+                        d.top_k, d.d_ffn, d.vocab, d.page_size, max_batch, 100000, max_pages)
+
+
+def decode(table):
+    rows = []
+    for r in table:
+        assert r[0, 0] == OP_HEADER
+        nl, nf = int(r[0, 1]), int(r[0, 2])
+        rows.append((r[1:1 + nl], r[1 + nl:1 + nl + nf]))
+    return rows
+
+
+def simulate(d, info, rows, batch, rng):
+    """Runs one step's worth of tasks; raises on deadlock."""
+    L, Hkv = d.n_layers, d.n_kv_heads
+    qkv_done = [0] * L
+    router_ticket = [0] * L
+    routed = [False] * L
+    attn_ticket = {}
+    attn_done = [0] * L
+    up_done = [0] * L
+    out_done = [0] * L
+    lm_ticket = [0]
+    queues = [[(l, t) for l in range(L) for t in lt] + [(L, t) for t in ft] for lt, ft in rows]
+    pos = [0] * len(queues)
+
+    def ready(l, t):
+        op = t[0]
+        if op in (OP_QKV, OP_ROUTER):
+            return l == 0 or out_done[l - 1] == info.n_out
+        if op == OP_ATTN:
+            return qkv_done[l] == info.n_qkv
+        if op == OP_UP:
+            return routed[l]
+        if op == OP_OUT:
+            return attn_done[l] == batch * Hkv and up_done[l] == info.n_up
+        if op == OP_LM:
+            return out_done[L - 1] == info.n_out
+        raise AssertionError(op)
+
+    def run(l, t):
+        op = t[0]
+        if op == OP_QKV:
+            qkv_done[l] += 1
+        elif op == OP_ROUTER:
+            router_ticket[l] += 1
+            routed[l] = router_ticket[l] == info.n_router
+        elif op == OP_ATTN:
+            key = (l, int(t[1]), int(t[2]))
+            attn_ticket[key] = attn_ticket.get(key, 0) + 1
+            if attn_ticket[key] == t[7]:
+                attn_done[l] += 1
+        elif op == OP_UP:
+            up_done[l] += 1
+        elif op == OP_OUT:
+            out_done[l] += 1
+        elif op == OP_LM:
+            lm_ticket[0] += 1
+
+    remaining = sum(len(q) for q in queues)
+    while remaining:
+        progressed = False
+        for c in rng.permutation(len(queues)):
+            if pos[c] < len(queues[c]) and ready(*queues[c][pos[c]]):
+                run(*queues[c][pos[c]])
+                pos[c] += 1
+                remaining -= 1
+                progressed = True
+        assert progressed, "deadlock: no CTA can run its next task"
+    assert all(x == info.n_qkv for x in qkv_done)
+    assert all(routed)
+    assert all(x == batch * Hkv for x in attn_done)
+    assert all(x == info.n_up for x in up_done)
+    assert all(x == info.n_out for x in out_done)
+    assert lm_ticket[0] == info.n_lm
+
+
+def check_coverage(d, info, rows, seq_lens):
+    D, Hq, Hkv, P = d.head_dim, d.n_q_heads, d.n_kv_heads, d.page_size
+    lt_all = [t for lt, _ in rows for t in lt]
+    ft_all = [t for _, ft in rows for t in ft]
+    for mat, n in ((0, Hq * D), (1, Hkv * D), (2, Hkv * D)):
+        cov = np.zeros(n, int)
+        for t in lt_all:
+            if t[0] == OP_QKV and t[1] == mat:
+                cov[t[2]:t[2] + t[3]] += 1
+        assert np.all(cov == 1), mat
+    cov = np.zeros(d.n_experts, int)
+    for t in lt_all:
+        if t[0] == OP_ROUTER:
+            cov[t[2]:t[2] + t[3]] += 1
+    assert np.all(cov == 1)
+    slots = []
+    for b, L in enumerate(seq_lens):
+        npages = -(-L // P)
+        for h in range(Hkv):
+            sp = [t for t in lt_all if t[0] == OP_ATTN and t[1] == b and t[2] == h]
+            assert len(sp) >= 1 and all(t[7] == len(sp) for t in sp)
+            assert sum(int(t[8]) for t in sp) == 1
+            cov = np.zeros(max(npages, 1), int)
+            for t in sp:
+                p1 = npages if t[4] < 0 else t[4]
+                assert (t[4] < 0) == bool(t[8])
+                cov[t[3]:p1] += 1
+            assert np.all(cov[:npages] == 1)
+            slot0 = {int(t[6]) for t in sp}
+            assert len(slot0) == 1
+            s0 = slot0.pop()
+            assert sorted(int(t[5]) for t in sp) == list(range(s0, s0 + len(sp)))
+            slots += [int(t[5]) for t in sp]
+    assert sorted(slots) == list(range(info.n_attn_slots))
+    ups = sorted((int(t[1]), int(t[2])) for t in lt_all if t[0] == OP_UP)
+    assert ups == [(i, info.n_up) for i in range(info.n_up)]
+    cov = np.zeros(d.d_model, int)
+    for t in lt_all:
+        if t[0] == OP_OUT:
+            assert 1 <= t[3] <= 64
+            cov[t[2]:t[2] + t[3]] += 1
+    assert np.all(cov == 1)
+    cov = np.zeros(d.vocab, int)
+    idx = []
+    for t in ft_all:
+        assert t[0] == OP_LM
+        cov[t[2]:t[2] + t[3]] += 1
+        idx.append(int(t[4]))
+    assert np.all(cov == 1) and sorted(idx) == list(range(info.n_lm))
+
+
+def phase_rank(t):
+    return {OP_ROUTER: 0, OP_QKV: 0, OP_ATTN: 1, OP_UP: 2, OP_OUT: 3}[int(t[0])]
+
+
+CASES = [
+    ("tiny", synth.TINY, 152, [64]),
+    ("tiny_b8", synth.TINY, 152, [64, 0, 15, 16, 17, 100, 3, 31]),
+    ("mid", synth.MID, 152, [2048]),
+    ("full_b1_8k", synth.FULL, 152, [8192]),
+    ("full_b1_8k_148sm", synth.FULL, 148, [8192]),
+    ("full_b8_ragged", synth.FULL, 152, synth.workloads()["full_b8"].seq_lens),
+    ("long_b1", synth.FULL, 152, [262144]),
+    ("long_b2", synth.FULL, 152, [131072, 131072]),
+    ("few_sms", synth.MID, 7, [300, 5]),
+]
+
+
+@pytest.mark.parametrize("name,d,n_sm,lens", CASES, ids=[c[0] for c in CASES])
+def test_schedule_is_complete_and_deadlock_free(name, d, n_sm, lens):
+    max_pages = max(-(-(L + 300) // d.page_size) for L in lens)
+    info, table = mk.mk_plan(cdims(d, 8, max_pages), n_sm, len(lens), lens)
+    assert info.n_cta == n_sm and table.shape == (n_sm, info.tasks_per_cta, 32)
+    rows = decode(table)
+    for lt, ft in rows:
+        ranks = [phase_rank(t) for t in lt]
+        assert ranks == sorted(ranks), "tasks of a layer must run in phase order"
+    check_coverage(d, info, rows, lens)
+    rng = np.random.default_rng(0)
+    for _ in range(2 if d.n_layers > 8 else 4):
+        simulate(d, info, rows, len(lens), rng)
+
+
+def test_attention_splits_are_balanced():
+    d = synth.FULL
+    lens = synth.workloads()["full_b8"].seq_lens
+    info, table = mk.mk_plan(cdims(d, 8, 1100), 152, 8, lens)
+    pages = np.zeros(152)
+    for c, (lt, _) in enumerate(decode(table)):
+        for t in lt:
+            if t[0] == OP_ATTN:
+                npages = -(-lens[t[1]] // 16)
+                p1 = npages if t[4] < 0 else t[4]
+                pages[c] += p1 - t[3]
+    total = sum(-(-L // 16) for L in lens) * d.n_kv_heads
+    assert pages.sum() == total
+    assert pages.max() <= 1.25 * total / 152 + 2
