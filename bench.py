@@ -1,0 +1,351 @@
+"""Decode throughput of the persistent MoE megakernel on the full-scale synthetic model.
+
+Workload (one GPU): the full-scale synthetic MoE shaped to the pages' model
+(48 layers, d 2048, 32 query / 4 KV heads of 128, 128 experts top-8 with
+F 768, vocab 152064, untied LM head; ~6.1 GB of active bf16 weights per
+token) at batch 1 with 8192 cached tokens, greedy decoding.  A "step" is one
+mk_decode_step: every layer's norm, QKV, RoPE + KV append, paged attention,
+router top-k, expert SwiGLU, output projection and residual, then the final
+norm, LM head and argmax -- one persistent kernel launch.
+
+Metric: decode tokens/s and the fraction of the HBM speed of light, where
+SOL time = algorithmic bytes (active weights from the observed routing + KV
+read) / measured HBM bandwidth (MEASURED_PEAKS.json).  Inputs are larger
+than L2 (6.9 GB streamed per step), so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mk|reference]
+
+--impl reference times the CPU oracle (the plain reference of the same step)
+on this machine's host cores, on a bounded sample of the same workload.
+Under torchrun each rank runs an independent replica (the path does not
+shard): weak scaling, max-over-ranks timing.
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode tok/s at batch 1/8 and % of HBM speed-of-light (bytes/step ÷ peak GB/s)"
+PEAK_FALLBACK_GBS = 6800.0
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    return PEAK_FALLBACK_GBS, "fallback"
+
+
+def weight_bytes_step(dims, sum_u_layers: float, batch: int) -> float:
+    """Algorithmic weight bytes of one step: attention projections, router,
+    norms, the distinct chosen experts (sum over layers of U_l), LM head,
+    final norm and the embedding rows."""
+    d, D, Hq, Hkv = dims.d_model, dims.head_dim, dims.n_q_heads, dims.n_kv_heads
+    E, F, V, L = dims.n_experts, dims.d_ffn, dims.vocab, dims.n_layers
+    per_layer = d * (Hq + 2 * Hkv) * D + Hq * D * d + E * d + d
+    return 2.0 * (L * per_layer + sum_u_layers * 3 * d * F + V * d + d + batch * d)
+
+
+def kv_bytes_step(dims, lens) -> float:
+    """K and V bytes read for one step: L_b + 1 positions per sequence."""
+    return float(sum(L + 1 for L in lens)) * dims.n_layers * 2 * dims.n_kv_heads * dims.head_dim * 2
+
+
+def sol_formula(bytes_per_step: float, bw_gbs: float, batch: int = 1) -> float:
+    """Speed-of-light tokens/s: batch tokens per (bytes / bandwidth)."""
+    return batch * bw_gbs * 1e9 / bytes_per_step
+
+
+def kernel_source_hash() -> str:
+    src = os.path.join(ROOT, "persistent_moe_decode_sm_gb300", "csrc", "mk_kernel.cu")
+    with open(src, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "mk_decode_kernel_full_b1_8k.md")
+    if not os.path.exists(p):
+        return None
+    txt = open(p).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    h = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", txt)
+    if not m or not h or h.group(1) != kernel_source_hash():
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"mk_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        self.proc.wait()
+        self.fh.close()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": float(rows[0][2]) if rows[0][2].replace(".", "").isdigit() else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+
+def run_mk(args, rank, world):
+    import torch
+
+    import persistent_moe_decode_sm_gb300 as mk
+    import synth
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    wl = synth.workloads()["full"]
+    dims = wl.dims
+    if args.layers:
+        # profiling captures only: the same model cut to its first layers
+        dims = dataclasses.replace(dims, n_layers=args.layers)
+    lens = list(wl.seq_lens)
+    B = len(lens)
+    e2e_steps = args.e2e_steps
+    reserve = args.warmup + args.steps + e2e_steps + 8
+    inp = synth.device_inputs(dims, lens, reserve, None, seed=0)
+    pl = inp.layout
+    stream = torch.cuda.current_stream(dev)
+    dec = mk.Decoder(dims, inp.tensors, pl.num_pages, pl.max_pages, max(B, 1),
+                     inp.bias_tensors, stream)
+    dec.build_schedule(lens, pl.page_tables)
+    tok = [torch.tensor(synth.first_tokens(dims, B), dtype=torch.int32, device=dev),
+           torch.zeros(B, dtype=torch.int32, device=dev)]
+    logits = torch.empty(B, dims.vocab, dtype=torch.float32, device=dev)
+
+    # warm-up (greedy: each step's argmax is the next step's input)
+    cur = 0
+    for _ in range(args.warmup):
+        dec.decode_step(tok[cur], logits, tok[cur ^ 1])
+        cur ^= 1
+    dec.sync()
+    st0 = dec.stats()
+    lens_at_start = [L + args.warmup for L in lens]
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for k in range(args.steps):
+        ev[k][0].record(stream)
+        dec.decode_step(tok[cur], logits, tok[cur ^ 1])
+        ev[k][1].record(stream)
+        cur ^= 1
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    dec.sync()
+    total_ms = t_start.elapsed_time(t_end)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    st1 = dec.stats()
+    sum_u = float(st1.sum_experts - st0.sum_experts)  # over steps and layers
+
+    # algorithmic bytes over the timed steps
+    w_bytes = sum(weight_bytes_step(dims, 0.0, B) for _ in range(args.steps)) + \
+        2.0 * sum_u * 3 * dims.d_model * dims.d_ffn
+    kv_bytes = sum(kv_bytes_step(dims, [L + k for L in lens_at_start]) for k in range(args.steps))
+    total_bytes = w_bytes + kv_bytes
+    bytes_per_step = total_bytes / args.steps
+    peak, peak_kind = load_peaks()
+    secs = total_ms / 1e3
+    tok_s = B * args.steps / secs * world
+    sol_tok_s = sol_formula(bytes_per_step, peak, B)
+    mean_launch_s = statistics.mean(launch_ms) / 1e3
+    achieved_gbs = bytes_per_step / mean_launch_s / 1e9
+
+    # end to end through the C ABI with host buffers: H2D of the token ids,
+    # the step, D2H of the next tokens, every step
+    h_tok = torch.tensor(synth.first_tokens(dims, B), dtype=torch.int32).pin_memory()
+    h_next = torch.empty(B, dtype=torch.int32).pin_memory()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        tok[0].copy_(h_tok, non_blocking=True)
+        dec.decode_step(tok[0], logits, tok[1])
+        h_next.copy_(tok[1], non_blocking=True)
+        stream.synchronize()
+        h_tok.copy_(h_next)
+    e2e_s = time.perf_counter() - t0
+    dec.sync()
+    e2e_tok_s = B * e2e_steps / e2e_s * world if e2e_steps else None
+    dec.close()
+    del inp
+
+    out = {
+        "metric": METRIC, "value": round(tok_s, 2), "unit": "tok/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded bf16 N(0,0.02) weights, N(0,1) KV; no trained weights)",
+        "config": {"workload": "full-scale synthetic MoE, batch 1 at 8192 cached tokens "
+                               "(48 layers, d 2048, 32/4 heads x 128, 128 experts top-8, "
+                               "F 768, vocab 152064)",
+                   "batch": B, "cached_tokens": lens, "decode_steps": args.steps,
+                   "l2": "inputs larger than L2 (6.9 GB streamed per step), no flush",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "sol": {"bytes_per_step": round(bytes_per_step), "weight_bytes_per_step":
+                round(w_bytes / args.steps), "kv_bytes_per_step": round(kv_bytes / args.steps),
+                "sol_tok_s": round(sol_tok_s, 1), "fraction": round(tok_s / world / sol_tok_s, 4),
+                "bw_gbs": peak, "bw_kind": peak_kind},
+        "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved_gbs / peak, 4),
+                     "traffic": profiled_traffic(), "kernel": "mk::decode_kernel<1>",
+                     "peak_kind": f"{peak_kind} (copy bandwidth)",
+                     "mean_launch_ms": round(mean_launch_s * 1e3, 4)},
+        "e2e": {"value": e2e_tok_s and round(e2e_tok_s, 2), "unit": "tok/s", "h2d_bytes_per_step": 4 * B,
+                "d2h_bytes_per_step": 4 * B, "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    return out
+
+
+# -------------------------------------------------------------- CPU oracle
+
+
+def oracle_step_time(max_seconds: float, max_steps: int):
+    """Times full-scale oracle decode steps (weights regenerated on the fly
+    from the seeded generator) until max_steps or max_seconds."""
+    import oracle
+    import synth
+
+    wl = synth.workloads()["full"]
+    dims = wl.dims
+    pl = synth.page_layout(dims, wl.seq_lens, max_steps + 2)
+    host = synth.host_inputs(dims, pl, materialise=False)
+    orc = oracle.Oracle(dims, host, wl.seq_lens, pl.page_tables)
+    tok = synth.first_tokens(dims, 1)
+    times = []
+    t_all = time.perf_counter()
+    for _ in range(max_steps):
+        t0 = time.perf_counter()
+        r = orc.step(tok)
+        times.append(time.perf_counter() - t0)
+        tok = r["next_tokens"]
+        if time.perf_counter() - t_all > max_seconds:
+            break
+    return times
+
+
+def cpu_baseline(max_seconds=30.0, max_steps=3):
+    times = oracle_step_time(max_seconds, max_steps)
+    return {"value": round(len(times) / sum(times), 4), "unit": "tok/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"{len(times)} full-scale decode step(s) of the oracle (batch 1, 8192 "
+                      "cached tokens; weights regenerated on the fly from the seeded "
+                      "generator, OpenMP over all host cores)"}
+
+
+def run_reference(args):
+    times = oracle_step_time(max_seconds=180.0, max_steps=max(1, args.steps))
+    v = len(times) / sum(times)
+    cb = {"value": round(v, 4), "unit": "tok/s", "cores": os.cpu_count(), "kind": "oracle",
+          "sample": f"{len(times)} of the requested {args.steps} full-scale decode steps "
+                    "(bounded to ~3 minutes of CPU time); weights regenerated on the fly"}
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "tok/s",
+            "n_gpus": 1, "steps": len(times), "warmup": 0,
+            "ms_per_step": round(1e3 * sum(times) / len(times), 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32-accumulate over bf16",
+            "data": "synthetic",
+            "config": {"workload": "full-scale synthetic MoE, batch 1 at 8192 cached tokens"},
+            "cpu_baseline": cb,
+            "e2e": {"value": round(v, 4), "unit": "tok/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", default="mk", choices=["mk", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=64)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling only: cut the model to its first N layers")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    out = run_mk(args, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -18,6 +18,7 @@ def run_steps(run, n, dumps=False):
     reps = []
     for _ in range(n):
         rep = run.step(dumps=dumps)
+        print({k: v for k, v in rep.items() if not isinstance(v, list)})
         reps.append(rep)
         assert run.ok(rep), rep
     return reps
@@ -76,8 +77,6 @@ def test_automatic_rebuild_after_growth():
 def test_continuous_batching_rebuild():
     """Membership change: the schedule is rebuilt over a new set of sequences
     whose pages the GPU has not written, so the oracle regenerates them."""
-    import oracle
-
     P = synth.TINY.page_size
     run = harness.ParityRun("tiny", seq_lens=[30, 12], reserve_steps=100, max_batch=4)
     steps = 3
@@ -94,8 +93,7 @@ def test_continuous_batching_rebuild():
         pt[b, :n] = free[at:at + n]
         at += n
     run.dec.build_schedule(new_lens, pt)
-    host = synth.host_inputs(run.dims, pl)
-    run.orc = oracle.Oracle(run.dims, host, new_lens, pt, run.dev.biases)
+    run.reset_oracles(synth.host_inputs(run.dims, pl), new_lens, pt)
     run.tokens = np.array([1, 2, 3], np.int32)
     run.alloc_io(3)
     run_steps(run, 3)
