@@ -58,7 +58,8 @@ enum {
   MK_ERR_DEVICE_TIMEOUT = 6,/* a device wait exceeded the wait limit (sticky) */
   MK_ERR_BAD_TASK = 7,      /* the kernel met an unknown task opcode (sticky) */
   MK_ERR_UNSUPPORTED = 8,   /* dims this build does not support (see mk_create) */
-  MK_ERR_NO_DEVICE = 9      /* no usable sm_103 device */
+  MK_ERR_NO_DEVICE = 9,     /* no usable sm_103 device */
+  MK_ERR_SCRATCH_LIMIT = 10 /* mk_decode_step_static: workspace larger than its static scratch */
 };
 
 /* Model dimensions.  page_size tokens per KV page; num_pages pages in each
@@ -124,6 +125,33 @@ mk_status mk_sync(mk_ctx *ctx);
 void mk_destroy(mk_ctx *ctx);
 
 const char *mk_status_string(mk_status s);
+
+/* One decode step that allocates no memory of its own: no cudaMalloc,
+ * cudaFree, cudaHostAlloc or allocating library routine.  The three pages
+ * have no counterpart of this call; it exists for callers that cannot
+ * allocate device memory themselves -- for example code whose device memory
+ * is entirely owned by an arena or caching allocator, or code running under a
+ * memory budget that is already handed out -- and so cannot use mk_create.
+ * It runs the same kernel as mk_decode_step, with all of that kernel's scratch
+ * (activations, partial sums, counters, routing, task table, page tables,
+ * RoPE rows) in one static device array of 16 MiB that every GPU loading the
+ * library holds until the process exits.  Workloads whose scratch does not fit
+ * (larger models, long contexts) get MK_ERR_SCRATCH_LIMIT.
+ *   dims, w      as for mk_create (w->layers is a HOST array);
+ *   batch, seq_lens, page_tables   as for mk_build_schedule (HOST arrays);
+ *   token_ids, out_logits (may be NULL), out_next_tokens   DEVICE, as for
+ *                mk_decode_step; the new K/V rows are written at L_b;
+ *   stream       a cudaStream_t (NULL = legacy default stream).
+ * Synchronous: returns after the step, with the kernel's status.  The first
+ * call on a device looks up the array's device address (cudaGetSymbolAddress)
+ * with that device current, so make that first call before any stream
+ * capture.  Calls share the array: the counters are cleared by each call, and
+ * calls that overlap on the GPU race (serialise them).  There is no sticky
+ * state: every call stands alone. */
+mk_status mk_decode_step_static(const mk_model_dims *dims, const mk_weights *w, int32_t batch,
+                                const int32_t *seq_lens, const int32_t *page_tables,
+                                const int32_t *token_ids, float *out_logits,
+                                int32_t *out_next_tokens, void *stream);
 
 /* ---- diagnostics (tests / benchmark) ------------------------------------- */
 

@@ -25,15 +25,17 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(BUILD, "libmk.so")
 
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
-SOURCES = ["mk_kernel.cu", "mk_api.cpp", "mk_schedule.cpp"]
+SOURCES = ["mk_kernel.cu", "mk_api.cpp", "mk_schedule.cpp", "mk_noalloc.cu"]
 
 MK_OK = 0
 STATUS_NAMES = {0: "MK_OK", 1: "MK_ERR_INVALID_ARG", 2: "MK_ERR_BATCH", 3: "MK_ERR_PAGE_OOB",
                 4: "MK_ERR_NO_SCHEDULE", 5: "MK_ERR_CUDA", 6: "MK_ERR_DEVICE_TIMEOUT",
-                7: "MK_ERR_BAD_TASK", 8: "MK_ERR_UNSUPPORTED", 9: "MK_ERR_NO_DEVICE"}
+                7: "MK_ERR_BAD_TASK", 8: "MK_ERR_UNSUPPORTED", 9: "MK_ERR_NO_DEVICE",
+                10: "MK_ERR_SCRATCH_LIMIT"}
 MK_ERR_INVALID_ARG, MK_ERR_BATCH, MK_ERR_PAGE_OOB, MK_ERR_NO_SCHEDULE = 1, 2, 3, 4
 MK_ERR_CUDA, MK_ERR_DEVICE_TIMEOUT, MK_ERR_BAD_TASK, MK_ERR_UNSUPPORTED = 5, 6, 7, 8
 MK_ERR_NO_DEVICE = 9
+MK_ERR_SCRATCH_LIMIT = 10
 
 
 def build_commands() -> List[List[str]]:
@@ -102,7 +104,7 @@ class mk_plan_info(ctypes.Structure):
 
 EXPORTS = ["mk_create", "mk_build_schedule", "mk_decode_step", "mk_sync", "mk_destroy",
            "mk_status_string", "mk_set_wait_limit_ns", "mk_debug_routing", "mk_debug_dump",
-           "mk_get_stats", "mk_debug_poison_wait", "mk_plan"]
+           "mk_get_stats", "mk_debug_poison_wait", "mk_plan", "mk_decode_step_static"]
 
 _lib = None
 
@@ -131,6 +133,9 @@ def lib():
         L.mk_debug_poison_wait.argtypes = [vp, i32, i32]
         L.mk_plan.argtypes = [ctypes.POINTER(mk_model_dims), i32, i32, vp,
                               ctypes.POINTER(mk_plan_info), vp, i64]
+        L.mk_decode_step_static.argtypes = [ctypes.POINTER(mk_model_dims),
+                                            ctypes.POINTER(mk_weights), i32, vp, vp, vp, vp, vp,
+                                            vp]
         for n in EXPORTS:
             if n not in ("mk_destroy", "mk_status_string"):
                 getattr(L, n).restype = i32
@@ -238,6 +243,19 @@ def mk_get_stats(ctx: int) -> mk_stats:
     st = mk_stats()
     _check(lib().mk_get_stats(ctx, ctypes.byref(st)), "mk_get_stats")
     return st
+
+
+def mk_decode_step_static(dims: mk_model_dims, weights: Weights, batch: int, seq_lens,
+                          page_tables, token_ids, out_logits, out_next_tokens,
+                          stream=None) -> None:
+    """One decode step with no allocation by the library (see include/mk.h)."""
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    pt = np.ascontiguousarray(page_tables, dtype=np.int32)
+    s = stream.cuda_stream if hasattr(stream, "cuda_stream") else (stream or 0)
+    _check(lib().mk_decode_step_static(ctypes.byref(dims), ctypes.byref(weights.c), batch,
+                                       sl.ctypes.data, pt.ctypes.data, _addr(token_ids),
+                                       _addr(out_logits), _addr(out_next_tokens), s),
+           "mk_decode_step_static")
 
 
 def mk_plan(dims: mk_model_dims, n_sm: int, batch: int, seq_lens):

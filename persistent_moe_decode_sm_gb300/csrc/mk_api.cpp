@@ -173,6 +173,7 @@ const char *mk_status_string(mk_status s) {
     case MK_ERR_BAD_TASK: return "corrupt task descriptor";
     case MK_ERR_UNSUPPORTED: return "unsupported dimensions";
     case MK_ERR_NO_DEVICE: return "no usable sm_103 device";
+    case MK_ERR_SCRATCH_LIMIT: return "workspace larger than the static scratch of mk_decode_step_static";
     default: return "unknown status";
   }
 }
