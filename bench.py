@@ -229,6 +229,18 @@ def run_mk(args, rank, world):
     e2e_s = time.perf_counter() - t0
     dec.sync()
     e2e_tok_s = B * e2e_steps / e2e_s * world if e2e_steps else None
+    trace_summary = None
+    if args.trace:
+        # one more step with the per-task trace on (outside the timed region)
+        from persistent_moe_decode_sm_gb300 import trace as mktrace
+
+        mk.mk_set_trace(dec.ctx, dims.n_layers * 16 + 16)
+        dec.decode_step(tok[0], logits, tok[1])
+        tr = mk.mk_get_trace(dec.ctx)
+        trace_summary = mktrace.summarize(tr, dims.n_layers)
+        with open(args.trace, "w") as f:
+            json.dump(trace_summary, f, indent=1)
+        mk.mk_set_trace(dec.ctx, 0)
     dec.close()
     del inp
 
@@ -257,6 +269,8 @@ def run_mk(args, rank, world):
         "gpu_launches": args.steps,
         "clocks": clocks,
     }
+    if trace_summary:
+        out["trace"] = {k: trace_summary[k] for k in ("step_us", "layer_us_median", "cta_time_split")}
     return out
 
 
@@ -321,6 +335,7 @@ def main():
     ap.add_argument("--impl", default="mk", choices=["mk", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--trace", default="", help="write a per-task trace summary (JSON) here")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: cut the model to its first N layers")
     args = ap.parse_args()

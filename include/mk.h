@@ -184,6 +184,19 @@ mk_status mk_get_stats(mk_ctx *ctx, mk_stats *out);
  * bounded-wait path (MK_ERR_DEVICE_TIMEOUT) can be exercised without a hang. */
 mk_status mk_debug_poison_wait(mk_ctx *ctx, int32_t layer, int32_t delta);
 
+/* Per-task timing trace of the following steps (diagnostic; each step
+ * overwrites the previous one).  events_per_cta = 0 turns it off; otherwise
+ * a buffer of n_sm * events_per_cta events is allocated.  Consumer thread 0
+ * of every CTA records, for each task it runs: [0] op | layer << 8 |
+ * task << 20, [1] entry, [2] dependency satisfied, [3] first data stage
+ * available (0 if none), [4] exit -- globaltimer nanoseconds, 8 words per
+ * event, unused events zero. */
+mk_status mk_set_trace(mk_ctx *ctx, int32_t events_per_cta);
+/* Copies the trace (synchronises).  host_out may be NULL to query the
+ * geometry; otherwise it must hold n_cta * events_per_cta * 8 words. */
+mk_status mk_get_trace(mk_ctx *ctx, uint64_t *host_out, uint64_t n_words, int32_t *n_cta,
+                       int32_t *events_per_cta);
+
 /* Host-only schedule planning (no GPU needed): the task table that
  * mk_build_schedule would upload for n_sm SMs.  Writes at most cap int32s of
  * [n_cta][tasks_per_cta][32] descriptors into table (may be NULL to query)

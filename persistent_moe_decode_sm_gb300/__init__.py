@@ -104,7 +104,8 @@ class mk_plan_info(ctypes.Structure):
 
 EXPORTS = ["mk_create", "mk_build_schedule", "mk_decode_step", "mk_sync", "mk_destroy",
            "mk_status_string", "mk_set_wait_limit_ns", "mk_debug_routing", "mk_debug_dump",
-           "mk_get_stats", "mk_debug_poison_wait", "mk_plan", "mk_decode_step_static"]
+           "mk_get_stats", "mk_debug_poison_wait", "mk_plan", "mk_decode_step_static",
+           "mk_set_trace", "mk_get_trace"]
 
 _lib = None
 
@@ -136,6 +137,8 @@ def lib():
         L.mk_decode_step_static.argtypes = [ctypes.POINTER(mk_model_dims),
                                             ctypes.POINTER(mk_weights), i32, vp, vp, vp, vp, vp,
                                             vp]
+        L.mk_set_trace.argtypes = [vp, i32]
+        L.mk_get_trace.argtypes = [vp, vp, u64, vp, vp]
         for n in EXPORTS:
             if n not in ("mk_destroy", "mk_status_string"):
                 getattr(L, n).restype = i32
@@ -256,6 +259,19 @@ def mk_decode_step_static(dims: mk_model_dims, weights: Weights, batch: int, seq
                                        sl.ctypes.data, pt.ctypes.data, _addr(token_ids),
                                        _addr(out_logits), _addr(out_next_tokens), s),
            "mk_decode_step_static")
+
+
+def mk_set_trace(ctx: int, events_per_cta: int) -> None:
+    _check(lib().mk_set_trace(ctx, events_per_cta), "mk_set_trace")
+
+
+def mk_get_trace(ctx: int) -> np.ndarray:
+    """The last step's trace as uint64 [n_cta][events][8]."""
+    n_cta, ev = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib().mk_get_trace(ctx, None, 0, ctypes.byref(n_cta), ctypes.byref(ev)), "mk_get_trace")
+    out = np.zeros((n_cta.value, ev.value, 8), np.uint64)
+    _check(lib().mk_get_trace(ctx, out.ctypes.data, out.size, None, None), "mk_get_trace")
+    return out
 
 
 def mk_plan(dims: mk_model_dims, n_sm: int, batch: int, seq_lens):

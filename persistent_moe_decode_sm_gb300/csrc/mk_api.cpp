@@ -79,6 +79,8 @@ struct mk_ctx {
   uint64_t steps = 0, rebuilds = 0;
   mk_status sticky = MK_OK;
   bool prepared[4] = {false, false, false, false}; /* kernel attributes set per batch bucket */
+  unsigned long long *trace = nullptr; /* [n_sm][trace_cap][MK_TRACE_WORDS] */
+  int trace_cap = 0;
 };
 
 namespace {
@@ -88,11 +90,15 @@ mk_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MK_OK : MK_ERR_
 int nb_for(int batch) { return batch <= 1 ? 1 : batch <= 2 ? 2 : batch <= 4 ? 4 : 8; }
 
 size_t xbuf_bytes_for(const mk_model_dims &d, int nb) {
-  const size_t HqD = (size_t)d.n_q_heads * d.head_dim;
-  size_t x = (size_t)nb * d.d_model * 2;
-  x = std::max(x, (size_t)nb * HqD * 2);
-  x = std::max(x, (size_t)2 * nb * d.d_ffn * 2);
+  /* activations are fp32 for one token, bf16 otherwise */
+  const size_t HqD = (size_t)d.n_q_heads * d.head_dim, xt = nb == 1 ? 4 : 2;
+  const size_t u_max = (size_t)std::min(d.n_experts, d.max_batch * d.top_k);
+  size_t x = (size_t)nb * d.d_model * (xt + 2); /* normed input + staged h */
+  x = std::max(x, (size_t)nb * HqD * xt);
+  x = std::max(x, (size_t)2 * nb * d.d_ffn * xt);
+  x = std::max(x, std::min(u_max * nb * d.d_ffn * xt, (size_t)32768)); /* all experts at once */
   x = std::max(x, (size_t)(8 + 2 + 32) * d.head_dim * 4); /* attention q, k, v, merge */
+  x = std::max(x, (size_t)(2 * 256 * MK_MAX_GROUP + 2 * MK_MAX_GROUP) * 4); /* split merge */
   return align_up(x, 1024);
 }
 
@@ -249,7 +255,7 @@ mk_status mk_create(const mk_model_dims *dims, const mk_weights *w, void *stream
   const size_t o_h = cv.take((size_t)(L + 1) * MB * d.d_model * 2);
   const size_t o_qkv = cv.take((size_t)L * MB * QKVD * 2);
   const size_t o_o = cv.take((size_t)L * MB * HqD * 2);
-  const size_t o_part = cv.take((size_t)L * c->n_slots_max * G * (d.head_dim + 2) * 4);
+  const size_t o_part = cv.take((size_t)L * c->n_slots_max * G * (d.head_dim + 4) * 4);
   const size_t o_rl = cv.take((size_t)L * MB * d.n_experts * 4);
   const size_t o_rt = cv.take((size_t)L * sizeof(mk_routing));
   const size_t o_act = cv.take((size_t)L * c->u_max * MB * d.d_ffn * 2);
@@ -457,6 +463,8 @@ mk_status mk_decode_step(mk_ctx *c, const int32_t *token_ids, float *out_logits,
   p.xbuf_bytes = (int32_t)xb;
   p.poison_layer = c->poison_layer;
   p.poison_delta = c->poison_delta;
+  p.trace = c->trace;
+  p.trace_cap = c->trace_cap;
   c->poison_layer = -1;
   c->poison_delta = 0;
 
@@ -489,7 +497,37 @@ void mk_destroy(mk_ctx *c) {
     if (c->stage_done[k]) cudaEventDestroy(c->stage_done[k]);
   }
   if (c->err_host) cudaFreeHost(c->err_host);
+  if (c->trace) cudaFree(c->trace);
   delete c;
+}
+
+mk_status mk_set_trace(mk_ctx *c, int32_t events_per_cta) {
+  if (!c || events_per_cta < 0) return MK_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(c->stream) != cudaSuccess) return MK_ERR_CUDA;
+  if (c->trace) cudaFree(c->trace);
+  c->trace = nullptr;
+  c->trace_cap = 0;
+  if (events_per_cta == 0) return MK_OK;
+  const size_t bytes = (size_t)c->n_sm * events_per_cta * MK_TRACE_WORDS * 8;
+  if (cudaMalloc(&c->trace, bytes) != cudaSuccess) return MK_ERR_CUDA;
+  if (cudaMemset(c->trace, 0, bytes) != cudaSuccess) return MK_ERR_CUDA;
+  c->trace_cap = events_per_cta;
+  return MK_OK;
+}
+
+mk_status mk_get_trace(mk_ctx *c, uint64_t *host_out, uint64_t n_words, int32_t *n_cta,
+                       int32_t *events_per_cta) {
+  if (!c) return MK_ERR_INVALID_ARG;
+  if (n_cta) *n_cta = c->n_sm;
+  if (events_per_cta) *events_per_cta = c->trace_cap;
+  if (!host_out) return MK_OK;
+  const uint64_t need = (uint64_t)c->n_sm * c->trace_cap * MK_TRACE_WORDS;
+  if (!c->trace || n_words < need) return MK_ERR_INVALID_ARG;
+  mk_status st = mk_sync(c);
+  if (st != MK_OK) return st;
+  if (cudaMemcpy(host_out, c->trace, need * 8, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MK_ERR_CUDA;
+  return MK_OK;
 }
 
 mk_status mk_set_wait_limit_ns(mk_ctx *c, uint64_t ns) {

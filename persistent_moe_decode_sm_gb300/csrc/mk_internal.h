@@ -103,7 +103,7 @@ typedef struct {
   uint16_t *h;                /* [L+1][MAXB][d]  (h[0] holds the embedding rows for dumps) */
   uint16_t *qkv;              /* [L][MAXB][(Hq+2Hkv)D] pre-RoPE q, k, v */
   uint16_t *o;                /* [L][MAXB][Hq D] */
-  float *attn_part;           /* [L][n_slots][G][D + 2] (m, l, o) */
+  float *attn_part;           /* [L][n_slots][G][D + 4] (m, l, -, -, o[D]) */
   float *router_logits;       /* [L][MAXB][E] */
   mk_routing *routing;        /* [L] */
   uint16_t *act;              /* [L][Umax][MAXB][F] */
@@ -125,7 +125,14 @@ typedef struct {
   int32_t ring_stages;        /* stages of MK_STAGE_BYTES in the shared ring */
   int32_t xbuf_bytes;         /* shared activation buffer */
   int32_t poison_layer, poison_delta; /* test hook: see mk_debug_poison_wait */
+  unsigned long long *trace;  /* NULL, or [n_cta][trace_cap][MK_TRACE_WORDS] task timestamps */
+  int32_t trace_cap;
 } mk_kparams;
+
+/* One trace event (per executed task, written by consumer thread 0):
+ * [0] op | layer << 8 | task << 20, [1] entry, [2] dependency satisfied,
+ * [3] first stage of data available, [4] exit (globaltimer ns). */
+#define MK_TRACE_WORDS 8
 
 #ifdef __CUDACC__
 #define MK_HD __host__ __device__

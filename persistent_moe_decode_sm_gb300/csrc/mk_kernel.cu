@@ -35,6 +35,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "mk.h"
 #include "mk_internal.h"
 
@@ -181,6 +183,25 @@ __device__ __forceinline__ bool reduce_leader(int lane) {
   return (lane & ((32 >> LOG) - 1)) == 0;
 }
 
+/* The DPL (= D / 32 <= 4) bf16 head dims of lane `lane` in a K or V row. */
+__device__ __forceinline__ void lane_dims(const uint16_t *row, int lane, int DPL, float (&o)[4]) {
+  if (DPL == 4) {
+    const uint2 v = *(const uint2 *)(row + lane * 4);
+    o[0] = __uint_as_float(v.x << 16);
+    o[1] = __uint_as_float(v.x & 0xFFFF0000u);
+    o[2] = __uint_as_float(v.y << 16);
+    o[3] = __uint_as_float(v.y & 0xFFFF0000u);
+  } else if (DPL == 2) {
+    const uint32_t v = *(const uint32_t *)(row + lane * 2);
+    o[0] = __uint_as_float(v << 16);
+    o[1] = __uint_as_float(v & 0xFFFF0000u);
+    o[2] = o[3] = 0.0f;
+  } else {
+    o[0] = bf2f(row[lane]);
+    o[1] = o[2] = o[3] = 0.0f;
+  }
+}
+
 /* acc[b] += w . x[b] over K elements (K % 8 == 0), w and x bf16 in shared
  * memory; lane l handles the 8-element chunks l, l + 32, ... */
 template <int NB>
@@ -320,218 +341,450 @@ __device__ bool wait_mbar(const Ctx &cx, uint64_t *bar, uint32_t parity, int tas
 }
 
 /* ============================================================== producer
- * Streams every task's immutable bytes into ring slot i % nstages (stage i).
+ * One thread (lane 0 of the producer warp) walks the CTA's task list stage
+ * by stage with two cursors over the same sequence:
+ *   - the load cursor copies stage i into ring slot i % nstages (TMA bulk
+ *     copies completing on full[slot]) once the consumers have released it;
+ *   - the prefetch cursor runs up to MK_PREFETCH_STAGES stages further and
+ *     asks L2 for those bytes (cp.async.bulk.prefetch.L2), so that when a
+ *     slot frees the copy is served from L2 rather than paying the loaded
+ *     HBM latency again.  It never waits: at a task whose bytes depend on
+ *     routing that is not known yet it pauses until the load cursor passes.
  * Consumers walk the same deterministic stage sequence. */
+
+#define MK_PREFETCH_STAGES 8
+
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+struct Seg {
+  const uint8_t *src;
+  uint32_t off, bytes;
+};
+
+enum { IT_STAGE = 1, IT_END = 0, IT_BLOCKED = -1, IT_FAIL = -2 };
+
+struct StageIter {
+  const mk_kparams *p;
+  const int32_t *row;
+  int nl, nf;
+  uint32_t epoch;
+  int layer, k;   /* current task (layer == L: the final tasks) */
+  bool started;
+  long count;     /* stages produced */
+  /* current task */
+  int op;
+  const int32_t *t;
+  const mk_layer_dev *ly;
+  const uint16_t *src; /* row streams */
+  int r, nrows, K;
+  int q, p1, b, kvh;   /* attention pages */
+  int64_t v, v1;       /* gate/up share */
+  int u, U;            /* OUT: u = -1 while on Wo rows, then the down slot */
+  const mk_routing *rt;
+
+  __device__ void init(const mk_kparams *pp, const int32_t *rw, uint32_t ep) {
+    p = pp;
+    row = rw;
+    nl = rw[1];
+    nf = rw[2];
+    epoch = ep;
+    layer = 0;
+    k = 0;
+    started = false;
+    count = 0;
+    if (nl == 0) layer = p->L; /* no layer tasks */
+  }
+
+  __device__ bool at_end() const { return layer > p->L || (layer == p->L && k >= nf); }
+
+  __device__ void next_task() {
+    started = false;
+    ++k;
+    if (layer < p->L && k >= nl) {
+      k = 0;
+      ++layer;
+      if (layer < p->L && nl == 0) layer = p->L;
+    }
+  }
+
+  /* Routing of this task's layer: known? (blocking: wait, bounded). */
+  __device__ int routing(bool block, const Ctx &cx) {
+    int32_t *c = lctr(*p, layer, CTR_ROUTED);
+    if ((int)(ld_acquire(c) - (int)(epoch + 1)) >= 0) return IT_STAGE;
+    if (!block) return IT_BLOCKED;
+    return wait_counter(cx, c, (int)(epoch + 1), -1, OP_UP, layer, CTR_ROUTED) ? IT_STAGE : IT_FAIL;
+  }
+
+  __device__ void rows_from(const uint16_t *s0, int n, int KK) {
+    src = s0;
+    r = 0;
+    nrows = n;
+    K = KK;
+  }
+
+  __device__ int begin(bool block, const Ctx &cx) {
+    t = row + MK_DESC_INTS * (1 + (layer < p->L ? k : nl + k));
+    op = t[0];
+    const int L = layer < p->L ? layer : p->L - 1;
+    ly = p->layers + L;
+    switch (op) {
+      case OP_QKV: {
+        const uint16_t *w = t[1] == 0 ? ly->wq : t[1] == 1 ? ly->wk : ly->wv;
+        rows_from(w + (size_t)t[2] * p->d, t[3], p->d);
+        return IT_STAGE;
+      }
+      case OP_ROUTER:
+        rows_from(ly->wr + (size_t)t[2] * p->d, t[3], p->d);
+        return IT_STAGE;
+      case OP_LM:
+        rows_from(p->lm_head + (size_t)t[2] * p->d, t[3], p->d);
+        return IT_STAGE;
+      case OP_ATTN:
+        b = t[1];
+        kvh = t[2];
+        q = t[3];
+        p1 = t[4] >= 0 ? t[4] : (__ldg(p->seq_lens + b) + p->P - 1) / p->P;
+        return IT_STAGE;
+      case OP_UP: {
+        const int rs = routing(block, cx);
+        if (rs != IT_STAGE) return rs;
+        rt = p->routing + layer;
+        U = __ldcg(&rt->U);
+        const int64_t T = (int64_t)U * p->F;
+        v = T * t[1] / t[2];
+        v1 = T * (t[1] + 1) / t[2];
+        return IT_STAGE;
+      }
+      case OP_OUT:
+        u = -1;
+        rows_from(ly->wo + (size_t)t[2] * p->Hq * p->D, t[3], p->Hq * p->D);
+        return IT_STAGE;
+      default:
+        return IT_FAIL; /* the consumers report the bad opcode */
+    }
+  }
+
+  __device__ bool row_stage(Seg *seg, int &nseg, uint32_t &total) {
+    if (r >= nrows) return false;
+    const uint32_t rb = (uint32_t)K * 2;
+    const int cnt = min(mk_rows_per_stage(rb), nrows - r);
+    seg[0].src = (const uint8_t *)(src + (size_t)r * K);
+    seg[0].off = 0;
+    seg[0].bytes = cnt * rb;
+    nseg = 1;
+    total = cnt * rb;
+    r += cnt;
+    return true;
+  }
+
+  /* IT_STAGE: a stage; IT_END: this task has no more; IT_BLOCKED / IT_FAIL */
+  __device__ int emit(Seg *seg, int &nseg, uint32_t &total, bool block, const Ctx &cx) {
+    switch (op) {
+      case OP_QKV:
+      case OP_ROUTER:
+      case OP_LM:
+        return row_stage(seg, nseg, total) ? IT_STAGE : IT_END;
+      case OP_ATTN: {
+        if (q >= p1) return IT_END;
+        const uint32_t pb = (uint32_t)p->P * p->D * 2;
+        const int cnt = min(mk_pages_per_stage(pb), p1 - q);
+        for (int j = 0; j < cnt; ++j) {
+          const int page = __ldg(p->page_table + b * p->max_pages + q + j);
+          const size_t blk = ((size_t)page * p->Hkv + kvh) * p->P * p->D;
+          seg[2 * j].src = (const uint8_t *)(ly->kc + blk);
+          seg[2 * j + 1].src = (const uint8_t *)(ly->vc + blk);
+          seg[2 * j].off = 2 * j * pb;
+          seg[2 * j + 1].off = (2 * j + 1) * pb;
+          seg[2 * j].bytes = seg[2 * j + 1].bytes = pb;
+        }
+        nseg = 2 * cnt;
+        total = 2 * cnt * pb;
+        q += cnt;
+        return IT_STAGE;
+      }
+      case OP_UP: {
+        if (v >= v1) return IT_END;
+        const int F = p->F, d = p->d;
+        const int uu = (int)(v / F), f0 = (int)(v % F);
+        const int f1 = (int)min((int64_t)F, f0 + (v1 - v));
+        const uint32_t rb = (uint32_t)d * 2;
+        const int cnt = min(mk_pairs_per_stage(rb), f1 - f0);
+        const int e = __ldcg(&rt->expert[uu]);
+        const size_t eo = (size_t)e * F * d + (size_t)f0 * d;
+        seg[0].src = (const uint8_t *)(ly->wg + eo);
+        seg[1].src = (const uint8_t *)(ly->wu + eo);
+        seg[0].off = 0;
+        seg[1].off = cnt * rb;
+        seg[0].bytes = seg[1].bytes = cnt * rb;
+        nseg = 2;
+        total = 2 * cnt * rb;
+        v += cnt;
+        return IT_STAGE;
+      }
+      case OP_OUT: {
+        while (true) {
+          if (row_stage(seg, nseg, total)) return IT_STAGE;
+          if (u == -1) {
+            const int rs = routing(block, cx);
+            if (rs != IT_STAGE) return rs;
+            rt = p->routing + layer;
+            U = __ldcg(&rt->U);
+          }
+          ++u;
+          if (u >= U) return IT_END;
+          const int e = __ldcg(&rt->expert[u]);
+          rows_from(ly->wd + ((size_t)e * p->d + t[2]) * p->F, t[3], p->F);
+        }
+      }
+      default:
+        return IT_FAIL;
+    }
+  }
+
+  /* The next stage of the stream. */
+  __device__ int next(Seg *seg, int &nseg, uint32_t &total, bool block, const Ctx &cx) {
+    while (true) {
+      if (at_end()) return IT_END;
+      if (!started) {
+        const int rs = begin(block, cx);
+        if (rs != IT_STAGE) return rs;
+        started = true;
+      }
+      const int rs = emit(seg, nseg, total, block, cx);
+      if (rs == IT_STAGE) {
+        ++count;
+        return IT_STAGE;
+      }
+      if (rs != IT_END) return rs;
+      next_task();
+    }
+  }
+};
 
 struct Producer {
   Ctx cx;
-  int i; /* stages issued */
   uint64_t policy;
-  int lane;
   int last_in_slot[MK_MAX_STAGES];
 
-  __device__ bool acquire_slot(uint8_t *&dst, uint64_t *&bar) {
-    const int slot = i % cx.nstages;
-    if (i >= cx.nstages) {
-      const uint32_t parity = (uint32_t)(((i / cx.nstages) - 1) & 1);
-      bool ok = true;
-      if (lane == 0) ok = wait_mbar(cx, &cx.m->empty[slot], parity, -1, -1, -1);
-      if (!__shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0)) return false;
-    }
-    dst = cx.ring + (size_t)slot * MK_STAGE_BYTES;
-    bar = &cx.m->full[slot];
-    return true;
-  }
-
-  /* One stage of nseg segments; lane k issues segment k (nseg <= 32). */
-  __device__ bool issue(int nseg, const uint8_t *const *src, const uint32_t *off,
-                        const uint32_t *bytes, uint32_t total) {
-    uint8_t *dst;
-    uint64_t *bar;
-    if (!acquire_slot(dst, bar)) return false;
-    if (lane == 0) mbar_expect_tx(bar, total);
-    __syncwarp();
-    if (lane < nseg) bulk_g2s(dst + off[lane], src[lane], bytes[lane], bar, policy);
-    last_in_slot[i % cx.nstages] = i;
-    ++i;
-    return true;
-  }
-
-  __device__ bool rows(const uint16_t *src, int nrows, int K) {
-    const uint32_t rb = (uint32_t)K * 2;
-    const int rps = mk_rows_per_stage(rb);
-    for (int r = 0; r < nrows; r += rps) {
-      const int cnt = min(rps, nrows - r);
-      const uint8_t *s = (const uint8_t *)(src + (size_t)r * K);
-      uint32_t off = 0, by = cnt * rb;
-      if (!issue(1, &s, &off, &by, by)) return false;
-    }
-    return true;
-  }
-
-  /* Gate and up rows [f0, f1) of one expert: cnt gate rows then cnt up rows. */
-  __device__ bool up_rows(const uint16_t *wg, const uint16_t *wu, int f0, int f1, int d) {
-    const uint32_t rb = (uint32_t)d * 2;
-    const int rps = mk_pairs_per_stage(rb);
-    for (int f = f0; f < f1; f += rps) {
-      const int cnt = min(rps, f1 - f);
-      const uint8_t *s[2] = {(const uint8_t *)(wg + (size_t)f * d),
-                             (const uint8_t *)(wu + (size_t)f * d)};
-      uint32_t off[2] = {0, cnt * rb}, by[2] = {cnt * rb, cnt * rb};
-      if (!issue(2, s, off, by, 2 * cnt * rb)) return false;
-    }
-    return true;
-  }
-
-  /* K and V blocks of logical pages [p0, p1) of sequence b, kv head kvh:
-   * page j of a stage brings K at 2j * pb and V at (2j + 1) * pb. */
-  __device__ bool pages(const mk_layer_dev &ly, int b, int kvh, int p0, int p1) {
-    const mk_kparams &p = *cx.p;
-    const uint32_t pb = (uint32_t)p.P * p.D * 2;
-    const int pps = mk_pages_per_stage(pb);
-    for (int q = p0; q < p1; q += pps) {
-      const int cnt = min(pps, p1 - q);
-      const uint8_t *s[16];
-      uint32_t off[16], by[16];
-      for (int j = 0; j < cnt; ++j) {
-        const int page = __ldg(p.page_table + b * p.max_pages + q + j);
-        const size_t blk = ((size_t)page * p.Hkv + kvh) * p.P * p.D;
-        s[2 * j] = (const uint8_t *)(ly.kc + blk);
-        s[2 * j + 1] = (const uint8_t *)(ly.vc + blk);
-        off[2 * j] = 2 * j * pb;
-        off[2 * j + 1] = (2 * j + 1) * pb;
-        by[2 * j] = by[2 * j + 1] = pb;
-      }
-      if (!issue(2 * cnt, s, off, by, 2 * cnt * pb)) return false;
-    }
-    return true;
-  }
-
-  __device__ bool routed_wait(int layer) {
-    bool ok = true;
-    if (lane == 0)
-      ok = wait_counter(cx, lctr(*cx.p, layer, CTR_ROUTED), (int)(cx.epoch + 1), -1, OP_UP, layer,
-                        CTR_ROUTED);
-    return __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
-  }
-
-  __device__ bool task(const int32_t *t, int layer) {
-    const mk_kparams &p = *cx.p;
-    switch (t[0]) {
-      case OP_QKV: {
-        const mk_layer_dev &ly = p.layers[layer];
-        const uint16_t *w = t[1] == 0 ? ly.wq : t[1] == 1 ? ly.wk : ly.wv;
-        return rows(w + (size_t)t[2] * p.d, t[3], p.d);
-      }
-      case OP_ROUTER:
-        return rows(p.layers[layer].wr + (size_t)t[2] * p.d, t[3], p.d);
-      case OP_ATTN: {
-        const int b = t[1];
-        const int p1 = t[4] >= 0 ? t[4] : (__ldg(p.seq_lens + b) + p.P - 1) / p.P;
-        return pages(p.layers[layer], b, t[2], t[3], p1);
-      }
-      case OP_UP: {
-        if (!routed_wait(layer)) return false;
-        const mk_routing *rt = p.routing + layer;
-        const int U = __ldcg(&rt->U);
-        const mk_layer_dev &ly = p.layers[layer];
-        const int64_t T = (int64_t)U * p.F;
-        int64_t v = T * t[1] / t[2];
-        const int64_t v1 = T * (t[1] + 1) / t[2];
-        while (v < v1) {
-          const int u = (int)(v / p.F), f0 = (int)(v % p.F);
-          const int f1 = (int)min((int64_t)p.F, f0 + (v1 - v));
-          const int e = __ldcg(&rt->expert[u]);
-          const size_t eo = (size_t)e * p.F * p.d;
-          if (!up_rows(ly.wg + eo, ly.wu + eo, f0, f1, p.d)) return false;
-          v += f1 - f0;
-        }
-        return true;
-      }
-      case OP_OUT: {
-        const mk_layer_dev &ly = p.layers[layer];
-        const int HqD = p.Hq * p.D;
-        if (!rows(ly.wo + (size_t)t[2] * HqD, t[3], HqD)) return false;
-        if (!routed_wait(layer)) return false;
-        const mk_routing *rt = p.routing + layer;
-        const int U = __ldcg(&rt->U);
-        for (int u = 0; u < U; ++u) {
-          const int e = __ldcg(&rt->expert[u]);
-          if (!rows(ly.wd + ((size_t)e * p.d + t[2]) * p.F, t[3], p.F)) return false;
-        }
-        return true;
-      }
-      case OP_LM:
-        return rows(p.lm_head + (size_t)t[2] * p.d, t[3], p.d);
-      default:
-        return false; /* the consumers report the bad opcode */
-    }
-  }
-
   __device__ void run(const int32_t *row) {
-    i = 0;
     for (int s = 0; s < MK_MAX_STAGES; ++s) last_in_slot[s] = -1;
-    const int nl = row[1], nf = row[2];
-    const mk_kparams &p = *cx.p;
-    bool ok = true;
-    for (int l = 0; l < p.L && ok; ++l)
-      for (int k = 0; k < nl && ok; ++k) ok = task(row + MK_DESC_INTS * (1 + k), l);
-    for (int k = 0; k < nf && ok; ++k) ok = task(row + MK_DESC_INTS * (1 + nl + k), p.L - 1);
+    StageIter ld, pf;
+    ld.init(cx.p, row, cx.epoch);
+    pf.init(cx.p, row, cx.epoch);
+    bool pf_end = false;
+    Seg seg[16];
+    int nseg;
+    uint32_t total;
+    while (true) {
+      /* run the prefetch cursor ahead of the load cursor */
+      while (!pf_end && pf.count < ld.count + MK_PREFETCH_STAGES) {
+        const int rs = pf.next(seg, nseg, total, false, cx);
+        if (rs == IT_STAGE) {
+          if (pf.count > ld.count)
+            for (int j = 0; j < nseg; ++j) prefetch_l2(seg[j].src, seg[j].bytes);
+        } else {
+          if (rs != IT_BLOCKED) pf_end = true;
+          break;
+        }
+      }
+      const int rs = ld.next(seg, nseg, total, true, cx);
+      if (rs != IT_STAGE) break; /* end, or a failed wait (already reported) */
+      const long i = ld.count - 1;
+      const int slot = (int)(i % cx.nstages);
+      if (i >= cx.nstages) {
+        const uint32_t parity = (uint32_t)(((i / cx.nstages) - 1) & 1);
+        if (!wait_mbar(cx, &cx.m->empty[slot], parity, -1, -1, -1)) break;
+      }
+      uint8_t *dst = cx.ring + (size_t)slot * MK_STAGE_BYTES;
+      uint64_t *bar = &cx.m->full[slot];
+      mbar_expect_tx(bar, total);
+      for (int j = 0; j < nseg; ++j) bulk_g2s(dst + seg[j].off, seg[j].src, seg[j].bytes, bar, policy);
+      last_in_slot[slot] = (int)i;
+    }
     /* Every copy issued must land before the CTA exits (normally the
      * consumers have waited for all of them already). */
-    if (lane == 0)
-      for (int s = 0; s < cx.nstages; ++s) {
-        const int k = last_in_slot[s];
-        if (k < 0) continue;
-        const uint32_t parity = (uint32_t)((k / cx.nstages) & 1);
-        const uint64_t t0 = gtimer();
-        while (!mbar_test(&cx.m->full[s], parity) && gtimer() - t0 < p.wait_limit_ns) {
-        }
+    for (int s = 0; s < cx.nstages; ++s) {
+      const int k = last_in_slot[s];
+      if (k < 0) continue;
+      const uint32_t parity = (uint32_t)((k / cx.nstages) & 1);
+      const uint64_t t0 = gtimer();
+      while (!mbar_test(&cx.m->full[s], parity) && gtimer() - t0 < cx.p->wait_limit_ns) {
       }
-    __syncwarp();
+    }
   }
 };
 
 /* ============================================================== consumers
- * Eight warps.  Every decision that can end a task early (a counter wait, a
- * stage wait) is taken by thread 0 and broadcast through a named barrier, so
- * all consumer threads always leave at the same point and no barrier can be
- * left half-arrived. */
+ * Eight warps.  Each warp waits for, reads and releases every ring stage on
+ * its own (lane 0 polls the stage's mbarrier, the warp follows), so warps
+ * work on different stages at the same time and no CTA-wide barrier sits on
+ * the streaming path.  Rows are owned by warps by their index within the
+ * task, so every output element has one writer.  A failed wait (time limit
+ * or abort) marks the warp; the consumers decide together at the next
+ * collective point (a barrier with an OR reduction), so all consumer threads
+ * always leave at the same point and no barrier is ever left half-arrived. */
+
+/* Consumer-wide barrier returning the OR of every thread's predicate. */
+__device__ __forceinline__ bool bar_any(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "n"(NCT)
+      : "memory");
+  return r != 0;
+}
+
+/* acc[r][b] += w_r . x[b] over K elements for R rows sharing the x loads;
+ * two accumulators per (row, token) keep the FMA chains short. */
+template <int NB, int R>
+__device__ __forceinline__ void dot_rows(const uint16_t *const (&w)[R], const uint16_t *x,
+                                         int xstride, int K, int lane, float (&acc)[R][NB]) {
+  float a2[R][NB][2];
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int b = 0; b < NB; ++b) a2[r][b][0] = a2[r][b][1] = 0.0f;
+  for (int c = lane * 8; c < K; c += 256) {
+    uint4 wv[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) wv[r] = *(const uint4 *)(w[r] + c);
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      float xf[8];
+      unpack8(*(const uint4 *)(x + b * xstride + c), xf);
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        float wf[8];
+        unpack8(wv[r], wf);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a2[r][b][i & 1] = fmaf(wf[i], xf[i], a2[r][b][i & 1]);
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int b = 0; b < NB; ++b) acc[r][b] = a2[r][b][0] + a2[r][b][1];
+}
+
+__device__ __forceinline__ unsigned long long pack2(uint32_t lo, uint32_t hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+
+__device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+__device__ __forceinline__ float sum2(unsigned long long v) {
+  uint32_t lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(v));
+  return __uint_as_float(lo) + __uint_as_float(hi);
+}
+
+/* Single-token rows against an fp32 activation (the batch-1 path): the bf16
+ * weight pairs become fp32 pairs with one shift and one mask, and packed
+ * f32x2 FMAs (two exact fp32 FMAs each) do the products. */
+template <int NB, int R>
+__device__ __forceinline__ void dot_rows(const uint16_t *const (&w)[R], const float *x, int xstride,
+                                         int K, int lane, float (&acc)[R][NB]) {
+  static_assert(NB == 1, "fp32 activations are the batch-1 path");
+  unsigned long long a2[R][2];
+#pragma unroll
+  for (int r = 0; r < R; ++r) a2[r][0] = a2[r][1] = 0ULL;
+  for (int c = lane * 8; c < K; c += 256) {
+    const uint4 xa = *(const uint4 *)(x + c), xb = *(const uint4 *)(x + c + 4);
+    const unsigned long long xp[4] = {pack2(xa.x, xa.y), pack2(xa.z, xa.w), pack2(xb.x, xb.y),
+                                      pack2(xb.z, xb.w)};
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const uint4 wv = *(const uint4 *)(w[r] + c);
+      const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        a2[r][j & 1] = ffma2(pack2(ww[j] << 16, ww[j] & 0xFFFF0000u), xp[j], a2[r][j & 1]);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r) acc[r][0] = sum2(a2[r][0]) + sum2(a2[r][1]);
+}
+
+/* activation element type: fp32 for one token, bf16 bits otherwise */
+template <class XT>
+__device__ __forceinline__ XT to_x(uint16_t bits);
+template <>
+__device__ __forceinline__ float to_x<float>(uint16_t bits) {
+  return bf2f(bits);
+}
+template <>
+__device__ __forceinline__ uint16_t to_x<uint16_t>(uint16_t bits) {
+  return bits;
+}
 
 template <int NB>
 struct Consumer {
+  using XT = typename std::conditional<NB == 1, float, uint16_t>::type;
   Ctx cx;
   int warp, lane, tid;
-  int si;   /* stages consumed */
-  int dseq; /* collective decisions taken */
+  int si;     /* stages consumed (the same sequence in every warp) */
+  bool wfail; /* this warp failed a stage wait */
+  unsigned long long *tr; /* this CTA's trace events, or NULL */
+  int tr_n;
+  uint64_t t_ready, t_stage, t_swait, t_mark;
+  int n_stages;
 
-  /* Thread 0's verdict (ok) becomes everyone's. */
-  __device__ bool decide(bool ok) {
-    const int slot = dseq & 1;
-    ++dseq;
-    if (tid == 0) cx.m->dec[slot] = ok ? 0 : 1;
-    bar_consumers();
-    return *(volatile int32_t *)&cx.m->dec[slot] == 0;
-  }
+  static constexpr int ROWS = NB <= 2 ? 2 : 1; /* rows per dot pass */
 
+  /* Thread 0 waits on a counter; every consumer learns whether the CTA goes
+   * on (false also when any warp has failed a stage wait). */
   __device__ bool cwait(int32_t *c, int target, int task, int op, int layer, int kind) {
-    bool ok = true;
-    if (tid == 0) ok = wait_counter(cx, c, target, task, op, layer, kind);
-    return decide(ok);
+    bool fail = wfail;
+    if (tid == 0) {
+      fail |= !wait_counter(cx, c, target, task, op, layer, kind);
+      if (tr && !t_ready) t_ready = gtimer();
+    }
+    return !bar_any(fail);
   }
 
-  __device__ bool stage_begin(uint8_t *&st, int task, int op, int layer) {
+  /* End of a task's streaming part: a consumer barrier, false if any warp
+   * failed. */
+  __device__ bool task_end() { return !bar_any(wfail); }
+
+  __device__ bool stage_wait(uint8_t *&st, int task, int op, int layer) {
+    if (wfail) return false;
     const int slot = si % cx.nstages;
     const uint32_t parity = (uint32_t)((si / cx.nstages) & 1);
-    bool ok = true;
-    if (tid == 0) ok = wait_mbar(cx, &cx.m->full[slot], parity, task, op, layer);
-    if (!decide(ok)) return false;
-    mbar_test(&cx.m->full[slot], parity); /* completed: gives this thread acquire order */
+    int ok = 1;
+    if (lane == 0) {
+      const bool trace = tr && warp == 0;
+      const uint64_t w0 = trace ? gtimer() : 0;
+      ok = wait_mbar(cx, &cx.m->full[slot], parity, task, op, layer) ? 1 : 0;
+      if (trace) {
+        const uint64_t w1 = gtimer();
+        if (!t_stage) t_stage = w1;
+        else t_swait += w1 - w0;
+        ++n_stages;
+      }
+    }
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    if (!ok) {
+      wfail = true;
+      return false;
+    }
+    mbar_test(&cx.m->full[slot], parity); /* completed: acquire order for this thread */
     st = cx.ring + (size_t)slot * MK_STAGE_BYTES;
     return true;
   }
 
-  __device__ void stage_end() {
+  __device__ void stage_release() {
     __syncwarp();
     if (lane == 0) mbar_arrive(&cx.m->empty[si % cx.nstages]);
     ++si;
@@ -563,31 +816,46 @@ struct Consumer {
     bar_consumers();
   }
 
-  /* xbuf[b][0..d) = bf16((h * (1/sqrtf(mean_fp32(h^2) + eps))) * g); rows b >= B zero. */
+  /* xbuf[b][0..d) = bf16((h * (1/sqrtf(mean_fp32(h^2) + eps))) * g) as XT;
+   * rows b >= B zero.  h is read once with 16-byte loads and staged behind
+   * the output in xbuf. */
   __device__ void norm_into_xbuf(int layer_tag, const uint16_t *const *hrows, const uint16_t *g) {
     const mk_kparams &p = *cx.p;
-    uint16_t *x = (uint16_t *)cx.xbuf;
+    XT *x = (XT *)cx.xbuf;
+    uint16_t *raw = (uint16_t *)(cx.xbuf + (size_t)NB * p.d * sizeof(XT));
+    const int n8 = p.d / 8;
     float ss[NB];
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
       ss[b] = 0.0f;
       if (b < p.B)
-        for (int i = tid; i < p.d; i += NCT) {
-          const float v = bf2f(__ldcg(hrows[b] + i));
-          ss[b] = fmaf(v, v, ss[b]);
+        for (int i = tid; i < n8; i += NCT) {
+          const uint4 v = __ldcg((const uint4 *)hrows[b] + i);
+          *(uint4 *)(raw + (size_t)b * p.d + 8 * i) = v;
+          float f[8];
+          unpack8(v, f);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) ss[b] = fmaf(f[k], f[k], ss[b]);
         }
     }
     block_sum(ss);
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
       const float r = 1.0f / sqrtf(ss[b] / (float)p.d + p.eps);
-      for (int i = tid; i < p.d; i += NCT) {
-        uint16_t o = 0;
+      for (int i = tid; i < n8; i += NCT) {
+        XT o[8];
         if (b < p.B) {
-          const float hv = bf2f(__ldcg(hrows[b] + i));
-          o = f2bf(__fmul_rn(__fmul_rn(hv, r), bf2f(__ldg(g + i))));
+          float hf[8], gf[8];
+          unpack8(*(const uint4 *)(raw + (size_t)b * p.d + 8 * i), hf);
+          unpack8(__ldg((const uint4 *)g + i), gf);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) o[k] = to_x<XT>(f2bf(__fmul_rn(__fmul_rn(hf[k], r), gf[k])));
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) o[k] = to_x<XT>(0);
         }
-        x[b * p.d + i] = o;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x[(size_t)b * p.d + 8 * i + k] = o[k];
       }
     }
     if (tid == 0) cx.m->norm_layer = layer_tag;
@@ -596,6 +864,12 @@ struct Consumer {
 
   __device__ void ensure_norm(int layer) {
     if (*(volatile int32_t *)&cx.m->norm_layer == layer) return;
+    struct Mark {
+      Consumer *c;
+      __device__ ~Mark() {
+        if (c->tr && c->tid == 0) c->t_mark = gtimer();
+      }
+    } mark{this};
     bar_consumers(); /* everyone has read the tag before it can change */
     const uint16_t *hr[NB];
 #pragma unroll
@@ -608,87 +882,72 @@ struct Consumer {
     if (tid == 0) cx.m->norm_layer = -2;
   }
 
+  /* After task_end(): thread 0 releases the downstream counter. */
   __device__ void signal(int32_t *c) {
-    bar_consumers();
     if (tid == 0) {
       __threadfence();
       red_release_add(c, 1);
     }
   }
 
-  /* Adds one to the ticket counter; true (for every consumer) if this task
-   * took the last ticket of the step. */
+  /* After task_end(): one increment of the ticket counter; true (for every
+   * consumer) if this task took the last ticket of the step. */
   __device__ bool ticket(int32_t *c, int per_step) {
-    bar_consumers();
     bool last = false;
     if (tid == 0) {
       __threadfence();
       const int old = atom_add_acq_rel(c, 1);
       last = old == (int)((cx.epoch + 1) * (uint32_t)per_step) - 1;
     }
-    return !decide(!last);
+    return bar_any(last);
   }
 
-  /* ---- GEMV of one stage: rows [0, cnt) of K elements at w.  S warps share
-   * a row (S = largest power of two with S * cnt <= 8); each writes the
-   * partial sum of its K segment to part[(row * S + seg) * NB + b]. */
-  static __device__ __forceinline__ int segs(int cnt) {
-    int S = 1;
-    while (S * 2 * cnt <= NC) S *= 2;
-    return S;
-  }
-
-  __device__ void partials(const uint16_t *w, int cnt, int K, const uint16_t *x, int xstride,
-                           float *part) {
-    const int S = segs(cnt);
-    const int seg = warp % S, kseg = K / S, k0 = seg * kseg;
-    for (int row = warp / S; row < cnt; row += NC / S) {
-      float acc[NB];
+  /* Reduce R rows' NB sums across the warp and hand them to epi(row, b, v)
+   * on the lane that owns token b. */
+  template <int R, class Epi>
+  __device__ __forceinline__ void finish_rows(float (&acc)[R][NB], const int (&rows)[R], Epi &epi) {
 #pragma unroll
-      for (int b = 0; b < NB; ++b) acc[b] = 0.0f;
-      dot_row<NB>(w + (size_t)row * K + k0, x + k0, xstride, kseg, lane, acc);
-      const float s = transpose_reduce<NB>(acc, lane);
-      if (reduce_leader<NB>(lane)) part[(row * S + seg) * NB + reduce_token<NB>(lane)] = s;
+    for (int r = 0; r < R; ++r) {
+      const float s = transpose_reduce<NB>(acc[r], lane);
+      if (reduce_leader<NB>(lane)) epi(rows[r], reduce_token<NB>(lane), s);
     }
   }
 
-  __device__ __forceinline__ float psum(const float *part, int row, int b, int S) const {
-    float s = 0.0f;
-    for (int g = 0; g < S; ++g) s += part[(row * S + g) * NB + b];
-    return s;
-  }
-
-  /* nrows streamed rows of K: epi(row, b, value) for every row and b < NB,
-   * run by one consumer thread per (row, b). */
+  /* nrows streamed rows of K elements; row r (index within the task) is
+   * computed by warp r % 8 and handed to epi(r, b, value). */
   template <class Epi>
-  __device__ bool gemv_task(int nrows, int K, const uint16_t *x, int xstride, int task, int op,
+  __device__ void gemv_task(int nrows, int K, const XT *x, int xstride, int task, int op,
                             int layer, Epi epi) {
     const int rps = mk_rows_per_stage(K * 2);
-    int prev_r0 = -1, prev_cnt = 0, buf = 0;
     for (int r0 = 0; r0 < nrows; r0 += rps) {
       const int cnt = min(rps, nrows - r0);
       uint8_t *st;
-      if (!stage_begin(st, task, op, layer)) return false;
-      if (prev_r0 >= 0) {
-        const float *pp = cx.m->part[buf ^ 1];
-        const int S = segs(prev_cnt);
-        for (int i = tid; i < prev_cnt * NB; i += NCT)
-          epi(prev_r0 + i / NB, i % NB, psum(pp, i / NB, i % NB, S));
+      if (!stage_wait(st, task, op, layer)) return;
+      const uint16_t *w = (const uint16_t *)st;
+      int j = ((warp - r0) % NC + NC) % NC;
+      if (ROWS == 2) {
+        for (; j + NC < cnt; j += 2 * NC) {
+          float acc[ROWS][NB];
+          const uint16_t *wr[ROWS];
+          int rr[ROWS];
+#pragma unroll
+          for (int r = 0; r < ROWS; ++r) {
+            wr[r] = w + (size_t)(j + r * NC) * K;
+            rr[r] = r0 + j + r * NC;
+          }
+          dot_rows<NB, ROWS>(wr, x, xstride, K, lane, acc);
+          finish_rows<ROWS>(acc, rr, epi);
+        }
       }
-      partials((const uint16_t *)st, cnt, K, x, xstride, cx.m->part[buf]);
-      stage_end();
-      prev_r0 = r0;
-      prev_cnt = cnt;
-      buf ^= 1;
+      for (; j < cnt; j += NC) {
+        float acc[1][NB];
+        const uint16_t *wr[1] = {w + (size_t)j * K};
+        const int rr[1] = {r0 + j};
+        dot_rows<NB, 1>(wr, x, xstride, K, lane, acc);
+        finish_rows<1>(acc, rr, epi);
+      }
+      stage_release();
     }
-    if (prev_r0 >= 0) {
-      bar_consumers();
-      const float *pp = cx.m->part[buf ^ 1];
-      const int S = segs(prev_cnt);
-      for (int i = tid; i < prev_cnt * NB; i += NCT)
-        epi(prev_r0 + i / NB, i % NB, psum(pp, i / NB, i % NB, S));
-    }
-    return true;
   }
 
   /* ---------------------------------------------------------------- QKV */
@@ -702,11 +961,11 @@ struct Consumer {
     const int base = (t[1] == 0 ? 0 : t[1] == 1 ? p.Hq * p.D : (p.Hq + p.Hkv) * p.D) + t[2];
     uint16_t *out = p.qkv + (size_t)layer * MK_MAX_BATCH * QKVD;
     const int B = p.B;
-    if (!gemv_task(t[3], p.d, (const uint16_t *)cx.xbuf, p.d, task, OP_QKV, layer,
-                   [&](int r, int b, float v) {
-                     if (b < B) out[(size_t)b * QKVD + base + r] = f2bf(v);
-                   }))
-      return false;
+    gemv_task(t[3], p.d, (const XT *)cx.xbuf, p.d, task, OP_QKV, layer,
+              [&](int r, int b, float v) {
+                if (b < B) out[(size_t)b * QKVD + base + r] = f2bf(v);
+              });
+    if (!task_end()) return false;
     signal(lctr(p, layer, CTR_QKV_DONE));
     return true;
   }
@@ -722,11 +981,11 @@ struct Consumer {
     float *lg = p.router_logits + (size_t)layer * MK_MAX_BATCH * p.E;
     const float *bias = p.layers[layer].bias;
     const int B = p.B, E = p.E;
-    if (!gemv_task(t[3], p.d, (const uint16_t *)cx.xbuf, p.d, task, OP_ROUTER, layer,
-                   [&](int r, int b, float v) {
-                     if (b < B) lg[(size_t)b * E + e0 + r] = bias ? v + __ldg(bias + e0 + r) : v;
-                   }))
-      return false;
+    gemv_task(t[3], p.d, (const XT *)cx.xbuf, p.d, task, OP_ROUTER, layer,
+              [&](int r, int b, float v) {
+                if (b < B) lg[(size_t)b * E + e0 + r] = bias ? v + __ldg(bias + e0 + r) : v;
+              });
+    if (!task_end()) return false;
     if (!ticket(lctr(p, layer, CTR_ROUTER_TICKET), p.n_router)) return true;
     route(layer);
     bar_consumers();
@@ -819,7 +1078,6 @@ struct Consumer {
       atomicAdd(&p.ctrl->sum_experts, (unsigned long long)U);
     }
   }
-
   /* ---------------------------------------------------------- attention
    * Split-K flash decoding over the pages of one (sequence, kv head).  Lane
    * l owns head dims [l*DPL, (l+1)*DPL) of all 8 head slots; the 8 partial
@@ -893,18 +1151,22 @@ struct Consumer {
     const float scale = p.attn_scale;
     auto &A = cx.m->u.at;
 
-    /* nt <= 8 keys (rows in shared memory, or fp32 vectors), all valid */
-    auto block = [&](const uint16_t *const *krow, const uint16_t *const *vrow, const float *kf,
-                     const float *vf, int nt) {
+    const uint16_t *kr[8], *vr[8];
+    /* nt <= 8 keys, all valid: rows kr/vr in shared memory, or (newkey) the
+     * new token's fp32 k and v vectors */
+    auto block = [&](int nt, bool newkey) {
       float s_t[8];
 #pragma unroll
       for (int tt = 0; tt < 8; ++tt) {
         s_t[tt] = -INFINITY;
         if (tt < nt) {
           float kv[4];
+          if (newkey) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            kv[i] = i < DPL ? (kf ? kf[lane * DPL + i] : bf2f(krow[tt][lane * DPL + i])) : 0.0f;
+            for (int i = 0; i < 4; ++i) kv[i] = i < DPL ? ks[lane * DPL + i] : 0.0f;
+          } else {
+            lane_dims(kr[tt], lane, DPL, kv);
+          }
           float part[8];
 #pragma unroll
           for (int g = 0; g < 8; ++g) {
@@ -935,22 +1197,32 @@ struct Consumer {
         A.alpha[warp][hg] = alpha;
       }
       __syncwarp();
+      {
+        const float4 a0 = *(const float4 *)&A.alpha[warp][0];
+        const float4 a1 = *(const float4 *)&A.alpha[warp][4];
+        const float al[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
-      for (int g = 0; g < 8; ++g) {
-        const float a = A.alpha[warp][g];
+        for (int g = 0; g < 8; ++g)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) orr[g][i] *= a;
+          for (int i = 0; i < 4; ++i) orr[g][i] *= al[g];
       }
-      for (int tt = 0; tt < nt; ++tt) {
-        float vv[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          vv[i] = i < DPL ? (vf ? vf[lane * DPL + i] : bf2f(vrow[tt][lane * DPL + i])) : 0.0f;
+      for (int tt = 0; tt < 8; ++tt) {
+        if (tt < nt) {
+          float vv[4];
+          if (newkey) {
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const float pg = A.pw[warp][tt][g];
+            for (int i = 0; i < 4; ++i) vv[i] = i < DPL ? vs[lane * DPL + i] : 0.0f;
+          } else {
+            lane_dims(vr[tt], lane, DPL, vv);
+          }
+          const float4 p0v = *(const float4 *)&A.pw[warp][tt][0];
+          const float4 p1v = *(const float4 *)&A.pw[warp][tt][4];
+          const float pg[8] = {p0v.x, p0v.y, p0v.z, p0v.w, p1v.x, p1v.y, p1v.z, p1v.w};
 #pragma unroll
-          for (int i = 0; i < 4; ++i) orr[g][i] = fmaf(pg, vv[i], orr[g][i]);
+          for (int g = 0; g < 8; ++g)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) orr[g][i] = fmaf(pg[g], vv[i], orr[g][i]);
         }
       }
       __syncwarp();
@@ -961,10 +1233,9 @@ struct Consumer {
     for (int q0 = p0; q0 < p1; q0 += pps) {
       const int cnt = min(pps, p1 - q0);
       uint8_t *st;
-      if (!stage_begin(st, task, OP_ATTN, layer)) return false;
+      if (!stage_wait(st, task, OP_ATTN, layer)) break;
       const int nkeys = cnt * P;
       const int valid_end = L_now - q0 * P;
-      const uint16_t *kr[8], *vr[8];
       int nt = 0;
       for (int kk = warp; kk < nkeys; kk += NC) {
         if (kk < valid_end) {
@@ -974,14 +1245,15 @@ struct Consumer {
           ++nt;
         }
         if (nt == 8) {
-          block(kr, vr, nullptr, nullptr, 8);
+          block(8, false);
           nt = 0;
         }
       }
-      if (nt > 0) block(kr, vr, nullptr, nullptr, nt);
-      stage_end();
+      if (nt > 0) block(nt, false);
+      stage_release();
     }
-    if (last && warp == 0) block(nullptr, nullptr, ks, vs, 1);
+    if (tr && tid == 0) t_mark = gtimer();
+    if (last && warp == 0) block(1, true);
 
     /* merge warp states pairwise: 8 -> 4 -> 2 -> 1 */
     for (int hw = NC / 2; hw >= 1; hw >>= 1) {
@@ -1020,46 +1292,96 @@ struct Consumer {
         m_run = M;
       }
     }
-    /* warp 0 holds this split's partial */
-    float *part = p.attn_part + ((size_t)layer * p.n_slots + t[5]) * G * (D + 2);
+    /* warp 0 holds this split's partial: per head [m, l, -, -, o[D]] */
+    const int PS = D + 4;
+    float *part = p.attn_part + ((size_t)layer * p.n_slots + t[5]) * G * PS;
     if (warp == 0) {
 #pragma unroll
       for (int g = 0; g < 8; ++g)
         if (g < G) {
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            if (i < DPL) part[(size_t)g * (D + 2) + 2 + lane * DPL + i] = orr[g][i];
+            if (i < DPL) part[(size_t)g * PS + 4 + lane * DPL + i] = orr[g][i];
         }
       if ((lane & 3) == 0 && hg < G) {
-        part[(size_t)hg * (D + 2)] = m_run;
-        part[(size_t)hg * (D + 2) + 1] = l_run;
+        part[(size_t)hg * PS] = m_run;
+        part[(size_t)hg * PS + 1] = l_run;
       }
     }
-    /* the last split of (b, kvh) to finish merges all splits */
+    /* the last split of (b, kvh) to finish merges all splits:
+     * o = sum_s f_s o_s with f_s = e^{m_s - M} / sum_s' e^{m_s' - M} l_s' */
+    if (!task_end()) return false;
     if (!ticket(lctr(p, layer, CTR_ATTN_TICKET0 + b * p.Hkv + kvh), t[7])) return true;
-    const float *parts = p.attn_part + ((size_t)layer * p.n_slots + t[6]) * G * (D + 2);
+    const float *parts = p.attn_part + ((size_t)layer * p.n_slots + t[6]) * G * PS;
     uint16_t *o = p.o + ((size_t)layer * MK_MAX_BATCH + b) * p.Hq * D + (size_t)kvh * G * D;
     const int ns = t[7];
-    for (int i = tid; i < G * D; i += NCT) {
-      const int g = i / D, j = i % D;
-      float M = -INFINITY;
-      for (int s = 0; s < ns; ++s) M = fmaxf(M, __ldcg(parts + ((size_t)s * G + g) * (D + 2)));
-      float num = 0.0f, den = 0.0f;
-      for (int s = 0; s < ns; ++s) {
-        const float *ps = parts + ((size_t)s * G + g) * (D + 2);
-        const float ms = __ldcg(ps);
-        if (ms == -INFINITY) continue;
-        const float f = expf(ms - M);
-        num = fmaf(f, __ldcg(ps + 2 + j), num);
-        den = fmaf(f, __ldcg(ps + 1), den);
-      }
-      o[(size_t)g * D + j] = f2bf(num / den);
+    float *fm = (float *)cx.xbuf;          /* [ns][G] m, then factors */
+    float *fl = fm + ns * G;               /* [ns][G] l */
+    float *hd = fl + ns * G;               /* [G] max, [G] 1 / denominator */
+    for (int i = tid; i < ns * G; i += NCT) {
+      fm[i] = __ldcg(parts + (size_t)i * PS);
+      fl[i] = __ldcg(parts + (size_t)i * PS + 1);
     }
+    bar_consumers();
+    if (tid < G) {
+      float M = -INFINITY;
+      for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, fm[s2 * G + tid]);
+      float den = 0.0f;
+      for (int s2 = 0; s2 < ns; ++s2) {
+        const float ms = fm[s2 * G + tid];
+        if (ms != -INFINITY) den = fmaf(expf(ms - M), fl[s2 * G + tid], den);
+      }
+      hd[tid] = M;
+      hd[G + tid] = 1.0f / den;
+    }
+    bar_consumers();
+    for (int i = tid; i < ns * G; i += NCT) {
+      const int g = i % G;
+      const float ms = fm[i];
+      fm[i] = ms == -INFINITY ? 0.0f : expf(ms - hd[g]) * hd[G + g];
+    }
+    bar_consumers();
+    const int D4 = D / 4;
+    for (int i = tid; i < G * D4; i += NCT) {
+      const int g = i / D4, j4 = i % D4;
+      float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      const float4 *src = (const float4 *)(parts + (size_t)g * PS + 4) + j4;
+      int s2 = 0;
+      for (; s2 + 8 <= ns; s2 += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = __ldcg(src + (size_t)(s2 + u) * G * PS / 4);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float f = fm[(s2 + u) * G + g];
+          acc.x = fmaf(f, v[u].x, acc.x);
+          acc.y = fmaf(f, v[u].y, acc.y);
+          acc.z = fmaf(f, v[u].z, acc.z);
+          acc.w = fmaf(f, v[u].w, acc.w);
+        }
+      }
+      for (; s2 < ns; ++s2) {
+        const float4 v = __ldcg(src + (size_t)s2 * G * PS / 4);
+        const float f = fm[s2 * G + g];
+        acc.x = fmaf(f, v.x, acc.x);
+        acc.y = fmaf(f, v.y, acc.y);
+        acc.z = fmaf(f, v.z, acc.z);
+        acc.w = fmaf(f, v.w, acc.w);
+      }
+      uint16_t *dst = o + (size_t)g * D + j4 * 4;
+      dst[0] = f2bf(acc.x);
+      dst[1] = f2bf(acc.y);
+      dst[2] = f2bf(acc.z);
+      dst[3] = f2bf(acc.w);
+    }
+    bar_consumers();
     signal(lctr(p, layer, CTR_ATTN_DONE));
     return true;
   }
 
-  /* ------------------------------------------------------ expert gate/up */
+  /* ------------------------------------------------------ expert gate/up
+   * Row pair j of the share (one gate row, one up row of the same expert
+   * and f) is computed by warp j % 8. */
   __device__ bool op_up(const int32_t *t, int task, int layer) {
     const mk_kparams &p = *cx.p;
     if (!cwait(lctr(p, layer, CTR_ROUTED), (int)(cx.epoch + 1), task, OP_UP, layer, CTR_ROUTED))
@@ -1071,43 +1393,37 @@ struct Consumer {
     const int64_t T = (int64_t)U * F;
     int64_t v = T * t[1] / t[2];
     const int64_t v1 = T * (t[1] + 1) / t[2];
-    const uint16_t *x = (const uint16_t *)cx.xbuf;
+    const XT *x = (const XT *)cx.xbuf;
     const int rps = mk_pairs_per_stage(2 * d);
-    int buf = 0, prev_cnt = 0;
-    uint16_t *prev_out = nullptr;
-    auto epi = [&](uint16_t *out, int cnt) {
-      const float *pp = cx.m->part[buf ^ 1];
-      const int S = segs(2 * cnt);
-      for (int i = tid; i < cnt * NB; i += NCT) {
-        const int j = i / NB, bb = i % NB;
-        if (bb < B) {
-          const float gb = rbf(psum(pp, j, bb, S)), ub = rbf(psum(pp, cnt + j, bb, S));
-          const float silu = gb / (1.0f + expf(-gb));
-          out[(size_t)bb * F + j] = f2bf(silu * ub);
-        }
-      }
-    };
-    while (v < v1) {
+    int pair0 = 0; /* pairs of this share before the current stage */
+    while (v < v1 && !wfail) {
       const int u = (int)(v / F), f0 = (int)(v % F);
       const int f1 = (int)min((int64_t)F, f0 + (v1 - v));
       uint16_t *out = p.act + (((size_t)layer * p.u_max + u) * MK_MAX_BATCH) * F;
       for (int f = f0; f < f1; f += rps) {
         const int cnt = min(rps, f1 - f);
         uint8_t *st;
-        if (!stage_begin(st, task, OP_UP, layer)) return false;
-        if (prev_out) epi(prev_out, prev_cnt);
-        partials((const uint16_t *)st, 2 * cnt, d, x, d, cx.m->part[buf]);
-        stage_end();
-        prev_out = out + f;
-        prev_cnt = cnt;
-        buf ^= 1;
+        if (!stage_wait(st, task, OP_UP, layer)) break;
+        const uint16_t *wg = (const uint16_t *)st, *wu = wg + (size_t)cnt * d;
+        for (int j = ((warp - pair0) % NC + NC) % NC; j < cnt; j += NC) {
+          float acc[2][NB];
+          const uint16_t *wr[2] = {wg + (size_t)j * d, wu + (size_t)j * d};
+          dot_rows<NB, 2>(wr, x, d, d, lane, acc);
+          const float g = transpose_reduce<NB>(acc[0], lane);
+          const float uu = transpose_reduce<NB>(acc[1], lane);
+          const int b = reduce_token<NB>(lane);
+          if (reduce_leader<NB>(lane) && b < B) {
+            const float gb = rbf(g), ub = rbf(uu);
+            const float silu = gb / (1.0f + expf(-gb));
+            out[(size_t)b * F + f + j] = f2bf(silu * ub);
+          }
+        }
+        stage_release();
+        pair0 += cnt;
       }
       v += f1 - f0;
     }
-    if (prev_out) {
-      bar_consumers();
-      epi(prev_out, prev_cnt);
-    }
+    if (!task_end()) return false;
     signal(lctr(p, layer, CTR_UP_DONE));
     return true;
   }
@@ -1121,17 +1437,17 @@ struct Consumer {
     if (!cwait(lctr(p, layer, CTR_ATTN_DONE), target, task, OP_OUT, layer, CTR_ATTN_DONE))
       return false;
     invalidate_norm();
-    uint16_t *x = (uint16_t *)cx.xbuf;
+    XT *x = (XT *)cx.xbuf;
     auto &O = cx.m->u.out;
     for (int i = tid; i < NB * HqD; i += NCT) {
       const int bb = i / HqD;
-      x[i] = bb < B ? __ldcg(p.o + ((size_t)layer * MK_MAX_BATCH + bb) * HqD + (i % HqD)) : 0;
+      x[i] = to_x<XT>(bb < B ? __ldcg(p.o + ((size_t)layer * MK_MAX_BATCH + bb) * HqD + (i % HqD))
+                             : (uint16_t)0);
     }
     for (int i = tid; i < MK_MAX_OUT_ROWS * MK_MAX_BATCH * 2; i += NCT) (&O.acc[0][0][0])[i] = 0.0f;
     bar_consumers();
-    if (!gemv_task(nr, HqD, x, HqD, task, OP_OUT, layer,
-                   [&](int r, int bb, float v) { O.acc[r][bb][0] = v; }))
-      return false;
+    gemv_task(nr, HqD, x, HqD, task, OP_OUT, layer,
+              [&](int r, int bb, float v) { O.acc[r][bb][0] = v; });
     if (!cwait(lctr(p, layer, CTR_UP_DONE), (int)((cx.epoch + 1) * p.n_up), task, OP_OUT, layer,
                CTR_UP_DONE))
       return false;
@@ -1140,18 +1456,31 @@ struct Consumer {
     for (int i = tid; i < U * MK_MAX_BATCH; i += NCT)
       O.slot_w[i / MK_MAX_BATCH][i % MK_MAX_BATCH] =
           __ldcg(&rt->slot_w[i / MK_MAX_BATCH][i % MK_MAX_BATCH]);
+    /* the experts' activations: all slots at once when they fit the buffer,
+     * else two slots at a time */
+    const int per = NB * F;
+    const int fit = (int)min((int64_t)U, (int64_t)cx.p->xbuf_bytes / ((int64_t)sizeof(XT) * per));
+    const bool all = fit >= U;
     for (int u = 0; u < U; ++u) {
-      uint16_t *xa = x + (size_t)(u & 1) * NB * F;
-      const uint16_t *a = p.act + (((size_t)layer * p.u_max + u) * MK_MAX_BATCH) * F;
-      for (int i = tid; i < NB * F; i += NCT) xa[i] = (i / F) < B ? __ldcg(a + i) : 0;
-      bar_consumers();
-      if (!gemv_task(nr, F, xa, F, task, OP_OUT, layer, [&](int r, int bb, float v) {
-            const float sw = O.slot_w[u][bb];
-            if (bb < B && sw != 0.0f) O.acc[r][bb][1] = fmaf(sw, v, O.acc[r][bb][1]);
-          }))
-        return false;
+      const int bufslot = all ? u : (u & 1);
+      XT *xa = x + (size_t)bufslot * per;
+      if (all ? u == 0 : true) {
+        const int n_load = all ? U : 1;
+        for (int k = 0; k < n_load; ++k) {
+          const int uu = all ? k : u;
+          XT *dst = x + (size_t)(all ? k : bufslot) * per;
+          const uint16_t *a = p.act + (((size_t)layer * p.u_max + uu) * MK_MAX_BATCH) * F;
+          for (int i = tid; i < per; i += NCT)
+            dst[i] = to_x<XT>((i / F) < B ? __ldcg(a + i) : (uint16_t)0);
+        }
+        bar_consumers();
+      }
+      gemv_task(nr, F, xa, F, task, OP_OUT, layer, [&](int r, int bb, float v) {
+        const float sw = O.slot_w[u][bb];
+        if (bb < B && sw != 0.0f) O.acc[r][bb][1] = fmaf(sw, v, O.acc[r][bb][1]);
+      });
     }
-    bar_consumers();
+    if (!task_end()) return false;
     for (int i = tid; i < nr * B; i += NCT) {
       const int r = i / B, bb = i % B;
       const uint16_t *hin = h_row(layer, bb);
@@ -1162,6 +1491,7 @@ struct Consumer {
           f2bf(__fadd_rn(__fadd_rn(hv, at), mo));
       if (layer == 0) p.h[(size_t)bb * d + r0 + r] = __ldg(hin + r0 + r);
     }
+    bar_consumers();
     signal(lctr(p, layer, CTR_OUT_DONE));
     return true;
   }
@@ -1186,37 +1516,23 @@ struct Consumer {
     int best_i = 0x7FFFFFFF;
     float *logits = p.out_logits;
     const int V = p.V;
-    /* one thread per (row, b) in each epilogue; NCT is a multiple of NB, so
-     * the token of a thread (tid % NB) never changes and it keeps a best */
-    if (!gemv_task(t[3], p.d, (const uint16_t *)cx.xbuf, p.d, task, OP_LM, L,
-                   [&](int r, int bb, float v) {
-                     if (bb < B) {
-                       if (logits) logits[(size_t)bb * V + v0 + r] = v;
-                       if (v > best_v || (v == best_v && v0 + r < best_i)) {
-                         best_v = v;
-                         best_i = v0 + r;
-                       }
-                     }
-                   }))
-      return false;
+    /* the lane that owns token b in each warp keeps that warp's best */
+    gemv_task(t[3], p.d, (const XT *)cx.xbuf, p.d, task, OP_LM, L,
+              [&](int r, int bb, float v) {
+                if (bb < B) {
+                  if (logits) logits[(size_t)bb * V + v0 + r] = v;
+                  if (v > best_v || (v == best_v && v0 + r < best_i)) {
+                    best_v = v;
+                    best_i = v0 + r;
+                  }
+                }
+              });
     auto &M = cx.m->u.lm;
-    {
-      const int bb = tid % NB;
-#pragma unroll
-      for (int m = 16; m >= NB; m >>= 1) {
-        const float ov = __shfl_xor_sync(0xFFFFFFFFu, best_v, m);
-        const int oi = __shfl_xor_sync(0xFFFFFFFFu, best_i, m);
-        if (ov > best_v || (ov == best_v && oi < best_i)) {
-          best_v = ov;
-          best_i = oi;
-        }
-      }
-      if (lane < NB) {
-        M.best[warp][bb][0] = best_v;
-        M.best[warp][bb][1] = __int_as_float(best_i);
-      }
+    if (reduce_leader<NB>(lane)) {
+      M.best[warp][reduce_token<NB>(lane)][0] = best_v;
+      M.best[warp][reduce_token<NB>(lane)][1] = __int_as_float(best_i);
     }
-    bar_consumers();
+    if (!task_end()) return false;
     if (tid < B) {
       float bv = -INFINITY;
       int bi = 0x7FFFFFFF;
@@ -1231,6 +1547,7 @@ struct Consumer {
       p.lm_part[((size_t)t[4] * MK_MAX_BATCH + tid) * 2] = bv;
       p.lm_part[((size_t)t[4] * MK_MAX_BATCH + tid) * 2 + 1] = __int_as_float(bi);
     }
+    bar_consumers();
     if (!ticket(gctr(p, GCTR_LM_TICKET), p.n_lm)) return true;
     if (tid < B) {
       float bv = -INFINITY;
@@ -1250,23 +1567,43 @@ struct Consumer {
   }
 
   __device__ bool dispatch(const int32_t *t, int task, int layer) {
+    uint64_t t0 = 0;
+    if (tr && tid == 0) {
+      t0 = gtimer();
+      t_ready = t_stage = t_swait = t_mark = 0;
+      n_stages = 0;
+    }
+    bool ok;
     switch (t[0]) {
-      case OP_QKV: return op_qkv(t, task, layer);
-      case OP_ROUTER: return op_router(t, task, layer);
-      case OP_ATTN: return op_attn(t, task, layer);
-      case OP_UP: return op_up(t, task, layer);
-      case OP_OUT: return op_out(t, task, layer);
-      case OP_LM: return op_lm(t, task);
+      case OP_QKV: ok = op_qkv(t, task, layer); break;
+      case OP_ROUTER: ok = op_router(t, task, layer); break;
+      case OP_ATTN: ok = op_attn(t, task, layer); break;
+      case OP_UP: ok = op_up(t, task, layer); break;
+      case OP_OUT: ok = op_out(t, task, layer); break;
+      case OP_LM: ok = op_lm(t, task); break;
       default:
         if (tid == 0) raise_error(*cx.p, MK_ERR_BAD_TASK, cx.cta, task, t[0], layer, -1, 0, 0);
-        return false;
+        ok = false;
     }
+    if (tr && tid == 0 && tr_n < cx.p->trace_cap) {
+      unsigned long long *e = tr + (size_t)tr_n * MK_TRACE_WORDS;
+      e[0] = (unsigned long long)(t[0] | (layer << 8) | (task << 20));
+      e[1] = t0;
+      e[2] = t_ready ? t_ready : t0;
+      e[3] = t_stage;
+      e[4] = gtimer();
+      e[5] = t_swait;
+      e[6] = (unsigned long long)n_stages;
+      e[7] = t_mark;
+      ++tr_n;
+    }
+    return ok;
   }
 
   /* returns false if the CTA stopped early */
   __device__ bool run(const int32_t *row) {
     si = 0;
-    dseq = 0;
+    wfail = false;
     const mk_kparams &p = *cx.p;
     const int nl = row[1], nf = row[2];
     for (int l = 0; l < p.L; ++l)
@@ -1305,17 +1642,21 @@ __global__ void __launch_bounds__(MK_THREADS, 1) decode_kernel(const mk_kparams 
   const bool header_ok = row[0] == OP_HEADER;
   if (header_ok) {
     if (warp == NC) {
-      Producer pr;
-      pr.cx = cx;
-      pr.lane = lane;
-      pr.policy = evict_first_policy();
-      pr.run(row);
+      if (lane == 0) {
+        Producer pr;
+        pr.cx = cx;
+        pr.policy = evict_first_policy();
+        pr.run(row);
+      }
+      __syncwarp();
     } else {
       Consumer<NB> c;
       c.cx = cx;
       c.warp = warp;
       c.lane = lane;
       c.tid = threadIdx.x;
+      c.tr = p.trace ? p.trace + (size_t)blockIdx.x * p.trace_cap * MK_TRACE_WORDS : nullptr;
+      c.tr_n = 0;
       const bool ok = c.run(row);
       if (threadIdx.x == 0 && !ok) s_ok = 0;
     }

@@ -141,7 +141,7 @@ extern "C" mk_status mk_decode_step_static(const mk_model_dims *dims, const mk_w
   const size_t o_h = take((size_t)(Lyr + 1) * MB * d.d_model * 2);
   const size_t o_qkv = take((size_t)Lyr * MB * QKVD * 2);
   const size_t o_o = take((size_t)Lyr * MB * HqD * 2);
-  const size_t o_part = take((size_t)Lyr * n_slots * G * (d.head_dim + 2) * 4);
+  const size_t o_part = take((size_t)Lyr * n_slots * G * (d.head_dim + 4) * 4);
   const size_t o_rl = take((size_t)Lyr * MB * d.n_experts * 4);
   const size_t o_rt = take((size_t)Lyr * sizeof(mk_routing));
   const size_t o_act = take((size_t)Lyr * u_max * MB * d.d_ffn * 2);
@@ -157,10 +157,13 @@ extern "C" mk_status mk_decode_step_static(const mk_model_dims *dims, const mk_w
 
   /* ---- shared memory plan (as for mk_decode_step) ---- */
   const int nb = batch <= 1 ? 1 : batch <= 2 ? 2 : batch <= 4 ? 4 : 8;
-  size_t xbuf = (size_t)nb * d.d_model * 2;
-  xbuf = std::max(xbuf, (size_t)nb * HqD * 2);
-  xbuf = std::max(xbuf, (size_t)2 * nb * d.d_ffn * 2);
+  const size_t xt = nb == 1 ? 4 : 2; /* activations fp32 for one token, else bf16 */
+  size_t xbuf = (size_t)nb * d.d_model * (xt + 2);
+  xbuf = std::max(xbuf, (size_t)nb * HqD * xt);
+  xbuf = std::max(xbuf, (size_t)2 * nb * d.d_ffn * xt);
+  xbuf = std::max(xbuf, std::min((size_t)u_max * nb * d.d_ffn * xt, (size_t)32768));
   xbuf = std::max(xbuf, (size_t)(8 + 2 + 32) * d.head_dim * 4);
+  xbuf = std::max(xbuf, (size_t)(2 * 256 * MK_MAX_GROUP + 2 * MK_MAX_GROUP) * 4);
   xbuf = up(xbuf, 1024);
   const size_t misc = up(mk_misc_bytes(), 128);
   const size_t budget = (size_t)optin - 1024;

@@ -81,7 +81,7 @@ mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int
                         MkPlan *out) {
   mk_status st = mk_validate_dims(dm);
   if (st != MK_OK) return st;
-  if (n_cta < 1 || !seq_lens || !out) return MK_ERR_INVALID_ARG;
+  if (n_cta < 1 || n_cta > 256 || !seq_lens || !out) return MK_ERR_INVALID_ARG;
   if (batch < 1 || batch > dm->max_batch) return MK_ERR_BATCH;
   const mk_model_dims &d = *dm;
   const int64_t cap_tokens = (int64_t)d.max_pages_per_seq * d.page_size;

@@ -1,0 +1,80 @@
+"""Summaries of the kernel's per-task trace (mk_set_trace / mk_get_trace).
+
+Each event is one task run by one CTA: entry, dependency satisfied, first
+data stage available, exit (globaltimer ns).  `summarize` reports, per
+phase (op) averaged over layers, when the phase starts and ends relative to
+the previous layer's end, and, over all CTAs, how the time splits into
+waiting for a dependency, waiting for data, and working.
+"""
+from __future__ import annotations
+
+from collections import defaultdict
+
+import numpy as np
+
+OPS = {1: "qkv", 2: "router", 3: "attn", 4: "up", 5: "out", 6: "lm"}
+
+
+def events(trace: np.ndarray):
+    """Flat list of (cta, op, layer, task, t_entry, t_ready, t_stage, t_exit,
+    stage_wait_ns, n_stages, t_mark)."""
+    out = []
+    for c in range(trace.shape[0]):
+        for e in trace[c]:
+            if e[1] == 0:
+                continue
+            w = int(e[0])
+            out.append((c, w & 0xFF, (w >> 8) & 0xFFF, w >> 20, int(e[1]), int(e[2]), int(e[3]),
+                        int(e[4]), int(e[5]), int(e[6]), int(e[7])))
+    return out
+
+
+def summarize(trace: np.ndarray, n_layers: int) -> dict:
+    ev = events(trace)
+    if not ev:
+        return {}
+    t0 = min(e[4] for e in ev)
+    t_end = max(e[7] for e in ev)
+    per = defaultdict(list)
+    for e in ev:
+        per[(e[2], e[1])].append(e)
+    layer_end = {}
+    for l in range(n_layers):
+        ends = [e[7] for k, v in per.items() if k[0] == l for e in v]
+        if ends:
+            layer_end[l] = max(ends)
+    phase = defaultdict(lambda: defaultdict(list))
+    for (l, op), v in per.items():
+        if op == 6 or l == 0 or l not in layer_end or (l - 1) not in layer_end:
+            continue
+        base = layer_end[l - 1]
+        phase[OPS[op]]["first_entry_us"].append((min(e[4] for e in v) - base) / 1e3)
+        phase[OPS[op]]["last_ready_us"].append((max(e[5] for e in v) - base) / 1e3)
+        st = [e[6] for e in v if e[6]]
+        if st:
+            phase[OPS[op]]["last_first_stage_us"].append((max(st) - base) / 1e3)
+        phase[OPS[op]]["last_exit_us"].append((max(e[7] for e in v) - base) / 1e3)
+        phase[OPS[op]]["mean_busy_us"].append(np.mean([(e[7] - max(e[5], e[6] or e[5])) / 1e3
+                                                       for e in v]))
+        phase[OPS[op]]["mean_stage_wait_us"].append(np.mean([e[8] / 1e3 for e in v]))
+        phase[OPS[op]]["mean_stages"].append(np.mean([e[9] for e in v]))
+        mk = [(e[10] - max(e[5], e[6] or e[5])) / 1e3 for e in v if e[10]]
+        if mk:
+            phase[OPS[op]]["mean_to_mark_us"].append(np.mean(mk))
+    phases = {op: {k: round(float(np.median(v)), 2) for k, v in d.items()}
+              for op, d in phase.items()}
+    layer_times = [(layer_end[l] - layer_end[l - 1]) / 1e3 for l in range(1, n_layers)
+                   if l in layer_end and l - 1 in layer_end]
+    wait_dep = sum(e[5] - e[4] for e in ev)
+    wait_data = sum(max(0, e[6] - e[5]) for e in ev if e[6])
+    busy = sum(e[7] - max(e[5], e[6] or e[5]) for e in ev)
+    total = (t_end - t0) * trace.shape[0]
+    return {
+        "step_us": round((t_end - t0) / 1e3, 1),
+        "layer_us_median": round(float(np.median(layer_times)), 2) if layer_times else None,
+        "lm_head_us": round((t_end - layer_end.get(n_layers - 1, t0)) / 1e3, 2),
+        "cta_time_split": {"wait_dependency": round(wait_dep / total, 3),
+                           "wait_first_data": round(wait_data / total, 3),
+                           "task_body": round(busy / total, 3)},
+        "phases_rel_prev_layer_end_us": phases,
+    }
