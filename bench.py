@@ -236,8 +236,9 @@ def run_mk(args, rank, world):
 
         mk.mk_set_trace(dec.ctx, dims.n_layers * 16 + 16)
         dec.decode_step(tok[0], logits, tok[1])
-        tr = mk.mk_get_trace(dec.ctx)
+        tr, stages = mk.mk_get_trace(dec.ctx)
         trace_summary = mktrace.summarize(tr, dims.n_layers)
+        trace_summary["stages_cta0"] = mktrace.stage_summary(stages)
         with open(args.trace, "w") as f:
             json.dump(trace_summary, f, indent=1)
         mk.mk_set_trace(dec.ctx, 0)

@@ -186,14 +186,21 @@ mk_status mk_debug_poison_wait(mk_ctx *ctx, int32_t layer, int32_t delta);
 
 /* Per-task timing trace of the following steps (diagnostic; each step
  * overwrites the previous one).  events_per_cta = 0 turns it off; otherwise
- * a buffer of n_sm * events_per_cta events is allocated.  Consumer thread 0
- * of every CTA records, for each task it runs: [0] op | layer << 8 |
- * task << 20, [1] entry, [2] dependency satisfied, [3] first data stage
- * available (0 if none), [4] exit -- globaltimer nanoseconds, 8 words per
- * event, unused events zero. */
+ * a buffer of n_sm * events_per_cta task events plus 4096 stage events is
+ * allocated.  Consumer thread 0 of every CTA records, for each task it runs:
+ * [0] op | layer << 8 | task << 20, [1] entry, [2] dependency satisfied,
+ * [3] first data stage available (0 if none), [4] exit, [5] ns spent
+ * waiting for later stages, [6] stages seen, [7] the task's mark (0 if
+ * none) -- globaltimer nanoseconds, 8 words per event, unused events zero.
+ * CTA 0 also records its first 4096 ring stages: [0] stage | warp << 20 |
+ * op << 24; the producer's [1] loop top, [2] stage known, [3] slot free,
+ * [4] copies issued; the owning warp's [5] wait start, [6] data seen, [7]
+ * slot released. */
 mk_status mk_set_trace(mk_ctx *ctx, int32_t events_per_cta);
 /* Copies the trace (synchronises).  host_out may be NULL to query the
- * geometry; otherwise it must hold n_cta * events_per_cta * 8 words. */
+ * geometry; otherwise it must hold (n_cta * events_per_cta + 4096) * 8
+ * words: the task events [n_cta][events_per_cta][8], then CTA 0's stage
+ * events [4096][8]. */
 mk_status mk_get_trace(mk_ctx *ctx, uint64_t *host_out, uint64_t n_words, int32_t *n_cta,
                        int32_t *events_per_cta);
 

@@ -265,13 +265,19 @@ def mk_set_trace(ctx: int, events_per_cta: int) -> None:
     _check(lib().mk_set_trace(ctx, events_per_cta), "mk_set_trace")
 
 
-def mk_get_trace(ctx: int) -> np.ndarray:
-    """The last step's trace as uint64 [n_cta][events][8]."""
+STAGE_TRACE_EVENTS = 4096
+
+
+def mk_get_trace(ctx: int):
+    """The last step's trace: (task events uint64 [n_cta][events][8], CTA 0's
+    stage events uint64 [STAGE_TRACE_EVENTS][8])."""
     n_cta, ev = ctypes.c_int32(), ctypes.c_int32()
     _check(lib().mk_get_trace(ctx, None, 0, ctypes.byref(n_cta), ctypes.byref(ev)), "mk_get_trace")
-    out = np.zeros((n_cta.value, ev.value, 8), np.uint64)
+    n_task = n_cta.value * ev.value * 8
+    out = np.zeros(n_task + STAGE_TRACE_EVENTS * 8, np.uint64)
     _check(lib().mk_get_trace(ctx, out.ctypes.data, out.size, None, None), "mk_get_trace")
-    return out
+    return (out[:n_task].reshape(n_cta.value, ev.value, 8),
+            out[n_task:].reshape(STAGE_TRACE_EVENTS, 8))
 
 
 def mk_plan(dims: mk_model_dims, n_sm: int, batch: int, seq_lens):

@@ -2,19 +2,21 @@
  * mk_api.cpp -- the C ABI (include/mk.h): validation, workspace, schedule
  * upload, launch of the persistent decode kernel, sticky device errors.
  */
+#include <cuda.h> /* tensor-map types; the encoder is reached through the runtime */
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "mk.h"
 #include "mk_internal.h"
 #include "mk_plan.h"
 
-extern "C" size_t mk_misc_bytes();
+extern "C" size_t mk_misc_bytes(int nb);
 extern "C" cudaError_t mk_kernel_prepare(int nb, size_t smem, int *blocks_per_sm);
 extern "C" cudaError_t mk_launch(const mk_kparams *p, int nb, int grid, size_t smem,
                                  cudaStream_t stream);
@@ -80,40 +82,13 @@ struct mk_ctx {
   mk_status sticky = MK_OK;
   bool prepared[4] = {false, false, false, false}; /* kernel attributes set per batch bucket */
   unsigned long long *trace = nullptr; /* [n_sm][trace_cap][MK_TRACE_WORDS] */
+  void *kv_maps = nullptr;             /* device [n_layers][2] tensor maps (in ws) */
   int trace_cap = 0;
 };
 
 namespace {
 
 mk_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MK_OK : MK_ERR_CUDA; }
-
-int nb_for(int batch) { return batch <= 1 ? 1 : batch <= 2 ? 2 : batch <= 4 ? 4 : 8; }
-
-size_t xbuf_bytes_for(const mk_model_dims &d, int nb) {
-  /* activations are fp32 for one token, bf16 otherwise */
-  const size_t HqD = (size_t)d.n_q_heads * d.head_dim, xt = nb == 1 ? 4 : 2;
-  const size_t u_max = (size_t)std::min(d.n_experts, d.max_batch * d.top_k);
-  size_t x = (size_t)nb * d.d_model * (xt + 2); /* normed input + staged h */
-  x = std::max(x, (size_t)nb * HqD * xt);
-  x = std::max(x, (size_t)2 * nb * d.d_ffn * xt);
-  x = std::max(x, std::min(u_max * nb * d.d_ffn * xt, (size_t)32768)); /* all experts at once */
-  x = std::max(x, (size_t)(8 + 2 + 32) * d.head_dim * 4); /* attention q, k, v, merge */
-  x = std::max(x, (size_t)(2 * 256 * MK_MAX_GROUP + 2 * MK_MAX_GROUP) * 4); /* split merge */
-  return align_up(x, 1024);
-}
-
-/* Shared memory plan for an nb-token kernel: the ring stages that fit. */
-bool smem_plan(const mk_ctx *c, int nb, int *stages, size_t *xbuf, size_t *total) {
-  const size_t misc = align_up(mk_misc_bytes(), 128);
-  *xbuf = xbuf_bytes_for(c->dims, nb);
-  const size_t budget = c->smem_optin - 1024; /* static shared memory of the kernel */
-  if (budget < *xbuf + misc + 2 * MK_STAGE_BYTES) return false;
-  int s = (int)((budget - *xbuf - misc) / MK_STAGE_BYTES);
-  s = std::min(s, MK_MAX_STAGES);
-  *stages = s;
-  *total = (size_t)s * MK_STAGE_BYTES + *xbuf + misc;
-  return true;
-}
 
 mk_status check_sticky(mk_ctx *c) {
   if (c->sticky != MK_OK) return c->sticky;
@@ -163,7 +138,54 @@ mk_status rebuild(mk_ctx *c) {
   return MK_OK;
 }
 
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn tensor_map_encoder() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiledFn)ptr;
+  });
+  return fn;
+}
+
 }  // namespace
+
+mk_status mk_encode_kv_maps(const mk_model_dims *dm, const void *const *k_pools,
+                            const void *const *v_pools, void *host_out) {
+  static_assert(sizeof(CUtensorMap) == 128, "tensor map size");
+  const mk_model_dims &d = *dm;
+  EncodeTiledFn enc = tensor_map_encoder();
+  if (!enc) return MK_ERR_CUDA;
+  /* 3-D view of a pool: {BI head dims, D / BI halves, token rows}; one box
+   * is a whole page of one kv head */
+  const int D = d.head_dim, bi = mk_box_inner(D), nbox = D / bi;
+  const cuuint64_t dims[3] = {(cuuint64_t)bi, (cuuint64_t)nbox,
+                              (cuuint64_t)d.num_pages * d.n_kv_heads * d.page_size};
+  if (dims[2] > 0xFFFFFFFFull) return MK_ERR_UNSUPPORTED;
+  const cuuint64_t strides[2] = {(cuuint64_t)bi * 2, (cuuint64_t)D * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)bi, (cuuint32_t)nbox, (cuuint32_t)d.page_size};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapSwizzle swz = D >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+  CUtensorMap *out = (CUtensorMap *)host_out;
+  for (int l = 0; l < d.n_layers; ++l)
+    for (int kv = 0; kv < 2; ++kv) {
+      void *base = const_cast<void *>(kv == 0 ? k_pools[l] : v_pools[l]);
+      if (enc(&out[2 * l + kv], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return MK_ERR_INVALID_ARG;
+    }
+  return MK_OK;
+}
 
 extern "C" {
 
@@ -233,13 +255,9 @@ mk_status mk_create(const mk_model_dims *dims, const mk_weights *w, void *stream
     D.kc = (uint16_t *)L.k_cache;
     D.vc = (uint16_t *)L.v_cache;
   }
-  for (int nb : {1, 2, 4, 8}) {
-    int stages;
-    size_t xb, total;
-    if (!smem_plan(c, nb, &stages, &xb, &total)) {
-      delete c;
-      return MK_ERR_UNSUPPORTED;
-    }
+  if (c->smem_optin < MK_SMEM_OPTIN) {
+    delete c;
+    return MK_ERR_NO_DEVICE;
   }
 
   /* workspace sizes */
@@ -266,6 +284,7 @@ mk_status mk_create(const mk_model_dims *dims, const mk_weights *w, void *stream
   const size_t o_len = cv.take((size_t)MB * 4);
   const size_t o_pt = cv.take((size_t)MB * d.max_pages_per_seq * 4);
   const size_t o_ly = cv.take((size_t)L * sizeof(mk_layer_dev));
+  const size_t o_maps = cv.take((size_t)L * 2 * 128);
   c->ws_bytes = cv.off;
 
   cudaError_t e = cudaMalloc(&c->ws, c->ws_bytes);
@@ -287,6 +306,21 @@ mk_status mk_create(const mk_model_dims *dims, const mk_weights *w, void *stream
   c->seq_lens_dev = (int32_t *)(c->ws + o_len);
   c->page_table_dev = (int32_t *)(c->ws + o_pt);
   c->layers_dev = (mk_layer_dev *)(c->ws + o_ly);
+  c->kv_maps = c->ws + o_maps;
+  std::vector<uint8_t> maps((size_t)L * 2 * 128);
+  {
+    std::vector<const void *> kp(L), vp(L);
+    for (int l = 0; l < L; ++l) {
+      kp[l] = w->layers[l].k_cache;
+      vp[l] = w->layers[l].v_cache;
+    }
+    const mk_status ms = mk_encode_kv_maps(&d, kp.data(), vp.data(), maps.data());
+    if (ms != MK_OK) {
+      cudaFree(c->ws);
+      delete c;
+      return ms;
+    }
+  }
 
   /* RoPE table: cos / sin of pos * base^(-2i/D) in double, stored as fp32 */
   std::vector<float> rope((size_t)c->rope_max_pos * (d.head_dim / 2) * 2);
@@ -308,6 +342,8 @@ mk_status mk_create(const mk_model_dims *dims, const mk_weights *w, void *stream
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(c->layers_dev, c->layers.data(), L * sizeof(mk_layer_dev),
                         cudaMemcpyHostToDevice, c->stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(c->kv_maps, maps.data(), maps.size(), cudaMemcpyHostToDevice, c->stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
   if (e == cudaSuccess) e = cudaHostAlloc(&c->err_host, 16 * sizeof(int32_t), cudaHostAllocMapped);
   if (e == cudaSuccess) {
@@ -395,15 +431,14 @@ mk_status mk_decode_step(mk_ctx *c, const int32_t *token_ids, float *out_logits,
       ++c->rebuilds;
     }
   }
-  const int nb = nb_for(c->batch);
-  int stages;
-  size_t xb, total;
-  if (!smem_plan(c, nb, &stages, &xb, &total)) return MK_ERR_UNSUPPORTED;
+  const int nb = mk_nb_for(c->batch);
+  MkSmem sm;
+  if (!mk_smem_plan(&d, nb, &sm)) return MK_ERR_UNSUPPORTED;
   cudaError_t e;
   const int ki = nb == 1 ? 0 : nb == 2 ? 1 : nb == 4 ? 2 : 3;
   if (!c->prepared[ki]) {
     int blocks = 0;
-    e = mk_kernel_prepare(nb, total, &blocks);
+    e = mk_kernel_prepare(nb, sm.dyn, &blocks);
     if (e != cudaSuccess) return MK_ERR_CUDA;
     if (blocks < 1) return MK_ERR_UNSUPPORTED;
     c->prepared[ki] = true;
@@ -459,16 +494,18 @@ mk_status mk_decode_step(mk_ctx *c, const int32_t *token_ids, float *out_logits,
   p.ctrs_per_layer = c->ctrs_per_layer;
   p.wait_limit_ns = c->wait_limit_ns;
   p.err_host = c->err_host_dev;
-  p.ring_stages = stages;
-  p.xbuf_bytes = (int32_t)xb;
+  p.stage_bytes = sm.stage_bytes;
+  p.kv_maps = c->kv_maps;
+  p.xbuf_bytes = (int32_t)sm.xbuf;
   p.poison_layer = c->poison_layer;
   p.poison_delta = c->poison_delta;
   p.trace = c->trace;
   p.trace_cap = c->trace_cap;
+  p.stage_trace = c->trace ? c->trace + (size_t)c->n_sm * c->trace_cap * MK_TRACE_WORDS : nullptr;
   c->poison_layer = -1;
   c->poison_delta = 0;
 
-  e = mk_launch(&p, nb, c->n_sm, total, c->stream);
+  e = mk_launch(&p, nb, c->n_sm, sm.dyn, c->stream);
   if (e != cudaSuccess) return MK_ERR_CUDA;
   for (int b = 0; b < c->batch; ++b) c->lens[b] += 1;
   ++c->steps;
@@ -508,7 +545,8 @@ mk_status mk_set_trace(mk_ctx *c, int32_t events_per_cta) {
   c->trace = nullptr;
   c->trace_cap = 0;
   if (events_per_cta == 0) return MK_OK;
-  const size_t bytes = (size_t)c->n_sm * events_per_cta * MK_TRACE_WORDS * 8;
+  const size_t bytes =
+      ((size_t)c->n_sm * events_per_cta + MK_STAGE_TRACE_EVENTS) * MK_TRACE_WORDS * 8;
   if (cudaMalloc(&c->trace, bytes) != cudaSuccess) return MK_ERR_CUDA;
   if (cudaMemset(c->trace, 0, bytes) != cudaSuccess) return MK_ERR_CUDA;
   c->trace_cap = events_per_cta;
@@ -521,7 +559,8 @@ mk_status mk_get_trace(mk_ctx *c, uint64_t *host_out, uint64_t n_words, int32_t 
   if (n_cta) *n_cta = c->n_sm;
   if (events_per_cta) *events_per_cta = c->trace_cap;
   if (!host_out) return MK_OK;
-  const uint64_t need = (uint64_t)c->n_sm * c->trace_cap * MK_TRACE_WORDS;
+  const uint64_t need =
+      ((uint64_t)c->n_sm * c->trace_cap + MK_STAGE_TRACE_EVENTS) * MK_TRACE_WORDS;
   if (!c->trace || n_words < need) return MK_ERR_INVALID_ARG;
   mk_status st = mk_sync(c);
   if (st != MK_OK) return st;

@@ -54,10 +54,14 @@ static inline int mk_ctrs_per_layer(int max_batch, int n_kv_heads) {
 #define MK_MAX_TOPK 16
 #define MK_MAX_GROUP 8          /* q heads per kv head */
 #define MK_MAX_OUT_ROWS 64      /* rows of d per OUT task */
-#define MK_STAGE_BYTES 32768    /* one ring stage */
-#define MK_MAX_STAGES 16
-#define MK_NC_WARPS 8           /* consumer warps */
+#define MK_NC_WARPS 8           /* consumer warps; ring slot w belongs to consumer warp w */
 #define MK_THREADS ((MK_NC_WARPS + 1) * 32)
+#define MK_MAX_STAGE_ROWS 64
+#define MK_MAX_STAGE_BYTES 32768
+#define MK_MAX_STAGE_PAGES 8
+#define MK_SMEM_OPTIN 232448    /* opt-in shared memory per block on sm_100-class parts */
+#define MK_SMEM_STATIC 1024     /* slack to align the ring to 1024 bytes */
+#define MK_SMEM_TASKS 32        /* task descriptors of a CTA kept in shared memory */
 
 /* Routing result of one layer, written by the last router task. */
 typedef struct {
@@ -122,17 +126,24 @@ typedef struct {
   int32_t ctrs_per_layer;
   unsigned long long wait_limit_ns;
   int32_t *err_host;          /* host-mapped mirror: [code, cta, task, op, layer, ctr, seen, target] */
-  int32_t ring_stages;        /* stages of MK_STAGE_BYTES in the shared ring */
+  int32_t stage_bytes;        /* bytes of one ring slot (a multiple of 1024) */
+  const void *kv_maps;        /* [L][2] CUtensorMap of the K and V pools (64-byte aligned) */
   int32_t xbuf_bytes;         /* shared activation buffer */
   int32_t poison_layer, poison_delta; /* test hook: see mk_debug_poison_wait */
   unsigned long long *trace;  /* NULL, or [n_cta][trace_cap][MK_TRACE_WORDS] task timestamps */
   int32_t trace_cap;
+  unsigned long long *stage_trace; /* NULL, or CTA 0's [MK_STAGE_TRACE_EVENTS][8] stage timestamps */
 } mk_kparams;
 
 /* One trace event (per executed task, written by consumer thread 0):
  * [0] op | layer << 8 | task << 20, [1] entry, [2] dependency satisfied,
  * [3] first stage of data available, [4] exit (globaltimer ns). */
 #define MK_TRACE_WORDS 8
+/* Stage events of CTA 0 (after the task events in the trace buffer):
+ * [0] stage | warp << 20 | op << 24, producer: [1] loop top, [2] stage
+ * known, [3] slot free, [4] copies issued; owner warp: [5] starts waiting,
+ * [6] data seen, [7] slot released. */
+#define MK_STAGE_TRACE_EVENTS 4096
 
 #ifdef __CUDACC__
 #define MK_HD __host__ __device__
@@ -140,26 +151,32 @@ typedef struct {
 #define MK_HD
 #endif
 
-/* Rows of row_bytes each that one ring stage carries (the producer and the
- * consumers must agree on it). */
-static inline MK_HD int mk_rows_per_stage(int row_bytes) {
-  int r = MK_STAGE_BYTES / row_bytes;
-  return r > 64 ? 64 : r;
+/* ---- ring stage geometry (the producer and the consumers must agree) -------
+ * A stage of streamed rows holds whole rows of K bf16, contiguous as in
+ * memory (pitch 2K bytes), so that one bulk copy fills it.  The tensor-core
+ * operand loads stay free of bank conflicts by reading the two halves of
+ * each 128-byte block in opposite order on even and odd rows (see
+ * mma_rows).  Activation vectors in shared memory use pitch K. */
+static inline MK_HD int mk_row_pitch(int K) { return 2 * K; }
+static inline MK_HD int mk_x_pitch(int K) { return K; }
+
+static inline MK_HD int mk_rows_per_stage(int K, int stage_bytes) {
+  int r = stage_bytes / mk_row_pitch(K);
+  return r > MK_MAX_STAGE_ROWS ? MK_MAX_STAGE_ROWS : r;
 }
 
-/* Gate/up row pairs per stage (a pair is one gate row and one up row of
- * row_bytes each); at most 32 so that 2 * pairs rows fit the partial-sum
- * buffer. */
-static inline MK_HD int mk_pairs_per_stage(int row_bytes) {
-  int r = MK_STAGE_BYTES / (2 * row_bytes);
-  return r > 32 ? 32 : r;
+/* Gate/up row pairs per stage: the n gate rows, then the n up rows. */
+static inline MK_HD int mk_pairs_per_stage(int K, int stage_bytes) {
+  return mk_rows_per_stage(K, stage_bytes) / 2;
 }
 
-/* KV pages per stage: each page brings a K block and a V block of
- * page_bytes each. */
-static inline MK_HD int mk_pages_per_stage(int page_bytes) {
-  int r = MK_STAGE_BYTES / (2 * page_bytes);
-  return r > 8 ? 8 : r;
+/* KV pages: one tensor-map box per page and pool covers min(D, 64) head dims
+ * x D / min(D, 64) halves x P tokens; a page's K box, then its V box. */
+static inline MK_HD int mk_box_inner(int D) { return D < 64 ? D : 64; }
+static inline MK_HD int mk_page_stage_bytes(int P, int D) { return 2 * P * D * 2; }
+static inline MK_HD int mk_pages_per_stage(int P, int D, int stage_bytes) {
+  int r = stage_bytes / mk_page_stage_bytes(P, D);
+  return r > MK_MAX_STAGE_PAGES ? MK_MAX_STAGE_PAGES : r;
 }
 
 #endif /* MK_INTERNAL_H */

@@ -11,13 +11,27 @@
  *   warps 0..7  consumers: wait on the task's counter, compute from shared
  *               memory, write outputs, signal the downstream counter;
  *   warp  8     producer:  streams each task's immutable bytes (weights,
- *               cached K/V pages) into a ring of shared-memory stages with
- *               cp.async.bulk (TMA) completing on mbarriers.  It runs ahead
- *               of the consumers and does NOT wait for a task's data
- *               dependency before loading its weights -- the weight
- *               prefetch ahead of dependencies that the aiweekly.co page
- *               ranks third among the method's gains (paragraph 4).  Only
- *               the expert weights wait, for the routing that names them.
+ *               cached K/V pages) into a ring of eight shared-memory slots
+ *               with TMA (cp.async.bulk for weight rows, tensor-map boxes
+ *               with a 128-byte swizzle for K/V pages) completing on
+ *               mbarriers.  It runs ahead of the consumers and does NOT wait
+ *               for a task's data dependency before loading its weights --
+ *               the weight prefetch ahead of dependencies that the
+ *               aiweekly.co page ranks third among the method's gains
+ *               (paragraph 4).  Only the expert weights wait, for the
+ *               routing that names them.
+ *
+ * Ring slot w belongs to consumer warp w: stage i of the CTA's stream lands
+ * in slot i % 8 and warp i % 8 consumes all of it on its own, so the eight
+ * warps work on eight stages at once with no CTA-wide barrier on the
+ * streaming path.  The dense contractions run on the tensor cores
+ * (mma.sync m16n8k16, bf16 in, fp32 accumulate):
+ *   - every GEMV: the up-to-8 tokens are the M side (rows 8-15 are zero),
+ *     eight weight rows the N side, so the fp32 sums come out of the
+ *     accumulator already reduced over K;
+ *   - attention: the GQA group of up to 8 query heads against 16-key tiles,
+ *     S = Q K^T and O += P V with P split into a bf16 high and low part so
+ *     that the probabilities keep about 16 significant bits.
  *
  * Counters ("Cohere megakernel serves 30B MoE 1.58x faster than vLLM",
  * paragraph 3): a task waits for ONE counter to reach a count, and signals
@@ -35,8 +49,6 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include <type_traits>
-
 #include "mk.h"
 #include "mk_internal.h"
 
@@ -44,6 +56,7 @@ namespace mk {
 
 constexpr int NC = MK_NC_WARPS;
 constexpr int NCT = NC * 32;
+#define NEG_INF (-INFINITY)
 
 /* ---------------------------------------------------------------- helpers */
 
@@ -61,6 +74,11 @@ __device__ __forceinline__ uint16_t f2bf(float f) {
 }
 
 __device__ __forceinline__ float rbf(float f) { return bf2f(f2bf(f)); }
+
+/* two bf16 in one register, `lo` in the low half (the lower k index) */
+__device__ __forceinline__ uint32_t pack_bf16(uint16_t lo, uint16_t hi) {
+  return (uint32_t)lo | ((uint32_t)hi << 16);
+}
 
 /* 8 bf16 packed in a uint4 -> 8 floats (exact). */
 __device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
@@ -108,6 +126,18 @@ __device__ __forceinline__ void bar_consumers() {
   asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory");
 }
 
+/* Consumer-wide barrier returning the OR of every thread's predicate. */
+__device__ __forceinline__ bool bar_any(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "n"(NCT)
+      : "memory");
+  return r != 0;
+}
+
 /* mbarriers (CTA scope) */
 __device__ __forceinline__ void mbar_init(uint64_t *b, int count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(b)), "r"(count) : "memory");
@@ -142,105 +172,160 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
       : "memory");
 }
 
+/* 3-D TMA tensor-map box global -> shared at coordinates {0, 0, z}. */
+__device__ __forceinline__ void tensor_g2s_3d(void *dst, const void *tmap, int z, uint64_t *bar,
+                                              uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(saddr(dst)),
+      "l"(tmap), "r"(0), "r"(0), "r"(z), "r"(saddr(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ uint64_t evict_first_policy() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
 
-/* Sum over 32 lanes of NB values at once: after log2(NB) "transposing"
- * rounds each lane keeps one value, then plain butterfly rounds finish the
- * sum.  Lane l ends with the sum of v[l >> (5 - log2 NB)]. */
-template <int NB>
-__device__ __forceinline__ float transpose_reduce(float (&v)[NB], int lane) {
-  constexpr int LOG = NB == 1 ? 0 : NB == 2 ? 1 : NB == 4 ? 2 : 3;
+/* ldmatrix: four 8x8 b16 matrices; lane l gives the row address of matrix
+ * l / 8, row l % 8.  Plain: thread (g, t) gets row g, columns 2t, 2t+1;
+ * transposed: rows 2t, 2t+1 of column g. */
+__device__ __forceinline__ void ldsm4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void ldsm4_t(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+/* c += A B, m16n8k16, bf16 x bf16 -> fp32.  Thread (g = lane/4, t = lane%4)
+ * holds A rows g (a0, a2) and g + 8 (a1, a3) at k-pairs 2t (a0, a1) and
+ * 2t + 8 (a2, a3); B column g at k-pairs 2t (b0) and 2t + 8 (b1); C rows g
+ * (c0, c1) and g + 8 (c2, c3) at columns 2t, 2t + 1. */
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7},"
+      " {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+/* -------------------------------------------------------- skinny GEMV tile
+ * out[v][b] = W_rm(v) . x_b for the R (virtual) rows v of one ring stage --
+ * stage row rm(v) at byte rm(v) * pitch -- and the NB token vectors x_b
+ * (pitch xp elements), on the tensor cores.  Eight weight rows are the N
+ * side of an m16n8k16 tile, the tokens the M side, and the fp32 sums come
+ * out of the accumulator already reduced over K.
+ *
+ * Bank conflicts without padding: each thread reads 16-byte pieces; a
+ * quarter-warp reads two rows (B columns g = 2i, 2i + 1) at the same
+ * offsets, which rows 2K bytes apart put in the same banks.  So odd-g
+ * threads read the upper half of each 128-byte block first.  That changes
+ * which columns feed which k slot on odd threads, so token b is entered
+ * twice on the M side: row 2b with the even order (A rows 0..7 hold tokens
+ * 0..3, rows 8..15 tokens 4..7), row 2b + 1 with the odd order, and C[m][n]
+ * is valid where m and n have the same parity -- thread (g, t) ends with
+ * column 2t + (g & 1) for tokens g / 2 (c0 or c1) and 4 + g / 2 (c2 or c3).
+ * Within a 64-column block the k order is a permutation of the columns,
+ * the same for A and B of a valid pair, so each sum is over all columns.
+ * Four accumulators (one per k step) keep the mma chains independent.
+ * epi(n0, sums of the n-tile at rows n0.., sums of the n-tile at n0 + 8..,
+ * whether that second tile exists) runs on every lane; see take_out. */
+template <int NB, class RowMap, class Epi>
+__device__ __forceinline__ void mma_rows(const uint8_t *st, int R, int pitch, int K,
+                                         const uint16_t *x, int xp, int lane, RowMap &&rm,
+                                         Epi &&epi) {
+  const int g = lane >> 2, t = lane & 3, q = g & 1;
+  const int ta = g >> 1, tb = 4 + (g >> 1);
+  const bool ha = ta < NB, hb = NB > 4 && tb < NB;
+  const int f0 = 8 * t + 32 * q;  /* first piece of each 64-column block */
+  const int sd = q ? -32 : 32;    /* the second piece, relative to the first */
+  const uint16_t *xa = x + (size_t)(ha ? ta : 0) * xp + f0;
+  const uint16_t *xb = x + (size_t)(hb ? tb : 0) * xp + f0;
+  for (int n0 = 0; n0 < R; n0 += 16) {
+    const bool two = n0 + 8 < R;
+    const uint16_t *wa = (const uint16_t *)(st + (size_t)rm(min(n0 + g, R - 1)) * pitch) + f0;
+    const uint16_t *wb = (const uint16_t *)(st + (size_t)rm(min(n0 + 8 + g, R - 1)) * pitch) + f0;
+    float ca[4][4], cb[4][4];
 #pragma unroll
-  for (int r = 0; r < LOG; ++r) {
-    const int half = NB >> (r + 1);
-    const int mask = 16 >> r;
-    const bool upper = (lane & mask) != 0;
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int i = 0; i < half; ++i) {
-      const float send = upper ? v[i] : v[i + half];
-      const float keep = upper ? v[i + half] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, mask);
+      for (int k = 0; k < 4; ++k) ca[i][k] = cb[i][k] = 0.0f;
+#pragma unroll 2
+    for (int c0 = 0; c0 < K; c0 += 64) {
+      uint4 af = make_uint4(0, 0, 0, 0), as = af, bf = af, bs = af;
+      if (ha) {
+        af = *(const uint4 *)(xa + c0);
+        as = *(const uint4 *)(xa + c0 + sd);
+      }
+      if (hb) {
+        bf = *(const uint4 *)(xb + c0);
+        bs = *(const uint4 *)(xb + c0 + sd);
+      }
+      const uint4 wf = *(const uint4 *)(wa + c0), ws = *(const uint4 *)(wa + c0 + sd);
+      mma16816(ca[0], af.x, bf.x, af.y, bf.y, wf.x, wf.y);
+      mma16816(ca[1], af.z, bf.z, af.w, bf.w, wf.z, wf.w);
+      mma16816(ca[2], as.x, bs.x, as.y, bs.y, ws.x, ws.y);
+      mma16816(ca[3], as.z, bs.z, as.w, bs.w, ws.z, ws.w);
+      if (two) {
+        const uint4 vf = *(const uint4 *)(wb + c0), vs = *(const uint4 *)(wb + c0 + sd);
+        mma16816(cb[0], af.x, bf.x, af.y, bf.y, vf.x, vf.y);
+        mma16816(cb[1], af.z, bf.z, af.w, bf.w, vf.z, vf.w);
+        mma16816(cb[2], as.x, bs.x, as.y, bs.y, vs.x, vs.y);
+        mma16816(cb[3], as.z, bs.z, as.w, bs.w, vs.z, vs.w);
+      }
     }
-  }
-  float s = v[0];
+    float sa[4], sb[4];
 #pragma unroll
-  for (int m = 16 >> LOG; m >= 1; m >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, m);
-  return s;
-}
-
-template <int NB>
-__device__ __forceinline__ int reduce_token(int lane) {
-  constexpr int LOG = NB == 1 ? 0 : NB == 2 ? 1 : NB == 4 ? 2 : 3;
-  return lane >> (5 - LOG);
-}
-template <int NB>
-__device__ __forceinline__ bool reduce_leader(int lane) {
-  constexpr int LOG = NB == 1 ? 0 : NB == 2 ? 1 : NB == 4 ? 2 : 3;
-  return (lane & ((32 >> LOG) - 1)) == 0;
-}
-
-/* The DPL (= D / 32 <= 4) bf16 head dims of lane `lane` in a K or V row. */
-__device__ __forceinline__ void lane_dims(const uint16_t *row, int lane, int DPL, float (&o)[4]) {
-  if (DPL == 4) {
-    const uint2 v = *(const uint2 *)(row + lane * 4);
-    o[0] = __uint_as_float(v.x << 16);
-    o[1] = __uint_as_float(v.x & 0xFFFF0000u);
-    o[2] = __uint_as_float(v.y << 16);
-    o[3] = __uint_as_float(v.y & 0xFFFF0000u);
-  } else if (DPL == 2) {
-    const uint32_t v = *(const uint32_t *)(row + lane * 2);
-    o[0] = __uint_as_float(v << 16);
-    o[1] = __uint_as_float(v & 0xFFFF0000u);
-    o[2] = o[3] = 0.0f;
-  } else {
-    o[0] = bf2f(row[lane]);
-    o[1] = o[2] = o[3] = 0.0f;
-  }
-}
-
-/* acc[b] += w . x[b] over K elements (K % 8 == 0), w and x bf16 in shared
- * memory; lane l handles the 8-element chunks l, l + 32, ... */
-template <int NB>
-__device__ __forceinline__ void dot_row(const uint16_t *w, const uint16_t *x, int xstride, int K,
-                                        int lane, float (&acc)[NB]) {
-  for (int c = lane * 8; c < K; c += 256) {
-    float wf[8];
-    unpack8(*(const uint4 *)(w + c), wf);
-#pragma unroll
-    for (int b = 0; b < NB; ++b) {
-      float xf[8];
-      unpack8(*(const uint4 *)(x + b * xstride + c), xf);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[b] = fmaf(wf[i], xf[i], acc[b]);
+    for (int k = 0; k < 4; ++k) {
+      sa[k] = (ca[0][k] + ca[1][k]) + (ca[2][k] + ca[3][k]);
+      sb[k] = (cb[0][k] + cb[1][k]) + (cb[2][k] + cb[3][k]);
     }
+    epi(n0, sa, sb, two);
+  }
+}
+
+/* The valid outputs of one n-tile of mma_rows on this lane: f(v, b, value)
+ * for virtual row v = n0 + 2t + (g & 1) (< R) and tokens g / 2 and
+ * 4 + g / 2 (< NB). */
+template <int NB, class F>
+__device__ __forceinline__ void take_out(int n0, const float (&c)[4], int R, int lane, F &&f) {
+  const int g = lane >> 2, t = lane & 3, q = g & 1, v = n0 + 2 * t + q;
+  if (v < R) {
+    if ((g >> 1) < NB) f(v, g >> 1, q ? c[1] : c[0]);
+    if (NB > 4 && 4 + (g >> 1) < NB) f(v, 4 + (g >> 1), q ? c[3] : c[2]);
   }
 }
 
 /* ----------------------------------------------------------- shared layout */
 
+template <int NB>
 struct Misc {
-  uint64_t full[MK_MAX_STAGES];
-  uint64_t empty[MK_MAX_STAGES];
-  int32_t dec[2];         /* collective decisions, double-buffered (0 ok, 1 abort) */
-  int32_t norm_layer;     /* layer whose normed input sits in xbuf (-2: none) */
-  int32_t pad0;
+  uint64_t full[NC];
+  uint64_t empty[NC];
+  int32_t norm_layer; /* layer whose normed input sits in xbuf (-2: none) */
+  int32_t ok;         /* 0 once a consumer stopped early */
+  int32_t pad0[2];
   float red[NC][MK_MAX_BATCH];
   float rsum[MK_MAX_BATCH];
-  float part[2][512];     /* GEMV partial sums [row * S + seg][b], double-buffered */
+  float am[NC / 2][8], al[NC / 2][8]; /* attention warp-merge exchange */
+  int32_t tasks[MK_SMEM_TASKS][MK_DESC_INTS]; /* this CTA's task-table row */
   union {
     struct {
-      float slot_w[128][MK_MAX_BATCH];
-      float acc[MK_MAX_OUT_ROWS][MK_MAX_BATCH][2]; /* attn, moe */
+      float slot_w[128][NB];
+      float acc_o[MK_MAX_OUT_ROWS][NB];         /* Wo rows (one writer each) */
+      float acc_w[NC][MK_MAX_OUT_ROWS][NB];     /* per-warp expert-down sums */
     } out;
-    struct {
-      float pw[NC][8][8]; /* p of up to 8 keys x 8 head slots, per warp */
-      float alpha[NC][8];
-      float m[8][8], l[8][8]; /* merge exchange */
-    } at;
     struct {
       float best[NC][MK_MAX_BATCH][2];
     } lm;
@@ -252,14 +337,22 @@ struct Misc {
   } u;
 };
 
+/* The kernel's dynamic shared memory.  Pointers into it are always formed
+ * from this symbol plus an offset in the function that dereferences them,
+ * so that the compiler emits shared-memory (not generic) accesses. */
+extern __shared__ __align__(1024) uint8_t mk_smem[];
+
 struct Ctx {
   const mk_kparams *p;
-  uint8_t *ring;
-  uint8_t *xbuf;
-  Misc *m;
+  uint32_t ring_off, xbuf_off, misc_off; /* byte offsets into mk_smem */
   uint32_t epoch;
   int cta;
-  int nstages;
+  int SB; /* bytes of one ring slot */
+  __device__ __forceinline__ uint8_t *ring() const { return mk_smem + ring_off; }
+  __device__ __forceinline__ uint8_t *xbuf() const { return mk_smem + xbuf_off; }
+  /* the mbarriers open the control block: full[NC], then empty[NC] */
+  __device__ __forceinline__ uint64_t *full() const { return (uint64_t *)(mk_smem + misc_off); }
+  __device__ __forceinline__ uint64_t *empty() const { return full() + NC; }
 };
 
 __device__ __forceinline__ int32_t *lctr(const mk_kparams &p, int layer, int kind) {
@@ -342,25 +435,29 @@ __device__ bool wait_mbar(const Ctx &cx, uint64_t *bar, uint32_t parity, int tas
 
 /* ============================================================== producer
  * One thread (lane 0 of the producer warp) walks the CTA's task list stage
- * by stage with two cursors over the same sequence:
- *   - the load cursor copies stage i into ring slot i % nstages (TMA bulk
- *     copies completing on full[slot]) once the consumers have released it;
- *   - the prefetch cursor runs up to MK_PREFETCH_STAGES stages further and
- *     asks L2 for those bytes (cp.async.bulk.prefetch.L2), so that when a
- *     slot frees the copy is served from L2 rather than paying the loaded
- *     HBM latency again.  It never waits: at a task whose bytes depend on
- *     routing that is not known yet it pauses until the load cursor passes.
- * Consumers walk the same deterministic stage sequence. */
+ * by stage and copies stage i into ring slot i % 8 (TMA copies completing
+ * on full[slot]) as soon as warp i % 8 has released the slot; eight slots of
+ * about 25 KB on each of the 152 SMs keep ~30 MB of copies in flight, more
+ * than HBM needs to run at its peak.  The consumers walk the same
+ * deterministic stage sequence.
+ *
+ * Stage contents (one bulk copy per contiguous block, since each copy
+ * costs the single producer thread tens of nanoseconds to issue):
+ *   ROWS   n whole rows of one matrix, consecutive as in memory (one copy);
+ *   PAIRS  the n gate rows, then the n up rows, of the same expert and ffn
+ *          indices (two copies);
+ *   PAGES  n KV pages of one (sequence, kv head): page j at stage byte
+ *          j * 4PD, its K box then its V box (P tokens x D dims, stored as
+ *          128-byte rows of 64 dims, swizzled when D >= 64; two copies). */
 
-#define MK_PREFETCH_STAGES 8
+enum { SK_ROWS = 0, SK_PAIRS = 1, SK_PAGES = 2 };
 
-__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
-struct Seg {
-  const uint8_t *src;
-  uint32_t off, bytes;
+struct StageDesc {
+  int kind, n;
+  const uint8_t *a, *b;
+  uint32_t row_bytes;
+  int layer, kvh, seq, q0;
+  int pages[MK_MAX_STAGE_PAGES]; /* PAGES: physical page ids */
 };
 
 enum { IT_STAGE = 1, IT_END = 0, IT_BLOCKED = -1, IT_FAIL = -2 };
@@ -368,7 +465,7 @@ enum { IT_STAGE = 1, IT_END = 0, IT_BLOCKED = -1, IT_FAIL = -2 };
 struct StageIter {
   const mk_kparams *p;
   const int32_t *row;
-  int nl, nf;
+  int nl, nf, SB;
   uint32_t epoch;
   int layer, k;   /* current task (layer == L: the final tasks) */
   bool started;
@@ -384,11 +481,12 @@ struct StageIter {
   int u, U;            /* OUT: u = -1 while on Wo rows, then the down slot */
   const mk_routing *rt;
 
-  __device__ void init(const mk_kparams *pp, const int32_t *rw, uint32_t ep) {
+  __device__ void init(const mk_kparams *pp, const int32_t *rw, uint32_t ep, int sb) {
     p = pp;
     row = rw;
     nl = rw[1];
     nf = rw[2];
+    SB = sb;
     epoch = ep;
     layer = 0;
     k = 0;
@@ -466,41 +564,35 @@ struct StageIter {
     }
   }
 
-  __device__ bool row_stage(Seg *seg, int &nseg, uint32_t &total) {
+  __device__ bool row_stage(StageDesc &sd) {
     if (r >= nrows) return false;
-    const uint32_t rb = (uint32_t)K * 2;
-    const int cnt = min(mk_rows_per_stage(rb), nrows - r);
-    seg[0].src = (const uint8_t *)(src + (size_t)r * K);
-    seg[0].off = 0;
-    seg[0].bytes = cnt * rb;
-    nseg = 1;
-    total = cnt * rb;
+    const int cnt = min(mk_rows_per_stage(K, SB), nrows - r);
+    sd.kind = SK_ROWS;
+    sd.n = cnt;
+    sd.a = (const uint8_t *)(src + (size_t)r * K);
+    sd.row_bytes = (uint32_t)K * 2;
     r += cnt;
     return true;
   }
 
   /* IT_STAGE: a stage; IT_END: this task has no more; IT_BLOCKED / IT_FAIL */
-  __device__ int emit(Seg *seg, int &nseg, uint32_t &total, bool block, const Ctx &cx) {
+  __device__ int emit(StageDesc &sd, bool block, const Ctx &cx) {
     switch (op) {
       case OP_QKV:
       case OP_ROUTER:
       case OP_LM:
-        return row_stage(seg, nseg, total) ? IT_STAGE : IT_END;
+        return row_stage(sd) ? IT_STAGE : IT_END;
       case OP_ATTN: {
         if (q >= p1) return IT_END;
-        const uint32_t pb = (uint32_t)p->P * p->D * 2;
-        const int cnt = min(mk_pages_per_stage(pb), p1 - q);
-        for (int j = 0; j < cnt; ++j) {
-          const int page = __ldg(p->page_table + b * p->max_pages + q + j);
-          const size_t blk = ((size_t)page * p->Hkv + kvh) * p->P * p->D;
-          seg[2 * j].src = (const uint8_t *)(ly->kc + blk);
-          seg[2 * j + 1].src = (const uint8_t *)(ly->vc + blk);
-          seg[2 * j].off = 2 * j * pb;
-          seg[2 * j + 1].off = (2 * j + 1) * pb;
-          seg[2 * j].bytes = seg[2 * j + 1].bytes = pb;
-        }
-        nseg = 2 * cnt;
-        total = 2 * cnt * pb;
+        const int cnt = min(mk_pages_per_stage(p->P, p->D, SB), p1 - q);
+        sd.kind = SK_PAGES;
+        sd.n = cnt;
+        sd.layer = layer;
+        sd.kvh = kvh;
+        sd.seq = b;
+        sd.q0 = q;
+        /* all page ids of the stage in one batch of independent loads */
+        for (int j = 0; j < cnt; ++j) sd.pages[j] = __ldg(p->page_table + b * p->max_pages + q + j);
         q += cnt;
         return IT_STAGE;
       }
@@ -509,23 +601,20 @@ struct StageIter {
         const int F = p->F, d = p->d;
         const int uu = (int)(v / F), f0 = (int)(v % F);
         const int f1 = (int)min((int64_t)F, f0 + (v1 - v));
-        const uint32_t rb = (uint32_t)d * 2;
-        const int cnt = min(mk_pairs_per_stage(rb), f1 - f0);
+        const int cnt = min(mk_pairs_per_stage(d, SB), f1 - f0);
         const int e = __ldcg(&rt->expert[uu]);
         const size_t eo = (size_t)e * F * d + (size_t)f0 * d;
-        seg[0].src = (const uint8_t *)(ly->wg + eo);
-        seg[1].src = (const uint8_t *)(ly->wu + eo);
-        seg[0].off = 0;
-        seg[1].off = cnt * rb;
-        seg[0].bytes = seg[1].bytes = cnt * rb;
-        nseg = 2;
-        total = 2 * cnt * rb;
+        sd.kind = SK_PAIRS;
+        sd.n = cnt;
+        sd.a = (const uint8_t *)(ly->wg + eo);
+        sd.b = (const uint8_t *)(ly->wu + eo);
+        sd.row_bytes = (uint32_t)d * 2;
         v += cnt;
         return IT_STAGE;
       }
       case OP_OUT: {
         while (true) {
-          if (row_stage(seg, nseg, total)) return IT_STAGE;
+          if (row_stage(sd)) return IT_STAGE;
           if (u == -1) {
             const int rs = routing(block, cx);
             if (rs != IT_STAGE) return rs;
@@ -544,7 +633,7 @@ struct StageIter {
   }
 
   /* The next stage of the stream. */
-  __device__ int next(Seg *seg, int &nseg, uint32_t &total, bool block, const Ctx &cx) {
+  __device__ int next(StageDesc &sd, bool block, const Ctx &cx) {
     while (true) {
       if (at_end()) return IT_END;
       if (!started) {
@@ -552,7 +641,7 @@ struct StageIter {
         if (rs != IT_STAGE) return rs;
         started = true;
       }
-      const int rs = emit(seg, nseg, total, block, cx);
+      const int rs = emit(sd, block, cx);
       if (rs == IT_STAGE) {
         ++count;
         return IT_STAGE;
@@ -566,182 +655,102 @@ struct StageIter {
 struct Producer {
   Ctx cx;
   uint64_t policy;
-  int last_in_slot[MK_MAX_STAGES];
+  int last_in_slot[NC];
 
-  __device__ void run(const int32_t *row) {
-    for (int s = 0; s < MK_MAX_STAGES; ++s) last_in_slot[s] = -1;
-    StageIter ld, pf;
-    ld.init(cx.p, row, cx.epoch);
-    pf.init(cx.p, row, cx.epoch);
-    bool pf_end = false;
-    Seg seg[16];
-    int nseg;
-    uint32_t total;
-    while (true) {
-      /* run the prefetch cursor ahead of the load cursor */
-      while (!pf_end && pf.count < ld.count + MK_PREFETCH_STAGES) {
-        const int rs = pf.next(seg, nseg, total, false, cx);
-        if (rs == IT_STAGE) {
-          if (pf.count > ld.count)
-            for (int j = 0; j < nseg; ++j) prefetch_l2(seg[j].src, seg[j].bytes);
-        } else {
-          if (rs != IT_BLOCKED) pf_end = true;
-          break;
+  __device__ void load(const StageDesc &sd, uint8_t *dst, uint64_t *bar) {
+    const mk_kparams &p = *cx.p;
+    switch (sd.kind) {
+      case SK_ROWS: {
+        const uint32_t bytes = sd.n * sd.row_bytes;
+        mbar_expect_tx(bar, bytes);
+        bulk_g2s(dst, sd.a, bytes, bar, policy);
+        break;
+      }
+      case SK_PAIRS: {
+        const uint32_t bytes = sd.n * sd.row_bytes;
+        mbar_expect_tx(bar, 2 * bytes);
+        bulk_g2s(dst, sd.a, bytes, bar, policy);
+        bulk_g2s(dst + bytes, sd.b, bytes, bar, policy);
+        break;
+      }
+      default: {
+        const int P = p.P;
+        const uint32_t half = (uint32_t)P * p.D * 2, pgb = 2 * half;
+        const uint8_t *kmap = (const uint8_t *)p.kv_maps + (size_t)sd.layer * 2 * 128;
+        const uint8_t *vmap = kmap + 128;
+        mbar_expect_tx(bar, sd.n * pgb);
+        for (int j = 0; j < sd.n; ++j) {
+          const int y = (sd.pages[j] * p.Hkv + sd.kvh) * P;
+          tensor_g2s_3d(dst + j * pgb, kmap, y, bar, policy);
+          tensor_g2s_3d(dst + j * pgb + half, vmap, y, bar, policy);
         }
       }
-      const int rs = ld.next(seg, nseg, total, true, cx);
+    }
+  }
+
+  __device__ __noinline__ void run(const int32_t *row) {
+    for (int s = 0; s < NC; ++s) last_in_slot[s] = -1;
+    StageIter ld;
+    ld.init(cx.p, row, cx.epoch, cx.SB);
+    StageDesc sd;
+    unsigned long long *strc = cx.cta == 0 ? cx.p->stage_trace : nullptr;
+    while (true) {
+      const uint64_t ta = strc ? gtimer() : 0;
+      const int rs = ld.next(sd, true, cx);
       if (rs != IT_STAGE) break; /* end, or a failed wait (already reported) */
       const long i = ld.count - 1;
-      const int slot = (int)(i % cx.nstages);
-      if (i >= cx.nstages) {
-        const uint32_t parity = (uint32_t)(((i / cx.nstages) - 1) & 1);
-        if (!wait_mbar(cx, &cx.m->empty[slot], parity, -1, -1, -1)) break;
+      const int slot = (int)(i % NC);
+      const uint64_t tb = strc ? gtimer() : 0;
+      if (i >= NC) {
+        const uint32_t parity = (uint32_t)(((i / NC) - 1) & 1);
+        if (!wait_mbar(cx, &cx.empty()[slot], parity, -1, -1, -1)) break;
       }
-      uint8_t *dst = cx.ring + (size_t)slot * MK_STAGE_BYTES;
-      uint64_t *bar = &cx.m->full[slot];
-      mbar_expect_tx(bar, total);
-      for (int j = 0; j < nseg; ++j) bulk_g2s(dst + seg[j].off, seg[j].src, seg[j].bytes, bar, policy);
+      const uint64_t tc = strc ? gtimer() : 0;
+      load(sd, cx.ring() + (size_t)slot * cx.SB, &cx.full()[slot]);
       last_in_slot[slot] = (int)i;
+      if (strc && i < MK_STAGE_TRACE_EVENTS) {
+        unsigned long long *e = strc + (size_t)i * 8;
+        e[1] = ta;
+        e[2] = tb;
+        e[3] = tc;
+        e[4] = gtimer();
+      }
     }
     /* Every copy issued must land before the CTA exits (normally the
      * consumers have waited for all of them already). */
-    for (int s = 0; s < cx.nstages; ++s) {
+    for (int s = 0; s < NC; ++s) {
       const int k = last_in_slot[s];
       if (k < 0) continue;
-      const uint32_t parity = (uint32_t)((k / cx.nstages) & 1);
+      const uint32_t parity = (uint32_t)((k / NC) & 1);
       const uint64_t t0 = gtimer();
-      while (!mbar_test(&cx.m->full[s], parity) && gtimer() - t0 < cx.p->wait_limit_ns) {
+      while (!mbar_test(&cx.full()[s], parity) && gtimer() - t0 < cx.p->wait_limit_ns) {
       }
     }
   }
 };
 
 /* ============================================================== consumers
- * Eight warps.  Each warp waits for, reads and releases every ring stage on
- * its own (lane 0 polls the stage's mbarrier, the warp follows), so warps
- * work on different stages at the same time and no CTA-wide barrier sits on
- * the streaming path.  Rows are owned by warps by their index within the
- * task, so every output element has one writer.  A failed wait (time limit
- * or abort) marks the warp; the consumers decide together at the next
- * collective point (a barrier with an OR reduction), so all consumer threads
- * always leave at the same point and no barrier is ever left half-arrived. */
-
-/* Consumer-wide barrier returning the OR of every thread's predicate. */
-__device__ __forceinline__ bool bar_any(bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n"
-      " selp.u32 %0, 1, 0, q;\n}\n"
-      : "=r"(r)
-      : "r"((uint32_t)pred), "n"(NCT)
-      : "memory");
-  return r != 0;
-}
-
-/* acc[r][b] += w_r . x[b] over K elements for R rows sharing the x loads;
- * two accumulators per (row, token) keep the FMA chains short. */
-template <int NB, int R>
-__device__ __forceinline__ void dot_rows(const uint16_t *const (&w)[R], const uint16_t *x,
-                                         int xstride, int K, int lane, float (&acc)[R][NB]) {
-  float a2[R][NB][2];
-#pragma unroll
-  for (int r = 0; r < R; ++r)
-#pragma unroll
-    for (int b = 0; b < NB; ++b) a2[r][b][0] = a2[r][b][1] = 0.0f;
-  for (int c = lane * 8; c < K; c += 256) {
-    uint4 wv[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) wv[r] = *(const uint4 *)(w[r] + c);
-#pragma unroll
-    for (int b = 0; b < NB; ++b) {
-      float xf[8];
-      unpack8(*(const uint4 *)(x + b * xstride + c), xf);
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        float wf[8];
-        unpack8(wv[r], wf);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) a2[r][b][i & 1] = fmaf(wf[i], xf[i], a2[r][b][i & 1]);
-      }
-    }
-  }
-#pragma unroll
-  for (int r = 0; r < R; ++r)
-#pragma unroll
-    for (int b = 0; b < NB; ++b) acc[r][b] = a2[r][b][0] + a2[r][b][1];
-}
-
-__device__ __forceinline__ unsigned long long pack2(uint32_t lo, uint32_t hi) {
-  unsigned long long r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
-  return r;
-}
-
-__device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsigned long long b,
-                                                     unsigned long long c) {
-  unsigned long long d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-
-__device__ __forceinline__ float sum2(unsigned long long v) {
-  uint32_t lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(v));
-  return __uint_as_float(lo) + __uint_as_float(hi);
-}
-
-/* Single-token rows against an fp32 activation (the batch-1 path): the bf16
- * weight pairs become fp32 pairs with one shift and one mask, and packed
- * f32x2 FMAs (two exact fp32 FMAs each) do the products. */
-template <int NB, int R>
-__device__ __forceinline__ void dot_rows(const uint16_t *const (&w)[R], const float *x, int xstride,
-                                         int K, int lane, float (&acc)[R][NB]) {
-  static_assert(NB == 1, "fp32 activations are the batch-1 path");
-  unsigned long long a2[R][2];
-#pragma unroll
-  for (int r = 0; r < R; ++r) a2[r][0] = a2[r][1] = 0ULL;
-  for (int c = lane * 8; c < K; c += 256) {
-    const uint4 xa = *(const uint4 *)(x + c), xb = *(const uint4 *)(x + c + 4);
-    const unsigned long long xp[4] = {pack2(xa.x, xa.y), pack2(xa.z, xa.w), pack2(xb.x, xb.y),
-                                      pack2(xb.z, xb.w)};
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const uint4 wv = *(const uint4 *)(w[r] + c);
-      const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        a2[r][j & 1] = ffma2(pack2(ww[j] << 16, ww[j] & 0xFFFF0000u), xp[j], a2[r][j & 1]);
-    }
-  }
-#pragma unroll
-  for (int r = 0; r < R; ++r) acc[r][0] = sum2(a2[r][0]) + sum2(a2[r][1]);
-}
-
-/* activation element type: fp32 for one token, bf16 bits otherwise */
-template <class XT>
-__device__ __forceinline__ XT to_x(uint16_t bits);
-template <>
-__device__ __forceinline__ float to_x<float>(uint16_t bits) {
-  return bf2f(bits);
-}
-template <>
-__device__ __forceinline__ uint16_t to_x<uint16_t>(uint16_t bits) {
-  return bits;
-}
+ * Eight warps.  Stage i of the CTA's stream belongs to warp i % 8 alone:
+ * its lane 0 polls the stage's mbarrier, the warp computes every row (or
+ * key) of the stage, and lane 0 releases the slot.  Outputs are written by
+ * the warp that owns their stage, so each has one writer.  A failed wait
+ * (time limit or abort) marks the warp; the consumers decide together at the
+ * next collective point (a barrier with an OR reduction), so all consumer
+ * threads always leave at the same point and no barrier is ever left
+ * half-arrived. */
 
 template <int NB>
 struct Consumer {
-  using XT = typename std::conditional<NB == 1, float, uint16_t>::type;
   Ctx cx;
   int warp, lane, tid;
-  int si;     /* stages consumed (the same sequence in every warp) */
+  int si;     /* stages of the stream before the current task (all warps agree) */
   bool wfail; /* this warp failed a stage wait */
   unsigned long long *tr; /* this CTA's trace events, or NULL */
   int tr_n;
   uint64_t t_ready, t_stage, t_swait, t_mark;
   int n_stages;
 
-  static constexpr int ROWS = NB <= 2 ? 2 : 1; /* rows per dot pass */
+  __device__ __forceinline__ Misc<NB> *M() const { return (Misc<NB> *)(mk_smem + cx.misc_off); }
 
   /* Thread 0 waits on a counter; every consumer learns whether the CTA goes
    * on (false also when any warp has failed a stage wait). */
@@ -758,20 +767,34 @@ struct Consumer {
    * failed. */
   __device__ bool task_end() { return !bar_any(wfail); }
 
-  __device__ bool stage_wait(uint8_t *&st, int task, int op, int layer) {
+  /* The first stage index j >= 0 of a task (stream stage si + j) that this
+   * warp owns. */
+  __device__ int first_mine() const { return (warp - si % NC + NC) % NC; }
+
+  __device__ bool stage_wait(int i, uint8_t *&st, int task, int op, int layer) {
     if (wfail) return false;
-    const int slot = si % cx.nstages;
-    const uint32_t parity = (uint32_t)((si / cx.nstages) & 1);
+    const int slot = i % NC;
+    const uint32_t parity = (uint32_t)((i / NC) & 1);
     int ok = 1;
     if (lane == 0) {
       const bool trace = tr && warp == 0;
-      const uint64_t w0 = trace ? gtimer() : 0;
-      ok = wait_mbar(cx, &cx.m->full[slot], parity, task, op, layer) ? 1 : 0;
-      if (trace) {
+      unsigned long long *se =
+          (tr && cx.cta == 0 && i < MK_STAGE_TRACE_EVENTS) ? cx.p->stage_trace + (size_t)i * 8
+                                                            : nullptr;
+      const uint64_t w0 = (trace || se) ? gtimer() : 0;
+      ok = wait_mbar(cx, &cx.full()[slot], parity, task, op, layer) ? 1 : 0;
+      if (trace || se) {
         const uint64_t w1 = gtimer();
-        if (!t_stage) t_stage = w1;
-        else t_swait += w1 - w0;
-        ++n_stages;
+        if (trace) {
+          if (!t_stage) t_stage = w1;
+          else t_swait += w1 - w0;
+          ++n_stages;
+        }
+        if (se) {
+          se[0] = (unsigned long long)(i | (warp << 20) | (op << 24));
+          se[5] = w0;
+          se[6] = w1;
+        }
       }
     }
     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -779,15 +802,17 @@ struct Consumer {
       wfail = true;
       return false;
     }
-    mbar_test(&cx.m->full[slot], parity); /* completed: acquire order for this thread */
-    st = cx.ring + (size_t)slot * MK_STAGE_BYTES;
+    mbar_test(&cx.full()[slot], parity); /* completed: acquire order for this thread */
+    st = cx.ring() + (size_t)slot * cx.SB;
     return true;
   }
 
-  __device__ void stage_release() {
+  __device__ void stage_release(int i) {
     __syncwarp();
-    if (lane == 0) mbar_arrive(&cx.m->empty[si % cx.nstages]);
-    ++si;
+    if (lane == 0) {
+      mbar_arrive(&cx.empty()[i % NC]);
+      if (tr && cx.cta == 0 && i < MK_STAGE_TRACE_EVENTS) cx.p->stage_trace[(size_t)i * 8 + 7] = gtimer();
+    }
   }
 
   __device__ const uint16_t *h_row(int layer, int b) const {
@@ -801,28 +826,29 @@ struct Consumer {
     for (int b = 0; b < NB; ++b) {
       float s = v[b];
 #pragma unroll
-      for (int m = 16; m >= 1; m >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, m);
-      if (lane == 0) cx.m->red[warp][b] = s;
+      for (int k = 16; k >= 1; k >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, k);
+      if (lane == 0) M()->red[warp][b] = s;
     }
     bar_consumers();
     if (tid < NB) {
       float s = 0.0f;
-      for (int w = 0; w < NC; ++w) s += cx.m->red[w][tid];
-      cx.m->rsum[tid] = s;
+      for (int w = 0; w < NC; ++w) s += M()->red[w][tid];
+      M()->rsum[tid] = s;
     }
     bar_consumers();
 #pragma unroll
-    for (int b = 0; b < NB; ++b) v[b] = cx.m->rsum[b];
+    for (int b = 0; b < NB; ++b) v[b] = M()->rsum[b];
     bar_consumers();
   }
 
-  /* xbuf[b][0..d) = bf16((h * (1/sqrtf(mean_fp32(h^2) + eps))) * g) as XT;
-   * rows b >= B zero.  h is read once with 16-byte loads and staged behind
-   * the output in xbuf. */
+  /* xbuf[b][0..d) (pitch d + 32) = bf16((h * (1/sqrtf(mean_fp32(h^2) +
+   * eps))) * g); rows b >= B zero.  h is read once with 16-byte loads and
+   * staged behind the output in xbuf. */
   __device__ void norm_into_xbuf(int layer_tag, const uint16_t *const *hrows, const uint16_t *g) {
     const mk_kparams &p = *cx.p;
-    XT *x = (XT *)cx.xbuf;
-    uint16_t *raw = (uint16_t *)(cx.xbuf + (size_t)NB * p.d * sizeof(XT));
+    const int xp = mk_x_pitch(p.d);
+    uint16_t *x = (uint16_t *)cx.xbuf();
+    uint16_t *raw = x + (size_t)NB * xp;
     const int n8 = p.d / 8;
     float ss[NB];
 #pragma unroll
@@ -843,27 +869,28 @@ struct Consumer {
     for (int b = 0; b < NB; ++b) {
       const float r = 1.0f / sqrtf(ss[b] / (float)p.d + p.eps);
       for (int i = tid; i < n8; i += NCT) {
-        XT o[8];
+        uint16_t o[8];
         if (b < p.B) {
           float hf[8], gf[8];
           unpack8(*(const uint4 *)(raw + (size_t)b * p.d + 8 * i), hf);
           unpack8(__ldg((const uint4 *)g + i), gf);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) o[k] = to_x<XT>(f2bf(__fmul_rn(__fmul_rn(hf[k], r), gf[k])));
+          for (int k = 0; k < 8; ++k) o[k] = f2bf(__fmul_rn(__fmul_rn(hf[k], r), gf[k]));
         } else {
 #pragma unroll
-          for (int k = 0; k < 8; ++k) o[k] = to_x<XT>(0);
+          for (int k = 0; k < 8; ++k) o[k] = 0;
         }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) x[(size_t)b * p.d + 8 * i + k] = o[k];
+        *(uint4 *)(x + (size_t)b * xp + 8 * i) =
+            make_uint4(pack_bf16(o[0], o[1]), pack_bf16(o[2], o[3]), pack_bf16(o[4], o[5]),
+                       pack_bf16(o[6], o[7]));
       }
     }
-    if (tid == 0) cx.m->norm_layer = layer_tag;
+    if (tid == 0) M()->norm_layer = layer_tag;
     bar_consumers();
   }
 
   __device__ void ensure_norm(int layer) {
-    if (*(volatile int32_t *)&cx.m->norm_layer == layer) return;
+    if (*(volatile int32_t *)&M()->norm_layer == layer) return;
     struct Mark {
       Consumer *c;
       __device__ ~Mark() {
@@ -879,7 +906,19 @@ struct Consumer {
 
   __device__ void invalidate_norm() {
     bar_consumers();
-    if (tid == 0) cx.m->norm_layer = -2;
+    if (tid == 0) M()->norm_layer = -2;
+  }
+
+  /* Copies NB vectors of n bf16 (global, row stride gstride) into xbuf at
+   * pitch n + 32; rows b >= B zero.  No barrier. */
+  __device__ void load_x(uint16_t *dst, const uint16_t *src, size_t gstride, int n) {
+    const int xp = mk_x_pitch(n), n8 = n / 8, B = cx.p->B;
+    for (int i = tid; i < NB * n8; i += NCT) {
+      const int b = i / n8, c = i % n8;
+      const uint4 v = b < B ? __ldcg((const uint4 *)(src + (size_t)b * gstride) + c)
+                            : make_uint4(0, 0, 0, 0);
+      *(uint4 *)(dst + (size_t)b * xp + 8 * c) = v;
+    }
   }
 
   /* After task_end(): thread 0 releases the downstream counter. */
@@ -902,52 +941,27 @@ struct Consumer {
     return bar_any(last);
   }
 
-  /* Reduce R rows' NB sums across the warp and hand them to epi(row, b, v)
-   * on the lane that owns token b. */
-  template <int R, class Epi>
-  __device__ __forceinline__ void finish_rows(float (&acc)[R][NB], const int (&rows)[R], Epi &epi) {
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const float s = transpose_reduce<NB>(acc[r], lane);
-      if (reduce_leader<NB>(lane)) epi(rows[r], reduce_token<NB>(lane), s);
-    }
-  }
-
-  /* nrows streamed rows of K elements; row r (index within the task) is
-   * computed by warp r % 8 and handed to epi(r, b, value). */
+  /* nrows streamed rows of K elements against the activations x (pitch
+   * K + 32); each stage is computed by the warp that owns it and row r
+   * (index within the task) handed to epi(r, b, value). */
   template <class Epi>
-  __device__ void gemv_task(int nrows, int K, const XT *x, int xstride, int task, int op,
-                            int layer, Epi epi) {
-    const int rps = mk_rows_per_stage(K * 2);
-    for (int r0 = 0; r0 < nrows; r0 += rps) {
-      const int cnt = min(rps, nrows - r0);
+  __device__ void gemv_rows(int nrows, int K, const uint16_t *x, int task, int op, int layer,
+                            Epi &&epi) {
+    const int rps = mk_rows_per_stage(K, cx.SB), pitch = mk_row_pitch(K), xp = mk_x_pitch(K);
+    const int n_st = (nrows + rps - 1) / rps;
+    for (int j = first_mine(); j < n_st; j += NC) {
       uint8_t *st;
-      if (!stage_wait(st, task, op, layer)) return;
-      const uint16_t *w = (const uint16_t *)st;
-      int j = ((warp - r0) % NC + NC) % NC;
-      if (ROWS == 2) {
-        for (; j + NC < cnt; j += 2 * NC) {
-          float acc[ROWS][NB];
-          const uint16_t *wr[ROWS];
-          int rr[ROWS];
-#pragma unroll
-          for (int r = 0; r < ROWS; ++r) {
-            wr[r] = w + (size_t)(j + r * NC) * K;
-            rr[r] = r0 + j + r * NC;
-          }
-          dot_rows<NB, ROWS>(wr, x, xstride, K, lane, acc);
-          finish_rows<ROWS>(acc, rr, epi);
-        }
-      }
-      for (; j < cnt; j += NC) {
-        float acc[1][NB];
-        const uint16_t *wr[1] = {w + (size_t)j * K};
-        const int rr[1] = {r0 + j};
-        dot_rows<NB, 1>(wr, x, xstride, K, lane, acc);
-        finish_rows<1>(acc, rr, epi);
-      }
-      stage_release();
+      if (!stage_wait(si + j, st, task, op, layer)) break;
+      const int r0 = j * rps, cnt = min(rps, nrows - r0);
+      mma_rows<NB>(st, cnt, pitch, K, x, xp, lane, [](int v) { return v; },
+                   [&](int n0, const float(&a)[4], const float(&b)[4], bool two) {
+                     auto f = [&](int r, int bb, float v) { epi(r0 + r, bb, v); };
+                     take_out<NB>(n0, a, cnt, lane, f);
+                     if (two) take_out<NB>(n0 + 8, b, cnt, lane, f);
+                   });
+      stage_release(si + j);
     }
+    si += n_st;
   }
 
   /* ---------------------------------------------------------------- QKV */
@@ -961,7 +975,7 @@ struct Consumer {
     const int base = (t[1] == 0 ? 0 : t[1] == 1 ? p.Hq * p.D : (p.Hq + p.Hkv) * p.D) + t[2];
     uint16_t *out = p.qkv + (size_t)layer * MK_MAX_BATCH * QKVD;
     const int B = p.B;
-    gemv_task(t[3], p.d, (const XT *)cx.xbuf, p.d, task, OP_QKV, layer,
+    gemv_rows(t[3], p.d, (const uint16_t *)cx.xbuf(), task, OP_QKV, layer,
               [&](int r, int b, float v) {
                 if (b < B) out[(size_t)b * QKVD + base + r] = f2bf(v);
               });
@@ -981,7 +995,7 @@ struct Consumer {
     float *lg = p.router_logits + (size_t)layer * MK_MAX_BATCH * p.E;
     const float *bias = p.layers[layer].bias;
     const int B = p.B, E = p.E;
-    gemv_task(t[3], p.d, (const XT *)cx.xbuf, p.d, task, OP_ROUTER, layer,
+    gemv_rows(t[3], p.d, (const uint16_t *)cx.xbuf(), task, OP_ROUTER, layer,
               [&](int r, int b, float v) {
                 if (b < B) lg[(size_t)b * E + e0 + r] = bias ? v + __ldg(bias + e0 + r) : v;
               });
@@ -1004,7 +1018,7 @@ struct Consumer {
     const mk_kparams &p = *cx.p;
     mk_routing *rt = p.routing + layer;
     const float *lg = p.router_logits + (size_t)layer * MK_MAX_BATCH * p.E;
-    auto &R = cx.m->u.rt;
+    auto &R = M()->u.rt;
     if (tid < 4) R.used[tid] = 0;
     bar_consumers();
     if (warp < p.B) {
@@ -1014,13 +1028,13 @@ struct Consumer {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         id[i] = lane + 32 * i;
-        v[i] = id[i] < p.E ? __ldcg(lg + (size_t)b * p.E + id[i]) : -INFINITY;
+        v[i] = id[i] < p.E ? __ldcg(lg + (size_t)b * p.E + id[i]) : NEG_INF;
         if (id[i] >= p.E) id[i] = 0x40000000;
       }
       float top_v[MK_MAX_TOPK];
       int top_i[MK_MAX_TOPK];
       for (int k = 0; k < p.K; ++k) {
-        float bv = -INFINITY;
+        float bv = NEG_INF;
         int bi = 0x7FFFFFFF;
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -1029,9 +1043,9 @@ struct Consumer {
             bi = id[i];
           }
 #pragma unroll
-        for (int m = 16; m >= 1; m >>= 1) {
-          const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, m);
-          const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, m);
+        for (int s = 16; s >= 1; s >>= 1) {
+          const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, s);
+          const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, s);
           if (ov > bv || (ov == bv && oi < bi)) {
             bv = ov;
             bi = oi;
@@ -1078,40 +1092,56 @@ struct Consumer {
       atomicAdd(&p.ctrl->sum_experts, (unsigned long long)U);
     }
   }
+
   /* ---------------------------------------------------------- attention
-   * Split-K flash decoding over the pages of one (sequence, kv head).  Lane
-   * l owns head dims [l*DPL, (l+1)*DPL) of all 8 head slots; the 8 partial
-   * dot products of a key are summed across lanes in 9 shuffles, leaving
-   * head slot (l >> 2) & 7 on lane l. */
-  __device__ bool op_attn(const int32_t *t, int task, int layer) {
+   * Split-K flash decoding over the pages of one (sequence, kv head).  Each
+   * warp runs the online softmax over the stages it owns on the tensor
+   * cores: per 16-key tile, S = Q K^T (A = the group's query heads in rows
+   * 0..G-1, B = the K tile read with ldmatrix from the swizzled boxes), then
+   * O += P V (A = P in the accumulator layout of S: rows 0..7 its bf16
+   * rounding, rows 8..15 the rounding error, so C rows g and g + 8 add up to
+   * P V with about 16 significant bits of P; B = the V tile read with a
+   * transposing ldmatrix).  Thread (g, t) owns
+   * head g: S of keys 2t, 2t+1 of each 8-key half, O of dims 8n + 2t, +1. */
+  template <int D>
+  __device__ __noinline__ bool op_attn(const int32_t *t, int task, int layer) {
+    constexpr int KS = D / 16;           /* k-steps of Q K^T; V n-tile pairs */
+    constexpr int NT = D / 8;            /* n-tiles of O */
+    constexpr int BI = D < 64 ? D : 64;  /* box inner size (head dims) */
+    constexpr int NBOX = D / BI;
+    constexpr int CPB = BI / 8;          /* 16-byte chunks per box row */
+    constexpr int ROWB = BI * 2;         /* bytes per box row */
+    constexpr bool SWZ = D >= 64;        /* 128-byte swizzle */
+    constexpr int GC = 2;                /* 16-key tiles per softmax update */
     const mk_kparams &p = *cx.p;
     const int b = t[1], kvh = t[2], p0 = t[3], last = t[8];
-    const int D = p.D, G = p.Hq / p.Hkv, P = p.P, half = D / 2;
+    const int G = p.Hq / p.Hkv, P = p.P, half = D / 2;
     const int L_now = __ldg(p.seq_lens + b);
     const int p1 = t[4] >= 0 ? t[4] : (L_now + P - 1) / P;
     if (!cwait(lctr(p, layer, CTR_QKV_DONE), (int)((cx.epoch + 1) * p.n_qkv), task, OP_ATTN,
                layer, CTR_QKV_DONE))
       return false;
     invalidate_norm();
-    float *qs = (float *)cx.xbuf; /* [8][D] */
-    float *ks = qs + 8 * D;       /* [D] */
-    float *vs = ks + D;           /* [D] */
-    float *mb = vs + D;           /* merge exchange [4][8][D] */
+    constexpr int QP = D + 8;                     /* q row pitch: conflict-free fragment loads */
+    uint16_t *qs = (uint16_t *)cx.xbuf();           /* [8][QP] post-RoPE q, bf16 */
+    float *ks = (float *)(cx.xbuf() + 16 * QP);     /* [D] new key */
+    float *vs = ks + D;                           /* [D] new value */
+    float *mb = vs + D;                           /* warp merge [4][8][D + 8] */
     const int QKVD = (p.Hq + 2 * p.Hkv) * D;
     const uint16_t *qkv = p.qkv + ((size_t)layer * MK_MAX_BATCH + b) * QKVD;
     const float *rp = p.rope + (size_t)L_now * half * 2;
     for (int i = tid; i < 8 * half; i += NCT) {
       const int g = i / half, j = i % half;
-      float o1 = 0.0f, o2 = 0.0f;
+      uint16_t o1 = 0, o2 = 0;
       if (g < G) {
         const uint16_t *src = qkv + (size_t)(kvh * G + g) * D;
         const float x1 = bf2f(__ldcg(src + j)), x2 = bf2f(__ldcg(src + j + half));
         const float c = __ldg(rp + 2 * j), s = __ldg(rp + 2 * j + 1);
-        o1 = rbf(__fmul_rn(x1, c) - __fmul_rn(x2, s));
-        o2 = rbf(__fmul_rn(x2, c) + __fmul_rn(x1, s));
+        o1 = f2bf(__fmul_rn(x1, c) - __fmul_rn(x2, s));
+        o2 = f2bf(__fmul_rn(x2, c) + __fmul_rn(x1, s));
       }
-      qs[g * D + j] = o1;
-      qs[g * D + j + half] = o2;
+      qs[g * QP + j] = o1;
+      qs[g * QP + j + half] = o2;
     }
     if (last) {
       const uint16_t *ksrc = qkv + (size_t)(p.Hq + kvh) * D;
@@ -1137,157 +1167,177 @@ struct Consumer {
     }
     bar_consumers();
 
-    const int DPL = D / 32;
-    float qr[8][4], orr[8][4];
+    const int g = lane >> 2, tq = lane & 3, mi = lane >> 3, rr = lane & 7;
+    /* A fragments of Q: head g, dims 16j + 2t (+1) and 16j + 2t + 8 (+9) */
+    const uint32_t *qf = (const uint32_t *)(qs + g * QP + 2 * tq);
+    float o[NT][4];
 #pragma unroll
-    for (int g = 0; g < 8; ++g)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        qr[g][i] = i < DPL ? qs[g * D + lane * DPL + i] : 0.0f;
-        orr[g][i] = 0.0f;
-      }
-    const int hg = (lane >> 2) & 7;
-    float m_run = -INFINITY, l_run = 0.0f;
+    for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
+    float m_run = NEG_INF, l_run = 0.0f;
     const float scale = p.attn_scale;
-    auto &A = cx.m->u.at;
 
-    const uint16_t *kr[8], *vr[8];
-    /* nt <= 8 keys, all valid: rows kr/vr in shared memory, or (newkey) the
-     * new token's fp32 k and v vectors */
-    auto block = [&](int nt, bool newkey) {
-      float s_t[8];
-#pragma unroll
-      for (int tt = 0; tt < 8; ++tt) {
-        s_t[tt] = -INFINITY;
-        if (tt < nt) {
-          float kv[4];
-          if (newkey) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) kv[i] = i < DPL ? ks[lane * DPL + i] : 0.0f;
-          } else {
-            lane_dims(kr[tt], lane, DPL, kv);
-          }
-          float part[8];
-#pragma unroll
-          for (int g = 0; g < 8; ++g) {
-            float a = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) a = fmaf(qr[g][i], kv[i], a);
-            part[g] = a;
-          }
-          s_t[tt] = transpose_reduce<8>(part, lane) * scale;
-        }
-      }
-      float mnew = m_run;
-#pragma unroll
-      for (int tt = 0; tt < 8; ++tt) mnew = fmaxf(mnew, s_t[tt]);
-      const float alpha = (m_run == -INFINITY) ? 0.0f : expf(m_run - mnew);
-      float lsum = 0.0f;
-#pragma unroll
-      for (int tt = 0; tt < 8; ++tt) {
-        const float pv = (s_t[tt] == -INFINITY) ? 0.0f : expf(s_t[tt] - mnew);
-        s_t[tt] = pv;
-        lsum += pv;
-      }
-      l_run = l_run * alpha + lsum;
-      m_run = mnew;
-      if ((lane & 3) == 0) {
-#pragma unroll
-        for (int tt = 0; tt < 8; ++tt) A.pw[warp][tt][hg] = s_t[tt];
-        A.alpha[warp][hg] = alpha;
-      }
-      __syncwarp();
-      {
-        const float4 a0 = *(const float4 *)&A.alpha[warp][0];
-        const float4 a1 = *(const float4 *)&A.alpha[warp][4];
-        const float al[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-#pragma unroll
-        for (int g = 0; g < 8; ++g)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) orr[g][i] *= al[g];
-      }
-#pragma unroll
-      for (int tt = 0; tt < 8; ++tt) {
-        if (tt < nt) {
-          float vv[4];
-          if (newkey) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) vv[i] = i < DPL ? vs[lane * DPL + i] : 0.0f;
-          } else {
-            lane_dims(vr[tt], lane, DPL, vv);
-          }
-          const float4 p0v = *(const float4 *)&A.pw[warp][tt][0];
-          const float4 p1v = *(const float4 *)&A.pw[warp][tt][4];
-          const float pg[8] = {p0v.x, p0v.y, p0v.z, p0v.w, p1v.x, p1v.y, p1v.z, p1v.w};
-#pragma unroll
-          for (int g = 0; g < 8; ++g)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) orr[g][i] = fmaf(pg[g], vv[i], orr[g][i]);
-        }
-      }
-      __syncwarp();
+    const int pps = mk_pages_per_stage(P, D, cx.SB), pgb = mk_page_stage_bytes(P, D);
+    const int kvb = P * D * 2; /* one page's K (or V) box */
+    /* byte offset of 16-byte chunk C (head dims 8C..8C+7) of token row r in a
+     * box: 128-byte rows of BI dims, row index r * NBOX + C / CPB, chunks
+     * XOR-swizzled by the row index mod 8 (the TMA 128-byte pattern) */
+    auto boff = [&](int r, int C) -> uint32_t {
+      const int r128 = r * NBOX + C / CPB, cb = C % CPB;
+      return r128 * ROWB + ((SWZ ? (cb ^ (r128 & 7)) : cb) << 4);
     };
-
-    const uint32_t pb = (uint32_t)P * D * 2;
-    const int pps = mk_pages_per_stage(pb);
-    for (int q0 = p0; q0 < p1; q0 += pps) {
-      const int cnt = min(pps, p1 - q0);
+    const int n_st = (p1 - p0 + pps - 1) / pps;
+    for (int j = first_mine(); j < n_st; j += NC) {
       uint8_t *st;
-      if (!stage_wait(st, task, OP_ATTN, layer)) break;
-      const int nkeys = cnt * P;
-      const int valid_end = L_now - q0 * P;
-      int nt = 0;
-      for (int kk = warp; kk < nkeys; kk += NC) {
-        if (kk < valid_end) {
-          const int pg = kk / P, sl = kk % P;
-          kr[nt] = (const uint16_t *)(st + 2 * pg * pb) + (size_t)sl * D;
-          vr[nt] = (const uint16_t *)(st + (2 * pg + 1) * pb) + (size_t)sl * D;
-          ++nt;
+      if (!stage_wait(si + j, st, task, OP_ATTN, layer)) break;
+      const int q0 = p0 + j * pps, cnt = min(pps, p1 - q0);
+      const int valid = min(cnt * P, L_now - q0 * P); /* cached keys in this stage */
+      const uint32_t sb = saddr(st);
+      for (int k0 = 0; k0 < valid; k0 += 16 * GC) {
+        const int ng = min(GC, (valid - k0 + 15) / 16); /* 16-key tiles in this chunk */
+        float s[GC][2][4];
+#pragma unroll
+        for (int gi = 0; gi < GC; ++gi) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) s[gi][h][0] = s[gi][h][1] = s[gi][h][2] = s[gi][h][3] = 0.0f;
+          if (gi < ng) {
+            const int kk0 = k0 + 16 * gi, pg = kk0 / P, r0 = kk0 % P;
+            const uint32_t kb = sb + pg * pgb;
+            const int kr = r0 + (mi >> 1) * 8 + rr;
+#pragma unroll
+            for (int jj = 0; jj < KS; ++jj) {
+              uint32_t r4[4];
+              ldsm4(r4, kb + boff(kr, 2 * jj + (mi & 1)));
+              const uint32_t qa0 = qf[8 * jj], qa1 = qf[8 * jj + 4];
+              mma16816(s[gi][0], qa0, 0u, qa1, 0u, r4[0], r4[1]);
+              mma16816(s[gi][1], qa0, 0u, qa1, 0u, r4[2], r4[3]);
+            }
+          }
         }
-        if (nt == 8) {
-          block(8, false);
-          nt = 0;
+        float mx = NEG_INF;
+#pragma unroll
+        for (int gi = 0; gi < GC; ++gi)
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int key = k0 + 16 * gi + 8 * h + 2 * tq + e;
+              const float v = (gi < ng && key < valid) ? s[gi][h][e] * scale : NEG_INF;
+              s[gi][h][e] = v;
+              mx = fmaxf(mx, v);
+            }
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+        const float m_new = fmaxf(m_run, mx);
+        const float alpha = m_run == NEG_INF ? 0.0f : expf(m_run - m_new);
+        l_run *= alpha;
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          o[n][0] *= alpha;
+          o[n][1] *= alpha;
+          o[n][2] *= alpha;
+          o[n][3] *= alpha;
+        }
+        m_run = m_new;
+#pragma unroll
+        for (int gi = 0; gi < GC; ++gi) {
+          if (gi < ng) {
+            /* A rows g: the bf16 part of P; rows g + 8: what bf16 lost */
+            uint32_t ah[2], al[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              uint16_t hb[2], lb[2];
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const float sv = s[gi][h][e];
+                const float pv = sv == NEG_INF ? 0.0f : expf(sv - m_new);
+                l_run += pv;
+                hb[e] = f2bf(pv);
+                lb[e] = f2bf(pv - bf2f(hb[e]));
+              }
+              ah[h] = pack_bf16(hb[0], hb[1]);
+              al[h] = pack_bf16(lb[0], lb[1]);
+            }
+            const int kk0 = k0 + 16 * gi, pg = kk0 / P, r0 = kk0 % P;
+            const uint32_t vb = sb + pg * pgb + kvb;
+            const int vr = r0 + (mi & 1) * 8 + rr;
+#pragma unroll
+            for (int i = 0; i < KS; ++i) {
+              uint32_t v4[4];
+              ldsm4_t(v4, vb + boff(vr, 2 * i + (mi >> 1)));
+              if (kk0 + 16 > valid) {
+                /* rows past the live length may hold anything (even NaN,
+                 * which a zero probability would not cancel): zero them */
+                const int ka = kk0 + 2 * tq;
+                const uint32_t m0 = (ka < valid ? 0xFFFFu : 0u) | (ka + 1 < valid ? 0xFFFF0000u : 0u);
+                const uint32_t m1 =
+                    (ka + 8 < valid ? 0xFFFFu : 0u) | (ka + 9 < valid ? 0xFFFF0000u : 0u);
+                v4[0] &= m0;
+                v4[2] &= m0;
+                v4[1] &= m1;
+                v4[3] &= m1;
+              }
+              mma16816(o[2 * i], ah[0], al[0], ah[1], al[1], v4[0], v4[1]);
+              mma16816(o[2 * i + 1], ah[0], al[0], ah[1], al[1], v4[2], v4[3]);
+            }
+          }
         }
       }
-      if (nt > 0) block(nt, false);
-      stage_release();
+      stage_release(si + j);
     }
+    si += n_st;
     if (tr && tid == 0) t_mark = gtimer();
-    if (last && warp == 0) block(1, true);
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      o[n][0] += o[n][2];
+      o[n][1] += o[n][3];
+    }
+    if (last && warp == 0) {
+      /* the new token's own key and value (not in the cache stream) */
+      float sp = 0.0f;
+      for (int d = tq; d < D; d += 4) sp = fmaf(bf2f(qs[g * QP + d]), ks[d], sp);
+      sp += __shfl_xor_sync(0xFFFFFFFFu, sp, 1);
+      sp += __shfl_xor_sync(0xFFFFFFFFu, sp, 2);
+      const float sn = sp * scale;
+      const float m_new = fmaxf(m_run, sn);
+      const float alpha = m_run == NEG_INF ? 0.0f : expf(m_run - m_new);
+      const float pn = expf(sn - m_new);
+      l_run = l_run * alpha + (tq == 0 ? pn : 0.0f);
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        o[n][0] = fmaf(pn, vs[8 * n + 2 * tq], o[n][0] * alpha);
+        o[n][1] = fmaf(pn, vs[8 * n + 2 * tq + 1], o[n][1] * alpha);
+      }
+      m_run = m_new;
+    }
+    l_run += __shfl_xor_sync(0xFFFFFFFFu, l_run, 1);
+    l_run += __shfl_xor_sync(0xFFFFFFFFu, l_run, 2);
 
     /* merge warp states pairwise: 8 -> 4 -> 2 -> 1 */
     for (int hw = NC / 2; hw >= 1; hw >>= 1) {
       bar_consumers();
       if (warp >= hw && warp < 2 * hw) {
         const int s = warp - hw;
-        if ((lane & 3) == 0) {
-          A.m[s][hg] = m_run;
-          A.l[s][hg] = l_run;
+        if (tq == 0) {
+          M()->am[s][g] = m_run;
+          M()->al[s][g] = l_run;
         }
+        float *dst = mb + (size_t)(s * 8 + g) * (D + 8) + 2 * tq;
 #pragma unroll
-        for (int g = 0; g < 8; ++g)
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            if (i < DPL) mb[((size_t)s * 8 + g) * D + lane * DPL + i] = orr[g][i];
+        for (int n = 0; n < NT; ++n) *(float2 *)(dst + 8 * n) = make_float2(o[n][0], o[n][1]);
       }
       bar_consumers();
       if (warp < hw) {
-        const float m2 = A.m[warp][hg], l2 = A.l[warp][hg];
+        const float m2 = M()->am[warp][g], l2 = M()->al[warp][g];
         const float M = fmaxf(m_run, m2);
-        const float f1 = m_run == -INFINITY ? 0.0f : expf(m_run - M);
-        const float f2 = m2 == -INFINITY ? 0.0f : expf(m2 - M);
+        const float f1 = m_run == NEG_INF ? 0.0f : expf(m_run - M);
+        const float f2 = m2 == NEG_INF ? 0.0f : expf(m2 - M);
         l_run = f1 * l_run + f2 * l2;
+        const float *src = mb + (size_t)(warp * 8 + g) * (D + 8) + 2 * tq;
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const float mg1 = __shfl_sync(0xFFFFFFFFu, m_run, g * 4);
-          const float mg2 = A.m[warp][g];
-          const float Mg = fmaxf(mg1, mg2);
-          const float a1 = mg1 == -INFINITY ? 0.0f : expf(mg1 - Mg);
-          const float a2 = mg2 == -INFINITY ? 0.0f : expf(mg2 - Mg);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            if (i < DPL)
-              orr[g][i] = a1 * orr[g][i] + a2 * mb[((size_t)warp * 8 + g) * D + lane * DPL + i];
+        for (int n = 0; n < NT; ++n) {
+          const float2 v = *(const float2 *)(src + 8 * n);
+          o[n][0] = f1 * o[n][0] + f2 * v.x;
+          o[n][1] = f1 * o[n][1] + f2 * v.y;
         }
         m_run = M;
       }
@@ -1295,27 +1345,23 @@ struct Consumer {
     /* warp 0 holds this split's partial: per head [m, l, -, -, o[D]] */
     const int PS = D + 4;
     float *part = p.attn_part + ((size_t)layer * p.n_slots + t[5]) * G * PS;
-    if (warp == 0) {
-#pragma unroll
-      for (int g = 0; g < 8; ++g)
-        if (g < G) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            if (i < DPL) part[(size_t)g * PS + 4 + lane * DPL + i] = orr[g][i];
-        }
-      if ((lane & 3) == 0 && hg < G) {
-        part[(size_t)hg * PS] = m_run;
-        part[(size_t)hg * PS + 1] = l_run;
+    if (warp == 0 && g < G) {
+      if (tq == 0) {
+        part[(size_t)g * PS] = m_run;
+        part[(size_t)g * PS + 1] = l_run;
       }
+#pragma unroll
+      for (int n = 0; n < NT; ++n)
+        *(float2 *)(part + (size_t)g * PS + 4 + 8 * n + 2 * tq) = make_float2(o[n][0], o[n][1]);
     }
     /* the last split of (b, kvh) to finish merges all splits:
      * o = sum_s f_s o_s with f_s = e^{m_s - M} / sum_s' e^{m_s' - M} l_s' */
     if (!task_end()) return false;
     if (!ticket(lctr(p, layer, CTR_ATTN_TICKET0 + b * p.Hkv + kvh), t[7])) return true;
     const float *parts = p.attn_part + ((size_t)layer * p.n_slots + t[6]) * G * PS;
-    uint16_t *o = p.o + ((size_t)layer * MK_MAX_BATCH + b) * p.Hq * D + (size_t)kvh * G * D;
+    uint16_t *ob = p.o + ((size_t)layer * MK_MAX_BATCH + b) * p.Hq * D + (size_t)kvh * G * D;
     const int ns = t[7];
-    float *fm = (float *)cx.xbuf;          /* [ns][G] m, then factors */
+    float *fm = (float *)cx.xbuf();          /* [ns][G] m, then factors */
     float *fl = fm + ns * G;               /* [ns][G] l */
     float *hd = fl + ns * G;               /* [G] max, [G] 1 / denominator */
     for (int i = tid; i < ns * G; i += NCT) {
@@ -1324,28 +1370,28 @@ struct Consumer {
     }
     bar_consumers();
     if (tid < G) {
-      float M = -INFINITY;
+      float M = NEG_INF;
       for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, fm[s2 * G + tid]);
       float den = 0.0f;
       for (int s2 = 0; s2 < ns; ++s2) {
         const float ms = fm[s2 * G + tid];
-        if (ms != -INFINITY) den = fmaf(expf(ms - M), fl[s2 * G + tid], den);
+        if (ms != NEG_INF) den = fmaf(expf(ms - M), fl[s2 * G + tid], den);
       }
       hd[tid] = M;
       hd[G + tid] = 1.0f / den;
     }
     bar_consumers();
     for (int i = tid; i < ns * G; i += NCT) {
-      const int g = i % G;
+      const int gg = i % G;
       const float ms = fm[i];
-      fm[i] = ms == -INFINITY ? 0.0f : expf(ms - hd[g]) * hd[G + g];
+      fm[i] = ms == NEG_INF ? 0.0f : expf(ms - hd[gg]) * hd[G + gg];
     }
     bar_consumers();
     const int D4 = D / 4;
     for (int i = tid; i < G * D4; i += NCT) {
-      const int g = i / D4, j4 = i % D4;
+      const int gg = i / D4, j4 = i % D4;
       float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-      const float4 *src = (const float4 *)(parts + (size_t)g * PS + 4) + j4;
+      const float4 *src = (const float4 *)(parts + (size_t)gg * PS + 4) + j4;
       int s2 = 0;
       for (; s2 + 8 <= ns; s2 += 8) {
         float4 v[8];
@@ -1353,7 +1399,7 @@ struct Consumer {
         for (int u = 0; u < 8; ++u) v[u] = __ldcg(src + (size_t)(s2 + u) * G * PS / 4);
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const float f = fm[(s2 + u) * G + g];
+          const float f = fm[(s2 + u) * G + gg];
           acc.x = fmaf(f, v[u].x, acc.x);
           acc.y = fmaf(f, v[u].y, acc.y);
           acc.z = fmaf(f, v[u].z, acc.z);
@@ -1362,17 +1408,14 @@ struct Consumer {
       }
       for (; s2 < ns; ++s2) {
         const float4 v = __ldcg(src + (size_t)s2 * G * PS / 4);
-        const float f = fm[s2 * G + g];
+        const float f = fm[s2 * G + gg];
         acc.x = fmaf(f, v.x, acc.x);
         acc.y = fmaf(f, v.y, acc.y);
         acc.z = fmaf(f, v.z, acc.z);
         acc.w = fmaf(f, v.w, acc.w);
       }
-      uint16_t *dst = o + (size_t)g * D + j4 * 4;
-      dst[0] = f2bf(acc.x);
-      dst[1] = f2bf(acc.y);
-      dst[2] = f2bf(acc.z);
-      dst[3] = f2bf(acc.w);
+      *(uint2 *)(ob + (size_t)gg * D + j4 * 4) =
+          make_uint2(pack_bf16(f2bf(acc.x), f2bf(acc.y)), pack_bf16(f2bf(acc.z), f2bf(acc.w)));
     }
     bar_consumers();
     signal(lctr(p, layer, CTR_ATTN_DONE));
@@ -1380,8 +1423,9 @@ struct Consumer {
   }
 
   /* ------------------------------------------------------ expert gate/up
-   * Row pair j of the share (one gate row, one up row of the same expert
-   * and f) is computed by warp j % 8. */
+   * A share of the (expert slot, ffn index) pairs; each stage holds gate and
+   * up rows interleaved, so the thread holding gate row 2j also holds up row
+   * 2j + 1 and applies SwiGLU directly. */
   __device__ bool op_up(const int32_t *t, int task, int layer) {
     const mk_kparams &p = *cx.p;
     if (!cwait(lctr(p, layer, CTR_ROUTED), (int)(cx.epoch + 1), task, OP_UP, layer, CTR_ROUTED))
@@ -1393,36 +1437,52 @@ struct Consumer {
     const int64_t T = (int64_t)U * F;
     int64_t v = T * t[1] / t[2];
     const int64_t v1 = T * (t[1] + 1) / t[2];
-    const XT *x = (const XT *)cx.xbuf;
-    const int rps = mk_pairs_per_stage(2 * d);
-    int pair0 = 0; /* pairs of this share before the current stage */
-    while (v < v1 && !wfail) {
+    const uint16_t *x = (const uint16_t *)cx.xbuf();
+    const int pps = mk_pairs_per_stage(d, cx.SB), pitch = mk_row_pitch(d), xp = mk_x_pitch(d);
+    int j = 0; /* stage index within the task */
+    while (v < v1) {
       const int u = (int)(v / F), f0 = (int)(v % F);
       const int f1 = (int)min((int64_t)F, f0 + (v1 - v));
       uint16_t *out = p.act + (((size_t)layer * p.u_max + u) * MK_MAX_BATCH) * F;
-      for (int f = f0; f < f1; f += rps) {
-        const int cnt = min(rps, f1 - f);
+      for (int f = f0; f < f1; f += pps, ++j) {
+        if ((si + j) % NC != warp) continue;
+        const int cnt = min(pps, f1 - f);
         uint8_t *st;
-        if (!stage_wait(st, task, OP_UP, layer)) break;
-        const uint16_t *wg = (const uint16_t *)st, *wu = wg + (size_t)cnt * d;
-        for (int j = ((warp - pair0) % NC + NC) % NC; j < cnt; j += NC) {
-          float acc[2][NB];
-          const uint16_t *wr[2] = {wg + (size_t)j * d, wu + (size_t)j * d};
-          dot_rows<NB, 2>(wr, x, d, d, lane, acc);
-          const float g = transpose_reduce<NB>(acc[0], lane);
-          const float uu = transpose_reduce<NB>(acc[1], lane);
-          const int b = reduce_token<NB>(lane);
-          if (reduce_leader<NB>(lane) && b < B) {
-            const float gb = rbf(g), ub = rbf(uu);
-            const float silu = gb / (1.0f + expf(-gb));
-            out[(size_t)b * F + f + j] = f2bf(silu * ub);
-          }
-        }
-        stage_release();
-        pair0 += cnt;
+        if (!stage_wait(si + j, st, task, OP_UP, layer)) continue;
+        /* virtual row 2j is gate row j, 2j + 1 up row j: the lanes of a
+         * token hold gate (even g) and up (odd g) of the same pair four
+         * lanes apart */
+        mma_rows<NB>(
+            st, 2 * cnt, pitch, d, x, xp, lane,
+            [cnt](int vr) { return (vr & 1) ? cnt + (vr >> 1) : (vr >> 1); },
+            [&](int n0, const float(&a)[4], const float(&b)[4], bool two) {
+              const int g = lane >> 2, tq = lane & 3, q = g & 1;
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                if (h == 1 && !two) break;
+                const float(&c)[4] = h ? b : a;
+                const float va = q ? c[1] : c[0], vb = q ? c[3] : c[2];
+                const float oa = __shfl_xor_sync(0xFFFFFFFFu, va, 4);
+                const float ob = __shfl_xor_sync(0xFFFFFFFFu, vb, 4);
+                const int pr = ((n0 + 8 * h) >> 1) + tq; /* pair within the stage */
+                if (q == 0 && pr < cnt) {
+                  auto swiglu = [&](int bb, float gv, float uv) {
+                    if (bb < B) {
+                      const float gb = rbf(gv), ub = rbf(uv);
+                      const float silu = gb / (1.0f + expf(-gb));
+                      out[(size_t)bb * F + f + pr] = f2bf(silu * ub);
+                    }
+                  };
+                  if ((g >> 1) < NB) swiglu(g >> 1, va, oa);
+                  if (NB > 4 && 4 + (g >> 1) < NB) swiglu(4 + (g >> 1), vb, ob);
+                }
+              }
+            });
+        stage_release(si + j);
       }
       v += f1 - f0;
     }
+    si += j;
     if (!task_end()) return false;
     signal(lctr(p, layer, CTR_UP_DONE));
     return true;
@@ -1437,58 +1497,64 @@ struct Consumer {
     if (!cwait(lctr(p, layer, CTR_ATTN_DONE), target, task, OP_OUT, layer, CTR_ATTN_DONE))
       return false;
     invalidate_norm();
-    XT *x = (XT *)cx.xbuf;
-    auto &O = cx.m->u.out;
-    for (int i = tid; i < NB * HqD; i += NCT) {
-      const int bb = i / HqD;
-      x[i] = to_x<XT>(bb < B ? __ldcg(p.o + ((size_t)layer * MK_MAX_BATCH + bb) * HqD + (i % HqD))
-                             : (uint16_t)0);
-    }
-    for (int i = tid; i < MK_MAX_OUT_ROWS * MK_MAX_BATCH * 2; i += NCT) (&O.acc[0][0][0])[i] = 0.0f;
+    uint16_t *x = (uint16_t *)cx.xbuf();
+    auto &O = M()->u.out;
+    load_x(x, p.o + (size_t)layer * MK_MAX_BATCH * HqD, HqD, HqD);
+    for (int i = tid; i < NC * MK_MAX_OUT_ROWS * NB; i += NCT) (&O.acc_w[0][0][0])[i] = 0.0f;
     bar_consumers();
-    gemv_task(nr, HqD, x, HqD, task, OP_OUT, layer,
-              [&](int r, int bb, float v) { O.acc[r][bb][0] = v; });
+    gemv_rows(nr, HqD, x, task, OP_OUT, layer, [&](int r, int bb, float v) { O.acc_o[r][bb] = v; });
     if (!cwait(lctr(p, layer, CTR_UP_DONE), (int)((cx.epoch + 1) * p.n_up), task, OP_OUT, layer,
                CTR_UP_DONE))
       return false;
     const mk_routing *rt = p.routing + layer;
     const int U = __ldcg(&rt->U);
-    for (int i = tid; i < U * MK_MAX_BATCH; i += NCT)
-      O.slot_w[i / MK_MAX_BATCH][i % MK_MAX_BATCH] =
-          __ldcg(&rt->slot_w[i / MK_MAX_BATCH][i % MK_MAX_BATCH]);
-    /* the experts' activations: all slots at once when they fit the buffer,
-     * else two slots at a time */
-    const int per = NB * F;
-    const int fit = (int)min((int64_t)U, (int64_t)cx.p->xbuf_bytes / ((int64_t)sizeof(XT) * per));
-    const bool all = fit >= U;
-    for (int u = 0; u < U; ++u) {
-      const int bufslot = all ? u : (u & 1);
-      XT *xa = x + (size_t)bufslot * per;
-      if (all ? u == 0 : true) {
-        const int n_load = all ? U : 1;
-        for (int k = 0; k < n_load; ++k) {
-          const int uu = all ? k : u;
-          XT *dst = x + (size_t)(all ? k : bufslot) * per;
-          const uint16_t *a = p.act + (((size_t)layer * p.u_max + uu) * MK_MAX_BATCH) * F;
-          for (int i = tid; i < per; i += NCT)
-            dst[i] = to_x<XT>((i / F) < B ? __ldcg(a + i) : (uint16_t)0);
+    for (int i = tid; i < U * NB; i += NCT)
+      O.slot_w[i / NB][i % NB] = __ldcg(&rt->slot_w[i / NB][i % NB]);
+    /* the experts' activations, as many experts at a time as xbuf holds */
+    const int xpf = mk_x_pitch(F), per = NB * xpf;
+    const int fit = max(1, (int)min((int64_t)U, (int64_t)p.xbuf_bytes / ((int64_t)2 * per)));
+    const int rps = mk_rows_per_stage(F, cx.SB), pitch = mk_row_pitch(F);
+    const int n_se = (nr + rps - 1) / rps; /* stages per expert */
+    for (int u0 = 0; u0 < U; u0 += fit) {
+      const int u1 = min(U, u0 + fit);
+      if (u0 > 0) bar_consumers(); /* the previous experts' activations are consumed */
+      for (int u = u0; u < u1; ++u)
+        load_x(x + (size_t)(u - u0) * per,
+               p.act + (((size_t)layer * p.u_max + u) * MK_MAX_BATCH) * F, F, F);
+      bar_consumers();
+      for (int u = u0; u < u1; ++u) {
+        const uint16_t *xa = x + (size_t)(u - u0) * per;
+        for (int jj = 0; jj < n_se; ++jj) {
+          const int j = u * n_se + jj;
+          if ((si + j) % NC != warp) continue;
+          uint8_t *st;
+          if (!stage_wait(si + j, st, task, OP_OUT, layer)) continue;
+          const int rb0 = jj * rps, cnt = min(rps, nr - rb0);
+          mma_rows<NB>(st, cnt, pitch, F, xa, xpf, lane, [](int vr) { return vr; },
+                       [&](int n0, const float(&a)[4], const float(&b)[4], bool two) {
+                         auto f = [&](int r, int bb, float v) {
+                           float &acc = O.acc_w[warp][rb0 + r][bb];
+                           acc = fmaf(O.slot_w[u][bb], v, acc);
+                         };
+                         take_out<NB>(n0, a, cnt, lane, f);
+                         if (two) take_out<NB>(n0 + 8, b, cnt, lane, f);
+                       });
+          stage_release(si + j);
         }
-        bar_consumers();
       }
-      gemv_task(nr, F, xa, F, task, OP_OUT, layer, [&](int r, int bb, float v) {
-        const float sw = O.slot_w[u][bb];
-        if (bb < B && sw != 0.0f) O.acc[r][bb][1] = fmaf(sw, v, O.acc[r][bb][1]);
-      });
     }
+    si += U * n_se;
     if (!task_end()) return false;
     for (int i = tid; i < nr * B; i += NCT) {
       const int r = i / B, bb = i % B;
       const uint16_t *hin = h_row(layer, bb);
       const float hv = bf2f(__ldcg(hin + r0 + r));
-      const float at = rbf(O.acc[r][bb][0]);
-      const float mo = rbf(O.acc[r][bb][1]);
+      const float at = rbf(O.acc_o[r][bb]);
+      float mo = 0.0f;
+#pragma unroll
+      for (int w = 0; w < NC; ++w) mo += O.acc_w[w][r][bb];
       p.h[((size_t)(layer + 1) * MK_MAX_BATCH + bb) * d + r0 + r] =
-          f2bf(__fadd_rn(__fadd_rn(hv, at), mo));
+          f2bf(__fadd_rn(__fadd_rn(hv, at), rbf(mo)));
       if (layer == 0) p.h[(size_t)bb * d + r0 + r] = __ldg(hin + r0 + r);
     }
     bar_consumers();
@@ -1503,7 +1569,7 @@ struct Consumer {
     if (!cwait(lctr(p, L - 1, CTR_OUT_DONE), (int)((cx.epoch + 1) * p.n_out), task, OP_LM, L,
                CTR_OUT_DONE))
       return false;
-    if (*(volatile int32_t *)&cx.m->norm_layer != L) {
+    if (*(volatile int32_t *)&M()->norm_layer != L) {
       bar_consumers();
       const uint16_t *hr[NB];
 #pragma unroll
@@ -1512,33 +1578,48 @@ struct Consumer {
       norm_into_xbuf(L, hr, p.final_norm);
     }
     const int v0 = t[2];
-    float best_v = -INFINITY;
-    int best_i = 0x7FFFFFFF;
+    /* each lane keeps the best of the rows it computed for its two tokens
+     * (g / 2 and 4 + g / 2) */
+    float best_v[2] = {NEG_INF, NEG_INF};
+    int best_i[2] = {0x7FFFFFFF, 0x7FFFFFFF};
     float *logits = p.out_logits;
     const int V = p.V;
-    /* the lane that owns token b in each warp keeps that warp's best */
-    gemv_task(t[3], p.d, (const XT *)cx.xbuf, p.d, task, OP_LM, L,
-              [&](int r, int bb, float v) {
-                if (bb < B) {
-                  if (logits) logits[(size_t)bb * V + v0 + r] = v;
-                  if (v > best_v || (v == best_v && v0 + r < best_i)) {
-                    best_v = v;
-                    best_i = v0 + r;
-                  }
-                }
-              });
-    auto &M = cx.m->u.lm;
-    if (reduce_leader<NB>(lane)) {
-      M.best[warp][reduce_token<NB>(lane)][0] = best_v;
-      M.best[warp][reduce_token<NB>(lane)][1] = __int_as_float(best_i);
+    gemv_rows(t[3], p.d, (const uint16_t *)cx.xbuf(), task, OP_LM, L, [&](int r, int bb, float v) {
+      if (bb < B) {
+        if (logits) logits[(size_t)bb * V + v0 + r] = v;
+        const int k = bb >= 4;
+        if (v > best_v[k] || (v == best_v[k] && v0 + r < best_i[k])) {
+          best_v[k] = v;
+          best_i[k] = v0 + r;
+        }
+      }
+    });
+    /* the eight lanes of a token (lanes 8b..8b+7), then the warps */
+    auto &LM = M()->u.lm;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+#pragma unroll
+      for (int s = 1; s <= 4; s <<= 1) {
+        const float ov = __shfl_xor_sync(0xFFFFFFFFu, best_v[k], s);
+        const int oi = __shfl_xor_sync(0xFFFFFFFFu, best_i[k], s);
+        if (ov > best_v[k] || (ov == best_v[k] && oi < best_i[k])) {
+          best_v[k] = ov;
+          best_i[k] = oi;
+        }
+      }
+      const int bb = 4 * k + (lane >> 3);
+      if ((lane & 7) == 0 && bb < NB) {
+        LM.best[warp][bb][0] = best_v[k];
+        LM.best[warp][bb][1] = __int_as_float(best_i[k]);
+      }
     }
     if (!task_end()) return false;
     if (tid < B) {
-      float bv = -INFINITY;
+      float bv = NEG_INF;
       int bi = 0x7FFFFFFF;
       for (int w = 0; w < NC; ++w) {
-        const float v = M.best[w][tid][0];
-        const int i = __float_as_int(M.best[w][tid][1]);
+        const float v = LM.best[w][tid][0];
+        const int i = __float_as_int(LM.best[w][tid][1]);
         if (v > bv || (v == bv && i < bi)) {
           bv = v;
           bi = i;
@@ -1550,7 +1631,7 @@ struct Consumer {
     bar_consumers();
     if (!ticket(gctr(p, GCTR_LM_TICKET), p.n_lm)) return true;
     if (tid < B) {
-      float bv = -INFINITY;
+      float bv = NEG_INF;
       int bi = 0x7FFFFFFF;
       for (int k = 0; k < p.n_lm; ++k) {
         const float v = __ldcg(p.lm_part + ((size_t)k * MK_MAX_BATCH + tid) * 2);
@@ -1577,7 +1658,11 @@ struct Consumer {
     switch (t[0]) {
       case OP_QKV: ok = op_qkv(t, task, layer); break;
       case OP_ROUTER: ok = op_router(t, task, layer); break;
-      case OP_ATTN: ok = op_attn(t, task, layer); break;
+      case OP_ATTN:
+        ok = cx.p->D == 128 ? op_attn<128>(t, task, layer)
+             : cx.p->D == 64 ? op_attn<64>(t, task, layer)
+                             : op_attn<32>(t, task, layer);
+        break;
       case OP_UP: ok = op_up(t, task, layer); break;
       case OP_OUT: ok = op_out(t, task, layer); break;
       case OP_LM: ok = op_lm(t, task); break;
@@ -1616,29 +1701,38 @@ struct Consumer {
 };
 
 template <int NB>
-__global__ void __launch_bounds__(MK_THREADS, 1) decode_kernel(const mk_kparams p) {
-  extern __shared__ __align__(1024) uint8_t smem[];
+__global__ void __launch_bounds__(MK_THREADS, 1) decode_kernel(const __grid_constant__ mk_kparams p) {
+  /* the ring starts on a 1024-byte boundary (128-byte swizzled TMA boxes);
+   * the launch adds MK_SMEM_STATIC bytes of slack for that */
   Ctx cx;
   cx.p = &p;
-  cx.nstages = p.ring_stages;
-  cx.ring = smem;
-  cx.xbuf = smem + (size_t)p.ring_stages * MK_STAGE_BYTES;
-  cx.m = (Misc *)(cx.xbuf + p.xbuf_bytes);
+  cx.SB = p.stage_bytes;
+  cx.ring_off = (1024u - (saddr(mk_smem) & 1023u)) & 1023u;
+  cx.xbuf_off = cx.ring_off + (uint32_t)NC * p.stage_bytes;
+  cx.misc_off = cx.xbuf_off + (uint32_t)p.xbuf_bytes;
+  Misc<NB> *misc = (Misc<NB> *)(mk_smem + cx.misc_off);
   cx.cta = blockIdx.x;
   cx.epoch = *(volatile uint32_t *)&p.ctrl->epoch;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __shared__ int32_t s_ok;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < cx.nstages; ++s) {
-      mbar_init(&cx.m->full[s], 1);
-      mbar_init(&cx.m->empty[s], NC);
+    for (int s = 0; s < NC; ++s) {
+      mbar_init(&misc->full[s], 1);
+      mbar_init(&misc->empty[s], 1);
     }
-    cx.m->norm_layer = -2;
-    s_ok = 1;
+    misc->norm_layer = -2;
+    misc->ok = 1;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  const int32_t *row = p.table + (size_t)blockIdx.x * p.tasks_per_cta * MK_DESC_INTS;
+  /* the CTA's task-table row, read by every task of every layer, is copied
+   * to shared memory when it fits */
+  const int32_t *grow = p.table + (size_t)blockIdx.x * p.tasks_per_cta * MK_DESC_INTS;
+  const bool row_in_smem = p.tasks_per_cta <= MK_SMEM_TASKS;
+  if (row_in_smem)
+    for (int i = threadIdx.x; i < p.tasks_per_cta * MK_DESC_INTS; i += MK_THREADS)
+      (&misc->tasks[0][0])[i] = __ldg(grow + i);
+  __syncthreads();
+  const int32_t *row = row_in_smem ? &misc->tasks[0][0] : grow;
   const bool header_ok = row[0] == OP_HEADER;
   if (header_ok) {
     if (warp == NC) {
@@ -1658,14 +1752,14 @@ __global__ void __launch_bounds__(MK_THREADS, 1) decode_kernel(const mk_kparams 
       c.tr = p.trace ? p.trace + (size_t)blockIdx.x * p.trace_cap * MK_TRACE_WORDS : nullptr;
       c.tr_n = 0;
       const bool ok = c.run(row);
-      if (threadIdx.x == 0 && !ok) s_ok = 0;
+      if (threadIdx.x == 0 && !ok) misc->ok = 0;
     }
   } else if (threadIdx.x == 0) {
     raise_error(p, MK_ERR_BAD_TASK, blockIdx.x, -1, row[0], -1, -1, 0, 0);
-    s_ok = 0;
+    misc->ok = 0;
   }
   __syncthreads();
-  if (threadIdx.x == 0 && s_ok && !ld_volatile(&p.ctrl->abort)) {
+  if (threadIdx.x == 0 && misc->ok && !ld_volatile(&p.ctrl->abort)) {
     /* the last CTA out advances the epoch */
     __threadfence();
     const int old = atom_add_acq_rel(gctr(p, GCTR_EXIT), 1);
@@ -1678,7 +1772,12 @@ __global__ void __launch_bounds__(MK_THREADS, 1) decode_kernel(const mk_kparams 
 
 /* ---- library-internal entry points (used by mk_api.cpp) ------------------ */
 
-extern "C" size_t mk_misc_bytes() { return sizeof(mk::Misc); }
+extern "C" size_t mk_misc_bytes(int nb) {
+  return nb == 1   ? sizeof(mk::Misc<1>)
+         : nb == 2 ? sizeof(mk::Misc<2>)
+         : nb == 4 ? sizeof(mk::Misc<4>)
+                   : sizeof(mk::Misc<8>);
+}
 
 static void *mk_kernel_fn(int nb) {
   return nb == 1   ? (void *)mk::decode_kernel<1>

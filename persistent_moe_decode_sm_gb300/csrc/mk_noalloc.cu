@@ -38,7 +38,6 @@
 #include "mk_internal.h"
 #include "mk_plan.h"
 
-extern "C" size_t mk_misc_bytes();
 extern "C" cudaError_t mk_kernel_prepare(int nb, size_t smem, int *blocks_per_sm);
 extern "C" cudaError_t mk_launch(const mk_kparams *p, int nb, int grid, size_t smem,
                                  cudaStream_t stream);
@@ -153,23 +152,14 @@ extern "C" mk_status mk_decode_step_static(const mk_model_dims *dims, const mk_w
   const size_t o_pt = take((size_t)MB * mp * 4);
   const size_t o_ly = take((size_t)Lyr * sizeof(mk_layer_dev));
   const size_t o_tab = take(plan.table.size() * sizeof(int32_t));
+  const size_t o_maps = take((size_t)Lyr * 2 * 128);
   if (off > MK_STATIC_SCRATCH_BYTES) return MK_ERR_SCRATCH_LIMIT;
 
   /* ---- shared memory plan (as for mk_decode_step) ---- */
-  const int nb = batch <= 1 ? 1 : batch <= 2 ? 2 : batch <= 4 ? 4 : 8;
-  const size_t xt = nb == 1 ? 4 : 2; /* activations fp32 for one token, else bf16 */
-  size_t xbuf = (size_t)nb * d.d_model * (xt + 2);
-  xbuf = std::max(xbuf, (size_t)nb * HqD * xt);
-  xbuf = std::max(xbuf, (size_t)2 * nb * d.d_ffn * xt);
-  xbuf = std::max(xbuf, std::min((size_t)u_max * nb * d.d_ffn * xt, (size_t)32768));
-  xbuf = std::max(xbuf, (size_t)(8 + 2 + 32) * d.head_dim * 4);
-  xbuf = std::max(xbuf, (size_t)(2 * 256 * MK_MAX_GROUP + 2 * MK_MAX_GROUP) * 4);
-  xbuf = up(xbuf, 1024);
-  const size_t misc = up(mk_misc_bytes(), 128);
-  const size_t budget = (size_t)optin - 1024;
-  if (budget < xbuf + misc + 2 * MK_STAGE_BYTES) return MK_ERR_UNSUPPORTED;
-  const int stages = std::min<int>((int)((budget - xbuf - misc) / MK_STAGE_BYTES), MK_MAX_STAGES);
-  const size_t smem = (size_t)stages * MK_STAGE_BYTES + xbuf + misc;
+  const int nb = mk_nb_for(batch);
+  MkSmem sm;
+  if (optin < MK_SMEM_OPTIN || !mk_smem_plan(dims, nb, &sm)) return MK_ERR_UNSUPPORTED;
+  const size_t smem = sm.dyn;
   {
     const int ki = nb == 1 ? 0 : nb == 2 ? 1 : nb == 4 ? 2 : 3;
     std::lock_guard<std::mutex> lk(g_setup_mu);
@@ -199,6 +189,16 @@ extern "C" mk_status mk_decode_step_static(const mk_model_dims *dims, const mk_w
     D.kc = (uint16_t *)L.k_cache;
     D.vc = (uint16_t *)L.v_cache;
   }
+  std::vector<uint8_t> maps((size_t)Lyr * 2 * 128);
+  {
+    std::vector<const void *> kp(Lyr), vp(Lyr);
+    for (int l = 0; l < Lyr; ++l) {
+      kp[l] = w->layers[l].k_cache;
+      vp[l] = w->layers[l].v_cache;
+    }
+    st = mk_encode_kv_maps(dims, kp.data(), vp.data(), maps.data());
+    if (st != MK_OK) return st;
+  }
   std::vector<int32_t> lens(MB, 0), pt((size_t)MB * mp, -1);
   std::copy(seq_lens, seq_lens + batch, lens.begin());
   std::memcpy(pt.data(), page_tables, (size_t)batch * mp * sizeof(int32_t));
@@ -218,6 +218,8 @@ extern "C" mk_status mk_decode_step_static(const mk_model_dims *dims, const mk_w
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(base + o_ly, layers.data(), Lyr * sizeof(mk_layer_dev),
                         cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(base + o_maps, maps.data(), maps.size(), cudaMemcpyHostToDevice, stream);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(base + o_len, lens.data(), MB * 4, cudaMemcpyHostToDevice, stream);
   if (e == cudaSuccess)
@@ -281,8 +283,9 @@ extern "C" mk_status mk_decode_step_static(const mk_model_dims *dims, const mk_w
   p.ctrs_per_layer = ctrs_per_layer;
   p.wait_limit_ns = 1000000000ULL;
   p.err_host = nullptr;
-  p.ring_stages = stages;
-  p.xbuf_bytes = (int32_t)xbuf;
+  p.stage_bytes = sm.stage_bytes;
+  p.kv_maps = base + o_maps;
+  p.xbuf_bytes = (int32_t)sm.xbuf;
   p.poison_layer = -1;
   p.poison_delta = 0;
 

@@ -16,6 +16,26 @@ struct MkPlan {
   std::vector<int32_t> built_lens; /* lengths the attention splits were cut for */
 };
 
+/* Dynamic shared memory of the nb-token kernel: NC ring slots of stage_bytes,
+ * the activation buffer, the control block (total), plus MK_SMEM_STATIC
+ * bytes of slack to align the ring to 1024 bytes (dyn, the launch size). */
+struct MkSmem {
+  int stage_bytes = 0;
+  size_t xbuf = 0, misc = 0, total = 0, dyn = 0;
+};
+/* false if the model does not fit (a row, a row pair or a KV page larger
+ * than one slot). */
+bool mk_smem_plan(const mk_model_dims *d, int nb, MkSmem *out);
+int mk_nb_for(int batch);
+
+/* Encodes the 3-D TMA tensor maps of every layer's K and V pools into
+ * host_out ([n_layers][2] maps of 128 bytes: K, V): dims {BI = min(head_dim,
+ * 64), head_dim / BI, num_pages * n_kv_heads * page_size}, box {BI,
+ * head_dim / BI, page_size} (one page of one kv head), 128-byte swizzle when
+ * head_dim >= 64. */
+mk_status mk_encode_kv_maps(const mk_model_dims *d, const void *const *k_pools,
+                            const void *const *v_pools, void *host_out);
+
 mk_status mk_validate_dims(const mk_model_dims *d);
 mk_status mk_build_plan(const mk_model_dims *d, int n_cta, int batch, const int32_t *seq_lens,
                         MkPlan *out);

@@ -52,7 +52,49 @@ Desc desc(int op) {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
 }  // namespace
+
+extern "C" size_t mk_misc_bytes(int nb);
+
+int mk_nb_for(int batch) { return batch <= 1 ? 1 : batch <= 2 ? 2 : batch <= 4 ? 4 : 8; }
+
+/* The activation buffer: the largest of what the task types stage there
+ * (bf16 vectors at the padded pitch K + 32). */
+static size_t xbuf_bytes_for(const mk_model_dims &d, int nb) {
+  const size_t HqD = (size_t)d.n_q_heads * d.head_dim, D = d.head_dim;
+  size_t x = (size_t)nb * 2 * (mk_x_pitch(d.d_model) + d.d_model); /* normed input + staged h */
+  x = std::max(x, (size_t)nb * 2 * mk_x_pitch((int)HqD));          /* attention output (Wo) */
+  x = std::max(x, (size_t)nb * 2 * mk_x_pitch(d.d_ffn));          /* one expert's activations */
+  /* attention: q (bf16 [8][D + 8]), new k and v (fp32 [D] each), merge
+   * scratch fp32 [4][8][D + 8] */
+  x = std::max(x, 8 * (D + 8) * 2 + 2 * D * 4 + 4 * 8 * (D + 8) * 4);
+  /* cross-split merge: m and l of up to 256 splits x 8 heads, then 2 x 8 */
+  x = std::max(x, (size_t)(2 * 256 * MK_MAX_GROUP + 2 * MK_MAX_GROUP) * 4);
+  return align_up(x, 1024);
+}
+
+bool mk_smem_plan(const mk_model_dims *dm, int nb, MkSmem *out) {
+  const mk_model_dims &d = *dm;
+  MkSmem s;
+  s.misc = align_up(mk_misc_bytes(nb), 128);
+  s.xbuf = xbuf_bytes_for(d, nb);
+  const size_t fixed = MK_SMEM_STATIC + s.xbuf + s.misc;
+  if (fixed >= MK_SMEM_OPTIN) return false;
+  size_t sb = (MK_SMEM_OPTIN - fixed) / MK_NC_WARPS / 1024 * 1024;
+  sb = std::min<size_t>(sb, MK_MAX_STAGE_BYTES);
+  s.stage_bytes = (int)sb;
+  const int HqD = d.n_q_heads * d.head_dim;
+  if (mk_rows_per_stage(d.d_model, s.stage_bytes) < 2 || mk_rows_per_stage(HqD, s.stage_bytes) < 1 ||
+      mk_rows_per_stage(d.d_ffn, s.stage_bytes) < 1 ||
+      mk_pages_per_stage(d.page_size, d.head_dim, s.stage_bytes) < 1)
+    return false;
+  s.total = (size_t)MK_NC_WARPS * sb + s.xbuf + s.misc;
+  s.dyn = s.total + MK_SMEM_STATIC;
+  *out = s;
+  return true;
+}
 
 mk_status mk_validate_dims(const mk_model_dims *dm) {
   if (!dm) return MK_ERR_INVALID_ARG;
@@ -66,14 +108,18 @@ mk_status mk_validate_dims(const mk_model_dims *dm) {
   if (!(d.rms_eps >= 0.0f) || !(d.rope_base > 0.0f)) return MK_ERR_INVALID_ARG;
   if (d.max_batch > MK_MAX_BATCH) return MK_ERR_BATCH;
   if (d.head_dim != 32 && d.head_dim != 64 && d.head_dim != 128) return MK_ERR_UNSUPPORTED;
+  /* attention runs on 16-token tensor-core tiles within a page */
+  if (d.page_size % 16 || d.page_size > 256) return MK_ERR_UNSUPPORTED;
   if (d.n_q_heads / d.n_kv_heads > MK_MAX_GROUP) return MK_ERR_UNSUPPORTED;
   if (d.top_k > MK_MAX_TOPK || d.n_experts > 128) return MK_ERR_UNSUPPORTED;
   if (d.d_model % 64 || d.d_ffn % 64 || (d.n_q_heads * d.head_dim) % 64) return MK_ERR_UNSUPPORTED;
-  /* every streamed unit must fit one ring stage */
-  const int64_t row_max = std::max<int64_t>(2LL * d.d_model, (int64_t)d.n_q_heads * d.head_dim);
-  if (row_max * 2 > MK_STAGE_BYTES) return MK_ERR_UNSUPPORTED;
-  if (2LL * d.page_size * d.head_dim * 2 > MK_STAGE_BYTES) return MK_ERR_UNSUPPORTED;
-  if ((int64_t)d.page_size * d.head_dim * 2 % 16) return MK_ERR_UNSUPPORTED;
+  if (d.d_model > 16384 || d.d_ffn > 16384 || d.n_q_heads * d.head_dim > 16384)
+    return MK_ERR_UNSUPPORTED;
+  /* every streamed unit must fit one ring slot of every batch bucket used */
+  for (int nb = 1; nb <= mk_nb_for(d.max_batch); nb *= 2) {
+    MkSmem sm;
+    if (!mk_smem_plan(&d, nb, &sm)) return MK_ERR_UNSUPPORTED;
+  }
   return MK_OK;
 }
 
@@ -95,9 +141,12 @@ mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int
   MkPlan &p = *out;
   p = MkPlan();
 
-  /* ROUTER: as many rows per task as fit one stage. */
+  /* ROUTER: one ring stage of rows per task, so that the router GEMV, which
+   * heads the MoE critical path, is spread over as many SMs as possible. */
   {
-    const int rpr = std::max(1, std::min(d.n_experts, MK_STAGE_BYTES / (2 * d.d_model)));
+    MkSmem sm;
+    if (!mk_smem_plan(&d, mk_nb_for(batch), &sm)) return MK_ERR_UNSUPPORTED;
+    const int rpr = std::max(1, std::min(d.n_experts, mk_rows_per_stage(d.d_model, sm.stage_bytes)));
     const int n = (int)ceil_div(d.n_experts, rpr);
     for (int i = 0; i < n; ++i) {
       Desc t = desc(OP_ROUTER);

@@ -78,3 +78,33 @@ def summarize(trace: np.ndarray, n_layers: int) -> dict:
                            "task_body": round(busy / total, 3)},
         "phases_rel_prev_layer_end_us": phases,
     }
+
+
+def stage_summary(stages: np.ndarray) -> dict:
+    """Per op, medians over CTA 0's ring stages (microseconds): the producer's
+    time to find the next stage (desc), to get its slot back (slot_wait),
+    to issue the copies (issue); the copy latency (issue -> data seen by the
+    owning warp, counting from when the warp started waiting if later); the
+    owning warp's wait and compute (data seen -> release); and the stage
+    interval (producer issue to issue)."""
+    ev = [e for e in stages if e[4] and e[6] and e[7]]
+    if not ev:
+        return {}
+    out = {}
+    issue = np.array(sorted(int(e[4]) for e in ev), np.int64)
+    per = defaultdict(list)
+    for e in ev:
+        per[OPS.get((int(e[0]) >> 24) & 0xFF, "?")].append(e)
+    for op, v in per.items():
+        a = np.array([[int(x) for x in e] for e in v], np.int64)
+        out[op] = {
+            "n": len(v),
+            "desc_us": round(float(np.median(a[:, 2] - a[:, 1])) / 1e3, 3),
+            "slot_wait_us": round(float(np.median(a[:, 3] - a[:, 2])) / 1e3, 3),
+            "issue_us": round(float(np.median(a[:, 4] - a[:, 3])) / 1e3, 3),
+            "copy_latency_us": round(float(np.median(a[:, 6] - a[:, 4])) / 1e3, 3),
+            "warp_wait_us": round(float(np.median(a[:, 6] - a[:, 5])) / 1e3, 3),
+            "compute_us": round(float(np.median(a[:, 7] - a[:, 6])) / 1e3, 3),
+        }
+    out["issue_interval_us"] = round(float(np.median(np.diff(issue))) / 1e3, 3) if len(issue) > 1 else None
+    return out
