@@ -59,7 +59,8 @@ enum {
   MK_ERR_BAD_TASK = 7,      /* the kernel met an unknown task opcode (sticky) */
   MK_ERR_UNSUPPORTED = 8,   /* dims this build does not support (see mk_create) */
   MK_ERR_NO_DEVICE = 9,     /* no usable sm_103 device */
-  MK_ERR_SCRATCH_LIMIT = 10 /* mk_decode_step_static: workspace larger than its static scratch */
+  MK_ERR_SCRATCH_LIMIT = 10,/* mk_decode_step_static: workspace larger than its static scratch */
+  MK_ERR_BAD_TOKEN = 11     /* a token id outside [0, vocab) reached the kernel (sticky) */
 };
 
 /* Model dimensions.  page_size tokens per KV page; num_pages pages in each
@@ -110,7 +111,9 @@ mk_status mk_build_schedule(mk_ctx *ctx, int32_t batch, const int32_t *seq_lens,
 
 /* One decode step for the scheduled batch.  token_ids: DEVICE int32 [batch];
  * out_logits: DEVICE fp32 [batch][vocab] or NULL; out_next_tokens: DEVICE
- * int32 [batch] (greedy argmax, ties -> lowest id).  Token b is processed at
+ * int32 [batch] (greedy argmax, ties -> lowest id).  A token id outside
+ * [0, vocab) fails the step with MK_ERR_BAD_TOKEN (sticky; the kernel reads
+ * embedding row 0 in its place, never outside the table).  Token b is processed at
  * position L_b and its K/V row is written there; L_b then advances by one
  * (on the device and in the context).  The page covering L_b must be present
  * in the page table (MK_ERR_PAGE_OOB otherwise).  When a sequence has grown

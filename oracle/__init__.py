@@ -176,7 +176,9 @@ class Oracle:
 
     def __init__(self, dims: synth.Dims, tensors: Dict[str, object], seq_lens: Sequence[int],
                  page_tables: np.ndarray, router_biases: Optional[List] = None,
-                 accum_double: bool = False, seed: int = 0):
+                 accum_double: bool = False, seed: int = 0, reverse: bool = False):
+        """accum_double: sums in double; reverse: fp32 sums in descending
+        index order (otherwise fp32 in ascending order)."""
         self.dims = dims
         self.B = len(seq_lens)
         self._keep = [v for v in tensors.values() if isinstance(v, np.ndarray)]
@@ -201,7 +203,7 @@ class Oracle:
         self.pt = _c(page_tables, np.int32)
         self.h = lib().orc_create(ctypes.byref(self.cd), ctypes.byref(self.w), self.B,
                                   _ptr(self.seq_lens), _ptr(self.pt), self.pt.shape[1],
-                                  int(accum_double))
+                                  1 if accum_double else (2 if reverse else 0))
         if not self.h:
             raise ValueError("orc_create rejected the arguments")
 

@@ -62,22 +62,31 @@ struct Tensor {
   }
 };
 
-/* ---- dot product: the only accumulation primitive ------------------------- */
+/* ---- dot product: the only accumulation primitive -------------------------
+ * acc: ACC_F32 (fp32, ascending index order), ACC_F64 (double), ACC_F32_REV
+ * (fp32, descending index order).  The method fixes fp32 accumulation but
+ * not the order of the sum; the two fp32 orders are equally faithful, and
+ * how far each lands from the double evaluation measures the method's own
+ * rounding noise. */
+enum { ACC_F32 = 0, ACC_F64 = 1, ACC_F32_REV = 2 };
 
-float dot(const float *a, const float *b, int64_t n, bool dbl) {
-  if (dbl) {
+float dot(const float *a, const float *b, int64_t n, int acc) {
+  if (acc == ACC_F64) {
     double s = 0.0;
     for (int64_t i = 0; i < n; ++i) s += (double)a[i] * (double)b[i];
     return (float)s;
   }
   float s = 0.0f;
-  for (int64_t i = 0; i < n; ++i) s += a[i] * b[i];
+  if (acc == ACC_F32_REV)
+    for (int64_t i = n - 1; i >= 0; --i) s += a[i] * b[i];
+  else
+    for (int64_t i = 0; i < n; ++i) s += a[i] * b[i];
   return s;
 }
 
 /* y[r] = dot(W[row0 + r], x), r < rows; W is a [*][cols] tensor. */
 void gemv(const Tensor &w, int64_t row0, int64_t rows, int64_t cols, const float *x,
-          bool dbl, float *y) {
+          int dbl, float *y) {
 #pragma omp parallel
   {
     std::vector<float> buf(cols);
@@ -93,16 +102,8 @@ void gemv(const Tensor &w, int64_t row0, int64_t rows, int64_t cols, const float
 
 /* RMSNorm (design reading R5): fp32 mean of squares, 1/sqrtf, one bf16
  * rounding of (h * r) * g. */
-void rmsnorm(const float *h, const Tensor &g, int64_t d, float eps, bool dbl, float *out) {
-  float ss;
-  if (dbl) {
-    double s = 0.0;
-    for (int64_t i = 0; i < d; ++i) s += (double)h[i] * (double)h[i];
-    ss = (float)s;
-  } else {
-    ss = 0.0f;
-    for (int64_t i = 0; i < d; ++i) ss += h[i] * h[i];
-  }
+void rmsnorm(const float *h, const Tensor &g, int64_t d, float eps, int dbl, float *out) {
+  const float ss = dot(h, h, d, dbl);
   const float mean = ss / (float)d;
   const float r = 1.0f / sqrtf(mean + eps);
   for (int64_t i = 0; i < d; ++i) out[i] = round_bf16((h[i] * r) * bf16_to_f32(g.bits(i)));
@@ -133,7 +134,7 @@ void rope(float *x, int64_t n_heads, int64_t D, int64_t pos, double base) {
 /* Attention of one query head over n keys (reading R7): s_j = fp32(q.k_j) *
  * (1/sqrt(D)); softmax in fp32; o = bf16((sum_j p_j v_j) / l). */
 void attention_head(const float *q, const float *keys, const float *vals, int64_t n,
-                    int64_t D, bool dbl, float *o) {
+                    int64_t D, int dbl, float *o) {
   const float scale = (float)(1.0 / sqrt((double)D));
   std::vector<float> s(n);
   float m = -std::numeric_limits<float>::infinity();
@@ -145,7 +146,7 @@ void attention_head(const float *q, const float *keys, const float *vals, int64_
   for (int64_t j = 0; j < n; ++j) p[j] = expf(s[j] - m);
   /* Each output dim sums over j in ascending order; the j-outer loop order
    * only keeps the value rows in cache. */
-  if (dbl) {
+  if (dbl == ACC_F64) {
     double l = 0.0;
     for (int64_t j = 0; j < n; ++j) l += (double)p[j];
     std::vector<double> acc(D, 0.0);
@@ -155,10 +156,12 @@ void attention_head(const float *q, const float *keys, const float *vals, int64_
     return;
   }
   float l = 0.0f;
-  for (int64_t j = 0; j < n; ++j) l += p[j];
   std::vector<float> acc(D, 0.0f);
-  for (int64_t j = 0; j < n; ++j)
+  for (int64_t jj = 0; jj < n; ++jj) {
+    const int64_t j = dbl == ACC_F32_REV ? n - 1 - jj : jj;
+    l += p[j];
     for (int64_t e = 0; e < D; ++e) acc[e] += p[j] * vals[j * D + e];
+  }
   for (int64_t e = 0; e < D; ++e) o[e] = round_bf16(acc[e] / l);
 }
 
@@ -196,7 +199,7 @@ float silu(float x) { return x / (1.0f + expf(-x)); }
 
 struct orc_model {
   orc_dims dims;
-  bool dbl;
+  int dbl; /* accumulation mode (ACC_*) */
   int32_t B, max_pages;
   Tensor embed, final_norm, lm_head;
   struct Layer {
@@ -234,7 +237,7 @@ orc_model *orc_create(const orc_dims *dims, const orc_weights *w, int32_t batch,
   if (dims->top_k < 1 || dims->top_k > dims->n_experts) return nullptr;
   orc_model *m = new orc_model();
   m->dims = *dims;
-  m->dbl = accum_double != 0;
+  m->dbl = accum_double;
   m->B = batch;
   m->max_pages = max_pages;
   m->embed = Tensor(w->embed);
@@ -274,7 +277,7 @@ int32_t orc_step(orc_model *m, const int32_t *tokens, const int32_t *forced_ids,
   const int64_t B = m->B, d = dm.d_model, Hq = dm.n_q_heads, Hkv = dm.n_kv_heads;
   const int64_t D = dm.head_dim, G = Hq / Hkv, E = dm.n_experts, K = dm.top_k;
   const int64_t F = dm.d_ffn, V = dm.vocab, L = dm.n_layers;
-  const bool dbl = m->dbl;
+  const int dbl = m->dbl;
   orc_step_out dummy;
   memset(&dummy, 0, sizeof(dummy));
   if (!out) out = &dummy;
@@ -453,7 +456,7 @@ void orc_rmsnorm(const uint16_t *h, const uint16_t *g, int32_t d, float eps,
   orc_tensor gt;
   memset(&gt, 0, sizeof(gt));
   gt.data = g;
-  rmsnorm(hf.data(), Tensor(gt), d, eps, accum_double != 0, of.data());
+  rmsnorm(hf.data(), Tensor(gt), d, eps, accum_double, of.data());
   for (int32_t i = 0; i < d; ++i) out[i] = f32_to_bf16(of[i]);
 }
 
@@ -464,7 +467,7 @@ void orc_gemv(const uint16_t *w, int32_t rows, int32_t cols, const uint16_t *x,
   orc_tensor wt;
   memset(&wt, 0, sizeof(wt));
   wt.data = w;
-  gemv(Tensor(wt), 0, rows, cols, xf.data(), accum_double != 0, out);
+  gemv(Tensor(wt), 0, rows, cols, xf.data(), accum_double, out);
 }
 
 void orc_rope(uint16_t *x, int32_t n_heads, int32_t head_dim, int64_t pos, double base) {
@@ -484,7 +487,7 @@ void orc_attention_head(const uint16_t *q, const uint16_t *keys, const uint16_t 
     kf[i] = bf16_to_f32(keys[i]);
     vf[i] = bf16_to_f32(vals[i]);
   }
-  attention_head(qf.data(), kf.data(), vf.data(), n, D, accum_double != 0, of.data());
+  attention_head(qf.data(), kf.data(), vf.data(), n, D, accum_double, of.data());
   for (int64_t i = 0; i < D; ++i) out[i] = f32_to_bf16(of[i]);
 }
 
@@ -497,7 +500,7 @@ float orc_silu(float x) { return silu(x); }
 
 void orc_expert(const uint16_t *n, const uint16_t *wg, const uint16_t *wu,
                 const uint16_t *wd, int32_t d, int32_t f, int32_t accum_double, float *y) {
-  const bool dbl = accum_double != 0;
+  const int dbl = accum_double;
   std::vector<float> nf(d), g(f), u(f), a(f);
   for (int32_t i = 0; i < d; ++i) nf[i] = bf16_to_f32(n[i]);
   orc_tensor t;

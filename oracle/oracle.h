@@ -24,9 +24,11 @@
  * the readings are listed in the repository's design notes; each function
  * below names the reading it implements.
  *
- * Precision: fp32 accumulation over bf16-rounded weights and activations
- * (accum_double = 1 switches every accumulation to double, to bound the
- * fp32 summation-order noise).  Every loop runs in its plain order.
+ * Precision: fp32 accumulation over bf16-rounded weights and activations.
+ * The accum_double argument selects the accumulation: 0 = fp32 in ascending
+ * index order (the plain order of every loop), 1 = double (to measure the
+ * fp32 summation-order noise against), 2 = fp32 in descending index order
+ * (a second, equally faithful fp32 evaluation).
  *
  * Parity: every function here is pinned by the not-gpu tests (closed forms,
  * invariants, library routines, brute force); none is "parity unpinned".

@@ -31,11 +31,12 @@ MK_OK = 0
 STATUS_NAMES = {0: "MK_OK", 1: "MK_ERR_INVALID_ARG", 2: "MK_ERR_BATCH", 3: "MK_ERR_PAGE_OOB",
                 4: "MK_ERR_NO_SCHEDULE", 5: "MK_ERR_CUDA", 6: "MK_ERR_DEVICE_TIMEOUT",
                 7: "MK_ERR_BAD_TASK", 8: "MK_ERR_UNSUPPORTED", 9: "MK_ERR_NO_DEVICE",
-                10: "MK_ERR_SCRATCH_LIMIT"}
+                10: "MK_ERR_SCRATCH_LIMIT", 11: "MK_ERR_BAD_TOKEN"}
 MK_ERR_INVALID_ARG, MK_ERR_BATCH, MK_ERR_PAGE_OOB, MK_ERR_NO_SCHEDULE = 1, 2, 3, 4
 MK_ERR_CUDA, MK_ERR_DEVICE_TIMEOUT, MK_ERR_BAD_TASK, MK_ERR_UNSUPPORTED = 5, 6, 7, 8
 MK_ERR_NO_DEVICE = 9
 MK_ERR_SCRATCH_LIMIT = 10
+MK_ERR_BAD_TOKEN = 11
 
 
 def build_commands() -> List[List[str]]:

@@ -52,7 +52,8 @@ struct mk_ctx {
   uint8_t *ws = nullptr;
   size_t ws_bytes = 0;
   uint16_t *h = nullptr, *qkv = nullptr, *o = nullptr, *act = nullptr;
-  float *attn_part = nullptr, *router_logits = nullptr, *lm_part = nullptr, *rope = nullptr;
+  float *attn_part = nullptr, *attn_part2 = nullptr, *router_logits = nullptr, *lm_part = nullptr,
+        *rope = nullptr;
   mk_routing *routing = nullptr;
   int32_t *ctr = nullptr, *seq_lens_dev = nullptr, *page_table_dev = nullptr;
   mk_ctrl *ctrl = nullptr;
@@ -202,6 +203,7 @@ const char *mk_status_string(mk_status s) {
     case MK_ERR_UNSUPPORTED: return "unsupported dimensions";
     case MK_ERR_NO_DEVICE: return "no usable sm_103 device";
     case MK_ERR_SCRATCH_LIMIT: return "workspace larger than the static scratch of mk_decode_step_static";
+    case MK_ERR_BAD_TOKEN: return "token id outside the vocabulary";
     default: return "unknown status";
   }
 }
@@ -274,6 +276,7 @@ mk_status mk_create(const mk_model_dims *dims, const mk_weights *w, void *stream
   const size_t o_qkv = cv.take((size_t)L * MB * QKVD * 2);
   const size_t o_o = cv.take((size_t)L * MB * HqD * 2);
   const size_t o_part = cv.take((size_t)L * c->n_slots_max * G * (d.head_dim + 4) * 4);
+  const size_t o_part2 = cv.take((size_t)L * c->n_slots_max * G * (d.head_dim + 4) * 4);
   const size_t o_rl = cv.take((size_t)L * MB * d.n_experts * 4);
   const size_t o_rt = cv.take((size_t)L * sizeof(mk_routing));
   const size_t o_act = cv.take((size_t)L * c->u_max * MB * d.d_ffn * 2);
@@ -296,6 +299,7 @@ mk_status mk_create(const mk_model_dims *dims, const mk_weights *w, void *stream
   c->qkv = (uint16_t *)(c->ws + o_qkv);
   c->o = (uint16_t *)(c->ws + o_o);
   c->attn_part = (float *)(c->ws + o_part);
+  c->attn_part2 = (float *)(c->ws + o_part2);
   c->router_logits = (float *)(c->ws + o_rl);
   c->routing = (mk_routing *)(c->ws + o_rt);
   c->act = (uint16_t *)(c->ws + o_act);
@@ -471,6 +475,7 @@ mk_status mk_decode_step(mk_ctx *c, const int32_t *token_ids, float *out_logits,
   p.qkv = c->qkv;
   p.o = c->o;
   p.attn_part = c->attn_part;
+  p.attn_part2 = c->attn_part2;
   p.router_logits = c->router_logits;
   p.routing = c->routing;
   p.act = c->act;
@@ -497,6 +502,7 @@ mk_status mk_decode_step(mk_ctx *c, const int32_t *token_ids, float *out_logits,
   p.stage_bytes = sm.stage_bytes;
   p.kv_maps = c->kv_maps;
   p.xbuf_bytes = (int32_t)sm.xbuf;
+  p.xn_bytes = (int32_t)sm.xn;
   p.poison_layer = c->poison_layer;
   p.poison_delta = c->poison_delta;
   p.trace = c->trace;

@@ -21,7 +21,10 @@ enum {
   OP_ROUTER = 2,   /* [2] row0 (expert), [3] nrows */
   OP_ATTN = 3,     /* [1] b, [2] kvh, [3] page0, [4] page1 (-1: up to the live length),
                       [5] slot (partial slot), [6] slot0 of (b,kvh), [7] n_splits,
-                      [8] is_last (handles and appends the new token) */
+                      [8] is_last (handles and appends the new token),
+                      [9] merge group, [10] splits in the group, [11] groups of (b,kvh),
+                      [12] first split slot of the group, [13] the group's level-2 slot,
+                      [14] first level-2 slot of (b,kvh) */
   OP_UP = 4,       /* [1] share, [2] n_shares */
   OP_OUT = 5,      /* [2] row0, [3] nrows */
   OP_LM = 6        /* [2] row0, [3] nrows, [4] lm task index */
@@ -40,13 +43,20 @@ enum {
   CTR_ATTN_DONE = 3,
   CTR_UP_DONE = 4,
   CTR_OUT_DONE = 5,
-  CTR_ATTN_TICKET0 = 6 /* + b * n_kv_heads + kvh */
+  CTR_ATTN_TICKET0 = 6 /* + (b * n_kv_heads + kvh) * (1 + MK_MAX_MERGE_GROUPS):
+                          the final merge ticket, then one ticket per merge group */
 };
 /* after the per-layer blocks: */
 enum { GCTR_LM_TICKET = 0, GCTR_EXIT = 1, GCTR_COUNT = 2 };
 
+/* Attention splits of one (sequence, kv head) merge in two levels: groups
+ * of up to MK_MERGE_GROUP splits (the last to finish merges its group),
+ * then the groups (the last group merger writes the output). */
+#define MK_MERGE_GROUP 8
+#define MK_MAX_MERGE_GROUPS 32
+
 static inline int mk_ctrs_per_layer(int max_batch, int n_kv_heads) {
-  return CTR_ATTN_TICKET0 + max_batch * n_kv_heads;
+  return CTR_ATTN_TICKET0 + max_batch * n_kv_heads * (1 + MK_MAX_MERGE_GROUPS);
 }
 
 /* ---- limits ----------------------------------------------------------------- */
@@ -55,7 +65,7 @@ static inline int mk_ctrs_per_layer(int max_batch, int n_kv_heads) {
 #define MK_MAX_GROUP 8          /* q heads per kv head */
 #define MK_MAX_OUT_ROWS 64      /* rows of d per OUT task */
 #define MK_NC_WARPS 8           /* consumer warps; ring slot w belongs to consumer warp w */
-#define MK_THREADS ((MK_NC_WARPS + 1) * 32)
+#define MK_THREADS ((MK_NC_WARPS + 1) * 32) /* + the producer warp */
 #define MK_MAX_STAGE_ROWS 64
 #define MK_MAX_STAGE_BYTES 32768
 #define MK_MAX_STAGE_PAGES 8
@@ -108,6 +118,7 @@ typedef struct {
   uint16_t *qkv;              /* [L][MAXB][(Hq+2Hkv)D] pre-RoPE q, k, v */
   uint16_t *o;                /* [L][MAXB][Hq D] */
   float *attn_part;           /* [L][n_slots][G][D + 4] (m, l, -, -, o[D]) */
+  float *attn_part2;          /* [L][n_slots][G][D + 4] merge-group partials */
   float *router_logits;       /* [L][MAXB][E] */
   mk_routing *routing;        /* [L] */
   uint16_t *act;              /* [L][Umax][MAXB][F] */
@@ -128,7 +139,8 @@ typedef struct {
   int32_t *err_host;          /* host-mapped mirror: [code, cta, task, op, layer, ctr, seen, target] */
   int32_t stage_bytes;        /* bytes of one ring slot (a multiple of 1024) */
   const void *kv_maps;        /* [L][2] CUtensorMap of the K and V pools (64-byte aligned) */
-  int32_t xbuf_bytes;         /* shared activation buffer */
+  int32_t xbuf_bytes;         /* shared scratch buffer */
+  int32_t xn_bytes;           /* shared normed-input buffer (kept across a layer's tasks) */
   int32_t poison_layer, poison_delta; /* test hook: see mk_debug_poison_wait */
   unsigned long long *trace;  /* NULL, or [n_cta][trace_cap][MK_TRACE_WORDS] task timestamps */
   int32_t trace_cap;

@@ -307,12 +307,130 @@ __device__ __forceinline__ void take_out(int n0, const float (&c)[4], int R, int
   }
 }
 
+/* Sum over 32 lanes of 8 values at once: three "transposing" rounds leave
+ * each lane one partial, two plain butterfly rounds finish: lanes 4r..4r+3
+ * end with the sum of v[r]. */
+__device__ __forceinline__ float transpose_reduce8(float (&v)[8], int lane) {
+#pragma unroll
+  for (int r = 0; r < 3; ++r) {
+    const int half = 8 >> (r + 1), mask = 16 >> r;
+    const bool upper = (lane & mask) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = upper ? v[i] : v[i + half];
+      const float keep = upper ? v[i + half] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, mask);
+    }
+  }
+  float s = v[0];
+  s += __shfl_xor_sync(0xFFFFFFFFu, s, 2);
+  s += __shfl_xor_sync(0xFFFFFFFFu, s, 1);
+  return s;
+}
+
+__device__ __forceinline__ unsigned long long pack2(uint32_t lo, uint32_t hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+
+/* two fp32 FMAs in one instruction (lanes of the pair independent) */
+__device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+__device__ __forceinline__ float sum2(unsigned long long v) {
+  uint32_t lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(v));
+  return __uint_as_float(lo) + __uint_as_float(hi);
+}
+
+/* a bf16 pair (one 32-bit word) as an fp32 pair */
+__device__ __forceinline__ unsigned long long bf2_f2(uint32_t w) {
+  return pack2(w << 16, w & 0xFFFF0000u);
+}
+
+/* NR rows (virtual n0 .. n0 + NR - 1) of one token on the CUDA cores; the
+ * row count is a template parameter so that every load of the block can be
+ * issued ahead of the FMAs.  v[r] gets this lane's partial sum of row r. */
+template <int NR, class RowMap>
+__device__ __forceinline__ void cc_block(const uint8_t *st, int n0, int pitch, int K,
+                                         const uint16_t *x, int lane, RowMap &rm, float (&v)[8]) {
+  const uint8_t *w[NR];
+#pragma unroll
+  for (int r = 0; r < NR; ++r) w[r] = st + (size_t)rm(n0 + r) * pitch + 8 * lane;
+  unsigned long long a[NR][2];
+#pragma unroll
+  for (int r = 0; r < NR; ++r) a[r][0] = a[r][1] = 0ULL;
+  const uint16_t *xl = x + 4 * lane;
+  const int K128 = K & ~127; /* K is a multiple of 64: a half block may remain */
+#pragma unroll 2
+  for (int c = 0; c < K128; c += 128) {
+    const uint2 xv = *(const uint2 *)(xl + c);
+    uint2 wv[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) wv[r] = *(const uint2 *)(w[r] + 2 * c);
+    const unsigned long long x0 = bf2_f2(xv.x), x1 = bf2_f2(xv.y);
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      a[r][0] = ffma2(bf2_f2(wv[r].x), x0, a[r][0]);
+      a[r][1] = ffma2(bf2_f2(wv[r].y), x1, a[r][1]);
+    }
+  }
+  if (K128 < K && lane < 16) {
+    const uint2 xv = *(const uint2 *)(xl + K128);
+    const unsigned long long x0 = bf2_f2(xv.x), x1 = bf2_f2(xv.y);
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      const uint2 wv = *(const uint2 *)(w[r] + 2 * K128);
+      a[r][0] = ffma2(bf2_f2(wv.x), x0, a[r][0]);
+      a[r][1] = ffma2(bf2_f2(wv.y), x1, a[r][1]);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < 8; ++r) v[r] = r < NR ? sum2(a[r < NR ? r : 0][0]) + sum2(a[r < NR ? r : 0][1]) : 0.0f;
+}
+
+/* One token on the CUDA cores (a tensor-core tile would use 1 of its 16 M
+ * rows): the rows of one ring stage (stage row rm(v), pitch bytes apart)
+ * against the bf16 activation x, up to eight rows per pass sharing each load
+ * of x.  Lane l handles columns 4l + 128i (K a multiple of 64); each pair of
+ * products is one packed fp32x2 FMA.  blk(n0, s, nr) runs on every lane
+ * with lane l holding the sum of virtual row n0 + l / 4 (valid for l / 4 <
+ * nr). */
+template <class RowMap, class Blk>
+__device__ __forceinline__ void cc_rows(const uint8_t *st, int R, int pitch, int K,
+                                        const uint16_t *x, int lane, RowMap &&rm, Blk &&blk) {
+  for (int n0 = 0; n0 < R; n0 += 8) {
+    const int nr = min(8, R - n0);
+    float v[8];
+    switch (nr) {
+      case 1: cc_block<1>(st, n0, pitch, K, x, lane, rm, v); break;
+      case 2: cc_block<2>(st, n0, pitch, K, x, lane, rm, v); break;
+      case 3: cc_block<3>(st, n0, pitch, K, x, lane, rm, v); break;
+      case 4: cc_block<4>(st, n0, pitch, K, x, lane, rm, v); break;
+      case 5: cc_block<5>(st, n0, pitch, K, x, lane, rm, v); break;
+      case 6: cc_block<6>(st, n0, pitch, K, x, lane, rm, v); break;
+      case 7: cc_block<7>(st, n0, pitch, K, x, lane, rm, v); break;
+      default: cc_block<8>(st, n0, pitch, K, x, lane, rm, v); break;
+    }
+    blk(n0, transpose_reduce8(v, lane), nr);
+  }
+}
+
 /* ----------------------------------------------------------- shared layout */
 
+#define MK_PAGE_CACHE 256
 template <int NB>
 struct Misc {
   uint64_t full[NC];
   uint64_t empty[NC];
+  /* the producer's caches (offsets independent of NB) */
+  int32_t pexp[128];          /* expert id of each slot of the current layer */
+  int32_t ppage[MK_PAGE_CACHE]; /* page ids of the current attention split */
   int32_t norm_layer; /* layer whose normed input sits in xbuf (-2: none) */
   int32_t ok;         /* 0 once a consumer stopped early */
   int32_t pad0[2];
@@ -344,15 +462,20 @@ extern __shared__ __align__(1024) uint8_t mk_smem[];
 
 struct Ctx {
   const mk_kparams *p;
-  uint32_t ring_off, xbuf_off, misc_off; /* byte offsets into mk_smem */
+  uint32_t ring_off, xn_off, xbuf_off, misc_off; /* byte offsets into mk_smem */
   uint32_t epoch;
   int cta;
   int SB; /* bytes of one ring slot */
   __device__ __forceinline__ uint8_t *ring() const { return mk_smem + ring_off; }
   __device__ __forceinline__ uint8_t *xbuf() const { return mk_smem + xbuf_off; }
+  /* the normed layer input [NB][d] bf16, kept while the layer's QKV, router
+   * and expert tasks run (the scratch buffer is reused in between) */
+  __device__ __forceinline__ uint16_t *xn() const { return (uint16_t *)(mk_smem + xn_off); }
   /* the mbarriers open the control block: full[NC], then empty[NC] */
   __device__ __forceinline__ uint64_t *full() const { return (uint64_t *)(mk_smem + misc_off); }
   __device__ __forceinline__ uint64_t *empty() const { return full() + NC; }
+  __device__ __forceinline__ int32_t *pexp() const { return (int32_t *)(empty() + NC); }
+  __device__ __forceinline__ int32_t *ppage() const { return pexp() + 128; }
 };
 
 __device__ __forceinline__ int32_t *lctr(const mk_kparams &p, int layer, int kind) {
@@ -460,12 +583,20 @@ struct StageDesc {
   int pages[MK_MAX_STAGE_PAGES]; /* PAGES: physical page ids */
 };
 
-enum { IT_STAGE = 1, IT_END = 0, IT_BLOCKED = -1, IT_FAIL = -2 };
+enum { IT_STAGE = 1, IT_END = 0, IT_FAIL = -2 };
 
+/* The producer's cursor over the CTA's stage sequence.  Everything it reads
+ * per stage is cached in registers at init or at the start of a task. */
 struct StageIter {
   const mk_kparams *p;
   const int32_t *row;
-  int nl, nf, SB;
+  /* cached parameters */
+  int L, d, HqD, F, P, D, Hkv, max_pages, SB, pps_kv, pps_up;
+  const mk_layer_dev *layers;
+  const uint16_t *lm_head;
+  const int32_t *page_table, *seq_lens;
+  const mk_routing *routing_base;
+  int nl, nf;
   uint32_t epoch;
   int layer, k;   /* current task (layer == L: the final tasks) */
   bool started;
@@ -475,44 +606,80 @@ struct StageIter {
   const int32_t *t;
   const mk_layer_dev *ly;
   const uint16_t *src; /* row streams */
-  int r, nrows, K;
+  int r, nrows, K, rps;
   int q, p1, b, kvh;   /* attention pages */
   int64_t v, v1;       /* gate/up share */
-  int u, U;            /* OUT: u = -1 while on Wo rows, then the down slot */
+  int u, U, r0o, nro;  /* OUT: u = -1 while on Wo rows, then the down slot */
   const mk_routing *rt;
+  int32_t *pexp, *ppage; /* shared-memory caches of expert and page ids */
+  int exp_layer;         /* layer whose expert ids pexp holds (-1: none) */
+  int p0a;               /* first page of the current attention split */
 
   __device__ void init(const mk_kparams *pp, const int32_t *rw, uint32_t ep, int sb) {
     p = pp;
     row = rw;
+    L = pp->L;
+    d = pp->d;
+    HqD = pp->Hq * pp->D;
+    F = pp->F;
+    P = pp->P;
+    D = pp->D;
+    Hkv = pp->Hkv;
+    max_pages = pp->max_pages;
+    SB = sb;
+    pps_kv = mk_pages_per_stage(P, D, sb);
+    pps_up = mk_pairs_per_stage(d, sb);
+    layers = pp->layers;
+    lm_head = pp->lm_head;
+    page_table = pp->page_table;
+    seq_lens = pp->seq_lens;
+    routing_base = pp->routing;
     nl = rw[1];
     nf = rw[2];
-    SB = sb;
     epoch = ep;
     layer = 0;
     k = 0;
     started = false;
     count = 0;
-    if (nl == 0) layer = p->L; /* no layer tasks */
+    exp_layer = -1;
+    if (nl == 0) layer = L; /* no layer tasks */
   }
 
-  __device__ bool at_end() const { return layer > p->L || (layer == p->L && k >= nf); }
+  /* Routing of this layer known: U and all expert ids into shared memory
+   * (independent loads in batches of 16, one round trip each). */
+  __device__ bool experts(const Ctx &cx) {
+    if (exp_layer == layer) return true;
+    if (!routing(cx)) return false;
+    rt = routing_base + layer;
+    U = __ldcg(&rt->U);
+    for (int u0 = 0; u0 < U; u0 += 16) {
+      int e[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) e[j] = u0 + j < U ? __ldcg(&rt->expert[u0 + j]) : 0;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) pexp[u0 + j] = e[j];
+    }
+    exp_layer = layer;
+    return true;
+  }
+
+  __device__ bool at_end() const { return layer > L || (layer == L && k >= nf); }
 
   __device__ void next_task() {
     started = false;
     ++k;
-    if (layer < p->L && k >= nl) {
+    if (layer < L && k >= nl) {
       k = 0;
       ++layer;
-      if (layer < p->L && nl == 0) layer = p->L;
+      if (layer < L && nl == 0) layer = L;
     }
   }
 
-  /* Routing of this task's layer: known? (blocking: wait, bounded). */
-  __device__ int routing(bool block, const Ctx &cx) {
+  /* Waits (bounded) until the routing of this task's layer is known. */
+  __device__ bool routing(const Ctx &cx) {
     int32_t *c = lctr(*p, layer, CTR_ROUTED);
-    if ((int)(ld_acquire(c) - (int)(epoch + 1)) >= 0) return IT_STAGE;
-    if (!block) return IT_BLOCKED;
-    return wait_counter(cx, c, (int)(epoch + 1), -1, OP_UP, layer, CTR_ROUTED) ? IT_STAGE : IT_FAIL;
+    if ((int)(ld_acquire(c) - (int)(epoch + 1)) >= 0) return true;
+    return wait_counter(cx, c, (int)(epoch + 1), -1, OP_UP, layer, CTR_ROUTED);
   }
 
   __device__ void rows_from(const uint16_t *s0, int n, int KK) {
@@ -520,44 +687,53 @@ struct StageIter {
     r = 0;
     nrows = n;
     K = KK;
+    rps = mk_rows_per_stage(KK, SB);
   }
 
-  __device__ int begin(bool block, const Ctx &cx) {
-    t = row + MK_DESC_INTS * (1 + (layer < p->L ? k : nl + k));
+  __device__ int begin(const Ctx &cx) {
+    t = row + MK_DESC_INTS * (1 + (layer < L ? k : nl + k));
     op = t[0];
-    const int L = layer < p->L ? layer : p->L - 1;
-    ly = p->layers + L;
+    ly = layers + (layer < L ? layer : L - 1);
     switch (op) {
       case OP_QKV: {
         const uint16_t *w = t[1] == 0 ? ly->wq : t[1] == 1 ? ly->wk : ly->wv;
-        rows_from(w + (size_t)t[2] * p->d, t[3], p->d);
+        rows_from(w + (size_t)t[2] * d, t[3], d);
         return IT_STAGE;
       }
       case OP_ROUTER:
-        rows_from(ly->wr + (size_t)t[2] * p->d, t[3], p->d);
+        rows_from(ly->wr + (size_t)t[2] * d, t[3], d);
         return IT_STAGE;
       case OP_LM:
-        rows_from(p->lm_head + (size_t)t[2] * p->d, t[3], p->d);
+        rows_from(lm_head + (size_t)t[2] * d, t[3], d);
         return IT_STAGE;
-      case OP_ATTN:
+      case OP_ATTN: {
         b = t[1];
         kvh = t[2];
-        q = t[3];
-        p1 = t[4] >= 0 ? t[4] : (__ldg(p->seq_lens + b) + p->P - 1) / p->P;
+        q = p0a = t[3];
+        p1 = t[4] >= 0 ? t[4] : (__ldg(seq_lens + b) + P - 1) / P;
+        /* the split's page ids (up to MK_PAGE_CACHE) in batches of 16 */
+        const int n = min(p1 - p0a, MK_PAGE_CACHE);
+        for (int j0 = 0; j0 < n; j0 += 16) {
+          int pg[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) pg[j] = j0 + j < n ? __ldg(page_table + b * max_pages + p0a + j0 + j) : 0;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) ppage[j0 + j] = pg[j];
+        }
         return IT_STAGE;
+      }
       case OP_UP: {
-        const int rs = routing(block, cx);
-        if (rs != IT_STAGE) return rs;
-        rt = p->routing + layer;
-        U = __ldcg(&rt->U);
-        const int64_t T = (int64_t)U * p->F;
+        if (!experts(cx)) return IT_FAIL;
+        const int64_t T = (int64_t)U * F;
         v = T * t[1] / t[2];
         v1 = T * (t[1] + 1) / t[2];
         return IT_STAGE;
       }
       case OP_OUT:
         u = -1;
-        rows_from(ly->wo + (size_t)t[2] * p->Hq * p->D, t[3], p->Hq * p->D);
+        r0o = t[2];
+        nro = t[3];
+        rows_from(ly->wo + (size_t)r0o * HqD, nro, HqD);
         return IT_STAGE;
       default:
         return IT_FAIL; /* the consumers report the bad opcode */
@@ -566,7 +742,7 @@ struct StageIter {
 
   __device__ bool row_stage(StageDesc &sd) {
     if (r >= nrows) return false;
-    const int cnt = min(mk_rows_per_stage(K, SB), nrows - r);
+    const int cnt = min(rps, nrows - r);
     sd.kind = SK_ROWS;
     sd.n = cnt;
     sd.a = (const uint8_t *)(src + (size_t)r * K);
@@ -575,8 +751,8 @@ struct StageIter {
     return true;
   }
 
-  /* IT_STAGE: a stage; IT_END: this task has no more; IT_BLOCKED / IT_FAIL */
-  __device__ int emit(StageDesc &sd, bool block, const Ctx &cx) {
+  /* IT_STAGE: a stage; IT_END: this task has no more; IT_FAIL */
+  __device__ int emit(StageDesc &sd, const Ctx &cx) {
     switch (op) {
       case OP_QKV:
       case OP_ROUTER:
@@ -584,25 +760,26 @@ struct StageIter {
         return row_stage(sd) ? IT_STAGE : IT_END;
       case OP_ATTN: {
         if (q >= p1) return IT_END;
-        const int cnt = min(mk_pages_per_stage(p->P, p->D, SB), p1 - q);
+        const int cnt = min(pps_kv, p1 - q);
         sd.kind = SK_PAGES;
         sd.n = cnt;
         sd.layer = layer;
         sd.kvh = kvh;
         sd.seq = b;
         sd.q0 = q;
-        /* all page ids of the stage in one batch of independent loads */
-        for (int j = 0; j < cnt; ++j) sd.pages[j] = __ldg(p->page_table + b * p->max_pages + q + j);
+        for (int j = 0; j < cnt; ++j) {
+          const int idx = q + j - p0a;
+          sd.pages[j] = idx < MK_PAGE_CACHE ? ppage[idx] : __ldg(page_table + b * max_pages + q + j);
+        }
         q += cnt;
         return IT_STAGE;
       }
       case OP_UP: {
         if (v >= v1) return IT_END;
-        const int F = p->F, d = p->d;
-        const int uu = (int)(v / F), f0 = (int)(v % F);
+        const int uu = (int)(v / F), f0 = (int)(v - (int64_t)uu * F);
         const int f1 = (int)min((int64_t)F, f0 + (v1 - v));
-        const int cnt = min(mk_pairs_per_stage(d, SB), f1 - f0);
-        const int e = __ldcg(&rt->expert[uu]);
+        const int cnt = min(pps_up, f1 - f0);
+        const int e = pexp[uu];
         const size_t eo = (size_t)e * F * d + (size_t)f0 * d;
         sd.kind = SK_PAIRS;
         sd.n = cnt;
@@ -615,16 +792,11 @@ struct StageIter {
       case OP_OUT: {
         while (true) {
           if (row_stage(sd)) return IT_STAGE;
-          if (u == -1) {
-            const int rs = routing(block, cx);
-            if (rs != IT_STAGE) return rs;
-            rt = p->routing + layer;
-            U = __ldcg(&rt->U);
-          }
+          if (u == -1 && !experts(cx)) return IT_FAIL;
           ++u;
           if (u >= U) return IT_END;
-          const int e = __ldcg(&rt->expert[u]);
-          rows_from(ly->wd + ((size_t)e * p->d + t[2]) * p->F, t[3], p->F);
+          const int e = pexp[u];
+          rows_from(ly->wd + ((size_t)e * d + r0o) * F, nro, F);
         }
       }
       default:
@@ -633,15 +805,15 @@ struct StageIter {
   }
 
   /* The next stage of the stream. */
-  __device__ int next(StageDesc &sd, bool block, const Ctx &cx) {
+  __device__ int next(StageDesc &sd, const Ctx &cx) {
     while (true) {
       if (at_end()) return IT_END;
       if (!started) {
-        const int rs = begin(block, cx);
+        const int rs = begin(cx);
         if (rs != IT_STAGE) return rs;
         started = true;
       }
-      const int rs = emit(sd, block, cx);
+      const int rs = emit(sd, cx);
       if (rs == IT_STAGE) {
         ++count;
         return IT_STAGE;
@@ -655,9 +827,9 @@ struct StageIter {
 struct Producer {
   Ctx cx;
   uint64_t policy;
-  int last_in_slot[NC];
 
-  __device__ void load(const StageDesc &sd, uint8_t *dst, uint64_t *bar) {
+  static __device__ void load(const StageDesc &sd, const Ctx &cx, uint64_t policy, uint8_t *dst,
+                              uint64_t *bar) {
     const mk_kparams &p = *cx.p;
     switch (sd.kind) {
       case SK_ROWS: {
@@ -689,25 +861,30 @@ struct Producer {
   }
 
   __device__ __noinline__ void run(const int32_t *row) {
-    for (int s = 0; s < NC; ++s) last_in_slot[s] = -1;
+    const Ctx c = cx; /* a register copy: `this` lives in local memory */
+    const uint64_t pol = policy;
+    int last_slot[NC];
+    for (int s = 0; s < NC; ++s) last_slot[s] = -1;
     StageIter ld;
-    ld.init(cx.p, row, cx.epoch, cx.SB);
+    ld.init(c.p, row, c.epoch, c.SB);
+    ld.pexp = c.pexp();
+    ld.ppage = c.ppage();
     StageDesc sd;
-    unsigned long long *strc = cx.cta == 0 ? cx.p->stage_trace : nullptr;
+    unsigned long long *strc = c.cta == 0 ? c.p->stage_trace : nullptr;
     while (true) {
       const uint64_t ta = strc ? gtimer() : 0;
-      const int rs = ld.next(sd, true, cx);
+      const int rs = ld.next(sd, c);
       if (rs != IT_STAGE) break; /* end, or a failed wait (already reported) */
-      const long i = ld.count - 1;
-      const int slot = (int)(i % NC);
+      const int i = (int)ld.count - 1;
+      const int slot = i % NC;
       const uint64_t tb = strc ? gtimer() : 0;
       if (i >= NC) {
         const uint32_t parity = (uint32_t)(((i / NC) - 1) & 1);
-        if (!wait_mbar(cx, &cx.empty()[slot], parity, -1, -1, -1)) break;
+        if (!wait_mbar(c, &c.empty()[slot], parity, -1, -1, -1)) break;
       }
       const uint64_t tc = strc ? gtimer() : 0;
-      load(sd, cx.ring() + (size_t)slot * cx.SB, &cx.full()[slot]);
-      last_in_slot[slot] = (int)i;
+      load(sd, c, pol, c.ring() + (size_t)slot * c.SB, &c.full()[slot]);
+      last_slot[slot] = i;
       if (strc && i < MK_STAGE_TRACE_EVENTS) {
         unsigned long long *e = strc + (size_t)i * 8;
         e[1] = ta;
@@ -719,11 +896,11 @@ struct Producer {
     /* Every copy issued must land before the CTA exits (normally the
      * consumers have waited for all of them already). */
     for (int s = 0; s < NC; ++s) {
-      const int k = last_in_slot[s];
+      const int k = last_slot[s];
       if (k < 0) continue;
       const uint32_t parity = (uint32_t)((k / NC) & 1);
       const uint64_t t0 = gtimer();
-      while (!mbar_test(&cx.full()[s], parity) && gtimer() - t0 < cx.p->wait_limit_ns) {
+      while (!mbar_test(&c.full()[s], parity) && gtimer() - t0 < c.p->wait_limit_ns) {
       }
     }
   }
@@ -817,7 +994,16 @@ struct Consumer {
 
   __device__ const uint16_t *h_row(int layer, int b) const {
     const mk_kparams &p = *cx.p;
-    if (layer == 0) return p.embed + (size_t)__ldg(p.tokens + b) * p.d;
+    if (layer == 0) {
+      /* a token id outside the vocabulary fails the step (sticky) and reads
+       * row 0 instead, so nothing outside the embedding table is touched */
+      int tok = __ldg(p.tokens + b);
+      if ((unsigned)tok >= (unsigned)p.V) {
+        raise_error(p, MK_ERR_BAD_TOKEN, cx.cta, -1, -1, 0, b, tok, p.V);
+        tok = 0;
+      }
+      return p.embed + (size_t)tok * p.d;
+    }
     return p.h + ((size_t)layer * MK_MAX_BATCH + b) * p.d;
   }
 
@@ -841,14 +1027,14 @@ struct Consumer {
     bar_consumers();
   }
 
-  /* xbuf[b][0..d) (pitch d + 32) = bf16((h * (1/sqrtf(mean_fp32(h^2) +
-   * eps))) * g); rows b >= B zero.  h is read once with 16-byte loads and
-   * staged behind the output in xbuf. */
+  /* xn[b][0..d) = bf16((h * (1/sqrtf(mean_fp32(h^2) + eps))) * g); rows
+   * b >= B zero.  h is read once with 16-byte loads and staged in the
+   * scratch buffer. */
   __device__ void norm_into_xbuf(int layer_tag, const uint16_t *const *hrows, const uint16_t *g) {
     const mk_kparams &p = *cx.p;
     const int xp = mk_x_pitch(p.d);
-    uint16_t *x = (uint16_t *)cx.xbuf();
-    uint16_t *raw = x + (size_t)NB * xp;
+    uint16_t *x = cx.xn();
+    uint16_t *raw = (uint16_t *)cx.xbuf();
     const int n8 = p.d / 8;
     float ss[NB];
 #pragma unroll
@@ -904,11 +1090,6 @@ struct Consumer {
     norm_into_xbuf(layer, hr, cx.p->layers[layer].norm);
   }
 
-  __device__ void invalidate_norm() {
-    bar_consumers();
-    if (tid == 0) M()->norm_layer = -2;
-  }
-
   /* Copies NB vectors of n bf16 (global, row stride gstride) into xbuf at
    * pitch n + 32; rows b >= B zero.  No barrier. */
   __device__ void load_x(uint16_t *dst, const uint16_t *src, size_t gstride, int n) {
@@ -953,12 +1134,19 @@ struct Consumer {
       uint8_t *st;
       if (!stage_wait(si + j, st, task, op, layer)) break;
       const int r0 = j * rps, cnt = min(rps, nrows - r0);
-      mma_rows<NB>(st, cnt, pitch, K, x, xp, lane, [](int v) { return v; },
-                   [&](int n0, const float(&a)[4], const float(&b)[4], bool two) {
-                     auto f = [&](int r, int bb, float v) { epi(r0 + r, bb, v); };
-                     take_out<NB>(n0, a, cnt, lane, f);
-                     if (two) take_out<NB>(n0 + 8, b, cnt, lane, f);
-                   });
+      if (NB == 1) {
+        cc_rows(st, cnt, pitch, K, x, lane, [](int v) { return v; },
+                [&](int n0, float sum, int nr) {
+                  if ((lane & 3) == 0 && (lane >> 2) < nr) epi(r0 + n0 + (lane >> 2), 0, sum);
+                });
+      } else {
+        mma_rows<NB>(st, cnt, pitch, K, x, xp, lane, [](int v) { return v; },
+                     [&](int n0, const float(&a)[4], const float(&b)[4], bool two) {
+                       auto f = [&](int r, int bb, float v) { epi(r0 + r, bb, v); };
+                       take_out<NB>(n0, a, cnt, lane, f);
+                       if (two) take_out<NB>(n0 + 8, b, cnt, lane, f);
+                     });
+      }
       stage_release(si + j);
     }
     si += n_st;
@@ -975,7 +1163,7 @@ struct Consumer {
     const int base = (t[1] == 0 ? 0 : t[1] == 1 ? p.Hq * p.D : (p.Hq + p.Hkv) * p.D) + t[2];
     uint16_t *out = p.qkv + (size_t)layer * MK_MAX_BATCH * QKVD;
     const int B = p.B;
-    gemv_rows(t[3], p.d, (const uint16_t *)cx.xbuf(), task, OP_QKV, layer,
+    gemv_rows(t[3], p.d, cx.xn(), task, OP_QKV, layer,
               [&](int r, int b, float v) {
                 if (b < B) out[(size_t)b * QKVD + base + r] = f2bf(v);
               });
@@ -995,7 +1183,7 @@ struct Consumer {
     float *lg = p.router_logits + (size_t)layer * MK_MAX_BATCH * p.E;
     const float *bias = p.layers[layer].bias;
     const int B = p.B, E = p.E;
-    gemv_rows(t[3], p.d, (const uint16_t *)cx.xbuf(), task, OP_ROUTER, layer,
+    gemv_rows(t[3], p.d, cx.xn(), task, OP_ROUTER, layer,
               [&](int r, int b, float v) {
                 if (b < B) lg[(size_t)b * E + e0 + r] = bias ? v + __ldg(bias + e0 + r) : v;
               });
@@ -1093,6 +1281,79 @@ struct Consumer {
     }
   }
 
+  /* Merges n attention partials (consecutive slots at `parts`; per head
+   * [m, l, -, -, o[D]] with o unnormalised): M = max_s m_s, L = sum_s
+   * e^{m_s - M} l_s, O = sum_s e^{m_s - M} o_s.  With `out` it writes the
+   * partial [M, L, -, -, O] there; otherwise bf16(O / L) to ob[g][D].  Each
+   * thread's loads for a column are independent (one round trip for n <= 8). */
+  __device__ void merge_parts(const float *parts, int n, int G, int D, float *out, uint16_t *ob) {
+    const int PS = D + 4;
+    float *fm = (float *)cx.xbuf(); /* [n][G] m, then the factors */
+    float *fl = fm + n * G;         /* [n][G] l */
+    float *hd = fl + n * G;         /* [G] M, [G] L (or 1 / L) */
+    for (int i = tid; i < n * G; i += NCT) {
+      fm[i] = __ldcg(parts + (size_t)i * PS);
+      fl[i] = __ldcg(parts + (size_t)i * PS + 1);
+    }
+    bar_consumers();
+    if (tid < G) {
+      float M = NEG_INF;
+      for (int s2 = 0; s2 < n; ++s2) M = fmaxf(M, fm[s2 * G + tid]);
+      float den = 0.0f;
+      for (int s2 = 0; s2 < n; ++s2) {
+        const float ms = fm[s2 * G + tid];
+        if (ms != NEG_INF) den = fmaf(expf(ms - M), fl[s2 * G + tid], den);
+      }
+      hd[tid] = M;
+      hd[G + tid] = out ? den : 1.0f / den;
+    }
+    bar_consumers();
+    for (int i = tid; i < n * G; i += NCT) {
+      const int gg = i % G;
+      const float ms = fm[i];
+      fm[i] = ms == NEG_INF ? 0.0f : expf(ms - hd[gg]) * (out ? 1.0f : hd[G + gg]);
+    }
+    bar_consumers();
+    const int D4 = D / 4;
+    for (int i = tid; i < G * D4; i += NCT) {
+      const int gg = i / D4, j4 = i % D4;
+      float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      const float4 *src = (const float4 *)(parts + (size_t)gg * PS + 4) + j4;
+      int s2 = 0;
+      for (; s2 + 8 <= n; s2 += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = __ldcg(src + (size_t)(s2 + u) * G * PS / 4);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float f = fm[(s2 + u) * G + gg];
+          acc.x = fmaf(f, v[u].x, acc.x);
+          acc.y = fmaf(f, v[u].y, acc.y);
+          acc.z = fmaf(f, v[u].z, acc.z);
+          acc.w = fmaf(f, v[u].w, acc.w);
+        }
+      }
+      for (; s2 < n; ++s2) {
+        const float4 v = __ldcg(src + (size_t)s2 * G * PS / 4);
+        const float f = fm[s2 * G + gg];
+        acc.x = fmaf(f, v.x, acc.x);
+        acc.y = fmaf(f, v.y, acc.y);
+        acc.z = fmaf(f, v.z, acc.z);
+        acc.w = fmaf(f, v.w, acc.w);
+      }
+      if (out)
+        *((float4 *)(out + (size_t)gg * PS + 4) + j4) = acc;
+      else
+        *(uint2 *)(ob + (size_t)gg * D + j4 * 4) =
+            make_uint2(pack_bf16(f2bf(acc.x), f2bf(acc.y)), pack_bf16(f2bf(acc.z), f2bf(acc.w)));
+    }
+    if (out && tid < G) {
+      out[(size_t)tid * PS] = hd[tid];
+      out[(size_t)tid * PS + 1] = hd[G + tid];
+    }
+    bar_consumers();
+  }
+
   /* ---------------------------------------------------------- attention
    * Split-K flash decoding over the pages of one (sequence, kv head).  Each
    * warp runs the online softmax over the stages it owns on the tensor
@@ -1121,7 +1382,6 @@ struct Consumer {
     if (!cwait(lctr(p, layer, CTR_QKV_DONE), (int)((cx.epoch + 1) * p.n_qkv), task, OP_ATTN,
                layer, CTR_QKV_DONE))
       return false;
-    invalidate_norm();
     constexpr int QP = D + 8;                     /* q row pitch: conflict-free fragment loads */
     uint16_t *qs = (uint16_t *)cx.xbuf();           /* [8][QP] post-RoPE q, bf16 */
     float *ks = (float *)(cx.xbuf() + 16 * QP);     /* [D] new key */
@@ -1276,8 +1536,17 @@ struct Consumer {
                 v4[1] &= m1;
                 v4[3] &= m1;
               }
-              mma16816(o[2 * i], ah[0], al[0], ah[1], al[1], v4[0], v4[1]);
-              mma16816(o[2 * i + 1], ah[0], al[0], ah[1], al[1], v4[2], v4[3]);
+              /* each tile's P V from a zero accumulator, added to O with
+               * IEEE fp32 adds: the running sum over thousands of keys stays
+               * out of the tensor core's internal adder */
+              float t0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, t1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+              mma16816(t0, ah[0], al[0], ah[1], al[1], v4[0], v4[1]);
+              mma16816(t1, ah[0], al[0], ah[1], al[1], v4[2], v4[3]);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                o[2 * i][k] += t0[k];
+                o[2 * i + 1][k] += t1[k];
+              }
             }
           }
         }
@@ -1354,70 +1623,25 @@ struct Consumer {
       for (int n = 0; n < NT; ++n)
         *(float2 *)(part + (size_t)g * PS + 4 + 8 * n + 2 * tq) = make_float2(o[n][0], o[n][1]);
     }
-    /* the last split of (b, kvh) to finish merges all splits:
-     * o = sum_s f_s o_s with f_s = e^{m_s - M} / sum_s' e^{m_s' - M} l_s' */
+    /* merge in two levels: the last split of a group to finish merges the
+     * group, the last group merger merges the groups and writes o (one
+     * level when there is a single group) */
     if (!task_end()) return false;
-    if (!ticket(lctr(p, layer, CTR_ATTN_TICKET0 + b * p.Hkv + kvh), t[7])) return true;
-    const float *parts = p.attn_part + ((size_t)layer * p.n_slots + t[6]) * G * PS;
+    const int ng = t[11], bh = b * p.Hkv + kvh;
+    const int tk0 = CTR_ATTN_TICKET0 + bh * (1 + MK_MAX_MERGE_GROUPS);
     uint16_t *ob = p.o + ((size_t)layer * MK_MAX_BATCH + b) * p.Hq * D + (size_t)kvh * G * D;
-    const int ns = t[7];
-    float *fm = (float *)cx.xbuf();          /* [ns][G] m, then factors */
-    float *fl = fm + ns * G;               /* [ns][G] l */
-    float *hd = fl + ns * G;               /* [G] max, [G] 1 / denominator */
-    for (int i = tid; i < ns * G; i += NCT) {
-      fm[i] = __ldcg(parts + (size_t)i * PS);
-      fl[i] = __ldcg(parts + (size_t)i * PS + 1);
+    const float *part1 = p.attn_part + (size_t)layer * p.n_slots * G * PS;
+    float *part2 = p.attn_part2 + (size_t)layer * p.n_slots * G * PS;
+    if (ng <= 1) {
+      if (!ticket(lctr(p, layer, tk0), t[7])) return true;
+      merge_parts(part1 + (size_t)t[6] * G * PS, t[7], G, D, nullptr, ob);
+    } else {
+      if (!ticket(lctr(p, layer, tk0 + 1 + t[9]), t[10])) return true;
+      merge_parts(part1 + (size_t)t[12] * G * PS, t[10], G, D, part2 + (size_t)t[13] * G * PS,
+                  nullptr);
+      if (!ticket(lctr(p, layer, tk0), ng)) return true;
+      merge_parts(part2 + (size_t)t[14] * G * PS, ng, G, D, nullptr, ob);
     }
-    bar_consumers();
-    if (tid < G) {
-      float M = NEG_INF;
-      for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, fm[s2 * G + tid]);
-      float den = 0.0f;
-      for (int s2 = 0; s2 < ns; ++s2) {
-        const float ms = fm[s2 * G + tid];
-        if (ms != NEG_INF) den = fmaf(expf(ms - M), fl[s2 * G + tid], den);
-      }
-      hd[tid] = M;
-      hd[G + tid] = 1.0f / den;
-    }
-    bar_consumers();
-    for (int i = tid; i < ns * G; i += NCT) {
-      const int gg = i % G;
-      const float ms = fm[i];
-      fm[i] = ms == NEG_INF ? 0.0f : expf(ms - hd[gg]) * hd[G + gg];
-    }
-    bar_consumers();
-    const int D4 = D / 4;
-    for (int i = tid; i < G * D4; i += NCT) {
-      const int gg = i / D4, j4 = i % D4;
-      float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-      const float4 *src = (const float4 *)(parts + (size_t)gg * PS + 4) + j4;
-      int s2 = 0;
-      for (; s2 + 8 <= ns; s2 += 8) {
-        float4 v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = __ldcg(src + (size_t)(s2 + u) * G * PS / 4);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const float f = fm[(s2 + u) * G + gg];
-          acc.x = fmaf(f, v[u].x, acc.x);
-          acc.y = fmaf(f, v[u].y, acc.y);
-          acc.z = fmaf(f, v[u].z, acc.z);
-          acc.w = fmaf(f, v[u].w, acc.w);
-        }
-      }
-      for (; s2 < ns; ++s2) {
-        const float4 v = __ldcg(src + (size_t)s2 * G * PS / 4);
-        const float f = fm[s2 * G + gg];
-        acc.x = fmaf(f, v.x, acc.x);
-        acc.y = fmaf(f, v.y, acc.y);
-        acc.z = fmaf(f, v.z, acc.z);
-        acc.w = fmaf(f, v.w, acc.w);
-      }
-      *(uint2 *)(ob + (size_t)gg * D + j4 * 4) =
-          make_uint2(pack_bf16(f2bf(acc.x), f2bf(acc.y)), pack_bf16(f2bf(acc.z), f2bf(acc.w)));
-    }
-    bar_consumers();
     signal(lctr(p, layer, CTR_ATTN_DONE));
     return true;
   }
@@ -1437,7 +1661,7 @@ struct Consumer {
     const int64_t T = (int64_t)U * F;
     int64_t v = T * t[1] / t[2];
     const int64_t v1 = T * (t[1] + 1) / t[2];
-    const uint16_t *x = (const uint16_t *)cx.xbuf();
+    const uint16_t *x = cx.xn();
     const int pps = mk_pairs_per_stage(d, cx.SB), pitch = mk_row_pitch(d), xp = mk_x_pitch(d);
     int j = 0; /* stage index within the task */
     while (v < v1) {
@@ -1449,35 +1673,44 @@ struct Consumer {
         const int cnt = min(pps, f1 - f);
         uint8_t *st;
         if (!stage_wait(si + j, st, task, OP_UP, layer)) continue;
-        /* virtual row 2j is gate row j, 2j + 1 up row j: the lanes of a
-         * token hold gate (even g) and up (odd g) of the same pair four
-         * lanes apart */
-        mma_rows<NB>(
-            st, 2 * cnt, pitch, d, x, xp, lane,
-            [cnt](int vr) { return (vr & 1) ? cnt + (vr >> 1) : (vr >> 1); },
-            [&](int n0, const float(&a)[4], const float(&b)[4], bool two) {
-              const int g = lane >> 2, tq = lane & 3, q = g & 1;
+        auto swiglu = [&](int bb, int pr, float gv, float uv) {
+          if (bb < B) {
+            const float gb = rbf(gv), ub = rbf(uv);
+            const float silu = gb / (1.0f + expf(-gb));
+            out[(size_t)bb * F + f + pr] = f2bf(silu * ub);
+          }
+        };
+        auto pairmap = [cnt](int vr) { return (vr & 1) ? cnt + (vr >> 1) : (vr >> 1); };
+        if (NB == 1) {
+          /* virtual row 2j is gate row j, 2j + 1 up row j: lanes 8j'..8j'+3
+           * hold the gate sum, the next four lanes the up sum */
+          cc_rows(st, 2 * cnt, pitch, d, x, lane, pairmap, [&](int n0, float sum, int nr) {
+            const float up = __shfl_xor_sync(0xFFFFFFFFu, sum, 4);
+            const int r = lane >> 2;
+            if ((lane & 7) == 0 && r + 1 < nr) swiglu(0, (n0 + r) >> 1, sum, up);
+          });
+        } else {
+          /* the lanes of a token hold gate (even g) and up (odd g) of the
+           * same pair four lanes apart */
+          mma_rows<NB>(
+              st, 2 * cnt, pitch, d, x, xp, lane, pairmap,
+              [&](int n0, const float(&a)[4], const float(&b)[4], bool two) {
+                const int g = lane >> 2, tq = lane & 3, q = g & 1;
 #pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                if (h == 1 && !two) break;
-                const float(&c)[4] = h ? b : a;
-                const float va = q ? c[1] : c[0], vb = q ? c[3] : c[2];
-                const float oa = __shfl_xor_sync(0xFFFFFFFFu, va, 4);
-                const float ob = __shfl_xor_sync(0xFFFFFFFFu, vb, 4);
-                const int pr = ((n0 + 8 * h) >> 1) + tq; /* pair within the stage */
-                if (q == 0 && pr < cnt) {
-                  auto swiglu = [&](int bb, float gv, float uv) {
-                    if (bb < B) {
-                      const float gb = rbf(gv), ub = rbf(uv);
-                      const float silu = gb / (1.0f + expf(-gb));
-                      out[(size_t)bb * F + f + pr] = f2bf(silu * ub);
-                    }
-                  };
-                  if ((g >> 1) < NB) swiglu(g >> 1, va, oa);
-                  if (NB > 4 && 4 + (g >> 1) < NB) swiglu(4 + (g >> 1), vb, ob);
+                for (int h = 0; h < 2; ++h) {
+                  if (h == 1 && !two) break;
+                  const float(&c)[4] = h ? b : a;
+                  const float va = q ? c[1] : c[0], vb = q ? c[3] : c[2];
+                  const float oa = __shfl_xor_sync(0xFFFFFFFFu, va, 4);
+                  const float ob = __shfl_xor_sync(0xFFFFFFFFu, vb, 4);
+                  const int pr = ((n0 + 8 * h) >> 1) + tq; /* pair within the stage */
+                  if (q == 0 && pr < cnt) {
+                    if ((g >> 1) < NB) swiglu(g >> 1, pr, va, oa);
+                    if (NB > 4 && 4 + (g >> 1) < NB) swiglu(4 + (g >> 1), pr, vb, ob);
+                  }
                 }
-              }
-            });
+              });
+        }
         stage_release(si + j);
       }
       v += f1 - f0;
@@ -1496,7 +1729,6 @@ struct Consumer {
                        (layer == p.poison_layer ? p.poison_delta : 0);
     if (!cwait(lctr(p, layer, CTR_ATTN_DONE), target, task, OP_OUT, layer, CTR_ATTN_DONE))
       return false;
-    invalidate_norm();
     uint16_t *x = (uint16_t *)cx.xbuf();
     auto &O = M()->u.out;
     load_x(x, p.o + (size_t)layer * MK_MAX_BATCH * HqD, HqD, HqD);
@@ -1530,15 +1762,22 @@ struct Consumer {
           uint8_t *st;
           if (!stage_wait(si + j, st, task, OP_OUT, layer)) continue;
           const int rb0 = jj * rps, cnt = min(rps, nr - rb0);
-          mma_rows<NB>(st, cnt, pitch, F, xa, xpf, lane, [](int vr) { return vr; },
-                       [&](int n0, const float(&a)[4], const float(&b)[4], bool two) {
-                         auto f = [&](int r, int bb, float v) {
-                           float &acc = O.acc_w[warp][rb0 + r][bb];
-                           acc = fmaf(O.slot_w[u][bb], v, acc);
-                         };
-                         take_out<NB>(n0, a, cnt, lane, f);
-                         if (two) take_out<NB>(n0 + 8, b, cnt, lane, f);
-                       });
+          auto acc = [&](int r, int bb, float v) {
+            float &a = O.acc_w[warp][rb0 + r][bb];
+            a = fmaf(O.slot_w[u][bb], v, a);
+          };
+          if (NB == 1) {
+            cc_rows(st, cnt, pitch, F, xa, lane, [](int vr) { return vr; },
+                    [&](int n0, float sum, int nr) {
+                      if ((lane & 3) == 0 && (lane >> 2) < nr) acc(n0 + (lane >> 2), 0, sum);
+                    });
+          } else {
+            mma_rows<NB>(st, cnt, pitch, F, xa, xpf, lane, [](int vr) { return vr; },
+                         [&](int n0, const float(&a)[4], const float(&b)[4], bool two) {
+                           take_out<NB>(n0, a, cnt, lane, acc);
+                           if (two) take_out<NB>(n0 + 8, b, cnt, lane, acc);
+                         });
+          }
           stage_release(si + j);
         }
       }
@@ -1584,7 +1823,7 @@ struct Consumer {
     int best_i[2] = {0x7FFFFFFF, 0x7FFFFFFF};
     float *logits = p.out_logits;
     const int V = p.V;
-    gemv_rows(t[3], p.d, (const uint16_t *)cx.xbuf(), task, OP_LM, L, [&](int r, int bb, float v) {
+    gemv_rows(t[3], p.d, cx.xn(), task, OP_LM, L, [&](int r, int bb, float v) {
       if (bb < B) {
         if (logits) logits[(size_t)bb * V + v0 + r] = v;
         const int k = bb >= 4;
@@ -1594,12 +1833,14 @@ struct Consumer {
         }
       }
     });
-    /* the eight lanes of a token (lanes 8b..8b+7), then the warps */
+    /* the lanes holding a token's rows (all 32 for one token on the CUDA
+     * cores; lanes 8b..8b+7 on the tensor cores), then the warps */
     auto &LM = M()->u.lm;
+    constexpr int LANES = NB == 1 ? 32 : 8;
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
 #pragma unroll
-      for (int s = 1; s <= 4; s <<= 1) {
+      for (int s = 1; s < LANES; s <<= 1) {
         const float ov = __shfl_xor_sync(0xFFFFFFFFu, best_v[k], s);
         const int oi = __shfl_xor_sync(0xFFFFFFFFu, best_i[k], s);
         if (ov > best_v[k] || (ov == best_v[k] && oi < best_i[k])) {
@@ -1607,8 +1848,8 @@ struct Consumer {
           best_i[k] = oi;
         }
       }
-      const int bb = 4 * k + (lane >> 3);
-      if ((lane & 7) == 0 && bb < NB) {
+      const int bb = 4 * k + lane / LANES;
+      if (lane % LANES == 0 && bb < NB) {
         LM.best[warp][bb][0] = best_v[k];
         LM.best[warp][bb][1] = __int_as_float(best_i[k]);
       }
@@ -1708,7 +1949,8 @@ __global__ void __launch_bounds__(MK_THREADS, 1) decode_kernel(const __grid_cons
   cx.p = &p;
   cx.SB = p.stage_bytes;
   cx.ring_off = (1024u - (saddr(mk_smem) & 1023u)) & 1023u;
-  cx.xbuf_off = cx.ring_off + (uint32_t)NC * p.stage_bytes;
+  cx.xn_off = cx.ring_off + (uint32_t)NC * p.stage_bytes;
+  cx.xbuf_off = cx.xn_off + (uint32_t)p.xn_bytes;
   cx.misc_off = cx.xbuf_off + (uint32_t)p.xbuf_bytes;
   Misc<NB> *misc = (Misc<NB> *)(mk_smem + cx.misc_off);
   cx.cta = blockIdx.x;

@@ -141,6 +141,7 @@ extern "C" mk_status mk_decode_step_static(const mk_model_dims *dims, const mk_w
   const size_t o_qkv = take((size_t)Lyr * MB * QKVD * 2);
   const size_t o_o = take((size_t)Lyr * MB * HqD * 2);
   const size_t o_part = take((size_t)Lyr * n_slots * G * (d.head_dim + 4) * 4);
+  const size_t o_part2 = take((size_t)Lyr * n_slots * G * (d.head_dim + 4) * 4);
   const size_t o_rl = take((size_t)Lyr * MB * d.n_experts * 4);
   const size_t o_rt = take((size_t)Lyr * sizeof(mk_routing));
   const size_t o_act = take((size_t)Lyr * u_max * MB * d.d_ffn * 2);
@@ -260,6 +261,7 @@ extern "C" mk_status mk_decode_step_static(const mk_model_dims *dims, const mk_w
   p.qkv = (uint16_t *)(base + o_qkv);
   p.o = (uint16_t *)(base + o_o);
   p.attn_part = (float *)(base + o_part);
+  p.attn_part2 = (float *)(base + o_part2);
   p.router_logits = (float *)(base + o_rl);
   p.routing = (mk_routing *)(base + o_rt);
   p.act = (uint16_t *)(base + o_act);
@@ -286,6 +288,7 @@ extern "C" mk_status mk_decode_step_static(const mk_model_dims *dims, const mk_w
   p.stage_bytes = sm.stage_bytes;
   p.kv_maps = base + o_maps;
   p.xbuf_bytes = (int32_t)sm.xbuf;
+  p.xn_bytes = (int32_t)sm.xn;
   p.poison_layer = -1;
   p.poison_delta = 0;
 

@@ -13,8 +13,10 @@
  * stays small (a few hundred descriptors) for any depth.
  *
  * Per-layer phases, in the order every CTA runs them:
- *   ROUTER  (a few CTAs; first, because routing heads the MoE critical path)
- *   QKV     (the Wq/Wk/Wv rows cut into one contiguous piece per CTA)
+ *   QKV     (the [Wq | Wk | Wv | Wrouter] rows cut into one contiguous
+ *   ROUTER   piece per CTA; the router rows of a piece form a ROUTER task,
+ *            after the CTA's QKV rows; the last router task to finish runs
+ *            the top-k)
  *   ATTN    (split-K attention: the CTAs are shared out among the
  *            (sequence, kv head) pairs in proportion to their pages, one
  *            split of about equal size per CTA)
@@ -60,11 +62,11 @@ extern "C" size_t mk_misc_bytes(int nb);
 
 int mk_nb_for(int batch) { return batch <= 1 ? 1 : batch <= 2 ? 2 : batch <= 4 ? 4 : 8; }
 
-/* The activation buffer: the largest of what the task types stage there
- * (bf16 vectors at the padded pitch K + 32). */
+/* The scratch buffer: the largest of what the task types stage there (bf16
+ * vectors at pitch K). */
 static size_t xbuf_bytes_for(const mk_model_dims &d, int nb) {
   const size_t HqD = (size_t)d.n_q_heads * d.head_dim, D = d.head_dim;
-  size_t x = (size_t)nb * 2 * (mk_x_pitch(d.d_model) + d.d_model); /* normed input + staged h */
+  size_t x = (size_t)nb * 2 * d.d_model;                         /* staged h of the norm */
   x = std::max(x, (size_t)nb * 2 * mk_x_pitch((int)HqD));          /* attention output (Wo) */
   x = std::max(x, (size_t)nb * 2 * mk_x_pitch(d.d_ffn));          /* one expert's activations */
   /* attention: q (bf16 [8][D + 8]), new k and v (fp32 [D] each), merge
@@ -80,7 +82,8 @@ bool mk_smem_plan(const mk_model_dims *dm, int nb, MkSmem *out) {
   MkSmem s;
   s.misc = align_up(mk_misc_bytes(nb), 128);
   s.xbuf = xbuf_bytes_for(d, nb);
-  const size_t fixed = MK_SMEM_STATIC + s.xbuf + s.misc;
+  s.xn = align_up((size_t)nb * 2 * mk_x_pitch(d.d_model), 128);
+  const size_t fixed = MK_SMEM_STATIC + s.xn + s.xbuf + s.misc;
   if (fixed >= MK_SMEM_OPTIN) return false;
   size_t sb = (MK_SMEM_OPTIN - fixed) / MK_NC_WARPS / 1024 * 1024;
   sb = std::min<size_t>(sb, MK_MAX_STAGE_BYTES);
@@ -90,7 +93,7 @@ bool mk_smem_plan(const mk_model_dims *dm, int nb, MkSmem *out) {
       mk_rows_per_stage(d.d_ffn, s.stage_bytes) < 1 ||
       mk_pages_per_stage(d.page_size, d.head_dim, s.stage_bytes) < 1)
     return false;
-  s.total = (size_t)MK_NC_WARPS * sb + s.xbuf + s.misc;
+  s.total = (size_t)MK_NC_WARPS * sb + s.xn + s.xbuf + s.misc;
   s.dyn = s.total + MK_SMEM_STATIC;
   *out = s;
   return true;
@@ -141,52 +144,65 @@ mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int
   MkPlan &p = *out;
   p = MkPlan();
 
-  /* ROUTER: one ring stage of rows per task, so that the router GEMV, which
-   * heads the MoE critical path, is spread over as many SMs as possible. */
+  /* QKV + ROUTER.  With enough CTAs the router rows go to the last n_rc
+   * CTAs alone, sized like a QKV piece: the last of them to finish runs the
+   * top-k, and since those CTAs get no attention split, that serial step
+   * delays no split (and so no attention merge).  The [q | k | v] rows are
+   * cut into equal contiguous pieces over the other CTAs, split again at
+   * matrix boundaries.  With few CTAs the router rows simply continue the
+   * concatenated row space. */
+  int n_rc = 0; /* router-only CTAs (no QKV rows, no attention split) */
   {
-    MkSmem sm;
-    if (!mk_smem_plan(&d, mk_nb_for(batch), &sm)) return MK_ERR_UNSUPPORTED;
-    const int rpr = std::max(1, std::min(d.n_experts, mk_rows_per_stage(d.d_model, sm.stage_bytes)));
-    const int n = (int)ceil_div(d.n_experts, rpr);
-    for (int i = 0; i < n; ++i) {
-      Desc t = desc(OP_ROUTER);
-      t[2] = i * rpr;
-      t[3] = std::min(rpr, d.n_experts - i * rpr);
-      const int c = (int)((int64_t)i * n_cta / n);
-      router_t[c].push_back(t);
+    const int64_t rows[4] = {(int64_t)Hq * D, (int64_t)Hkv * D, (int64_t)Hkv * D,
+                             (int64_t)d.n_experts};
+    const int64_t Rq = rows[0] + rows[1] + rows[2];
+    if (n_cta >= 16) {
+      const double per = (double)(Rq + rows[3]) / n_cta;
+      n_rc = (int)std::max<int64_t>(1, std::min<int64_t>(n_cta / 8, (int64_t)(rows[3] / per + 0.5)));
     }
-    p.n_router = n;
-  }
-
-  /* QKV: the concatenated [q | k | v] rows cut into n_cta contiguous pieces,
-   * each split again at matrix boundaries. */
-  {
-    const int64_t rows[3] = {(int64_t)Hq * D, (int64_t)Hkv * D, (int64_t)Hkv * D};
-    const int64_t R = rows[0] + rows[1] + rows[2];
-    const int pieces = (int)std::min<int64_t>(n_cta, R);
-    int n = 0;
-    for (int c = 0; c < pieces; ++c) {
-      const int64_t a = R * c / pieces, b = R * (c + 1) / pieces;
-      int64_t base = 0;
-      for (int m = 0; m < 3; ++m) {
-        const int64_t lo = std::max(a, base), hi = std::min(b, base + rows[m]);
-        if (lo < hi) {
-          Desc t = desc(OP_QKV);
-          t[1] = m;
-          t[2] = (int32_t)(lo - base);
-          t[3] = (int32_t)(hi - lo);
-          qkv_t[c].push_back(t);
-          ++n;
+    int nq = 0, nr = 0;
+    auto cut = [&](int64_t R, int c0, int pieces, int m_lo, int m_hi) {
+      for (int c = 0; c < pieces; ++c) {
+        const int64_t a = R * c / pieces, b = R * (c + 1) / pieces;
+        int64_t base = 0;
+        for (int m = 0; m < 4; ++m) {
+          if (m < m_lo || m > m_hi) continue;
+          const int64_t lo = std::max(a, base), hi = std::min(b, base + rows[m]);
+          if (lo < hi) {
+            Desc t = desc(m < 3 ? OP_QKV : OP_ROUTER);
+            t[1] = m;
+            t[2] = (int32_t)(lo - base);
+            t[3] = (int32_t)(hi - lo);
+            if (m < 3) {
+              qkv_t[c0 + c].push_back(t);
+              ++nq;
+            } else {
+              router_t[c0 + c].push_back(t);
+              ++nr;
+            }
+          }
+          base += rows[m];
         }
-        base += rows[m];
       }
+    };
+    if (n_rc > 0) {
+      cut(Rq, 0, (int)std::min<int64_t>(n_cta - n_rc, Rq), 0, 2);
+      cut(rows[3], n_cta - n_rc, (int)std::min<int64_t>(n_rc, rows[3]), 3, 3);
+    } else {
+      cut(Rq + rows[3], 0, (int)std::min<int64_t>(n_cta, Rq + rows[3]), 0, 3);
     }
-    p.n_qkv = n;
+    p.n_qkv = nq;
+    p.n_router = nr;
   }
+  const int n_acta = n_cta - n_rc; /* CTAs that take attention splits */
 
   /* ATTN: split-K over pages. */
   {
-    struct Split { int b, kvh, p0, p1, slot, slot0, ns, last; int64_t pages; };
+    struct Split {
+      int b, kvh, p0, p1, slot, slot0, ns, last;
+      int gi, gn, ng, gslot0, g2slot, g2slot0; /* two-level merge */
+      int64_t pages;
+    };
     std::vector<Split> splits;
     int64_t T = 0;
     std::vector<int64_t> npages(batch);
@@ -195,25 +211,25 @@ mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int
       T += npages[b] * Hkv;
     }
     /* CTAs per (b, kvh) in proportion to its pages (largest remainder), so
-     * that every CTA gets one split of about T / n_cta pages. */
+     * that every attention CTA gets one split of about T / n_acta pages. */
     const int nbh = batch * Hkv;
     std::vector<int64_t> share(nbh, 1);
-    if (nbh <= n_cta && T > 0) {
+    if (nbh <= n_acta && T > 0) {
       std::vector<double> rem(nbh);
       int64_t used = 0;
       for (int i = 0; i < nbh; ++i) {
-        const double q = (double)npages[i / Hkv] * n_cta / (double)T;
+        const double q = (double)npages[i / Hkv] * n_acta / (double)T;
         share[i] = std::max<int64_t>(1, (int64_t)q);
         rem[i] = q - (double)share[i];
         used += share[i];
       }
-      while (used < n_cta) {
+      while (used < n_acta) {
         const int best = (int)(std::max_element(rem.begin(), rem.end()) - rem.begin());
         share[best] += 1;
         rem[best] -= 1.0;
         ++used;
       }
-      while (used > n_cta) {
+      while (used > n_acta) {
         int best = -1;
         for (int i = 0; i < nbh; ++i)
           if (share[i] > 1 && (best < 0 || rem[i] < rem[best])) best = i;
@@ -223,11 +239,12 @@ mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int
         --used;
       }
     }
-    int slot = 0;
+    int slot = 0, slot2 = 0;
     for (int b = 0; b < batch; ++b)
       for (int h = 0; h < Hkv; ++h) {
         const int64_t n = npages[b];
         const int ns = (int)std::max<int64_t>(1, std::min<int64_t>(share[b * Hkv + h], n));
+        const int ng = (ns + MK_MERGE_GROUP - 1) / MK_MERGE_GROUP;
         for (int i = 0; i < ns; ++i) {
           Split s;
           s.b = b;
@@ -238,10 +255,17 @@ mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int
           s.slot0 = slot;
           s.ns = ns;
           s.last = (i == ns - 1);
+          s.gi = i / MK_MERGE_GROUP;
+          s.gn = std::min(MK_MERGE_GROUP, ns - s.gi * MK_MERGE_GROUP);
+          s.ng = ng;
+          s.gslot0 = slot + s.gi * MK_MERGE_GROUP;
+          s.g2slot = slot2 + s.gi;
+          s.g2slot0 = slot2;
           s.pages = s.p1 - s.p0 + (s.last ? 1 : 0);
           splits.push_back(s);
         }
         slot += ns;
+        slot2 += ng;
       }
     p.n_attn_slots = slot;
     p.n_attn = (int)splits.size();
@@ -250,14 +274,14 @@ mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int
     std::iota(order.begin(), order.end(), 0);
     std::stable_sort(order.begin(), order.end(),
                      [&](int x, int y) { return splits[x].pages > splits[y].pages; });
-    std::vector<int64_t> load(n_cta, 0);
-    std::vector<std::vector<int>> mine(n_cta);
+    std::vector<int64_t> load(n_acta, 0);
+    std::vector<std::vector<int>> mine(n_acta);
     for (int idx : order) {
       const int c = (int)(std::min_element(load.begin(), load.end()) - load.begin());
       load[c] += splits[idx].pages + 1;
       mine[c].push_back(idx);
     }
-    for (int c = 0; c < n_cta; ++c) {
+    for (int c = 0; c < n_acta; ++c) {
       std::sort(mine[c].begin(), mine[c].end());
       for (int idx : mine[c]) {
         const Split &s = splits[idx];
@@ -270,6 +294,12 @@ mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int
         t[6] = s.slot0;
         t[7] = s.ns;
         t[8] = s.last;
+        t[9] = s.gi;
+        t[10] = s.gn;
+        t[11] = s.ng;
+        t[12] = s.gslot0;
+        t[13] = s.g2slot;
+        t[14] = s.g2slot0;
         attn_t[c].push_back(t);
       }
     }
@@ -314,7 +344,7 @@ mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int
 
   int width = 0, lmax = 0;
   for (int c = 0; c < n_cta; ++c) {
-    for (auto *v : {&router_t[c], &qkv_t[c], &attn_t[c], &up_t[c], &out_t[c]})
+    for (auto *v : {&qkv_t[c], &router_t[c], &attn_t[c], &up_t[c], &out_t[c]})
       lt[c].insert(lt[c].end(), v->begin(), v->end());
     width = std::max<int>(width, 1 + (int)lt[c].size() + (int)ft[c].size());
     lmax = std::max<int>(lmax, (int)lt[c].size());

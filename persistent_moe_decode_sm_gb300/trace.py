@@ -48,6 +48,8 @@ def summarize(trace: np.ndarray, n_layers: int) -> dict:
         if op == 6 or l == 0 or l not in layer_end or (l - 1) not in layer_end:
             continue
         base = layer_end[l - 1]
+        phase[OPS[op]]["p50_ready_us"].append((float(np.median([e[5] for e in v])) - base) / 1e3)
+        phase[OPS[op]]["p50_exit_us"].append((float(np.median([e[7] for e in v])) - base) / 1e3)
         phase[OPS[op]]["first_entry_us"].append((min(e[4] for e in v) - base) / 1e3)
         phase[OPS[op]]["last_ready_us"].append((max(e[5] for e in v) - base) / 1e3)
         st = [e[6] for e in v if e[6]]

@@ -10,10 +10,13 @@ inputs from synth/.  Per step:
      anything else is a routing mismatch (must be 0);
   3. logits must agree within LOGIT_MAX_ABS / LOGIT_REL_L2.  The reference
      is the oracle with exact (double) sums and the method's bf16 rounding
-     points.  A second oracle instance with plain fp32 sums runs the same
-     step with the same routing; where its own deviation from the exact
-     evaluation approaches the stated bound (large batch x vocabulary), the
-     bound becomes NOISE_FACTOR times that measured fp32 noise floor;
+     points.  Two more oracle instances with plain fp32 sums -- ascending and
+     descending summation order, both faithful to the method, which fixes
+     fp32 accumulation but not the order -- run the same step with the same
+     routing; the fp32 noise floor is the largest of their deviations from
+     the exact evaluation and from each other, and where it approaches the
+     stated bound (deep models, large batch x vocabulary) the bound becomes
+     NOISE_FACTOR times that floor;
   4. the greedy token must be identical where the oracle's top-1/top-2
      margin exceeds TIE_EPS, else the GPU's token must be within TIE_EPS of
      the oracle's maximum; both continue with the GPU's token.
@@ -39,7 +42,11 @@ import synth  # noqa: E402
 TIE_EPS = 1e-2
 LOGIT_MAX_ABS = 3e-2
 LOGIT_REL_L2 = 1e-2
-NOISE_FACTOR = 1.5
+# One step's fp32 noise is a single sample of a chaotic quantity (bf16
+# rounding flips amplified layer by layer): on the 8-layer mid model the
+# fp32 deviation from the exact evaluation went 0.0197 -> 0.0352 between
+# consecutive steps, so the bound allows twice the floor measured on the step.
+NOISE_FACTOR = 2.0
 
 # d, F and Hq*D multiples of 64, head_dim 32, group 3: an odd small shape
 ODD = synth.Dims(2, 192, 6, 2, 32, 6, 2, 128, 300)
@@ -76,6 +83,9 @@ class ParityRun:
         self.orc32 = (oracle.Oracle(dims, host, self.seq_lens, pl.page_tables, self.dev.biases,
                                     accum_double=False, seed=seed)
                       if noise_floor and accum_double else None)
+        self.orc32r = (oracle.Oracle(dims, host, self.seq_lens, pl.page_tables, self.dev.biases,
+                                     accum_double=False, seed=seed, reverse=True)
+                       if noise_floor and accum_double else None)
         self.tokens = (np.asarray(tokens, np.int32) if tokens is not None
                        else synth.first_tokens(dims, self.B, seed))
         self.alloc_io(self.B)
@@ -87,6 +97,8 @@ class ParityRun:
         if self.orc32 is not None:
             self.orc32 = oracle.Oracle(self.dims, host, seq_lens, page_tables, self.dev.biases,
                                        accum_double=False)
+            self.orc32r = oracle.Oracle(self.dims, host, seq_lens, page_tables, self.dev.biases,
+                                        accum_double=False, reverse=True)
 
     def alloc_io(self, B):
         torch = self.torch
@@ -111,10 +123,12 @@ class ParityRun:
                "route_mismatch": int(r["route_mismatch"])}
         rep["bound_max_abs"], rep["bound_rel_l2"] = LOGIT_MAX_ABS, LOGIT_REL_L2
         if self.orc32 is not None:
-            r32 = self.orc32.step(self.tokens, forced_ids=gpu_ids, tie_eps=TIE_EPS)
-            nd = r32["logits"] - ol
-            rep["noise_max_abs"] = float(np.abs(nd).max())
-            rep["noise_rel_l2"] = float(np.linalg.norm(nd) / max(np.linalg.norm(ol), 1e-30))
+            a = self.orc32.step(self.tokens, forced_ids=gpu_ids, tie_eps=TIE_EPS)["logits"]
+            b = self.orc32r.step(self.tokens, forced_ids=gpu_ids, tie_eps=TIE_EPS)["logits"]
+            nol = max(np.linalg.norm(ol), 1e-30)
+            diffs = (a - ol, b - ol, a - b)
+            rep["noise_max_abs"] = float(max(np.abs(x).max() for x in diffs))
+            rep["noise_rel_l2"] = float(max(np.linalg.norm(x) for x in diffs) / nol)
             rep["bound_max_abs"] = max(LOGIT_MAX_ABS, NOISE_FACTOR * rep["noise_max_abs"])
             rep["bound_rel_l2"] = max(LOGIT_REL_L2, NOISE_FACTOR * rep["noise_rel_l2"])
         clear = r["route_margin"] > TIE_EPS

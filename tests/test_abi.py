@@ -32,8 +32,9 @@ def test_every_declared_symbol_is_exported():
 
 
 def test_status_strings():
-    for code in range(10):
+    for code in range(12):
         assert mk.status_string(code) not in ("", "unknown status")
+        assert code in mk.STATUS_NAMES
     assert mk.status_string(99) == "unknown status"
 
 

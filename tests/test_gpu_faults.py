@@ -40,6 +40,23 @@ def test_unsatisfiable_wait_times_out_and_recovers():
     run2.close()
 
 
+def test_out_of_vocabulary_token_fails_the_step_without_reading_outside_the_table():
+    run = harness.ParityRun("tiny")
+    assert run.ok(run.step())
+    bad = run.tok_d.clone()
+    bad[0] = run.dims.vocab + 7  # outside [0, vocab): the kernel must not index with it
+    run.dec.decode_step(bad, run.logits_d, run.next_d)
+    rc = mk.lib().mk_sync(run.dec.ctx)
+    assert rc == mk.MK_ERR_BAD_TOKEN, mk.STATUS_NAMES.get(rc, rc)
+    with pytest.raises(mk.MkError) as e:  # sticky
+        run.dec.decode_step(run.tok_d, run.logits_d, run.next_d)
+    assert e.value.code == mk.MK_ERR_BAD_TOKEN
+    run.close()
+    run2 = harness.ParityRun("tiny")
+    assert run2.ok(run2.step())
+    run2.close()
+
+
 def test_host_side_argument_errors():
     run = harness.ParityRun("tiny", seq_lens=[62], reserve_steps=2)
     pl = run.dev.layout

@@ -162,6 +162,24 @@ def test_oracle_double_accumulation_agrees_with_brute_force_closely():
     assert np.abs(r["logits"] - logits).max() < 2e-3
 
 
+def test_reverse_order_fp32_mode_is_the_same_sums_reordered():
+    """The descending-order fp32 mode (used only to measure the fp32 noise
+    floor) computes the same sums as the other modes: it agrees with the
+    float64 brute force as closely as the ascending mode does, and it is a
+    genuinely different rounding order (some logit differs in its low bits)."""
+    t, pl = tiny_inputs()
+    fwd = oracle.Oracle(TINY, t, [64], pl.page_tables)
+    rev = oracle.Oracle(TINY, t, [64], pl.page_tables, reverse=True)
+    bf = BruteForce(TINY, t, [64], pl.page_tables)
+    tok = synth.first_tokens(TINY, 1)
+    rf, rr = fwd.step(tok), rev.step(tok)
+    logits, _ = bf.step(tok)
+    assert np.abs(rr["logits"] - logits).max() < 2e-2
+    assert np.linalg.norm(rr["logits"] - logits) / np.linalg.norm(logits) < 1e-2
+    assert np.abs(rr["logits"] - rf["logits"]).max() < 2e-2
+    assert not np.array_equal(rr["logits"], rf["logits"])
+
+
 # ------------------------------------------------------------------ invariants
 
 

@@ -37,6 +37,7 @@ def simulate(d, info, rows, batch, rng):
     router_ticket = [0] * L
     routed = [False] * L
     attn_ticket = {}
+    group_ticket = {}
     attn_done = [0] * L
     up_done = [0] * L
     out_done = [0] * L
@@ -66,9 +67,17 @@ def simulate(d, info, rows, batch, rng):
             router_ticket[l] += 1
             routed[l] = router_ticket[l] == info.n_router
         elif op == OP_ATTN:
+            # two-level merge: the last split of a group merges the group,
+            # the last group merger merges the groups
             key = (l, int(t[1]), int(t[2]))
+            ng = int(t[11])
+            if ng > 1:
+                gkey = key + (int(t[9]),)
+                group_ticket[gkey] = group_ticket.get(gkey, 0) + 1
+                if group_ticket[gkey] != t[10]:
+                    return
             attn_ticket[key] = attn_ticket.get(key, 0) + 1
-            if attn_ticket[key] == t[7]:
+            if attn_ticket[key] == (ng if ng > 1 else t[7]):
                 attn_done[l] += 1
         elif op == OP_UP:
             up_done[l] += 1
@@ -111,6 +120,7 @@ def check_coverage(d, info, rows, seq_lens):
             cov[t[2]:t[2] + t[3]] += 1
     assert np.all(cov == 1)
     slots = []
+    slots2 = []
     for b, L in enumerate(seq_lens):
         npages = -(-L // P)
         for h in range(Hkv):
@@ -128,7 +138,20 @@ def check_coverage(d, info, rows, seq_lens):
             s0 = slot0.pop()
             assert sorted(int(t[5]) for t in sp) == list(range(s0, s0 + len(sp)))
             slots += [int(t[5]) for t in sp]
+            # merge groups: consecutive slots in groups of 8
+            ns, ng = len(sp), -(-len(sp) // 8)
+            g2 = {int(t[14]) for t in sp}
+            assert len(g2) == 1
+            g20 = g2.pop()
+            for t in sp:
+                gi = (int(t[5]) - s0) // 8
+                assert int(t[9]) == gi and int(t[11]) == ng
+                assert int(t[10]) == min(8, ns - 8 * gi) and int(t[12]) == s0 + 8 * gi
+                assert int(t[13]) == g20 + gi
+            slots2.append((g20, ng))
     assert sorted(slots) == list(range(info.n_attn_slots))
+    s2 = sorted(g + i for g, n in slots2 for i in range(n))
+    assert s2 == list(range(len(s2)))  # level-2 slots distinct and dense
     ups = sorted((int(t[1]), int(t[2])) for t in lt_all if t[0] == OP_UP)
     assert ups == [(i, info.n_up) for i in range(info.n_up)]
     cov = np.zeros(d.d_model, int)
@@ -192,3 +215,14 @@ def test_attention_splits_are_balanced():
     total = sum(-(-L // 16) for L in lens) * d.n_kv_heads
     assert pages.sum() == total
     assert pages.max() <= 1.25 * total / 152 + 2
+
+
+def test_router_rows_sit_on_ctas_without_attention_splits():
+    d = synth.FULL
+    info, table = mk.mk_plan(cdims(d, 8, 600), 152, 1, [8192])
+    rows = decode(table)
+    router_ctas = {c for c, (lt, _) in enumerate(rows) if any(t[0] == OP_ROUTER for t in lt)}
+    assert 1 <= len(router_ctas) <= 152 // 8
+    for c in router_ctas:
+        ops = {int(t[0]) for t in rows[c][0]}
+        assert OP_ATTN not in ops and OP_QKV not in ops, (c, ops)
