@@ -266,7 +266,7 @@ mk_status mk_create(const mk_model_dims *dims, const mk_weights *w, void *stream
   const int L = d.n_layers, MB = MK_MAX_BATCH, G = d.n_q_heads / d.n_kv_heads;
   const size_t QKVD = (size_t)(d.n_q_heads + 2 * d.n_kv_heads) * d.head_dim;
   const size_t HqD = (size_t)d.n_q_heads * d.head_dim;
-  c->n_slots_max = c->n_sm + d.max_batch * d.n_kv_heads;
+  c->n_slots_max = 256 + d.max_batch * d.n_kv_heads; /* splits: at most 256, one per pair */
   c->u_max = std::min(d.n_experts, d.max_batch * d.top_k);
   c->rope_max_pos = d.max_pages_per_seq * d.page_size;
   c->ctrs_per_layer = mk_ctrs_per_layer(MB, d.n_kv_heads);
@@ -275,8 +275,8 @@ mk_status mk_create(const mk_model_dims *dims, const mk_weights *w, void *stream
   const size_t o_h = cv.take((size_t)(L + 1) * MB * d.d_model * 2);
   const size_t o_qkv = cv.take((size_t)L * MB * QKVD * 2);
   const size_t o_o = cv.take((size_t)L * MB * HqD * 2);
-  const size_t o_part = cv.take((size_t)L * c->n_slots_max * G * (d.head_dim + 4) * 4);
-  const size_t o_part2 = cv.take((size_t)L * c->n_slots_max * G * (d.head_dim + 4) * 4);
+  const size_t o_part = cv.take((size_t)c->n_slots_max * G * (d.head_dim + 4) * 4);
+  const size_t o_part2 = cv.take((size_t)c->n_slots_max * G * (d.head_dim + 4) * 4);
   const size_t o_rl = cv.take((size_t)L * MB * d.n_experts * 4);
   const size_t o_rt = cv.take((size_t)L * sizeof(mk_routing));
   const size_t o_act = cv.take((size_t)L * c->u_max * MB * d.d_ffn * 2);

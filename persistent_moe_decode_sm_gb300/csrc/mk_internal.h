@@ -65,7 +65,8 @@ static inline int mk_ctrs_per_layer(int max_batch, int n_kv_heads) {
 #define MK_MAX_GROUP 8          /* q heads per kv head */
 #define MK_MAX_OUT_ROWS 64      /* rows of d per OUT task */
 #define MK_NC_WARPS 8           /* consumer warps; ring slot w belongs to consumer warp w */
-#define MK_THREADS ((MK_NC_WARPS + 1) * 32) /* + the producer warp */
+#define MK_NP_WARPS 4           /* producer warps; producer k fills the ring slots = k mod 4 */
+#define MK_THREADS ((MK_NC_WARPS + MK_NP_WARPS) * 32)
 #define MK_MAX_STAGE_ROWS 64
 #define MK_MAX_STAGE_BYTES 32768
 #define MK_MAX_STAGE_PAGES 8
@@ -117,8 +118,8 @@ typedef struct {
   uint16_t *h;                /* [L+1][MAXB][d]  (h[0] holds the embedding rows for dumps) */
   uint16_t *qkv;              /* [L][MAXB][(Hq+2Hkv)D] pre-RoPE q, k, v */
   uint16_t *o;                /* [L][MAXB][Hq D] */
-  float *attn_part;           /* [L][n_slots][G][D + 4] (m, l, -, -, o[D]) */
-  float *attn_part2;          /* [L][n_slots][G][D + 4] merge-group partials */
+  float *attn_part;           /* [n_slots][G][D + 4] (m, l, -, -, o[D]), reused by every layer */
+  float *attn_part2;          /* [n_slots][G][D + 4] merge-group partials */
   float *router_logits;       /* [L][MAXB][E] */
   mk_routing *routing;        /* [L] */
   uint16_t *act;              /* [L][Umax][MAXB][F] */
@@ -151,10 +152,11 @@ typedef struct {
  * [0] op | layer << 8 | task << 20, [1] entry, [2] dependency satisfied,
  * [3] first stage of data available, [4] exit (globaltimer ns). */
 #define MK_TRACE_WORDS 8
-/* Stage events of CTA 0 (after the task events in the trace buffer):
- * [0] stage | warp << 20 | op << 24, producer: [1] loop top, [2] stage
- * known, [3] slot free, [4] copies issued; owner warp: [5] starts waiting,
- * [6] data seen, [7] slot released. */
+/* Stage events of CTA 0 (after the task events in the trace buffer), in SM
+ * clock cycles: [0] stage | warp << 20 | op << 24, producer: [1] loop top,
+ * [2] stage known, [3] slot free, [4] copies issued; owner warp: [5] starts
+ * waiting, [6] data seen, [7] slot released.  The last event holds the
+ * clock anchors (globaltimer, SM clock) at the kernel's start and end. */
 #define MK_STAGE_TRACE_EVENTS 4096
 
 #ifdef __CUDACC__

@@ -56,6 +56,7 @@ namespace mk {
 
 constexpr int NC = MK_NC_WARPS;
 constexpr int NCT = NC * 32;
+static_assert(NC % MK_NP_WARPS == 0, "each ring slot must have one producer");
 #define NEG_INF (-INFINITY)
 
 /* ---------------------------------------------------------------- helpers */
@@ -91,6 +92,10 @@ __device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
   f[6] = __uint_as_float(v.w << 16);
   f[7] = __uint_as_float(v.w & 0xFFFF0000u);
 }
+
+/* SM cycle counter: cheap enough for per-stage timestamps (the stage trace
+ * converts it to globaltimer time with an anchor pair) */
+__device__ __forceinline__ uint64_t sclock() { return clock64(); }
 
 __device__ __forceinline__ uint64_t gtimer() {
   uint64_t t;
@@ -428,9 +433,9 @@ template <int NB>
 struct Misc {
   uint64_t full[NC];
   uint64_t empty[NC];
-  /* the producer's caches (offsets independent of NB) */
-  int32_t pexp[128];          /* expert id of each slot of the current layer */
-  int32_t ppage[MK_PAGE_CACHE]; /* page ids of the current attention split */
+  /* each producer's caches (offsets independent of NB) */
+  int32_t pexp[MK_NP_WARPS][128];            /* expert id of each slot of the current layer */
+  int32_t ppage[MK_NP_WARPS][MK_PAGE_CACHE]; /* page ids of the current attention split */
   int32_t norm_layer; /* layer whose normed input sits in xbuf (-2: none) */
   int32_t ok;         /* 0 once a consumer stopped early */
   int32_t pad0[2];
@@ -441,6 +446,7 @@ struct Misc {
   union {
     struct {
       float slot_w[128][NB];
+      float hres[MK_MAX_OUT_ROWS][NB];          /* the layer input h at the task's rows */
       float acc_o[MK_MAX_OUT_ROWS][NB];         /* Wo rows (one writer each) */
       float acc_w[NC][MK_MAX_OUT_ROWS][NB];     /* per-warp expert-down sums */
     } out;
@@ -474,8 +480,12 @@ struct Ctx {
   /* the mbarriers open the control block: full[NC], then empty[NC] */
   __device__ __forceinline__ uint64_t *full() const { return (uint64_t *)(mk_smem + misc_off); }
   __device__ __forceinline__ uint64_t *empty() const { return full() + NC; }
-  __device__ __forceinline__ int32_t *pexp() const { return (int32_t *)(empty() + NC); }
-  __device__ __forceinline__ int32_t *ppage() const { return pexp() + 128; }
+  __device__ __forceinline__ int32_t *pexp(int k) const {
+    return (int32_t *)(empty() + NC) + k * 128;
+  }
+  __device__ __forceinline__ int32_t *ppage(int k) const {
+    return (int32_t *)(empty() + NC) + MK_NP_WARPS * 128 + k * MK_PAGE_CACHE;
+  }
 };
 
 __device__ __forceinline__ int32_t *lctr(const mk_kparams &p, int layer, int kind) {
@@ -609,6 +619,7 @@ struct StageIter {
   int r, nrows, K, rps;
   int q, p1, b, kvh;   /* attention pages */
   int64_t v, v1;       /* gate/up share */
+  int uc, fc;          /* current (slot, ffn index) of the share */
   int u, U, r0o, nro;  /* OUT: u = -1 while on Wo rows, then the down slot */
   const mk_routing *rt;
   int32_t *pexp, *ppage; /* shared-memory caches of expert and page ids */
@@ -727,6 +738,8 @@ struct StageIter {
         const int64_t T = (int64_t)U * F;
         v = T * t[1] / t[2];
         v1 = T * (t[1] + 1) / t[2];
+        uc = (int)(v / F);
+        fc = (int)(v - (int64_t)uc * F);
         return IT_STAGE;
       }
       case OP_OUT:
@@ -751,8 +764,9 @@ struct StageIter {
     return true;
   }
 
-  /* IT_STAGE: a stage; IT_END: this task has no more; IT_FAIL */
-  __device__ int emit(StageDesc &sd, const Ctx &cx) {
+  /* IT_STAGE: a stage; IT_END: this task has no more; IT_FAIL.  Page ids
+   * are looked up only for a stage this producer fills. */
+  __device__ int emit(StageDesc &sd, const Ctx &cx, bool fill) {
     switch (op) {
       case OP_QKV:
       case OP_ROUTER:
@@ -767,26 +781,31 @@ struct StageIter {
         sd.kvh = kvh;
         sd.seq = b;
         sd.q0 = q;
-        for (int j = 0; j < cnt; ++j) {
-          const int idx = q + j - p0a;
-          sd.pages[j] = idx < MK_PAGE_CACHE ? ppage[idx] : __ldg(page_table + b * max_pages + q + j);
-        }
+        if (fill)
+          for (int j = 0; j < cnt; ++j) {
+            const int idx = q + j - p0a;
+            sd.pages[j] = idx < MK_PAGE_CACHE ? ppage[idx] : __ldg(page_table + b * max_pages + q + j);
+          }
         q += cnt;
         return IT_STAGE;
       }
       case OP_UP: {
         if (v >= v1) return IT_END;
-        const int uu = (int)(v / F), f0 = (int)(v - (int64_t)uu * F);
-        const int f1 = (int)min((int64_t)F, f0 + (v1 - v));
-        const int cnt = min(pps_up, f1 - f0);
-        const int e = pexp[uu];
-        const size_t eo = (size_t)e * F * d + (size_t)f0 * d;
+        const int f1 = (int)min((int64_t)F, fc + (v1 - v));
+        const int cnt = min(pps_up, f1 - fc);
+        const int e = pexp[uc];
+        const size_t eo = ((size_t)e * F + fc) * d;
         sd.kind = SK_PAIRS;
         sd.n = cnt;
         sd.a = (const uint8_t *)(ly->wg + eo);
         sd.b = (const uint8_t *)(ly->wu + eo);
         sd.row_bytes = (uint32_t)d * 2;
         v += cnt;
+        fc += cnt;
+        if (fc == F) {
+          ++uc;
+          fc = 0;
+        }
         return IT_STAGE;
       }
       case OP_OUT: {
@@ -804,8 +823,8 @@ struct StageIter {
     }
   }
 
-  /* The next stage of the stream. */
-  __device__ int next(StageDesc &sd, const Ctx &cx) {
+  /* The next stage of the stream (its descriptor complete only if fill). */
+  __device__ int next(StageDesc &sd, const Ctx &cx, bool fill) {
     while (true) {
       if (at_end()) return IT_END;
       if (!started) {
@@ -813,7 +832,7 @@ struct StageIter {
         if (rs != IT_STAGE) return rs;
         started = true;
       }
-      const int rs = emit(sd, cx);
+      const int rs = emit(sd, cx, fill);
       if (rs == IT_STAGE) {
         ++count;
         return IT_STAGE;
@@ -860,37 +879,43 @@ struct Producer {
     }
   }
 
-  __device__ __noinline__ void run(const int32_t *row) {
+  /* Producer k of MK_NP_WARPS walks the whole stage sequence and fills the
+   * stages i with i % MK_NP_WARPS == k, i.e. the ring slots = k mod
+   * MK_NP_WARPS: issuing a copy costs the issuing thread tens of
+   * nanoseconds, so several issuers keep HBM busy where one could not. */
+  __device__ __noinline__ void run(const int32_t *row, int k) {
     const Ctx c = cx; /* a register copy: `this` lives in local memory */
     const uint64_t pol = policy;
     int last_slot[NC];
     for (int s = 0; s < NC; ++s) last_slot[s] = -1;
     StageIter ld;
     ld.init(c.p, row, c.epoch, c.SB);
-    ld.pexp = c.pexp();
-    ld.ppage = c.ppage();
+    ld.pexp = c.pexp(k);
+    ld.ppage = c.ppage(k);
     StageDesc sd;
     unsigned long long *strc = c.cta == 0 ? c.p->stage_trace : nullptr;
     while (true) {
-      const uint64_t ta = strc ? gtimer() : 0;
-      const int rs = ld.next(sd, c);
+      const uint64_t ta = strc ? sclock() : 0;
+      const bool mine = (int)(ld.count % MK_NP_WARPS) == k; /* the stage about to be walked */
+      const int rs = ld.next(sd, c, mine);
       if (rs != IT_STAGE) break; /* end, or a failed wait (already reported) */
       const int i = (int)ld.count - 1;
+      if (!mine) continue;
       const int slot = i % NC;
-      const uint64_t tb = strc ? gtimer() : 0;
+      const uint64_t tb = strc ? sclock() : 0;
       if (i >= NC) {
         const uint32_t parity = (uint32_t)(((i / NC) - 1) & 1);
         if (!wait_mbar(c, &c.empty()[slot], parity, -1, -1, -1)) break;
       }
-      const uint64_t tc = strc ? gtimer() : 0;
+      const uint64_t tc = strc ? sclock() : 0;
       load(sd, c, pol, c.ring() + (size_t)slot * c.SB, &c.full()[slot]);
       last_slot[slot] = i;
-      if (strc && i < MK_STAGE_TRACE_EVENTS) {
+      if (strc && i < MK_STAGE_TRACE_EVENTS - 1) {
         unsigned long long *e = strc + (size_t)i * 8;
         e[1] = ta;
         e[2] = tb;
         e[3] = tc;
-        e[4] = gtimer();
+        e[4] = sclock();
       }
     }
     /* Every copy issued must land before the CTA exits (normally the
@@ -956,22 +981,20 @@ struct Consumer {
     if (lane == 0) {
       const bool trace = tr && warp == 0;
       unsigned long long *se =
-          (tr && cx.cta == 0 && i < MK_STAGE_TRACE_EVENTS) ? cx.p->stage_trace + (size_t)i * 8
-                                                            : nullptr;
-      const uint64_t w0 = (trace || se) ? gtimer() : 0;
+          (tr && cx.cta == 0 && i < MK_STAGE_TRACE_EVENTS - 1) ? cx.p->stage_trace + (size_t)i * 8
+                                                                : nullptr;
+      const uint64_t w0 = trace ? gtimer() : 0, c0 = se ? sclock() : 0;
       ok = wait_mbar(cx, &cx.full()[slot], parity, task, op, layer) ? 1 : 0;
-      if (trace || se) {
+      if (trace) {
         const uint64_t w1 = gtimer();
-        if (trace) {
-          if (!t_stage) t_stage = w1;
-          else t_swait += w1 - w0;
-          ++n_stages;
-        }
-        if (se) {
-          se[0] = (unsigned long long)(i | (warp << 20) | (op << 24));
-          se[5] = w0;
-          se[6] = w1;
-        }
+        if (!t_stage) t_stage = w1;
+        else t_swait += w1 - w0;
+        ++n_stages;
+      }
+      if (se) {
+        se[0] = (unsigned long long)(i | (warp << 20) | (op << 24));
+        se[5] = c0;
+        se[6] = sclock();
       }
     }
     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -988,7 +1011,7 @@ struct Consumer {
     __syncwarp();
     if (lane == 0) {
       mbar_arrive(&cx.empty()[i % NC]);
-      if (tr && cx.cta == 0 && i < MK_STAGE_TRACE_EVENTS) cx.p->stage_trace[(size_t)i * 8 + 7] = gtimer();
+      if (tr && cx.cta == 0 && i < MK_STAGE_TRACE_EVENTS - 1) cx.p->stage_trace[(size_t)i * 8 + 7] = sclock();
     }
   }
 
@@ -1194,6 +1217,10 @@ struct Consumer {
     if (tid == 0) {
       __threadfence();
       st_release(lctr(p, layer, CTR_ROUTED), (int)(cx.epoch + 1));
+      /* the statistic after the release: off the experts' critical path */
+      auto &R = M()->u.rt;
+      const int U = __popc(R.used[0]) + __popc(R.used[1]) + __popc(R.used[2]) + __popc(R.used[3]);
+      atomicAdd(&p.ctrl->sum_experts, (unsigned long long)U);
     }
     return true;
   }
@@ -1274,11 +1301,8 @@ struct Consumer {
         }
       }
     }
-    if (tid == 0) {
-      const int U = __popc(R.used[0]) + __popc(R.used[1]) + __popc(R.used[2]) + __popc(R.used[3]);
-      rt->U = U;
-      atomicAdd(&p.ctrl->sum_experts, (unsigned long long)U);
-    }
+    if (tid == 0)
+      rt->U = __popc(R.used[0]) + __popc(R.used[1]) + __popc(R.used[2]) + __popc(R.used[3]);
   }
 
   /* Merges n attention partials (consecutive slots at `parts`; per head
@@ -1613,7 +1637,10 @@ struct Consumer {
     }
     /* warp 0 holds this split's partial: per head [m, l, -, -, o[D]] */
     const int PS = D + 4;
-    float *part = p.attn_part + ((size_t)layer * p.n_slots + t[5]) * G * PS;
+    /* one layer's slots serve every layer: a layer's partials are merged
+     * before its attention-done count completes, which every later layer
+     * waits for */
+    float *part = p.attn_part + (size_t)t[5] * G * PS;
     if (warp == 0 && g < G) {
       if (tq == 0) {
         part[(size_t)g * PS] = m_run;
@@ -1630,8 +1657,8 @@ struct Consumer {
     const int ng = t[11], bh = b * p.Hkv + kvh;
     const int tk0 = CTR_ATTN_TICKET0 + bh * (1 + MK_MAX_MERGE_GROUPS);
     uint16_t *ob = p.o + ((size_t)layer * MK_MAX_BATCH + b) * p.Hq * D + (size_t)kvh * G * D;
-    const float *part1 = p.attn_part + (size_t)layer * p.n_slots * G * PS;
-    float *part2 = p.attn_part2 + (size_t)layer * p.n_slots * G * PS;
+    const float *part1 = p.attn_part;
+    float *part2 = p.attn_part2;
     if (ng <= 1) {
       if (!ticket(lctr(p, layer, tk0), t[7])) return true;
       merge_parts(part1 + (size_t)t[6] * G * PS, t[7], G, D, nullptr, ob);
@@ -1727,10 +1754,23 @@ struct Consumer {
     const int r0 = t[2], nr = t[3], B = p.B, d = p.d, F = p.F, HqD = p.Hq * p.D;
     const int target = (int)((cx.epoch + 1) * p.n_attn_done) +
                        (layer == p.poison_layer ? p.poison_delta : 0);
+    auto &O = M()->u.out;
+    /* before waiting on the outputs: the residual input rows (final since
+     * the layer began), then -- once the layer's routing is known, which it
+     * normally is by now -- the routing weights */
+    const mk_routing *rt = p.routing + layer;
+    for (int i = tid; i < nr * B; i += NCT) {
+      const int r = i / B, bb = i % B;
+      O.hres[r][bb] = bf2f(__ldcg(h_row(layer, bb) + r0 + r));
+    }
+    if (!cwait(lctr(p, layer, CTR_ROUTED), (int)(cx.epoch + 1), task, OP_OUT, layer, CTR_ROUTED))
+      return false;
+    const int U = __ldcg(&rt->U);
+    for (int i = tid; i < U * NB; i += NCT)
+      O.slot_w[i / NB][i % NB] = __ldcg(&rt->slot_w[i / NB][i % NB]);
     if (!cwait(lctr(p, layer, CTR_ATTN_DONE), target, task, OP_OUT, layer, CTR_ATTN_DONE))
       return false;
     uint16_t *x = (uint16_t *)cx.xbuf();
-    auto &O = M()->u.out;
     load_x(x, p.o + (size_t)layer * MK_MAX_BATCH * HqD, HqD, HqD);
     for (int i = tid; i < NC * MK_MAX_OUT_ROWS * NB; i += NCT) (&O.acc_w[0][0][0])[i] = 0.0f;
     bar_consumers();
@@ -1738,10 +1778,6 @@ struct Consumer {
     if (!cwait(lctr(p, layer, CTR_UP_DONE), (int)((cx.epoch + 1) * p.n_up), task, OP_OUT, layer,
                CTR_UP_DONE))
       return false;
-    const mk_routing *rt = p.routing + layer;
-    const int U = __ldcg(&rt->U);
-    for (int i = tid; i < U * NB; i += NCT)
-      O.slot_w[i / NB][i % NB] = __ldcg(&rt->slot_w[i / NB][i % NB]);
     /* the experts' activations, as many experts at a time as xbuf holds */
     const int xpf = mk_x_pitch(F), per = NB * xpf;
     const int fit = max(1, (int)min((int64_t)U, (int64_t)p.xbuf_bytes / ((int64_t)2 * per)));
@@ -1786,15 +1822,14 @@ struct Consumer {
     if (!task_end()) return false;
     for (int i = tid; i < nr * B; i += NCT) {
       const int r = i / B, bb = i % B;
-      const uint16_t *hin = h_row(layer, bb);
-      const float hv = bf2f(__ldcg(hin + r0 + r));
+      const float hv = O.hres[r][bb];
       const float at = rbf(O.acc_o[r][bb]);
       float mo = 0.0f;
 #pragma unroll
       for (int w = 0; w < NC; ++w) mo += O.acc_w[w][r][bb];
       p.h[((size_t)(layer + 1) * MK_MAX_BATCH + bb) * d + r0 + r] =
           f2bf(__fadd_rn(__fadd_rn(hv, at), rbf(mo)));
-      if (layer == 0) p.h[(size_t)bb * d + r0 + r] = __ldg(hin + r0 + r);
+      if (layer == 0) p.h[(size_t)bb * d + r0 + r] = f2bf(hv);
     }
     bar_consumers();
     signal(lctr(p, layer, CTR_OUT_DONE));
@@ -1968,6 +2003,14 @@ __global__ void __launch_bounds__(MK_THREADS, 1) decode_kernel(const __grid_cons
   __syncthreads();
   /* the CTA's task-table row, read by every task of every layer, is copied
    * to shared memory when it fits */
+  /* the stage trace's clock anchors: (globaltimer, SM clock) at start and end */
+  unsigned long long *anchor =
+      (p.stage_trace && blockIdx.x == 0) ? p.stage_trace + (size_t)(MK_STAGE_TRACE_EVENTS - 1) * 8
+                                         : nullptr;
+  if (anchor && threadIdx.x == 0) {
+    anchor[0] = gtimer();
+    anchor[1] = sclock();
+  }
   const int32_t *grow = p.table + (size_t)blockIdx.x * p.tasks_per_cta * MK_DESC_INTS;
   const bool row_in_smem = p.tasks_per_cta <= MK_SMEM_TASKS;
   if (row_in_smem)
@@ -1977,12 +2020,12 @@ __global__ void __launch_bounds__(MK_THREADS, 1) decode_kernel(const __grid_cons
   const int32_t *row = row_in_smem ? &misc->tasks[0][0] : grow;
   const bool header_ok = row[0] == OP_HEADER;
   if (header_ok) {
-    if (warp == NC) {
+    if (warp >= NC) {
       if (lane == 0) {
         Producer pr;
         pr.cx = cx;
         pr.policy = evict_first_policy();
-        pr.run(row);
+        pr.run(row, warp - NC);
       }
       __syncwarp();
     } else {
@@ -2001,6 +2044,10 @@ __global__ void __launch_bounds__(MK_THREADS, 1) decode_kernel(const __grid_cons
     misc->ok = 0;
   }
   __syncthreads();
+  if (anchor && threadIdx.x == 0) {
+    anchor[2] = gtimer();
+    anchor[3] = sclock();
+  }
   if (threadIdx.x == 0 && misc->ok && !ld_volatile(&p.ctrl->abort)) {
     /* the last CTA out advances the epoch */
     __threadfence();

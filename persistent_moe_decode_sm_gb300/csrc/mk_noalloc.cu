@@ -140,8 +140,8 @@ extern "C" mk_status mk_decode_step_static(const mk_model_dims *dims, const mk_w
   const size_t o_h = take((size_t)(Lyr + 1) * MB * d.d_model * 2);
   const size_t o_qkv = take((size_t)Lyr * MB * QKVD * 2);
   const size_t o_o = take((size_t)Lyr * MB * HqD * 2);
-  const size_t o_part = take((size_t)Lyr * n_slots * G * (d.head_dim + 4) * 4);
-  const size_t o_part2 = take((size_t)Lyr * n_slots * G * (d.head_dim + 4) * 4);
+  const size_t o_part = take((size_t)n_slots * G * (d.head_dim + 4) * 4);
+  const size_t o_part2 = take((size_t)n_slots * G * (d.head_dim + 4) * 4);
   const size_t o_rl = take((size_t)Lyr * MB * d.n_experts * 4);
   const size_t o_rt = take((size_t)Lyr * sizeof(mk_routing));
   const size_t o_act = take((size_t)Lyr * u_max * MB * d.d_ffn * 2);

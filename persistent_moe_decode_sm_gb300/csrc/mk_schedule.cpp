@@ -32,6 +32,7 @@
  * as long as all CTAs are co-resident (the launch is cooperative).
  */
 #include <algorithm>
+#include <cmath>
 #include <array>
 #include <cstring>
 #include <numeric>
@@ -186,7 +187,38 @@ mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int
       }
     };
     if (n_rc > 0) {
-      cut(Rq, 0, (int)std::min<int64_t>(n_cta - n_rc, Rq), 0, 2);
+      /* CTAs to each of q, k, v in proportion to its rows (largest
+       * remainder, at least one each), each matrix cut evenly: one QKV task
+       * per CTA, none straddling a matrix boundary */
+      const int nq_cta = n_cta - n_rc;
+      int share[3];
+      double rem[3];
+      int used = 0;
+      for (int m = 0; m < 3; ++m) {
+        const double q = (double)rows[m] * nq_cta / (double)Rq;
+        share[m] = std::max(1, (int)q);
+        rem[m] = q - share[m];
+        used += share[m];
+      }
+      while (used < nq_cta) {
+        const int m = (int)(std::max_element(rem, rem + 3) - rem);
+        ++share[m];
+        rem[m] -= 1.0;
+        ++used;
+      }
+      int c0 = 0;
+      for (int m = 0; m < 3; ++m) {
+        const int pieces = (int)std::min<int64_t>(share[m], rows[m]);
+        for (int c = 0; c < pieces; ++c) {
+          Desc t = desc(OP_QKV);
+          t[1] = m;
+          t[2] = (int32_t)(rows[m] * c / pieces);
+          t[3] = (int32_t)(rows[m] * (c + 1) / pieces - t[2]);
+          qkv_t[c0 + c].push_back(t);
+          ++nq;
+        }
+        c0 += share[m];
+      }
       cut(rows[3], n_cta - n_rc, (int)std::min<int64_t>(n_rc, rows[3]), 3, 3);
     } else {
       cut(Rq + rows[3], 0, (int)std::min<int64_t>(n_cta, Rq + rows[3]), 0, 3);
@@ -194,7 +226,27 @@ mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int
     p.n_qkv = nq;
     p.n_router = nr;
   }
-  const int n_acta = n_cta - n_rc; /* CTAs that take attention splits */
+  /* Roles.  With enough CTAs, attention and the experts run side by side on
+   * different SMs, as the pages run them from the same normed input
+   * ("Cohere Packs the Entire Decoding Step Into a Single CUDA Megakernel",
+   * ainews.surl.tw, paragraph 2): CTAs [0, n_acta) take the attention splits
+   * (QKV, ATTN, OUT), the others the expert gate/up shares (QKV or ROUTER,
+   * UP, OUT).  The split follows the bytes each side streams: the KV cache
+   * against the expected distinct experts' gate/up rows, so a CTA of either
+   * kind streams about as much per layer.  With few CTAs every CTA does
+   * everything. */
+  int n_acta = n_cta - n_rc;
+  if (n_rc > 0) {
+    double kv = 0.0;
+    for (int b = 0; b < batch; ++b) kv += (double)seq_lens[b] * Hkv * D * 2 * 2;
+    const double E = d.n_experts, K = d.top_k;
+    const double u_exp = E * (1.0 - std::pow(1.0 - K / E, (double)batch));
+    const double up = u_exp * 2.0 * d.d_ffn * d.d_model * 2;
+    const double frac = kv / std::max(kv + up, 1.0);
+    const int lo = std::min(batch * Hkv, n_cta - n_rc - 1), hi = n_cta - n_rc - 1;
+    n_acta = std::max(std::max(lo, 1), std::min(hi, (int)std::lround(n_cta * frac)));
+  }
+  const bool roles = n_acta < n_cta - n_rc; /* attention CTAs take no expert share */
 
   /* ATTN: split-K over pages. */
   {
@@ -210,26 +262,30 @@ mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int
       npages[b] = ceil_div(seq_lens[b], P);
       T += npages[b] * Hkv;
     }
-    /* CTAs per (b, kvh) in proportion to its pages (largest remainder), so
-     * that every attention CTA gets one split of about T / n_acta pages. */
+    /* Splits per (b, kvh) in proportion to its pages (largest remainder):
+     * one split of about T / n_acta pages per attention CTA, or -- when the
+     * pairs are many for the CTAs, so that rounding a pair's share would
+     * leave whole pairs on one CTA -- twice as many half-size splits, packed
+     * below largest first. */
     const int nbh = batch * Hkv;
+    const int n_splits = nbh * 4 > n_acta ? std::min(2 * n_acta, 256) : n_acta;
     std::vector<int64_t> share(nbh, 1);
-    if (nbh <= n_acta && T > 0) {
+    if (nbh <= n_splits && T > 0) {
       std::vector<double> rem(nbh);
       int64_t used = 0;
       for (int i = 0; i < nbh; ++i) {
-        const double q = (double)npages[i / Hkv] * n_acta / (double)T;
+        const double q = (double)npages[i / Hkv] * n_splits / (double)T;
         share[i] = std::max<int64_t>(1, (int64_t)q);
         rem[i] = q - (double)share[i];
         used += share[i];
       }
-      while (used < n_acta) {
+      while (used < n_splits) {
         const int best = (int)(std::max_element(rem.begin(), rem.end()) - rem.begin());
         share[best] += 1;
         rem[best] -= 1.0;
         ++used;
       }
-      while (used > n_acta) {
+      while (used > n_splits) {
         int best = -1;
         for (int i = 0; i < nbh; ++i)
           if (share[i] > 1 && (best < 0 || rem[i] < rem[best])) best = i;
@@ -305,14 +361,18 @@ mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int
     }
   }
 
-  /* UP: one share per CTA, resolved on the device once routing is known. */
-  for (int c = 0; c < n_cta; ++c) {
-    Desc t = desc(OP_UP);
-    t[1] = c;
-    t[2] = n_cta;
-    up_t[c].push_back(t);
+  /* UP: one share per expert CTA (every CTA without roles), resolved on the
+   * device once routing is known. */
+  {
+    const int c0 = roles ? n_acta : 0, n = n_cta - c0;
+    for (int c = c0; c < n_cta; ++c) {
+      Desc t = desc(OP_UP);
+      t[1] = c - c0;
+      t[2] = n;
+      up_t[c].push_back(t);
+    }
+    p.n_up = n;
   }
-  p.n_up = n_cta;
 
   /* OUT: rows of d. */
   {

@@ -82,6 +82,20 @@ def summarize(trace: np.ndarray, n_layers: int) -> dict:
     }
 
 
+def stage_times_ns(stages: np.ndarray) -> np.ndarray:
+    """The stage events with their SM-clock columns converted to globaltimer
+    nanoseconds (through the anchor pair in the last event)."""
+    a = stages[-1].astype(np.float64)
+    out = stages[:-1].astype(np.float64).copy()
+    if a[3] <= a[1]:
+        return out
+    ns_per_clk = (a[2] - a[0]) / (a[3] - a[1])
+    for c in range(1, 8):
+        nz = out[:, c] != 0
+        out[nz, c] = a[0] + (out[nz, c] - a[1]) * ns_per_clk
+    return out
+
+
 def stage_summary(stages: np.ndarray) -> dict:
     """Per op, medians over CTA 0's ring stages (microseconds): the producer's
     time to find the next stage (desc), to get its slot back (slot_wait),
@@ -89,7 +103,7 @@ def stage_summary(stages: np.ndarray) -> dict:
     owning warp, counting from when the warp started waiting if later); the
     owning warp's wait and compute (data seen -> release); and the stage
     interval (producer issue to issue)."""
-    ev = [e for e in stages if e[4] and e[6] and e[7]]
+    ev = [e for e in stage_times_ns(stages) if e[4] and e[6] and e[7]]
     if not ev:
         return {}
     out = {}

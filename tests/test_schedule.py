@@ -214,7 +214,25 @@ def test_attention_splits_are_balanced():
                 pages[c] += p1 - t[3]
     total = sum(-(-L // 16) for L in lens) * d.n_kv_heads
     assert pages.sum() == total
-    assert pages.max() <= 1.25 * total / 152 + 2
+    n_att = int((pages > 0).sum())  # the CTAs given attention splits
+    assert pages.max() <= 1.25 * total / n_att + 2
+
+
+def test_roles_balance_streamed_bytes():
+    """Attention CTAs take no expert share and expert CTAs no attention
+    split; the two sides stream about the same bytes per CTA."""
+    d = synth.FULL
+    for lens in ([8192], [262144], synth.workloads()["full_b8"].seq_lens):
+        info, table = mk.mk_plan(cdims(d, 8, 17000), 152, len(lens), lens)
+        rows = decode(table)
+        att = [c for c, (lt, _) in enumerate(rows) if any(t[0] == OP_ATTN for t in lt)]
+        exp = [c for c, (lt, _) in enumerate(rows) if any(t[0] == OP_UP for t in lt)]
+        assert not set(att) & set(exp) and len(att) + len(exp) == 152
+        kv = sum(lens) * d.n_kv_heads * d.head_dim * 4 / len(att)
+        e, k = d.n_experts, d.top_k
+        u = e * (1 - (1 - k / e) ** len(lens))
+        up = u * 2 * d.d_ffn * d.d_model * 2 / len(exp)
+        assert 0.6 < kv / up < 1.6, (lens[:2], kv, up)
 
 
 def test_router_rows_sit_on_ctas_without_attention_splits():
