@@ -195,13 +195,16 @@ mk_status mk_debug_poison_wait(mk_ctx *ctx, int32_t layer, int32_t delta);
  * [3] first data stage available (0 if none), [4] exit, [5] ns spent
  * waiting for later stages, [6] stages seen, [7] the task's mark (0 if
  * none) -- globaltimer nanoseconds, 8 words per event, unused events zero.
- * CTA 0 also records its first 4095 ring stages in SM clock cycles: [0]
+ * One CTA (mk_set_stage_trace_cta, default 0) also records its first 4095
+ * ring stages in SM clock cycles: [0]
  * stage | warp << 20 | op << 24; the producer's [1] loop top, [2] stage
  * known, [3] slot free, [4] copies issued; the owning warp's [5] wait start,
  * [6] data seen, [7] slot released.  Stage event 4095 holds the clock
  * anchors: [0] globaltimer and [1] SM clock at the kernel's start, [2], [3]
  * the same at its end. */
 mk_status mk_set_trace(mk_ctx *ctx, int32_t events_per_cta);
+/* Which CTA records the stage events (default 0). */
+mk_status mk_set_stage_trace_cta(mk_ctx *ctx, int32_t cta);
 /* Copies the trace (synchronises).  host_out may be NULL to query the
  * geometry; otherwise it must hold (n_cta * events_per_cta + 4096) * 8
  * words: the task events [n_cta][events_per_cta][8], then CTA 0's stage

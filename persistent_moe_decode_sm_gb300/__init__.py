@@ -106,7 +106,7 @@ class mk_plan_info(ctypes.Structure):
 EXPORTS = ["mk_create", "mk_build_schedule", "mk_decode_step", "mk_sync", "mk_destroy",
            "mk_status_string", "mk_set_wait_limit_ns", "mk_debug_routing", "mk_debug_dump",
            "mk_get_stats", "mk_debug_poison_wait", "mk_plan", "mk_decode_step_static",
-           "mk_set_trace", "mk_get_trace"]
+           "mk_set_trace", "mk_get_trace", "mk_set_stage_trace_cta"]
 
 _lib = None
 
@@ -140,6 +140,7 @@ def lib():
                                             vp]
         L.mk_set_trace.argtypes = [vp, i32]
         L.mk_get_trace.argtypes = [vp, vp, u64, vp, vp]
+        L.mk_set_stage_trace_cta.argtypes = [vp, i32]
         for n in EXPORTS:
             if n not in ("mk_destroy", "mk_status_string"):
                 getattr(L, n).restype = i32
@@ -267,6 +268,10 @@ def mk_set_trace(ctx: int, events_per_cta: int) -> None:
 
 
 STAGE_TRACE_EVENTS = 4096
+
+
+def mk_set_stage_trace_cta(ctx: int, cta: int) -> None:
+    _check(lib().mk_set_stage_trace_cta(ctx, cta), "mk_set_stage_trace_cta")
 
 
 def mk_get_trace(ctx: int):

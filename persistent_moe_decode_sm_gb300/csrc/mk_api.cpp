@@ -83,6 +83,7 @@ struct mk_ctx {
   mk_status sticky = MK_OK;
   bool prepared[4] = {false, false, false, false}; /* kernel attributes set per batch bucket */
   unsigned long long *trace = nullptr; /* [n_sm][trace_cap][MK_TRACE_WORDS] */
+  int stage_trace_cta = 0;
   void *kv_maps = nullptr;             /* device [n_layers][2] tensor maps (in ws) */
   int trace_cap = 0;
 };
@@ -508,6 +509,7 @@ mk_status mk_decode_step(mk_ctx *c, const int32_t *token_ids, float *out_logits,
   p.trace = c->trace;
   p.trace_cap = c->trace_cap;
   p.stage_trace = c->trace ? c->trace + (size_t)c->n_sm * c->trace_cap * MK_TRACE_WORDS : nullptr;
+  p.stage_trace_cta = c->stage_trace_cta;
   c->poison_layer = -1;
   c->poison_delta = 0;
 
@@ -556,6 +558,12 @@ mk_status mk_set_trace(mk_ctx *c, int32_t events_per_cta) {
   if (cudaMalloc(&c->trace, bytes) != cudaSuccess) return MK_ERR_CUDA;
   if (cudaMemset(c->trace, 0, bytes) != cudaSuccess) return MK_ERR_CUDA;
   c->trace_cap = events_per_cta;
+  return MK_OK;
+}
+
+mk_status mk_set_stage_trace_cta(mk_ctx *c, int32_t cta) {
+  if (!c || cta < 0 || cta >= c->n_sm) return MK_ERR_INVALID_ARG;
+  c->stage_trace_cta = cta;
   return MK_OK;
 }
 

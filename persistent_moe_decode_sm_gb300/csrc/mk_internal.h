@@ -145,7 +145,8 @@ typedef struct {
   int32_t poison_layer, poison_delta; /* test hook: see mk_debug_poison_wait */
   unsigned long long *trace;  /* NULL, or [n_cta][trace_cap][MK_TRACE_WORDS] task timestamps */
   int32_t trace_cap;
-  unsigned long long *stage_trace; /* NULL, or CTA 0's [MK_STAGE_TRACE_EVENTS][8] stage timestamps */
+  unsigned long long *stage_trace; /* NULL, or one CTA's [MK_STAGE_TRACE_EVENTS][8] stage timestamps */
+  int32_t stage_trace_cta;         /* the CTA that records them */
 } mk_kparams;
 
 /* One trace event (per executed task, written by consumer thread 0):

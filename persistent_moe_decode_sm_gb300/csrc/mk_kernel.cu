@@ -165,6 +165,20 @@ __device__ __forceinline__ bool mbar_test(uint64_t *b, uint32_t parity) {
   return ok != 0;
 }
 
+/* As mbar_test, but the thread may be suspended (for up to ns nanoseconds)
+ * until the phase completes instead of returning at once: a waiting warp
+ * then takes no issue slots from the warps computing beside it. */
+__device__ __forceinline__ bool mbar_wait_hint(uint64_t *b, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(saddr(b)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 /* 1-D TMA bulk copy global -> shared, completing on an mbarrier.  The
  * weights and cached K/V are streamed once per step: evict them first from
  * L2 so that activations and partials stay resident. */
@@ -399,43 +413,68 @@ __device__ __forceinline__ void cc_block(const uint8_t *st, int n0, int pitch, i
   for (int r = 0; r < 8; ++r) v[r] = r < NR ? sum2(a[r < NR ? r : 0][0]) + sum2(a[r < NR ? r : 0][1]) : 0.0f;
 }
 
+/* One block of up to 8 rows of one token on the CUDA cores, out of line:
+ * the one copy of this loop serves every task type, which keeps the
+ * instruction footprint of the kernel small.  Rows are virtual rows n0 ..
+ * n0 + nr - 1 mapped to stage rows by identity, or (pairs > 0) as gate row
+ * v / 2 for even v and up row pairs + v / 2 for odd v.  Returns this lane's
+ * share of the transposing reduction: lane l holds the sum of virtual row
+ * n0 + l / 4. */
+__device__ __noinline__ float cc_block_sum(const uint8_t *st, int n0, int nr, int pitch, int K,
+                                           const uint16_t *x, int lane, int pairs) {
+  auto rm = [pairs](int v) { return pairs ? ((v & 1) ? pairs + (v >> 1) : (v >> 1)) : v; };
+  float v[8];
+  switch (nr) {
+    case 1: cc_block<1>(st, n0, pitch, K, x, lane, rm, v); break;
+    case 2: cc_block<2>(st, n0, pitch, K, x, lane, rm, v); break;
+    case 3: cc_block<3>(st, n0, pitch, K, x, lane, rm, v); break;
+    case 4: cc_block<4>(st, n0, pitch, K, x, lane, rm, v); break;
+    case 5: cc_block<5>(st, n0, pitch, K, x, lane, rm, v); break;
+    case 6: cc_block<6>(st, n0, pitch, K, x, lane, rm, v); break;
+    case 7: cc_block<7>(st, n0, pitch, K, x, lane, rm, v); break;
+    default: cc_block<8>(st, n0, pitch, K, x, lane, rm, v); break;
+  }
+  return transpose_reduce8(v, lane);
+}
+
 /* One token on the CUDA cores (a tensor-core tile would use 1 of its 16 M
- * rows): the rows of one ring stage (stage row rm(v), pitch bytes apart)
- * against the bf16 activation x, up to eight rows per pass sharing each load
- * of x.  Lane l handles columns 4l + 128i (K a multiple of 64); each pair of
- * products is one packed fp32x2 FMA.  blk(n0, s, nr) runs on every lane
- * with lane l holding the sum of virtual row n0 + l / 4 (valid for l / 4 <
- * nr). */
-template <class RowMap, class Blk>
+ * rows): the rows of one ring stage (pitch bytes apart) against the bf16
+ * activation x, up to eight rows per pass sharing each load of x.  Lane l
+ * handles columns 4l + 128i (K a multiple of 64); each pair of products is
+ * one packed fp32x2 FMA.  blk(n0, s, nr) runs on every lane with lane l
+ * holding the sum of virtual row n0 + l / 4 (valid for l / 4 < nr). */
+template <class Blk>
 __device__ __forceinline__ void cc_rows(const uint8_t *st, int R, int pitch, int K,
-                                        const uint16_t *x, int lane, RowMap &&rm, Blk &&blk) {
+                                        const uint16_t *x, int lane, int pairs, Blk &&blk) {
   for (int n0 = 0; n0 < R; n0 += 8) {
     const int nr = min(8, R - n0);
-    float v[8];
-    switch (nr) {
-      case 1: cc_block<1>(st, n0, pitch, K, x, lane, rm, v); break;
-      case 2: cc_block<2>(st, n0, pitch, K, x, lane, rm, v); break;
-      case 3: cc_block<3>(st, n0, pitch, K, x, lane, rm, v); break;
-      case 4: cc_block<4>(st, n0, pitch, K, x, lane, rm, v); break;
-      case 5: cc_block<5>(st, n0, pitch, K, x, lane, rm, v); break;
-      case 6: cc_block<6>(st, n0, pitch, K, x, lane, rm, v); break;
-      case 7: cc_block<7>(st, n0, pitch, K, x, lane, rm, v); break;
-      default: cc_block<8>(st, n0, pitch, K, x, lane, rm, v); break;
-    }
-    blk(n0, transpose_reduce8(v, lane), nr);
+    blk(n0, cc_block_sum(st, n0, nr, pitch, K, x, lane, pairs), nr);
   }
 }
 
 /* ----------------------------------------------------------- shared layout */
 
-#define MK_PAGE_CACHE 256
+enum { SK_ROWS = 0, SK_PAIRS = 1, SK_PAGES = 2 };
+
+/* One stage's copies: ROWS n rows of row_bytes at a (one copy); PAIRS n gate
+ * rows at a and n up rows at b (two copies); PAGES n pages of one (layer, kv
+ * head) (two tensor boxes each). */
+struct QDesc {
+  const uint8_t *a, *b;
+  int32_t kind, n;
+  uint32_t row_bytes;
+  int32_t layer_kvh; /* PAGES: layer << 8 | kvh */
+  int32_t pages[MK_MAX_STAGE_PAGES];
+};
+
+#define MK_QBATCH 16 /* descriptors a producer warp plans at once */
+
 template <int NB>
 struct Misc {
   uint64_t full[NC];
   uint64_t empty[NC];
-  /* each producer's caches (offsets independent of NB) */
-  int32_t pexp[MK_NP_WARPS][128];            /* expert id of each slot of the current layer */
-  int32_t ppage[MK_NP_WARPS][MK_PAGE_CACHE]; /* page ids of the current attention split */
+  /* each producer warp's planned stage descriptors (offset independent of NB) */
+  QDesc qd[MK_NP_WARPS][MK_QBATCH];
   int32_t norm_layer; /* layer whose normed input sits in xbuf (-2: none) */
   int32_t ok;         /* 0 once a consumer stopped early */
   int32_t pad0[2];
@@ -457,6 +496,7 @@ struct Misc {
       uint32_t used[4];
       int32_t ids[MK_MAX_BATCH][MK_MAX_TOPK];
       float w[MK_MAX_BATCH][MK_MAX_TOPK];
+      int32_t rank_of[128];
     } rt;
   } u;
 };
@@ -480,12 +520,6 @@ struct Ctx {
   /* the mbarriers open the control block: full[NC], then empty[NC] */
   __device__ __forceinline__ uint64_t *full() const { return (uint64_t *)(mk_smem + misc_off); }
   __device__ __forceinline__ uint64_t *empty() const { return full() + NC; }
-  __device__ __forceinline__ int32_t *pexp(int k) const {
-    return (int32_t *)(empty() + NC) + k * 128;
-  }
-  __device__ __forceinline__ int32_t *ppage(int k) const {
-    return (int32_t *)(empty() + NC) + MK_NP_WARPS * 128 + k * MK_PAGE_CACHE;
-  }
 };
 
 __device__ __forceinline__ int32_t *lctr(const mk_kparams &p, int layer, int kind) {
@@ -548,19 +582,17 @@ __device__ bool wait_counter(const Ctx &cx, int32_t *c, int target, int task, in
   }
 }
 
-/* Waits for an mbarrier phase.  Bounded like wait_counter. */
+/* Waits for an mbarrier phase, suspended in hardware between checks of the
+ * abort flag and the time limit.  Bounded like wait_counter. */
 __device__ bool wait_mbar(const Ctx &cx, uint64_t *bar, uint32_t parity, int task, int op,
                           int layer) {
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = gtimer();
-  uint32_t spins = 0;
-  while (!mbar_test(bar, parity)) {
-    if ((++spins & 127) == 0) {
-      if (ld_volatile(&cx.p->ctrl->abort)) return false;
-      if (gtimer() - t0 > cx.p->wait_limit_ns) {
-        raise_error(*cx.p, MK_ERR_DEVICE_TIMEOUT, cx.cta, task, op, layer, -1, 0, 0);
-        return false;
-      }
+  while (!mbar_wait_hint(bar, parity, 20000)) {
+    if (ld_volatile(&cx.p->ctrl->abort)) return false;
+    if (gtimer() - t0 > cx.p->wait_limit_ns) {
+      raise_error(*cx.p, MK_ERR_DEVICE_TIMEOUT, cx.cta, task, op, layer, -1, 0, 0);
+      return false;
     }
   }
   return true;
@@ -583,353 +615,243 @@ __device__ bool wait_mbar(const Ctx &cx, uint64_t *bar, uint32_t parity, int tas
  *          j * 4PD, its K box then its V box (P tokens x D dims, stored as
  *          128-byte rows of 64 dims, swizzled when D >= 64; two copies). */
 
-enum { SK_ROWS = 0, SK_PAIRS = 1, SK_PAGES = 2 };
 
-struct StageDesc {
-  int kind, n;
-  const uint8_t *a, *b;
-  uint32_t row_bytes;
-  int layer, kvh, seq, q0;
-  int pages[MK_MAX_STAGE_PAGES]; /* PAGES: physical page ids */
-};
-
-enum { IT_STAGE = 1, IT_END = 0, IT_FAIL = -2 };
-
-/* The producer's cursor over the CTA's stage sequence.  Everything it reads
- * per stage is cached in registers at init or at the start of a task. */
-struct StageIter {
-  const mk_kparams *p;
-  const int32_t *row;
-  /* cached parameters */
-  int L, d, HqD, F, P, D, Hkv, max_pages, SB, pps_kv, pps_up;
-  const mk_layer_dev *layers;
-  const uint16_t *lm_head;
-  const int32_t *page_table, *seq_lens;
-  const mk_routing *routing_base;
-  int nl, nf;
-  uint32_t epoch;
-  int layer, k;   /* current task (layer == L: the final tasks) */
-  bool started;
-  long count;     /* stages produced */
-  /* current task */
-  int op;
-  const int32_t *t;
-  const mk_layer_dev *ly;
-  const uint16_t *src; /* row streams */
-  int r, nrows, K, rps;
-  int q, p1, b, kvh;   /* attention pages */
-  int64_t v, v1;       /* gate/up share */
-  int uc, fc;          /* current (slot, ffn index) of the share */
-  int u, U, r0o, nro;  /* OUT: u = -1 while on Wo rows, then the down slot */
-  const mk_routing *rt;
-  int32_t *pexp, *ppage; /* shared-memory caches of expert and page ids */
-  int exp_layer;         /* layer whose expert ids pexp holds (-1: none) */
-  int p0a;               /* first page of the current attention split */
-
-  __device__ void init(const mk_kparams *pp, const int32_t *rw, uint32_t ep, int sb) {
-    p = pp;
-    row = rw;
-    L = pp->L;
-    d = pp->d;
-    HqD = pp->Hq * pp->D;
-    F = pp->F;
-    P = pp->P;
-    D = pp->D;
-    Hkv = pp->Hkv;
-    max_pages = pp->max_pages;
-    SB = sb;
-    pps_kv = mk_pages_per_stage(P, D, sb);
-    pps_up = mk_pairs_per_stage(d, sb);
-    layers = pp->layers;
-    lm_head = pp->lm_head;
-    page_table = pp->page_table;
-    seq_lens = pp->seq_lens;
-    routing_base = pp->routing;
-    nl = rw[1];
-    nf = rw[2];
-    epoch = ep;
-    layer = 0;
-    k = 0;
-    started = false;
-    count = 0;
-    exp_layer = -1;
-    if (nl == 0) layer = L; /* no layer tasks */
-  }
-
-  /* Routing of this layer known: U and all expert ids into shared memory
-   * (independent loads in batches of 16, one round trip each). */
-  __device__ bool experts(const Ctx &cx) {
-    if (exp_layer == layer) return true;
-    if (!routing(cx)) return false;
-    rt = routing_base + layer;
-    U = __ldcg(&rt->U);
-    for (int u0 = 0; u0 < U; u0 += 16) {
-      int e[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) e[j] = u0 + j < U ? __ldcg(&rt->expert[u0 + j]) : 0;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) pexp[u0 + j] = e[j];
-    }
-    exp_layer = layer;
-    return true;
-  }
-
-  __device__ bool at_end() const { return layer > L || (layer == L && k >= nf); }
-
-  __device__ void next_task() {
-    started = false;
-    ++k;
-    if (layer < L && k >= nl) {
-      k = 0;
-      ++layer;
-      if (layer < L && nl == 0) layer = L;
-    }
-  }
-
-  /* Waits (bounded) until the routing of this task's layer is known. */
-  __device__ bool routing(const Ctx &cx) {
-    int32_t *c = lctr(*p, layer, CTR_ROUTED);
-    if ((int)(ld_acquire(c) - (int)(epoch + 1)) >= 0) return true;
-    return wait_counter(cx, c, (int)(epoch + 1), -1, OP_UP, layer, CTR_ROUTED);
-  }
-
-  __device__ void rows_from(const uint16_t *s0, int n, int KK) {
-    src = s0;
-    r = 0;
-    nrows = n;
-    K = KK;
-    rps = mk_rows_per_stage(KK, SB);
-  }
-
-  __device__ int begin(const Ctx &cx) {
-    t = row + MK_DESC_INTS * (1 + (layer < L ? k : nl + k));
-    op = t[0];
-    ly = layers + (layer < L ? layer : L - 1);
-    switch (op) {
-      case OP_QKV: {
-        const uint16_t *w = t[1] == 0 ? ly->wq : t[1] == 1 ? ly->wk : ly->wv;
-        rows_from(w + (size_t)t[2] * d, t[3], d);
-        return IT_STAGE;
-      }
-      case OP_ROUTER:
-        rows_from(ly->wr + (size_t)t[2] * d, t[3], d);
-        return IT_STAGE;
-      case OP_LM:
-        rows_from(lm_head + (size_t)t[2] * d, t[3], d);
-        return IT_STAGE;
-      case OP_ATTN: {
-        b = t[1];
-        kvh = t[2];
-        q = p0a = t[3];
-        p1 = t[4] >= 0 ? t[4] : (__ldg(seq_lens + b) + P - 1) / P;
-        /* the split's page ids (up to MK_PAGE_CACHE) in batches of 16 */
-        const int n = min(p1 - p0a, MK_PAGE_CACHE);
-        for (int j0 = 0; j0 < n; j0 += 16) {
-          int pg[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) pg[j] = j0 + j < n ? __ldg(page_table + b * max_pages + p0a + j0 + j) : 0;
-#pragma unroll
-          for (int j = 0; j < 16; ++j) ppage[j0 + j] = pg[j];
-        }
-        return IT_STAGE;
-      }
-      case OP_UP: {
-        if (!experts(cx)) return IT_FAIL;
-        const int64_t T = (int64_t)U * F;
-        v = T * t[1] / t[2];
-        v1 = T * (t[1] + 1) / t[2];
-        uc = (int)(v / F);
-        fc = (int)(v - (int64_t)uc * F);
-        return IT_STAGE;
-      }
-      case OP_OUT:
-        u = -1;
-        r0o = t[2];
-        nro = t[3];
-        rows_from(ly->wo + (size_t)r0o * HqD, nro, HqD);
-        return IT_STAGE;
-      default:
-        return IT_FAIL; /* the consumers report the bad opcode */
-    }
-  }
-
-  __device__ bool row_stage(StageDesc &sd) {
-    if (r >= nrows) return false;
-    const int cnt = min(rps, nrows - r);
-    sd.kind = SK_ROWS;
-    sd.n = cnt;
-    sd.a = (const uint8_t *)(src + (size_t)r * K);
-    sd.row_bytes = (uint32_t)K * 2;
-    r += cnt;
-    return true;
-  }
-
-  /* IT_STAGE: a stage; IT_END: this task has no more; IT_FAIL.  Page ids
-   * are looked up only for a stage this producer fills. */
-  __device__ int emit(StageDesc &sd, const Ctx &cx, bool fill) {
-    switch (op) {
-      case OP_QKV:
-      case OP_ROUTER:
-      case OP_LM:
-        return row_stage(sd) ? IT_STAGE : IT_END;
-      case OP_ATTN: {
-        if (q >= p1) return IT_END;
-        const int cnt = min(pps_kv, p1 - q);
-        sd.kind = SK_PAGES;
-        sd.n = cnt;
-        sd.layer = layer;
-        sd.kvh = kvh;
-        sd.seq = b;
-        sd.q0 = q;
-        if (fill)
-          for (int j = 0; j < cnt; ++j) {
-            const int idx = q + j - p0a;
-            sd.pages[j] = idx < MK_PAGE_CACHE ? ppage[idx] : __ldg(page_table + b * max_pages + q + j);
-          }
-        q += cnt;
-        return IT_STAGE;
-      }
-      case OP_UP: {
-        if (v >= v1) return IT_END;
-        const int f1 = (int)min((int64_t)F, fc + (v1 - v));
-        const int cnt = min(pps_up, f1 - fc);
-        const int e = pexp[uc];
-        const size_t eo = ((size_t)e * F + fc) * d;
-        sd.kind = SK_PAIRS;
-        sd.n = cnt;
-        sd.a = (const uint8_t *)(ly->wg + eo);
-        sd.b = (const uint8_t *)(ly->wu + eo);
-        sd.row_bytes = (uint32_t)d * 2;
-        v += cnt;
-        fc += cnt;
-        if (fc == F) {
-          ++uc;
-          fc = 0;
-        }
-        return IT_STAGE;
-      }
-      case OP_OUT: {
-        while (true) {
-          if (row_stage(sd)) return IT_STAGE;
-          if (u == -1 && !experts(cx)) return IT_FAIL;
-          ++u;
-          if (u >= U) return IT_END;
-          const int e = pexp[u];
-          rows_from(ly->wd + ((size_t)e * d + r0o) * F, nro, F);
-        }
-      }
-      default:
-        return IT_FAIL;
-    }
-  }
-
-  /* The next stage of the stream (its descriptor complete only if fill). */
-  __device__ int next(StageDesc &sd, const Ctx &cx, bool fill) {
-    while (true) {
-      if (at_end()) return IT_END;
-      if (!started) {
-        const int rs = begin(cx);
-        if (rs != IT_STAGE) return rs;
-        started = true;
-      }
-      const int rs = emit(sd, cx, fill);
-      if (rs == IT_STAGE) {
-        ++count;
-        return IT_STAGE;
-      }
-      if (rs != IT_END) return rs;
-      next_task();
-    }
-  }
-};
-
+/* Producer warp k of MK_NP_WARPS.  The stage sequence is fixed by the task
+ * list (and, for the expert stages, by the layer's routing); stage i goes to
+ * ring slot i % 8 and is filled by warp i % MK_NP_WARPS, so each slot has
+ * one producer.  Per task, the warp's lanes compute the descriptors of the
+ * warp's own stages in parallel from closed forms (rows, pages, expert
+ * segments), then lane 0 issues them in order, each as soon as its slot is
+ * free.  Issuing a copy costs the issuing thread tens of nanoseconds, which
+ * is why there are several producer warps; planning in parallel keeps the
+ * issuing thread free of everything else. */
 struct Producer {
   Ctx cx;
   uint64_t policy;
+  int k, lane;
+  QDesc *buf; /* this warp's MK_QBATCH planned descriptors (shared memory) */
+  int last_slot[NC];
+  unsigned long long *strc;
 
-  static __device__ void load(const StageDesc &sd, const Ctx &cx, uint64_t policy, uint8_t *dst,
-                              uint64_t *bar) {
-    const mk_kparams &p = *cx.p;
-    switch (sd.kind) {
-      case SK_ROWS: {
-        const uint32_t bytes = sd.n * sd.row_bytes;
-        mbar_expect_tx(bar, bytes);
-        bulk_g2s(dst, sd.a, bytes, bar, policy);
-        break;
-      }
-      case SK_PAIRS: {
-        const uint32_t bytes = sd.n * sd.row_bytes;
-        mbar_expect_tx(bar, 2 * bytes);
-        bulk_g2s(dst, sd.a, bytes, bar, policy);
-        bulk_g2s(dst + bytes, sd.b, bytes, bar, policy);
-        break;
-      }
-      default: {
-        const int P = p.P;
-        const uint32_t half = (uint32_t)P * p.D * 2, pgb = 2 * half;
-        const uint8_t *kmap = (const uint8_t *)p.kv_maps + (size_t)sd.layer * 2 * 128;
-        const uint8_t *vmap = kmap + 128;
-        mbar_expect_tx(bar, sd.n * pgb);
-        for (int j = 0; j < sd.n; ++j) {
-          const int y = (sd.pages[j] * p.Hkv + sd.kvh) * P;
-          tensor_g2s_3d(dst + j * pgb, kmap, y, bar, policy);
-          tensor_g2s_3d(dst + j * pgb + half, vmap, y, bar, policy);
-        }
-      }
+  /* bounded wait for the layer's routing, on lane 0; false on timeout/abort */
+  __device__ bool routed(int layer) const {
+    int ok = 1;
+    if (lane == 0) {
+      int32_t *c = lctr(*cx.p, layer, CTR_ROUTED);
+      if ((int)(ld_acquire(c) - (int)(cx.epoch + 1)) < 0)
+        ok = wait_counter(cx, c, (int)(cx.epoch + 1), -1, OP_UP, layer, CTR_ROUTED) ? 1 : 0;
     }
+    return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
   }
 
-  /* Producer k of MK_NP_WARPS walks the whole stage sequence and fills the
-   * stages i with i % MK_NP_WARPS == k, i.e. the ring slots = k mod
-   * MK_NP_WARPS: issuing a copy costs the issuing thread tens of
-   * nanoseconds, so several issuers keep HBM busy where one could not. */
-  __device__ __noinline__ void run(const int32_t *row, int k) {
-    const Ctx c = cx; /* a register copy: `this` lives in local memory */
-    const uint64_t pol = policy;
-    int last_slot[NC];
-    for (int s = 0; s < NC; ++s) last_slot[s] = -1;
-    StageIter ld;
-    ld.init(c.p, row, c.epoch, c.SB);
-    ld.pexp = c.pexp(k);
-    ld.ppage = c.ppage(k);
-    StageDesc sd;
-    unsigned long long *strc = c.cta == 0 ? c.p->stage_trace : nullptr;
-    while (true) {
-      const uint64_t ta = strc ? sclock() : 0;
-      const bool mine = (int)(ld.count % MK_NP_WARPS) == k; /* the stage about to be walked */
-      const int rs = ld.next(sd, c, mine);
-      if (rs != IT_STAGE) break; /* end, or a failed wait (already reported) */
-      const int i = (int)ld.count - 1;
-      if (!mine) continue;
-      const int slot = i % NC;
-      const uint64_t tb = strc ? sclock() : 0;
-      if (i >= NC) {
-        const uint32_t parity = (uint32_t)(((i / NC) - 1) & 1);
-        if (!wait_mbar(c, &c.empty()[slot], parity, -1, -1, -1)) break;
+  /* issues one planned stage (lane 0); false on a failed wait */
+  __device__ bool issue(const QDesc &d, int i) {
+    const mk_kparams &p = *cx.p;
+    const uint64_t ta = strc ? sclock() : 0;
+    const int slot = i % NC;
+    if (i >= NC && !wait_mbar(cx, &cx.empty()[slot], (uint32_t)(((i / NC) - 1) & 1), -1, -1, -1))
+      return false;
+    const uint64_t tb = strc ? sclock() : 0;
+    uint8_t *dst = cx.ring() + (size_t)slot * cx.SB;
+    uint64_t *bar = &cx.full()[slot];
+    if (d.kind == SK_ROWS) {
+      const uint32_t bytes = d.n * d.row_bytes;
+      mbar_expect_tx(bar, bytes);
+      bulk_g2s(dst, d.a, bytes, bar, policy);
+    } else if (d.kind == SK_PAIRS) {
+      const uint32_t bytes = d.n * d.row_bytes;
+      mbar_expect_tx(bar, 2 * bytes);
+      bulk_g2s(dst, d.a, bytes, bar, policy);
+      bulk_g2s(dst + bytes, d.b, bytes, bar, policy);
+    } else {
+      const int P = p.P, layer = d.layer_kvh >> 8, kvh = d.layer_kvh & 0xFF;
+      const uint32_t half = (uint32_t)P * p.D * 2, pgb = 2 * half;
+      const uint8_t *kmap = (const uint8_t *)p.kv_maps + (size_t)layer * 2 * 128;
+      const uint8_t *vmap = kmap + 128;
+      mbar_expect_tx(bar, d.n * pgb);
+      for (int j = 0; j < d.n; ++j) {
+        const int y = (d.pages[j] * p.Hkv + kvh) * P;
+        tensor_g2s_3d(dst + j * pgb, kmap, y, bar, policy);
+        tensor_g2s_3d(dst + j * pgb + half, vmap, y, bar, policy);
       }
-      const uint64_t tc = strc ? sclock() : 0;
-      load(sd, c, pol, c.ring() + (size_t)slot * c.SB, &c.full()[slot]);
-      last_slot[slot] = i;
-      if (strc && i < MK_STAGE_TRACE_EVENTS - 1) {
-        unsigned long long *e = strc + (size_t)i * 8;
-        e[1] = ta;
-        e[2] = tb;
-        e[3] = tc;
-        e[4] = sclock();
+    }
+    last_slot[slot] = i;
+    if (strc && i < MK_STAGE_TRACE_EVENTS - 1) {
+      unsigned long long *e = strc + (size_t)i * 8;
+      e[1] = ta;
+      e[2] = ta;
+      e[3] = tb;
+      e[4] = sclock();
+    }
+    return true;
+  }
+
+  /* Plans and issues this warp's stages among stages [j_lo, j_hi) of a task
+   * whose first stage is stream stage `base`; plan(j, d) fills stage j's
+   * descriptor (called on the planning lanes). */
+  template <class Plan>
+  __device__ bool run_stages(int base, int j_lo, int j_hi, Plan &&plan) {
+    int j0 = j_lo + ((k - (base + j_lo) % MK_NP_WARPS) % MK_NP_WARPS + MK_NP_WARPS) % MK_NP_WARPS;
+    for (; j0 < j_hi; j0 += MK_QBATCH * MK_NP_WARPS) {
+      const int j = j0 + lane * MK_NP_WARPS;
+      if (lane < MK_QBATCH && j < j_hi) plan(j, buf[lane]);
+      __syncwarp();
+      int ok = 1;
+      if (lane == 0)
+        for (int l = 0; l < MK_QBATCH; ++l) {
+          const int jj = j0 + l * MK_NP_WARPS;
+          if (jj >= j_hi) break;
+          if (!issue(buf[l], base + jj)) {
+            ok = 0;
+            break;
+          }
+        }
+      if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) return false;
+    }
+    return true;
+  }
+
+  __device__ __forceinline__ void run(const int32_t *row) {
+    const Ctx c = cx;
+    const mk_kparams &p = *c.p;
+    for (int s = 0; s < NC; ++s) last_slot[s] = -1;
+    const int nl = row[1], nf = row[2], SB = c.SB;
+    const int d = p.d, F = p.F, HqD = p.Hq * p.D, P = p.P;
+    int base = 0;
+    bool ok = true;
+    for (int layer = 0; layer <= p.L && ok; ++layer) {
+      const int ntask = layer < p.L ? nl : nf;
+      for (int kt = 0; kt < ntask && ok; ++kt) {
+        const int32_t *t = row + MK_DESC_INTS * (1 + (layer < p.L ? kt : nl + kt));
+        const mk_layer_dev *ly = p.layers + (layer < p.L ? layer : p.L - 1);
+        const int op = t[0];
+        if (op == OP_QKV || op == OP_ROUTER || op == OP_LM) {
+          const uint16_t *w = op == OP_LM       ? p.lm_head
+                              : op == OP_ROUTER ? ly->wr
+                              : t[1] == 0       ? ly->wq
+                              : t[1] == 1       ? ly->wk
+                                                : ly->wv;
+          const uint16_t *src = w + (size_t)t[2] * d;
+          const int nrows = t[3], rps = mk_rows_per_stage(d, SB);
+          const int n_st = (nrows + rps - 1) / rps;
+          ok = run_stages(base, 0, n_st, [&](int j, QDesc &q) {
+            q.kind = SK_ROWS;
+            q.n = min(rps, nrows - j * rps);
+            q.a = (const uint8_t *)(src + (size_t)j * rps * d);
+            q.row_bytes = (uint32_t)d * 2;
+          });
+          base += n_st;
+        } else if (op == OP_ATTN) {
+          const int b = t[1], kvh = t[2], p0 = t[3];
+          const int p1 = t[4] >= 0 ? t[4] : (__ldg(p.seq_lens + b) + P - 1) / P;
+          const int pps = mk_pages_per_stage(P, p.D, SB);
+          const int n_st = (p1 - p0 + pps - 1) / pps;
+          ok = run_stages(base, 0, n_st, [&](int j, QDesc &q) {
+            const int q0 = p0 + j * pps, cnt = min(pps, p1 - q0);
+            q.kind = SK_PAGES;
+            q.n = cnt;
+            q.layer_kvh = (layer << 8) | kvh;
+            for (int jj = 0; jj < cnt; ++jj) q.pages[jj] = __ldg(p.page_table + b * p.max_pages + q0 + jj);
+          });
+          base += n_st;
+        } else if (op == OP_UP) {
+          if (!routed(layer)) {
+            ok = false;
+            break;
+          }
+          const mk_routing *rt = p.routing + layer;
+          const int U = __ldcg(&rt->U), pps = mk_pairs_per_stage(d, SB);
+          const int64_t T = (int64_t)U * F;
+          const int64_t v = T * t[1] / t[2], v1 = T * (t[1] + 1) / t[2];
+          /* stages per expert segment, as the consumers walk them */
+          const int u0 = (int)(v / F), u1 = v1 > v ? (int)((v1 - 1) / F) : u0 - 1;
+          int n_st = 0;
+          for (int u = u0; u <= u1; ++u) {
+            const int64_t lo = max(v, (int64_t)u * F), hi = min(v1, (int64_t)(u + 1) * F);
+            n_st += (int)((hi - lo + pps - 1) / pps);
+          }
+          ok = run_stages(base, 0, n_st, [&](int j, QDesc &q) {
+            int u = u0, jr = j;
+            int64_t lo = 0, hi = 0;
+            for (; u <= u1; ++u) {
+              lo = max(v, (int64_t)u * F);
+              hi = min(v1, (int64_t)(u + 1) * F);
+              const int ns = (int)((hi - lo + pps - 1) / pps);
+              if (jr < ns) break;
+              jr -= ns;
+            }
+            const int f0 = (int)(lo - (int64_t)u * F) + jr * pps;
+            const int cnt = min(pps, (int)(hi - (int64_t)u * F) - f0);
+            const int e = __ldcg(&rt->expert[u]);
+            const size_t eo = ((size_t)e * F + f0) * d;
+            q.kind = SK_PAIRS;
+            q.n = cnt;
+            q.a = (const uint8_t *)(ly->wg + eo);
+            q.b = (const uint8_t *)(ly->wu + eo);
+            q.row_bytes = (uint32_t)d * 2;
+          });
+          base += n_st;
+        } else if (op == OP_OUT) {
+          const int r0 = t[2], nr = t[3];
+          const int rps_o = mk_rows_per_stage(HqD, SB), n_wo = (nr + rps_o - 1) / rps_o;
+          const uint16_t *wo = ly->wo + (size_t)r0 * HqD;
+          /* the Wo rows first: they need no routing */
+          ok = run_stages(base, 0, n_wo, [&](int j, QDesc &q) {
+            q.kind = SK_ROWS;
+            q.n = min(rps_o, nr - j * rps_o);
+            q.a = (const uint8_t *)(wo + (size_t)j * rps_o * HqD);
+            q.row_bytes = (uint32_t)HqD * 2;
+          });
+          if (!ok || !routed(layer)) {
+            ok = false;
+            break;
+          }
+          const mk_routing *rt = p.routing + layer;
+          const int U = __ldcg(&rt->U);
+          const int rps_f = mk_rows_per_stage(F, SB), n_se = (nr + rps_f - 1) / rps_f;
+          const int n_st = n_wo + U * n_se;
+          ok = run_stages(base, n_wo, n_st, [&](int j, QDesc &q) {
+            const int u = (j - n_wo) / n_se, jj = (j - n_wo) % n_se;
+            const int e = __ldcg(&rt->expert[u]);
+            q.kind = SK_ROWS;
+            q.n = min(rps_f, nr - jj * rps_f);
+            q.a = (const uint8_t *)(ly->wd + ((size_t)e * d + r0 + (size_t)jj * rps_f) * F);
+            q.row_bytes = (uint32_t)F * 2;
+          });
+          base += n_st;
+        } else {
+          ok = false; /* the consumers report the bad opcode */
+        }
       }
     }
     /* Every copy issued must land before the CTA exits (normally the
      * consumers have waited for all of them already). */
-    for (int s = 0; s < NC; ++s) {
-      const int k = last_slot[s];
-      if (k < 0) continue;
-      const uint32_t parity = (uint32_t)((k / NC) & 1);
-      const uint64_t t0 = gtimer();
-      while (!mbar_test(&c.full()[s], parity) && gtimer() - t0 < c.p->wait_limit_ns) {
+    if (lane == 0)
+      for (int s = 0; s < NC; ++s) {
+        const int kk = last_slot[s];
+        if (kk < 0) continue;
+        const uint32_t parity = (uint32_t)((kk / NC) & 1);
+        const uint64_t t0 = gtimer();
+        while (!mbar_test(&c.full()[s], parity) && gtimer() - t0 < p.wait_limit_ns) {
+        }
       }
-    }
+    __syncwarp();
   }
 };
+
+/* A producer warp's whole life, out of line so that its registers are
+ * allocated apart from the consumers', with its state passed by value. */
+__device__ __noinline__ void produce(const Ctx cx, int k, int lane, QDesc *buf,
+                                     unsigned long long *strc, const int32_t *row) {
+  Producer pr;
+  pr.cx = cx;
+  pr.policy = evict_first_policy();
+  pr.k = k;
+  pr.lane = lane;
+  pr.buf = buf;
+  pr.strc = strc;
+  pr.run(row);
+}
 
 /* ============================================================== consumers
  * Eight warps.  Stage i of the CTA's stream belongs to warp i % 8 alone:
@@ -981,8 +903,9 @@ struct Consumer {
     if (lane == 0) {
       const bool trace = tr && warp == 0;
       unsigned long long *se =
-          (tr && cx.cta == 0 && i < MK_STAGE_TRACE_EVENTS - 1) ? cx.p->stage_trace + (size_t)i * 8
-                                                                : nullptr;
+          (tr && cx.cta == cx.p->stage_trace_cta && i < MK_STAGE_TRACE_EVENTS - 1)
+              ? cx.p->stage_trace + (size_t)i * 8
+              : nullptr;
       const uint64_t w0 = trace ? gtimer() : 0, c0 = se ? sclock() : 0;
       ok = wait_mbar(cx, &cx.full()[slot], parity, task, op, layer) ? 1 : 0;
       if (trace) {
@@ -1011,7 +934,8 @@ struct Consumer {
     __syncwarp();
     if (lane == 0) {
       mbar_arrive(&cx.empty()[i % NC]);
-      if (tr && cx.cta == 0 && i < MK_STAGE_TRACE_EVENTS - 1) cx.p->stage_trace[(size_t)i * 8 + 7] = sclock();
+      if (tr && cx.cta == cx.p->stage_trace_cta && i < MK_STAGE_TRACE_EVENTS - 1)
+        cx.p->stage_trace[(size_t)i * 8 + 7] = sclock();
     }
   }
 
@@ -1100,17 +1024,12 @@ struct Consumer {
 
   __device__ void ensure_norm(int layer) {
     if (*(volatile int32_t *)&M()->norm_layer == layer) return;
-    struct Mark {
-      Consumer *c;
-      __device__ ~Mark() {
-        if (c->tr && c->tid == 0) c->t_mark = gtimer();
-      }
-    } mark{this};
     bar_consumers(); /* everyone has read the tag before it can change */
     const uint16_t *hr[NB];
 #pragma unroll
     for (int b = 0; b < NB; ++b) hr[b] = b < cx.p->B ? h_row(layer, b) : nullptr;
     norm_into_xbuf(layer, hr, cx.p->layers[layer].norm);
+    if (tr && tid == 0) t_mark = gtimer();
   }
 
   /* Copies NB vectors of n bf16 (global, row stride gstride) into xbuf at
@@ -1158,7 +1077,7 @@ struct Consumer {
       if (!stage_wait(si + j, st, task, op, layer)) break;
       const int r0 = j * rps, cnt = min(rps, nrows - r0);
       if (NB == 1) {
-        cc_rows(st, cnt, pitch, K, x, lane, [](int v) { return v; },
+        cc_rows(st, cnt, pitch, K, x, lane, 0,
                 [&](int n0, float sum, int nr) {
                   if ((lane & 3) == 0 && (lane >> 2) < nr) epi(r0 + n0 + (lane >> 2), 0, sum);
                 });
@@ -1246,8 +1165,9 @@ struct Consumer {
         v[i] = id[i] < p.E ? __ldcg(lg + (size_t)b * p.E + id[i]) : NEG_INF;
         if (id[i] >= p.E) id[i] = 0x40000000;
       }
-      float top_v[MK_MAX_TOPK];
-      int top_i[MK_MAX_TOPK];
+      /* k rounds of a warp argmax; lane k keeps the k-th pick */
+      float my_v = NEG_INF, v0 = 0.0f, z = 0.0f;
+      int my_i = 0;
       for (int k = 0; k < p.K; ++k) {
         float bv = NEG_INF;
         int bi = 0x7FFFFFFF;
@@ -1266,44 +1186,48 @@ struct Consumer {
             bi = oi;
           }
         }
-        top_v[k] = bv;
-        top_i[k] = bi;
+        if (k == 0) v0 = bv;
+        z += expf(bv - v0);
+        if (lane == k) {
+          my_v = bv;
+          my_i = bi;
+        }
 #pragma unroll
         for (int i = 0; i < 4; ++i)
           if (id[i] == bi) id[i] = 0x40000000; /* taken */
       }
-      if (lane == 0) {
-        float z = 0.0f;
-        for (int k = 0; k < p.K; ++k) z += expf(top_v[k] - top_v[0]);
-        for (int k = 0; k < p.K; ++k) {
-          const float w = expf(top_v[k] - top_v[0]) / z;
-          R.ids[b][k] = top_i[k];
-          R.w[b][k] = w;
-          rt->ids[b][k] = top_i[k];
-          rt->w[b][k] = w;
-          atomicOr(&R.used[top_i[k] >> 5], 1u << (top_i[k] & 31));
-        }
+      if (lane < p.K) {
+        const float w = expf(my_v - v0) / z;
+        R.ids[b][lane] = my_i;
+        R.w[b][lane] = w;
+        rt->ids[b][lane] = my_i;
+        rt->w[b][lane] = w;
+        atomicOr(&R.used[my_i >> 5], 1u << (my_i & 31));
       }
     }
     bar_consumers();
+    /* slots in ascending expert id; every slot's weights start at zero */
     if (tid < p.E) {
       const int e = tid;
       if ((R.used[e >> 5] >> (e & 31)) & 1u) {
         int rank = __popc(R.used[e >> 5] & ((1u << (e & 31)) - 1u));
         for (int w = 0; w < (e >> 5); ++w) rank += __popc(R.used[w]);
+        R.rank_of[e] = rank;
         rt->expert[rank] = e;
-        for (int b = 0; b < MK_MAX_BATCH; ++b) {
-          float w = 0.0f;
-          if (b < p.B)
-            for (int k = 0; k < p.K; ++k)
-              if (R.ids[b][k] == e) w = R.w[b][k];
-          rt->slot_w[rank][b] = w;
-        }
+#pragma unroll
+        for (int b = 0; b < MK_MAX_BATCH; ++b) rt->slot_w[rank][b] = 0.0f;
       }
+    }
+    bar_consumers();
+    /* then each (token, pick) sets its slot's weight */
+    if (tid < p.B * p.K) {
+      const int b = tid / p.K, k = tid % p.K;
+      rt->slot_w[R.rank_of[R.ids[b][k]]][b] = R.w[b][k];
     }
     if (tid == 0)
       rt->U = __popc(R.used[0]) + __popc(R.used[1]) + __popc(R.used[2]) + __popc(R.used[3]);
   }
+
 
   /* Merges n attention partials (consecutive slots at `parts`; per head
    * [m, l, -, -, o[D]] with o unnormalised): M = max_s m_s, L = sum_s
@@ -1389,7 +1313,7 @@ struct Consumer {
    * transposing ldmatrix).  Thread (g, t) owns
    * head g: S of keys 2t, 2t+1 of each 8-key half, O of dims 8n + 2t, +1. */
   template <int D>
-  __device__ __noinline__ bool op_attn(const int32_t *t, int task, int layer) {
+  __device__ bool op_attn(const int32_t *t, int task, int layer) {
     constexpr int KS = D / 16;           /* k-steps of Q K^T; V n-tile pairs */
     constexpr int NT = D / 8;            /* n-tiles of O */
     constexpr int BI = D < 64 ? D : 64;  /* box inner size (head dims) */
@@ -1711,7 +1635,7 @@ struct Consumer {
         if (NB == 1) {
           /* virtual row 2j is gate row j, 2j + 1 up row j: lanes 8j'..8j'+3
            * hold the gate sum, the next four lanes the up sum */
-          cc_rows(st, 2 * cnt, pitch, d, x, lane, pairmap, [&](int n0, float sum, int nr) {
+          cc_rows(st, 2 * cnt, pitch, d, x, lane, cnt, [&](int n0, float sum, int nr) {
             const float up = __shfl_xor_sync(0xFFFFFFFFu, sum, 4);
             const int r = lane >> 2;
             if ((lane & 7) == 0 && r + 1 < nr) swiglu(0, (n0 + r) >> 1, sum, up);
@@ -1803,7 +1727,7 @@ struct Consumer {
             a = fmaf(O.slot_w[u][bb], v, a);
           };
           if (NB == 1) {
-            cc_rows(st, cnt, pitch, F, xa, lane, [](int vr) { return vr; },
+            cc_rows(st, cnt, pitch, F, xa, lane, 0,
                     [&](int n0, float sum, int nr) {
                       if ((lane & 3) == 0 && (lane >> 2) < nr) acc(n0 + (lane >> 2), 0, sum);
                     });
@@ -2005,8 +1929,9 @@ __global__ void __launch_bounds__(MK_THREADS, 1) decode_kernel(const __grid_cons
    * to shared memory when it fits */
   /* the stage trace's clock anchors: (globaltimer, SM clock) at start and end */
   unsigned long long *anchor =
-      (p.stage_trace && blockIdx.x == 0) ? p.stage_trace + (size_t)(MK_STAGE_TRACE_EVENTS - 1) * 8
-                                         : nullptr;
+      (p.stage_trace && (int)blockIdx.x == p.stage_trace_cta)
+          ? p.stage_trace + (size_t)(MK_STAGE_TRACE_EVENTS - 1) * 8
+          : nullptr;
   if (anchor && threadIdx.x == 0) {
     anchor[0] = gtimer();
     anchor[1] = sclock();
@@ -2021,13 +1946,8 @@ __global__ void __launch_bounds__(MK_THREADS, 1) decode_kernel(const __grid_cons
   const bool header_ok = row[0] == OP_HEADER;
   if (header_ok) {
     if (warp >= NC) {
-      if (lane == 0) {
-        Producer pr;
-        pr.cx = cx;
-        pr.policy = evict_first_policy();
-        pr.run(row, warp - NC);
-      }
-      __syncwarp();
+      produce(cx, warp - NC, lane, misc->qd[warp - NC],
+              (int)blockIdx.x == p.stage_trace_cta ? p.stage_trace : nullptr, row);
     } else {
       Consumer<NB> c;
       c.cx = cx;
