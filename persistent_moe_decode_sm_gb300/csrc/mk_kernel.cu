@@ -372,26 +372,38 @@ __device__ __forceinline__ unsigned long long bf2_f2(uint32_t w) {
   return pack2(w << 16, w & 0xFFFF0000u);
 }
 
+/* 8 bytes of shared memory at a shared-window address */
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+
 /* NR rows (virtual n0 .. n0 + NR - 1) of one token on the CUDA cores; the
  * row count is a template parameter so that every load of the block can be
- * issued ahead of the FMAs.  v[r] gets this lane's partial sum of row r. */
-template <int NR, class RowMap>
-__device__ __forceinline__ void cc_block(const uint8_t *st, int n0, int pitch, int K,
-                                         const uint16_t *x, int lane, RowMap &rm, float (&v)[8]) {
-  const uint8_t *w[NR];
+ * issued ahead of the FMAs.  st and x are shared-window addresses, read with
+ * explicit shared loads.  v[r] gets this lane's partial sum of row r. */
+template <int NR>
+__device__ __forceinline__ void cc_block(uint32_t st, int n0, int pitch, int K, uint32_t x,
+                                         int lane, int pairs, float (&v)[8]) {
+  uint32_t w[NR];
 #pragma unroll
-  for (int r = 0; r < NR; ++r) w[r] = st + (size_t)rm(n0 + r) * pitch + 8 * lane;
+  for (int r = 0; r < NR; ++r) {
+    const int vr = n0 + r;
+    const int row = pairs ? ((vr & 1) ? pairs + (vr >> 1) : (vr >> 1)) : vr;
+    w[r] = st + (uint32_t)(row * pitch) + 8u * lane;
+  }
   unsigned long long a[NR][2];
 #pragma unroll
   for (int r = 0; r < NR; ++r) a[r][0] = a[r][1] = 0ULL;
-  const uint16_t *xl = x + 4 * lane;
+  const uint32_t xl = x + 8u * lane;
   const int K128 = K & ~127; /* K is a multiple of 64: a half block may remain */
 #pragma unroll 2
   for (int c = 0; c < K128; c += 128) {
-    const uint2 xv = *(const uint2 *)(xl + c);
+    const uint2 xv = lds64(xl + 2u * c);
     uint2 wv[NR];
 #pragma unroll
-    for (int r = 0; r < NR; ++r) wv[r] = *(const uint2 *)(w[r] + 2 * c);
+    for (int r = 0; r < NR; ++r) wv[r] = lds64(w[r] + 2u * c);
     const unsigned long long x0 = bf2_f2(xv.x), x1 = bf2_f2(xv.y);
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
@@ -400,11 +412,11 @@ __device__ __forceinline__ void cc_block(const uint8_t *st, int n0, int pitch, i
     }
   }
   if (K128 < K && lane < 16) {
-    const uint2 xv = *(const uint2 *)(xl + K128);
+    const uint2 xv = lds64(xl + 2u * K128);
     const unsigned long long x0 = bf2_f2(xv.x), x1 = bf2_f2(xv.y);
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
-      const uint2 wv = *(const uint2 *)(w[r] + 2 * K128);
+      const uint2 wv = lds64(w[r] + 2u * K128);
       a[r][0] = ffma2(bf2_f2(wv.x), x0, a[r][0]);
       a[r][1] = ffma2(bf2_f2(wv.y), x1, a[r][1]);
     }
@@ -420,19 +432,18 @@ __device__ __forceinline__ void cc_block(const uint8_t *st, int n0, int pitch, i
  * v / 2 for even v and up row pairs + v / 2 for odd v.  Returns this lane's
  * share of the transposing reduction: lane l holds the sum of virtual row
  * n0 + l / 4. */
-__device__ __noinline__ float cc_block_sum(const uint8_t *st, int n0, int nr, int pitch, int K,
-                                           const uint16_t *x, int lane, int pairs) {
-  auto rm = [pairs](int v) { return pairs ? ((v & 1) ? pairs + (v >> 1) : (v >> 1)) : v; };
+__device__ __noinline__ float cc_block_sum(uint32_t st, int n0, int nr, int pitch, int K,
+                                           uint32_t x, int lane, int pairs) {
   float v[8];
   switch (nr) {
-    case 1: cc_block<1>(st, n0, pitch, K, x, lane, rm, v); break;
-    case 2: cc_block<2>(st, n0, pitch, K, x, lane, rm, v); break;
-    case 3: cc_block<3>(st, n0, pitch, K, x, lane, rm, v); break;
-    case 4: cc_block<4>(st, n0, pitch, K, x, lane, rm, v); break;
-    case 5: cc_block<5>(st, n0, pitch, K, x, lane, rm, v); break;
-    case 6: cc_block<6>(st, n0, pitch, K, x, lane, rm, v); break;
-    case 7: cc_block<7>(st, n0, pitch, K, x, lane, rm, v); break;
-    default: cc_block<8>(st, n0, pitch, K, x, lane, rm, v); break;
+    case 1: cc_block<1>(st, n0, pitch, K, x, lane, pairs, v); break;
+    case 2: cc_block<2>(st, n0, pitch, K, x, lane, pairs, v); break;
+    case 3: cc_block<3>(st, n0, pitch, K, x, lane, pairs, v); break;
+    case 4: cc_block<4>(st, n0, pitch, K, x, lane, pairs, v); break;
+    case 5: cc_block<5>(st, n0, pitch, K, x, lane, pairs, v); break;
+    case 6: cc_block<6>(st, n0, pitch, K, x, lane, pairs, v); break;
+    case 7: cc_block<7>(st, n0, pitch, K, x, lane, pairs, v); break;
+    default: cc_block<8>(st, n0, pitch, K, x, lane, pairs, v); break;
   }
   return transpose_reduce8(v, lane);
 }
@@ -446,9 +457,10 @@ __device__ __noinline__ float cc_block_sum(const uint8_t *st, int n0, int nr, in
 template <class Blk>
 __device__ __forceinline__ void cc_rows(const uint8_t *st, int R, int pitch, int K,
                                         const uint16_t *x, int lane, int pairs, Blk &&blk) {
+  const uint32_t sst = saddr(st), sx = saddr(x);
   for (int n0 = 0; n0 < R; n0 += 8) {
     const int nr = min(8, R - n0);
-    blk(n0, cc_block_sum(st, n0, nr, pitch, K, x, lane, pairs), nr);
+    blk(n0, cc_block_sum(sst, n0, nr, pitch, K, sx, lane, pairs), nr);
   }
 }
 
@@ -920,12 +932,16 @@ struct Consumer {
         se[6] = sclock();
       }
     }
+    /* Lane 0's completed wait acquired the stage's bytes; the warp barrier
+     * orders the other lanes after it (bar.warp.sync orders memory among
+     * its threads).  Every lane testing the mbarrier itself costs more:
+     * under load the lanes' tests serialise. */
+    __syncwarp();
     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
     if (!ok) {
       wfail = true;
       return false;
     }
-    mbar_test(&cx.full()[slot], parity); /* completed: acquire order for this thread */
     st = cx.ring() + (size_t)slot * cx.SB;
     return true;
   }
