@@ -154,6 +154,21 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *b, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint64_t *b) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(b)) : "memory");
 }
+/* mbarrier arrive by the lanes with p set, as one predicated instruction:
+ * no branch, so the warp stays converged */
+__device__ __forceinline__ void mbar_arrive_if(uint64_t *b, bool p) {
+  asm volatile(
+      "{\n .reg .pred q;\n setp.ne.u32 q, %1, 0;\n @q mbarrier.arrive.shared::cta.b64 _, [%0];\n}\n" ::"r"(
+          saddr(b)),
+      "r"((uint32_t)p)
+      : "memory");
+}
+/* 64-bit global store by the lanes with p set (one predicated instruction) */
+__device__ __forceinline__ void st64_if(unsigned long long *a, unsigned long long v, bool p) {
+  asm volatile("{\n .reg .pred q;\n setp.ne.u32 q, %2, 0;\n @q st.global.u64 [%0], %1;\n}\n" ::"l"(a),
+               "l"(v), "r"((uint32_t)p)
+               : "memory");
+}
 __device__ __forceinline__ bool mbar_test(uint64_t *b, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -907,38 +922,32 @@ struct Consumer {
    * warp owns. */
   __device__ int first_mine() const { return (warp - si % NC + NC) % NC; }
 
+  /* Every lane of the warp waits for the stage itself, and the stage
+   * bookkeeping below is branch-free (predicated single stores and
+   * arrives): a wait or a multi-instruction region run by one lane alone
+   * leaves the warp split, and a split warp runs the stage's compute once
+   * per lane group. */
   __device__ bool stage_wait(int i, uint8_t *&st, int task, int op, int layer) {
     if (wfail) return false;
     const int slot = i % NC;
     const uint32_t parity = (uint32_t)((i / NC) & 1);
-    int ok = 1;
-    if (lane == 0) {
-      const bool trace = tr && warp == 0;
-      unsigned long long *se =
-          (tr && cx.cta == cx.p->stage_trace_cta && i < MK_STAGE_TRACE_EVENTS - 1)
-              ? cx.p->stage_trace + (size_t)i * 8
-              : nullptr;
-      const uint64_t w0 = trace ? gtimer() : 0, c0 = se ? sclock() : 0;
-      ok = wait_mbar(cx, &cx.full()[slot], parity, task, op, layer) ? 1 : 0;
-      if (trace) {
-        const uint64_t w1 = gtimer();
-        if (!t_stage) t_stage = w1;
-        else t_swait += w1 - w0;
-        ++n_stages;
-      }
-      if (se) {
-        se[0] = (unsigned long long)(i | (warp << 20) | (op << 24));
-        se[5] = c0;
-        se[6] = sclock();
-      }
+    const bool trace = tr && warp == 0;
+    const bool sev = tr && cx.cta == cx.p->stage_trace_cta && i < MK_STAGE_TRACE_EVENTS - 1;
+    const uint64_t w0 = trace ? gtimer() : 0, c0 = sev ? sclock() : 0;
+    const bool ok = wait_mbar(cx, &cx.full()[slot], parity, task, op, layer);
+    if (trace) {
+      const uint64_t w1 = gtimer();
+      if (!t_stage) t_stage = w1;
+      else t_swait += w1 - w0;
+      ++n_stages;
     }
-    /* Lane 0's completed wait acquired the stage's bytes; the warp barrier
-     * orders the other lanes after it (bar.warp.sync orders memory among
-     * its threads).  Every lane testing the mbarrier itself costs more:
-     * under load the lanes' tests serialise. */
-    __syncwarp();
-    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-    if (!ok) {
+    if (sev) {
+      unsigned long long *se = cx.p->stage_trace + (size_t)i * 8;
+      st64_if(se, (unsigned long long)(i | (warp << 20) | (op << 24)), lane == 0);
+      st64_if(se + 5, c0, lane == 0);
+      st64_if(se + 6, sclock(), lane == 0);
+    }
+    if (!__all_sync(0xFFFFFFFFu, ok)) {
       wfail = true;
       return false;
     }
@@ -947,12 +956,10 @@ struct Consumer {
   }
 
   __device__ void stage_release(int i) {
-    __syncwarp();
-    if (lane == 0) {
-      mbar_arrive(&cx.empty()[i % NC]);
-      if (tr && cx.cta == cx.p->stage_trace_cta && i < MK_STAGE_TRACE_EVENTS - 1)
-        cx.p->stage_trace[(size_t)i * 8 + 7] = sclock();
-    }
+    __syncwarp(); /* every lane's reads of the slot precede the release */
+    mbar_arrive_if(&cx.empty()[i % NC], lane == 0);
+    if (tr && cx.cta == cx.p->stage_trace_cta && i < MK_STAGE_TRACE_EVENTS - 1)
+      st64_if(cx.p->stage_trace + (size_t)i * 8 + 7, sclock(), lane == 0);
   }
 
   __device__ const uint16_t *h_row(int layer, int b) const {
