@@ -819,33 +819,35 @@ struct Producer {
           });
           base += n_st;
         } else if (op == OP_OUT) {
+          /* the chosen experts' down rows first (their activations are
+           * ready before the attention output), then the Wo rows */
           const int r0 = t[2], nr = t[3];
-          const int rps_o = mk_rows_per_stage(HqD, SB), n_wo = (nr + rps_o - 1) / rps_o;
-          const uint16_t *wo = ly->wo + (size_t)r0 * HqD;
-          /* the Wo rows first: they need no routing */
-          ok = run_stages(base, 0, n_wo, [&](int j, QDesc &q) {
-            q.kind = SK_ROWS;
-            q.n = min(rps_o, nr - j * rps_o);
-            q.a = (const uint8_t *)(wo + (size_t)j * rps_o * HqD);
-            q.row_bytes = (uint32_t)HqD * 2;
-          });
-          if (!ok || !routed(layer)) {
+          if (!routed(layer)) {
             ok = false;
             break;
           }
           const mk_routing *rt = p.routing + layer;
           const int U = __ldcg(&rt->U);
           const int rps_f = mk_rows_per_stage(F, SB), n_se = (nr + rps_f - 1) / rps_f;
-          const int n_st = n_wo + U * n_se;
-          ok = run_stages(base, n_wo, n_st, [&](int j, QDesc &q) {
-            const int u = (j - n_wo) / n_se, jj = (j - n_wo) % n_se;
-            const int e = __ldcg(&rt->expert[u]);
+          const int n_dn = U * n_se;
+          const int rps_o = mk_rows_per_stage(HqD, SB), n_wo = (nr + rps_o - 1) / rps_o;
+          const uint16_t *wo = ly->wo + (size_t)r0 * HqD;
+          ok = run_stages(base, 0, n_dn + n_wo, [&](int j, QDesc &q) {
             q.kind = SK_ROWS;
-            q.n = min(rps_f, nr - jj * rps_f);
-            q.a = (const uint8_t *)(ly->wd + ((size_t)e * d + r0 + (size_t)jj * rps_f) * F);
-            q.row_bytes = (uint32_t)F * 2;
+            if (j < n_dn) {
+              const int u = j / n_se, jj = j % n_se;
+              const int e = __ldcg(&rt->expert[u]);
+              q.n = min(rps_f, nr - jj * rps_f);
+              q.a = (const uint8_t *)(ly->wd + ((size_t)e * d + r0 + (size_t)jj * rps_f) * F);
+              q.row_bytes = (uint32_t)F * 2;
+            } else {
+              const int jw = j - n_dn;
+              q.n = min(rps_o, nr - jw * rps_o);
+              q.a = (const uint8_t *)(wo + (size_t)jw * rps_o * HqD);
+              q.row_bytes = (uint32_t)HqD * 2;
+            }
           });
-          base += n_st;
+          base += n_dn + n_wo;
         } else {
           ok = false; /* the consumers report the bad opcode */
         }
@@ -1715,13 +1717,10 @@ struct Consumer {
     const int U = __ldcg(&rt->U);
     for (int i = tid; i < U * NB; i += NCT)
       O.slot_w[i / NB][i % NB] = __ldcg(&rt->slot_w[i / NB][i % NB]);
-    if (!cwait(lctr(p, layer, CTR_ATTN_DONE), target, task, OP_OUT, layer, CTR_ATTN_DONE))
-      return false;
     uint16_t *x = (uint16_t *)cx.xbuf();
-    load_x(x, p.o + (size_t)layer * MK_MAX_BATCH * HqD, HqD, HqD);
     for (int i = tid; i < NC * MK_MAX_OUT_ROWS * NB; i += NCT) (&O.acc_w[0][0][0])[i] = 0.0f;
-    bar_consumers();
-    gemv_rows(nr, HqD, x, task, OP_OUT, layer, [&](int r, int bb, float v) { O.acc_o[r][bb] = v; });
+    /* the experts' down rows first: their activations are complete once
+     * every gate/up share is, normally before the attention output */
     if (!cwait(lctr(p, layer, CTR_UP_DONE), (int)((cx.epoch + 1) * p.n_up), task, OP_OUT, layer,
                CTR_UP_DONE))
       return false;
@@ -1766,6 +1765,13 @@ struct Consumer {
       }
     }
     si += U * n_se;
+    /* then Wo against the attention output */
+    if (!cwait(lctr(p, layer, CTR_ATTN_DONE), target, task, OP_OUT, layer, CTR_ATTN_DONE))
+      return false;
+    bar_consumers(); /* every warp is done with the activations in xbuf */
+    load_x(x, p.o + (size_t)layer * MK_MAX_BATCH * HqD, HqD, HqD);
+    bar_consumers();
+    gemv_rows(nr, HqD, x, task, OP_OUT, layer, [&](int r, int bb, float v) { O.acc_o[r][bb] = v; });
     if (!task_end()) return false;
     for (int i = tid; i < nr * B; i += NCT) {
       const int r = i / B, bb = i % B;

@@ -231,10 +231,10 @@ mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int
    * ("Cohere Packs the Entire Decoding Step Into a Single CUDA Megakernel",
    * ainews.surl.tw, paragraph 2): CTAs [0, n_acta) take the attention splits
    * (QKV, ATTN, OUT), the others the expert gate/up shares (QKV or ROUTER,
-   * UP, OUT).  The split follows the bytes each side streams: the KV cache
-   * against the expected distinct experts' gate/up rows, so a CTA of either
-   * kind streams about as much per layer.  With few CTAs every CTA does
-   * everything. */
+   * UP, OUT).  The split follows the time each side takes: the KV cache's
+   * bytes, weighted by the attention stage's higher compute per byte, against
+   * the expected distinct experts' gate/up bytes.  With few CTAs every CTA
+   * does everything. */
   int n_acta = n_cta - n_rc;
   if (n_rc > 0) {
     double kv = 0.0;
@@ -242,7 +242,11 @@ mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int
     const double E = d.n_experts, K = d.top_k;
     const double u_exp = E * (1.0 - std::pow(1.0 - K / E, (double)batch));
     const double up = u_exp * 2.0 * d.d_ffn * d.d_model * 2;
-    const double frac = kv / std::max(kv + up, 1.0);
+    /* SM cycles of a 24 KB attention stage (48 keys x 8 query heads, both
+     * products and the online softmax) over those of a gate/up stage of the
+     * same bytes, as measured on GB300 */
+    constexpr double kAttnCostPerByte = 1.5;
+    const double frac = kAttnCostPerByte * kv / std::max(kAttnCostPerByte * kv + up, 1.0);
     const int lo = std::min(batch * Hkv, n_cta - n_rc - 1), hi = n_cta - n_rc - 1;
     n_acta = std::max(std::max(lo, 1), std::min(hi, (int)std::lround(n_cta * frac)));
   }

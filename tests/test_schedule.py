@@ -220,7 +220,9 @@ def test_attention_splits_are_balanced():
 
 def test_roles_balance_streamed_bytes():
     """Attention CTAs take no expert share and expert CTAs no attention
-    split; the two sides stream about the same bytes per CTA."""
+    split; the split weights the KV bytes by the attention stage's higher
+    compute cost (1.5x a gate/up stage's), so an attention CTA streams
+    somewhat fewer bytes than an expert CTA."""
     d = synth.FULL
     for lens in ([8192], [262144], synth.workloads()["full_b8"].seq_lens):
         info, table = mk.mk_plan(cdims(d, 8, 17000), 152, len(lens), lens)
@@ -232,7 +234,7 @@ def test_roles_balance_streamed_bytes():
         e, k = d.n_experts, d.top_k
         u = e * (1 - (1 - k / e) ** len(lens))
         up = u * 2 * d.d_ffn * d.d_model * 2 / len(exp)
-        assert 0.6 < kv / up < 1.6, (lens[:2], kv, up)
+        assert 0.45 < kv / up < 1.1, (lens[:2], kv, up)
 
 
 def test_router_rows_sit_on_ctas_without_attention_splits():
