@@ -49,10 +49,13 @@ enum {
 /* after the per-layer blocks: */
 enum { GCTR_LM_TICKET = 0, GCTR_EXIT = 1, GCTR_COUNT = 2 };
 
-/* Attention splits of one (sequence, kv head) merge in two levels: groups
- * of up to MK_MERGE_GROUP splits (the last to finish merges its group),
- * then the groups (the last group merger writes the output). */
+/* Attention splits of one (sequence, kv head) merge in one level when there
+ * are at most MK_SINGLE_MERGE of them (the last to finish merges all),
+ * else in two: groups of up to MK_MERGE_GROUP splits (the last to finish
+ * merges its group), then the groups (the last group merger writes the
+ * output). */
 #define MK_MERGE_GROUP 8
+#define MK_SINGLE_MERGE 16
 #define MK_MAX_MERGE_GROUPS 32
 
 static inline int mk_ctrs_per_layer(int max_batch, int n_kv_heads) {

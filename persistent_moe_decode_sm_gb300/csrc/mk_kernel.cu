@@ -163,6 +163,13 @@ __device__ __forceinline__ void mbar_arrive_if(uint64_t *b, bool p) {
       "r"((uint32_t)p)
       : "memory");
 }
+/* 32-bit shared store by the lanes with p set (one predicated instruction) */
+__device__ __forceinline__ void sts32_if(float *a, float v, bool p) {
+  asm volatile("{\n .reg .pred q;\n setp.ne.u32 q, %2, 0;\n @q st.shared.f32 [%0], %1;\n}\n" ::"r"(
+                   saddr(a)),
+               "f"(v), "r"((uint32_t)p)
+               : "memory");
+}
 /* 64-bit global store by the lanes with p set (one predicated instruction) */
 __device__ __forceinline__ void st64_if(unsigned long long *a, unsigned long long v, bool p) {
   asm volatile("{\n .reg .pred q;\n setp.ne.u32 q, %2, 0;\n @q st.global.u64 [%0], %1;\n}\n" ::"l"(a),
@@ -1257,72 +1264,67 @@ struct Consumer {
   /* Merges n attention partials (consecutive slots at `parts`; per head
    * [m, l, -, -, o[D]] with o unnormalised): M = max_s m_s, L = sum_s
    * e^{m_s - M} l_s, O = sum_s e^{m_s - M} o_s.  With `out` it writes the
-   * partial [M, L, -, -, O] there; otherwise bf16(O / L) to ob[g][D].  Each
-   * thread's loads for a column are independent (one round trip for n <= 8). */
+   * partial [M, L, -, -, O] there; otherwise bf16(O / L) to ob[g][D].
+   * Each thread owns 4 columns of one head and loads every partial's m, l
+   * and its columns at once (16 partials per round trip), then combines
+   * them in registers: no shared memory, no barrier, one L2 round trip for
+   * up to 16 partials. */
   __device__ void merge_parts(const float *parts, int n, int G, int D, float *out, uint16_t *ob) {
-    const int PS = D + 4;
-    float *fm = (float *)cx.xbuf(); /* [n][G] m, then the factors */
-    float *fl = fm + n * G;         /* [n][G] l */
-    float *hd = fl + n * G;         /* [G] M, [G] L (or 1 / L) */
-    for (int i = tid; i < n * G; i += NCT) {
-      fm[i] = __ldcg(parts + (size_t)i * PS);
-      fl[i] = __ldcg(parts + (size_t)i * PS + 1);
-    }
-    bar_consumers();
-    if (tid < G) {
-      float M = NEG_INF;
-      for (int s2 = 0; s2 < n; ++s2) M = fmaxf(M, fm[s2 * G + tid]);
-      float den = 0.0f;
-      for (int s2 = 0; s2 < n; ++s2) {
-        const float ms = fm[s2 * G + tid];
-        if (ms != NEG_INF) den = fmaf(expf(ms - M), fl[s2 * G + tid], den);
-      }
-      hd[tid] = M;
-      hd[G + tid] = out ? den : 1.0f / den;
-    }
-    bar_consumers();
-    for (int i = tid; i < n * G; i += NCT) {
-      const int gg = i % G;
-      const float ms = fm[i];
-      fm[i] = ms == NEG_INF ? 0.0f : expf(ms - hd[gg]) * (out ? 1.0f : hd[G + gg]);
-    }
-    bar_consumers();
-    const int D4 = D / 4;
+    const int PS = D + 4, D4 = D / 4;
     for (int i = tid; i < G * D4; i += NCT) {
       const int gg = i / D4, j4 = i % D4;
+      float M = NEG_INF, den = 0.0f;
       float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-      const float4 *src = (const float4 *)(parts + (size_t)gg * PS + 4) + j4;
-      int s2 = 0;
-      for (; s2 + 8 <= n; s2 += 8) {
-        float4 v[8];
+      for (int s0 = 0; s0 < n; s0 += 16) {
+        float m[16], l[16];
+        float4 v[16];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = __ldcg(src + (size_t)(s2 + u) * G * PS / 4);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const float f = fm[(s2 + u) * G + gg];
-          acc.x = fmaf(f, v[u].x, acc.x);
-          acc.y = fmaf(f, v[u].y, acc.y);
-          acc.z = fmaf(f, v[u].z, acc.z);
-          acc.w = fmaf(f, v[u].w, acc.w);
+        for (int u = 0; u < 16; ++u) {
+          m[u] = NEG_INF;
+          l[u] = 0.0f;
+          v[u] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          if (s0 + u < n) {
+            const float *ps = parts + ((size_t)(s0 + u) * G + gg) * PS;
+            m[u] = __ldcg(ps);
+            l[u] = __ldcg(ps + 1);
+            v[u] = __ldcg((const float4 *)(ps + 4) + j4);
+          }
         }
+        float Mc = M;
+#pragma unroll
+        for (int u = 0; u < 16; ++u) Mc = fmaxf(Mc, m[u]);
+        if (M != NEG_INF) { /* a later chunk raised the maximum: rescale */
+          const float sc = expf(M - Mc);
+          den *= sc;
+          acc.x *= sc;
+          acc.y *= sc;
+          acc.z *= sc;
+          acc.w *= sc;
+        }
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          if (m[u] != NEG_INF) {
+            const float f = expf(m[u] - Mc);
+            den = fmaf(f, l[u], den);
+            acc.x = fmaf(f, v[u].x, acc.x);
+            acc.y = fmaf(f, v[u].y, acc.y);
+            acc.z = fmaf(f, v[u].z, acc.z);
+            acc.w = fmaf(f, v[u].w, acc.w);
+          }
+        M = Mc;
       }
-      for (; s2 < n; ++s2) {
-        const float4 v = __ldcg(src + (size_t)s2 * G * PS / 4);
-        const float f = fm[s2 * G + gg];
-        acc.x = fmaf(f, v.x, acc.x);
-        acc.y = fmaf(f, v.y, acc.y);
-        acc.z = fmaf(f, v.z, acc.z);
-        acc.w = fmaf(f, v.w, acc.w);
-      }
-      if (out)
+      if (out) {
         *((float4 *)(out + (size_t)gg * PS + 4) + j4) = acc;
-      else
+        if (j4 == 0) {
+          out[(size_t)gg * PS] = M;
+          out[(size_t)gg * PS + 1] = den;
+        }
+      } else {
+        const float r = 1.0f / den;
         *(uint2 *)(ob + (size_t)gg * D + j4 * 4) =
-            make_uint2(pack_bf16(f2bf(acc.x), f2bf(acc.y)), pack_bf16(f2bf(acc.z), f2bf(acc.w)));
-    }
-    if (out && tid < G) {
-      out[(size_t)tid * PS] = hd[tid];
-      out[(size_t)tid * PS + 1] = hd[G + tid];
+            make_uint2(pack_bf16(f2bf(acc.x * r), f2bf(acc.y * r)),
+                       pack_bf16(f2bf(acc.z * r), f2bf(acc.w * r)));
+      }
     }
     bar_consumers();
   }
@@ -1749,10 +1751,13 @@ struct Consumer {
             a = fmaf(O.slot_w[u][bb], v, a);
           };
           if (NB == 1) {
-            cc_rows(st, cnt, pitch, F, xa, lane, 0,
-                    [&](int n0, float sum, int nr) {
-                      if ((lane & 3) == 0 && (lane >> 2) < nr) acc(n0 + (lane >> 2), 0, sum);
-                    });
+            /* branch-free: every lane updates a valid row's accumulator
+             * value, the lane that owns the row stores it */
+            cc_rows(st, cnt, pitch, F, xa, lane, 0, [&](int n0, float sum, int nr) {
+              const int r = n0 + min(lane >> 2, nr - 1);
+              float *a = &O.acc_w[warp][rb0 + r][0];
+              sts32_if(a, fmaf(O.slot_w[u][0], sum, *a), (lane & 3) == 0 && (lane >> 2) < nr);
+            });
           } else {
             mma_rows<NB>(st, cnt, pitch, F, xa, xpf, lane, [](int vr) { return vr; },
                          [&](int n0, const float(&a)[4], const float(&b)[4], bool two) {

@@ -244,8 +244,9 @@ mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int
     const double up = u_exp * 2.0 * d.d_ffn * d.d_model * 2;
     /* SM cycles of a 24 KB attention stage (48 keys x 8 query heads, both
      * products and the online softmax) over those of a gate/up stage of the
-     * same bytes, as measured on GB300 */
-    constexpr double kAttnCostPerByte = 1.5;
+     * same bytes (~1.5, measured on GB300), plus the merge at the end of
+     * the attention side */
+    constexpr double kAttnCostPerByte = 1.6;
     const double frac = kAttnCostPerByte * kv / std::max(kAttnCostPerByte * kv + up, 1.0);
     const int lo = std::min(batch * Hkv, n_cta - n_rc - 1), hi = n_cta - n_rc - 1;
     n_acta = std::max(std::max(lo, 1), std::min(hi, (int)std::lround(n_cta * frac)));
@@ -304,7 +305,10 @@ mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int
       for (int h = 0; h < Hkv; ++h) {
         const int64_t n = npages[b];
         const int ns = (int)std::max<int64_t>(1, std::min<int64_t>(share[b * Hkv + h], n));
-        const int ng = (ns + MK_MERGE_GROUP - 1) / MK_MERGE_GROUP;
+        /* up to MK_SINGLE_MERGE splits merge in one level (one round trip
+         * fewer on the layer's critical path); more merge in groups */
+        const int grp = ns <= MK_SINGLE_MERGE ? ns : MK_MERGE_GROUP;
+        const int ng = (ns + grp - 1) / grp;
         for (int i = 0; i < ns; ++i) {
           Split s;
           s.b = b;
@@ -315,10 +319,10 @@ mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int
           s.slot0 = slot;
           s.ns = ns;
           s.last = (i == ns - 1);
-          s.gi = i / MK_MERGE_GROUP;
-          s.gn = std::min(MK_MERGE_GROUP, ns - s.gi * MK_MERGE_GROUP);
+          s.gi = i / grp;
+          s.gn = std::min(grp, ns - s.gi * grp);
           s.ng = ng;
-          s.gslot0 = slot + s.gi * MK_MERGE_GROUP;
+          s.gslot0 = slot + s.gi * grp;
           s.g2slot = slot2 + s.gi;
           s.g2slot0 = slot2;
           s.pages = s.p1 - s.p0 + (s.last ? 1 : 0);

@@ -138,15 +138,18 @@ def check_coverage(d, info, rows, seq_lens):
             s0 = slot0.pop()
             assert sorted(int(t[5]) for t in sp) == list(range(s0, s0 + len(sp)))
             slots += [int(t[5]) for t in sp]
-            # merge groups: consecutive slots in groups of 8
-            ns, ng = len(sp), -(-len(sp) // 8)
+            # merge groups: consecutive slots, one group of all splits when
+            # there are at most 16, else groups of 8
+            ns = len(sp)
+            grp = ns if ns <= 16 else 8
+            ng = -(-ns // grp)
             g2 = {int(t[14]) for t in sp}
             assert len(g2) == 1
             g20 = g2.pop()
             for t in sp:
-                gi = (int(t[5]) - s0) // 8
+                gi = (int(t[5]) - s0) // grp
                 assert int(t[9]) == gi and int(t[11]) == ng
-                assert int(t[10]) == min(8, ns - 8 * gi) and int(t[12]) == s0 + 8 * gi
+                assert int(t[10]) == min(grp, ns - grp * gi) and int(t[12]) == s0 + grp * gi
                 assert int(t[13]) == g20 + gi
             slots2.append((g20, ng))
     assert sorted(slots) == list(range(info.n_attn_slots))
@@ -221,7 +224,7 @@ def test_attention_splits_are_balanced():
 def test_roles_balance_streamed_bytes():
     """Attention CTAs take no expert share and expert CTAs no attention
     split; the split weights the KV bytes by the attention stage's higher
-    compute cost (1.5x a gate/up stage's), so an attention CTA streams
+    compute cost (1.5x a gate/up stage's, plus the merge), so an attention CTA streams
     somewhat fewer bytes than an expert CTA."""
     d = synth.FULL
     for lens in ([8192], [262144], synth.workloads()["full_b8"].seq_lens):
