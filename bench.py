@@ -272,7 +272,65 @@ def run_mk(args, rank, world):
     }
     if trace_summary:
         out["trace"] = {k: trace_summary[k] for k in ("step_us", "layer_us_median", "cta_time_split")}
+    batches = [int(x) for x in args.batches.split(",") if x.strip()]
+    if batches and world == 1 and not args.layers:
+        out["batches"] = batch_sweep(dims, dev, stream, batches)
     return out
+
+
+def batch_sweep(dims, dev, stream, batches, steps=16, warmup=4):
+    """Decode tok/s and speed-of-light fraction of the same full-scale model
+    at other batch sizes, every sequence at 8192 cached tokens (short
+    CUDA-event-timed runs after the headline measurement)."""
+    import torch
+
+    import persistent_moe_decode_sm_gb300 as mk
+    import synth
+
+    if not batches:
+        return []
+    lens_all = [8192] * max(batches)
+    inp = synth.device_inputs(dims, lens_all, warmup + steps + 8, None, seed=0)
+    pl = inp.layout
+    peak, _ = load_peaks()
+    res = []
+    for B in batches:
+        lens = lens_all[:B]
+        dec = mk.Decoder(dims, inp.tensors, pl.num_pages, pl.max_pages, B, inp.bias_tensors, stream)
+        dec.build_schedule(lens, pl.page_tables[:B])
+        tok = [torch.tensor(synth.first_tokens(dims, B), dtype=torch.int32, device=dev),
+               torch.zeros(B, dtype=torch.int32, device=dev)]
+        logits = torch.empty(B, dims.vocab, dtype=torch.float32, device=dev)
+        cur = 0
+        for _ in range(warmup):
+            dec.decode_step(tok[cur], logits, tok[cur ^ 1])
+            cur ^= 1
+        dec.sync()
+        st0 = dec.stats()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            dec.decode_step(tok[cur], logits, tok[cur ^ 1])
+            cur ^= 1
+        b.record(stream)
+        torch.cuda.synchronize()
+        dec.sync()
+        ms = a.elapsed_time(b)
+        sum_u = float(dec.stats().sum_experts - st0.sum_experts)
+        w = steps * weight_bytes_step(dims, 0.0, B) + 2.0 * sum_u * 3 * dims.d_model * dims.d_ffn
+        kv = sum(kv_bytes_step(dims, [L + warmup + k for L in lens]) for k in range(steps))
+        per_step = (w + kv) / steps
+        tok_s = B * steps / (ms / 1e3)
+        sol = sol_formula(per_step, peak, B)
+        res.append({"batch": B, "cached_tokens": 8192, "tok_s": round(tok_s, 2),
+                    "ms_per_step": round(ms / steps, 4), "bytes_per_step": round(per_step),
+                    "sol_tok_s": round(sol, 1), "sol_fraction": round(tok_s / sol, 4),
+                    "steps": steps, "warmup": warmup})
+        dec.close()
+    del inp
+    return res
 
 
 # -------------------------------------------------------------- CPU oracle
@@ -336,6 +394,8 @@ def main():
     ap.add_argument("--impl", default="mk", choices=["mk", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batches", default="2,4,8",
+                    help="also time these batch sizes at 8192 cached tokens ('' to skip)")
     ap.add_argument("--trace", default="", help="write a per-task trace summary (JSON) here")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: cut the model to its first N layers")

@@ -66,7 +66,7 @@ static inline int mk_ctrs_per_layer(int max_batch, int n_kv_heads) {
 #define MK_MAX_BATCH 8
 #define MK_MAX_TOPK 16
 #define MK_MAX_GROUP 8          /* q heads per kv head */
-#define MK_MAX_OUT_ROWS 64      /* rows of d per OUT task */
+#define MK_MAX_OUT_ROWS 32      /* rows of d per OUT task (more rows: more tasks) */
 #define MK_NC_WARPS 8           /* consumer warps; ring slot w belongs to consumer warp w */
 #define MK_NP_WARPS 4           /* producer warps; producer k fills the ring slots = k mod 4 */
 #define MK_THREADS ((MK_NC_WARPS + MK_NP_WARPS) * 32)
@@ -75,7 +75,7 @@ static inline int mk_ctrs_per_layer(int max_batch, int n_kv_heads) {
 #define MK_MAX_STAGE_PAGES 8
 #define MK_SMEM_OPTIN 232448    /* opt-in shared memory per block on sm_100-class parts */
 #define MK_SMEM_STATIC 1024     /* slack to align the ring to 1024 bytes */
-#define MK_SMEM_TASKS 32        /* task descriptors of a CTA kept in shared memory */
+#define MK_SMEM_TASKS 16        /* task descriptors of a CTA kept in shared memory (more: read from global) */
 
 /* Routing result of one layer, written by the last router task. */
 typedef struct {

@@ -1774,9 +1774,14 @@ struct Consumer {
     if (!cwait(lctr(p, layer, CTR_ATTN_DONE), target, task, OP_OUT, layer, CTR_ATTN_DONE))
       return false;
     bar_consumers(); /* every warp is done with the activations in xbuf */
-    load_x(x, p.o + (size_t)layer * MK_MAX_BATCH * HqD, HqD, HqD);
+    /* Wo's input spans the normed-input buffer and the scratch buffer after
+     * it (the normed input is dead: this is the CTA's last task of the
+     * layer); the next norm must recompute it */
+    uint16_t *xo = cx.xn();
+    if (tid == 0) M()->norm_layer = -2;
+    load_x(xo, p.o + (size_t)layer * MK_MAX_BATCH * HqD, HqD, HqD);
     bar_consumers();
-    gemv_rows(nr, HqD, x, task, OP_OUT, layer, [&](int r, int bb, float v) { O.acc_o[r][bb] = v; });
+    gemv_rows(nr, HqD, xo, task, OP_OUT, layer, [&](int r, int bb, float v) { O.acc_o[r][bb] = v; });
     if (!task_end()) return false;
     for (int i = tid; i < nr * B; i += NCT) {
       const int r = i / B, bb = i % B;

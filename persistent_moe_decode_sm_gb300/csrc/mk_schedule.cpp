@@ -65,17 +65,24 @@ int mk_nb_for(int batch) { return batch <= 1 ? 1 : batch <= 2 ? 2 : batch <= 4 ?
 
 /* The scratch buffer: the largest of what the task types stage there (bf16
  * vectors at pitch K). */
+static size_t xn_bytes_for(const mk_model_dims &d, int nb) {
+  return align_up((size_t)nb * 2 * mk_x_pitch(d.d_model), 128);
+}
+
 static size_t xbuf_bytes_for(const mk_model_dims &d, int nb) {
   const size_t HqD = (size_t)d.n_q_heads * d.head_dim, D = d.head_dim;
   size_t x = (size_t)nb * 2 * d.d_model;                         /* staged h of the norm */
-  x = std::max(x, (size_t)nb * 2 * mk_x_pitch((int)HqD));          /* attention output (Wo) */
+  /* the attention output (Wo's input) is staged across the normed-input
+   * buffer and this one, which follows it: the normed input is dead by then */
+  const size_t wo_in = (size_t)nb * 2 * mk_x_pitch((int)HqD), xn = xn_bytes_for(d, nb);
+  x = std::max(x, wo_in > xn ? wo_in - xn : (size_t)0);
   x = std::max(x, (size_t)nb * 2 * mk_x_pitch(d.d_ffn));          /* one expert's activations */
   /* attention: q (bf16 [8][D + 8]), new k and v (fp32 [D] each), merge
    * scratch fp32 [4][8][D + 8] */
   x = std::max(x, 8 * (D + 8) * 2 + 2 * D * 4 + 4 * 8 * (D + 8) * 4);
   /* cross-split merge: m and l of up to 256 splits x 8 heads, then 2 x 8 */
   x = std::max(x, (size_t)(2 * 256 * MK_MAX_GROUP + 2 * MK_MAX_GROUP) * 4);
-  return align_up(x, 1024);
+  return align_up(x, 128); /* only the ring needs 1024-byte alignment */
 }
 
 bool mk_smem_plan(const mk_model_dims *dm, int nb, MkSmem *out) {
@@ -83,7 +90,7 @@ bool mk_smem_plan(const mk_model_dims *dm, int nb, MkSmem *out) {
   MkSmem s;
   s.misc = align_up(mk_misc_bytes(nb), 128);
   s.xbuf = xbuf_bytes_for(d, nb);
-  s.xn = align_up((size_t)nb * 2 * mk_x_pitch(d.d_model), 128);
+  s.xn = xn_bytes_for(d, nb);
   const size_t fixed = MK_SMEM_STATIC + s.xn + s.xbuf + s.misc;
   if (fixed >= MK_SMEM_OPTIN) return false;
   size_t sb = (MK_SMEM_OPTIN - fixed) / MK_NC_WARPS / 1024 * 1024;
