@@ -70,9 +70,13 @@ def sol_formula(bytes_per_step: float, bw_gbs: float, batch: int = 1) -> float:
 
 
 def kernel_source_hash() -> str:
-    src = os.path.join(ROOT, "persistent_moe_decode_sm_gb300", "csrc", "mk_kernel.cu")
-    with open(src, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Hash of the kernel's compile inputs (its source and the headers that
+    fix its limits and layouts)."""
+    h = hashlib.sha256()
+    for name in ("mk_kernel.cu", "mk_internal.h"):
+        with open(os.path.join(ROOT, "persistent_moe_decode_sm_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def profiled_traffic():

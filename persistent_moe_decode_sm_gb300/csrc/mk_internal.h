@@ -75,7 +75,7 @@ static inline int mk_ctrs_per_layer(int max_batch, int n_kv_heads) {
 #define MK_MAX_STAGE_PAGES 8
 #define MK_SMEM_OPTIN 232448    /* opt-in shared memory per block on sm_100-class parts */
 #define MK_SMEM_STATIC 1024     /* slack to align the ring to 1024 bytes */
-#define MK_SMEM_TASKS 16        /* task descriptors of a CTA kept in shared memory (more: read from global) */
+#define MK_SMEM_TASKS 32        /* task descriptors of a CTA kept in shared memory (more: read from global) */
 
 /* Routing result of one layer, written by the last router task. */
 typedef struct {
