@@ -249,3 +249,19 @@ def test_router_rows_sit_on_ctas_without_attention_splits():
     for c in router_ctas:
         ops = {int(t[0]) for t in rows[c][0]}
         assert OP_ATTN not in ops and OP_QKV not in ops, (c, ops)
+
+
+def test_out_tasks_fit_the_per_task_row_cap():
+    """OUT tasks take at most 32 rows of d (the kernel's per-warp down
+    accumulators hold 32); with fewer CTAs than d / 32 the rows are cut into
+    more tasks, and the tasks still cover d exactly once."""
+    for d, n_sm in ((synth.FULL, 152), (synth.FULL, 16), (synth.FULL, 4)):
+        info, table = mk.mk_plan(cdims(d, 1, 600), n_sm, 1, [8192])
+        rows = decode(table)
+        outs = [t for lt, _ in rows for t in lt if t[0] == OP_OUT]
+        assert len(outs) == info.n_out
+        assert all(1 <= int(t[3]) <= 32 for t in outs)
+        cov = np.zeros(d.d_model, int)
+        for t in outs:
+            cov[t[2]:t[2] + t[3]] += 1
+        assert np.all(cov == 1)
