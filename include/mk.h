@@ -207,8 +207,8 @@ mk_status mk_set_trace(mk_ctx *ctx, int32_t events_per_cta);
 mk_status mk_set_stage_trace_cta(mk_ctx *ctx, int32_t cta);
 /* Copies the trace (synchronises).  host_out may be NULL to query the
  * geometry; otherwise it must hold (n_cta * events_per_cta + 4096) * 8
- * words: the task events [n_cta][events_per_cta][8], then CTA 0's stage
- * events [4096][8]. */
+ * words: the task events [n_cta][events_per_cta][8], then the stage events
+ * [4096][8] of the CTA chosen with mk_set_stage_trace_cta. */
 mk_status mk_get_trace(mk_ctx *ctx, uint64_t *host_out, uint64_t n_words, int32_t *n_cta,
                        int32_t *events_per_cta);
 
