@@ -136,21 +136,26 @@ const char *mk_status_string(mk_status s);
  * is entirely owned by an arena or caching allocator, or code running under a
  * memory budget that is already handed out -- and so cannot use mk_create.
  * It runs the same kernel as mk_decode_step, with all of that kernel's scratch
- * (activations, partial sums, counters, routing, task table, page tables,
- * RoPE rows) in one static device array of 16 MiB that every GPU loading the
- * library holds until the process exits.  Workloads whose scratch does not fit
- * (larger models, long contexts) get MK_ERR_SCRATCH_LIMIT.
+ * (activations, partial sums, counters, routing, task table, page tables, one
+ * RoPE row per sequence) in one static device array of 16 MiB that every GPU
+ * loading the library holds until the process exits.  Workloads whose scratch
+ * does not fit (deep or wide models at batch 8, very long page tables) get
+ * MK_ERR_SCRATCH_LIMIT before anything is launched.
  *   dims, w      as for mk_create (w->layers is a HOST array);
  *   batch, seq_lens, page_tables   as for mk_build_schedule (HOST arrays);
  *   token_ids, out_logits (may be NULL), out_next_tokens   DEVICE, as for
  *                mk_decode_step; the new K/V rows are written at L_b;
  *   stream       a cudaStream_t (NULL = legacy default stream).
- * Synchronous: returns after the step, with the kernel's status.  The first
- * call on a device looks up the array's device address (cudaGetSymbolAddress)
- * with that device current, so make that first call before any stream
- * capture.  Calls share the array: the counters are cleared by each call, and
- * calls that overlap on the GPU race (serialise them).  There is no sticky
- * state: every call stands alone. */
+ * Synchronous: it copies its host-side tables from pageable memory and reads
+ * the kernel's status back before it returns, so it must not be called while
+ * its stream is being captured.  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current.
+ * Calls share the array: the counters are cleared by each call, and calls
+ * that overlap on the GPU race (serialise them).  Every device wait gives up
+ * after a fixed 1 s (there is no context to set mk_set_wait_limit_ns on) and
+ * the call returns MK_ERR_DEVICE_TIMEOUT.  There is no sticky state: every
+ * call stands alone.  Given the same inputs and lengths it returns the same
+ * bits as mk_decode_step after mk_build_schedule for those lengths. */
 mk_status mk_decode_step_static(const mk_model_dims *dims, const mk_weights *w, int32_t batch,
                                 const int32_t *seq_lens, const int32_t *page_tables,
                                 const int32_t *token_ids, float *out_logits,

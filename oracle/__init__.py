@@ -83,6 +83,15 @@ def lib():
         L.orc_destroy.argtypes = [vp]
         L.orc_step.argtypes = [vp, vp, vp, ctypes.c_float, ctypes.POINTER(StepOut)]
         L.orc_step.restype = i32
+        L.orc_layer_step.argtypes = [vp, i32, vp, vp, ctypes.c_float, i32, vp,
+                                     ctypes.POINTER(StepOut)]
+        L.orc_layer_step.restype = i32
+        L.orc_head.argtypes = [vp, vp, ctypes.POINTER(StepOut)]
+        L.orc_head.restype = i32
+        L.orc_advance.argtypes = [vp]
+        L.orc_advance.restype = i32
+        L.orc_reset_seq.argtypes = [vp, i32, i32, vp]
+        L.orc_reset_seq.restype = i32
         L.orc_rmsnorm.argtypes = [vp, vp, i32, ctypes.c_float, i32, vp]
         L.orc_gemv.argtypes = [vp, i32, i32, vp, i32, vp]
         L.orc_rope.argtypes = [vp, i32, i32, i64, ctypes.c_double]
@@ -243,3 +252,69 @@ class Oracle:
             raise ValueError(f"orc_step failed ({rc})")
         res["route_mismatch"] = so.route_mismatch
         return res
+
+    # ------------------------------------------------ teacher-forced evaluation
+
+    def layer(self, layer: int, h_in, forced_ids=None, tie_eps: float = 1e-2, keep: bool = False,
+              dumps: Sequence[str] = ()) -> Dict[str, np.ndarray]:
+        """Layer `layer` of the step from the residual h_in (bf16 bits [B][d]),
+        e.g. another implementation's; returns the residual entering the next
+        layer ("h_out", bf16 bits) plus the routing and the requested one-layer
+        dumps ("n", "q", "k", "v", "o", "attn", "moe", "router_logits").  keep:
+        keep the new K/V rows (replaying a whole step; call advance() after
+        the last layer)."""
+        d = self.dims
+        B, k, E = self.B, d.top_k, d.n_experts
+        D, Hq, Hkv, dm = d.head_dim, d.n_q_heads, d.n_kv_heads, d.d_model
+        res = {"h_out": np.empty((B, dm), np.uint16),
+               "route_ids": np.empty((B, k), np.int32),
+               "route_w": np.empty((B, k), np.float32),
+               "route_margin": np.empty(B, np.float32)}
+        shapes = {"router_logits": ((B, E), np.float32), "n": ((B, dm), np.uint16),
+                  "q": ((B, Hq * D), np.uint16), "k": ((B, Hkv * D), np.uint16),
+                  "v": ((B, Hkv * D), np.uint16), "o": ((B, Hq * D), np.uint16),
+                  "attn": ((B, dm), np.uint16), "moe": ((B, dm), np.uint16)}
+        for name in dumps:
+            shp, dt = shapes[name]
+            res[name] = np.empty(shp, dt)
+        so = StepOut()
+        for name, arr in res.items():
+            if name != "h_out":
+                setattr(so, name, arr.ctypes.data)
+        h = _c(h_in, np.uint16)
+        fid = None if forced_ids is None else _c(forced_ids, np.int32)
+        rc = lib().orc_layer_step(self.h, layer, _ptr(h), _ptr(fid), tie_eps, int(keep),
+                                  _ptr(res["h_out"]), ctypes.byref(so))
+        if rc != 0:
+            raise ValueError(f"orc_layer_step failed ({rc})")
+        res["route_mismatch"] = so.route_mismatch
+        return res
+
+    def head(self, h_final) -> Dict[str, np.ndarray]:
+        """Final norm, LM head and argmax of the final residual h_final (bf16
+        bits [B][d])."""
+        B, V = self.B, self.dims.vocab
+        res = {"logits": np.empty((B, V), np.float32), "next_tokens": np.empty(B, np.int32),
+               "argmax_margin": np.empty(B, np.float32)}
+        so = StepOut()
+        for name, arr in res.items():
+            setattr(so, name, arr.ctypes.data)
+        h = _c(h_final, np.uint16)
+        if lib().orc_head(self.h, _ptr(h), ctypes.byref(so)) != 0:
+            raise ValueError("orc_head failed")
+        return res
+
+    def advance(self) -> None:
+        """Every sequence's length advances by one (the end of a replayed step)."""
+        if lib().orc_advance(self.h) != 0:
+            raise ValueError("orc_advance failed")
+
+    def reset_seq(self, b: int, new_len: int, page_row) -> None:
+        """Slot b gets a new sequence of new_len cached tokens in the pages of
+        page_row (continuous batching); the other slots keep their state."""
+        pr = _c(page_row, np.int32)
+        if pr.size != self.pt.shape[1]:
+            raise ValueError("page_row must have max_pages entries")
+        if lib().orc_reset_seq(self.h, b, new_len, _ptr(pr)) != 0:
+            raise ValueError("orc_reset_seq failed")
+        self.pt[b] = pr

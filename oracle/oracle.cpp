@@ -270,166 +270,169 @@ orc_model *orc_create(const orc_dims *dims, const orc_weights *w, int32_t batch,
 
 void orc_destroy(orc_model *m) { delete m; }
 
-int32_t orc_step(orc_model *m, const int32_t *tokens, const int32_t *forced_ids,
-                 float tie_eps, orc_step_out *out) {
-  if (!m || !tokens) return -1;
+}  // extern "C"
+
+namespace {
+
+void dump16(uint16_t *dst, const float *src, int64_t n) {
+  if (dst)
+    for (int64_t i = 0; i < n; ++i) dst[i] = f32_to_bf16(src[i]);
+}
+
+/* One layer of the step (a1-a11) for the whole batch: h [B][d] (bf16 values
+ * held as floats) is the residual entering layer l and becomes the residual
+ * entering layer l + 1.  Per-(layer, token) dumps go to row `row` of out's
+ * arrays.  forced_l ([B][k] or NULL) is another implementation's routing of
+ * this layer (see orc_step).  Each token's new K/V row joins the state for
+ * this layer's attention; unless `keep` it is taken out again afterwards, so
+ * that a teacher-forced evaluation leaves the state as it found it. */
+void layer_forward(orc_model *m, int64_t l, std::vector<float> &h, const int32_t *forced_l,
+                   float tie_eps, orc_step_out *out, int64_t row, bool keep) {
   const orc_dims &dm = m->dims;
   const int64_t B = m->B, d = dm.d_model, Hq = dm.n_q_heads, Hkv = dm.n_kv_heads;
   const int64_t D = dm.head_dim, G = Hq / Hkv, E = dm.n_experts, K = dm.top_k;
-  const int64_t F = dm.d_ffn, V = dm.vocab, L = dm.n_layers;
+  const int64_t F = dm.d_ffn;
   const int dbl = m->dbl;
-  orc_step_out dummy;
-  memset(&dummy, 0, sizeof(dummy));
-  if (!out) out = &dummy;
-  out->route_mismatch = 0;
-
-  for (int64_t b = 0; b < B; ++b)
-    if (tokens[b] < 0 || tokens[b] >= V) return -2;
-
-  /* a0: embedding rows. h holds bf16 values as floats. */
-  std::vector<float> h(B * d);
-  for (int64_t b = 0; b < B; ++b) m->embed.row(tokens[b], d, &h[b * d]);
-
-  auto dump16 = [](uint16_t *dst, const float *src, int64_t n) {
-    if (dst)
-      for (int64_t i = 0; i < n; ++i) dst[i] = f32_to_bf16(src[i]);
-  };
-
   std::vector<float> n(B * d), q(Hq * D), kk(Hkv * D), vv(Hkv * D), o(Hq * D);
   std::vector<float> attn(B * d), moe(B * d), r(E), y(d), acc(d), a(F), g(F), u(F);
   std::vector<int32_t> ids(K);
   std::vector<float> wts(K);
+  const orc_model::Layer &Ly = m->layers[l];
 
-  for (int64_t l = 0; l < L; ++l) {
-    const orc_model::Layer &Ly = m->layers[l];
-    if (out->h) dump16(out->h + (l * B) * d, h.data(), B * d);
+  for (int64_t b = 0; b < B; ++b) {
+    const float *hb = &h[b * d];
+    float *nb = &n[b * d];
+    /* a1: one RMSNorm; attention and MoE both read nb (reading R1). */
+    rmsnorm(hb, Ly.norm, d, dm.rms_eps, dbl, nb);
+    if (out->n) dump16(out->n + (row * B + b) * d, nb, d);
 
-    for (int64_t b = 0; b < B; ++b) {
-      const float *hb = &h[b * d];
-      float *nb = &n[b * d];
-      /* a1: one RMSNorm; attention and MoE both read nb (reading R1). */
-      rmsnorm(hb, Ly.norm, d, dm.rms_eps, dbl, nb);
-      if (out->n) dump16(out->n + (l * B + b) * d, nb, d);
+    /* a2: QKV projections, bf16 outputs (reading R3). */
+    gemv(Ly.wq, 0, Hq * D, d, nb, dbl, q.data());
+    gemv(Ly.wk, 0, Hkv * D, d, nb, dbl, kk.data());
+    gemv(Ly.wv, 0, Hkv * D, d, nb, dbl, vv.data());
+    for (auto &x : q) x = round_bf16(x);
+    for (auto &x : kk) x = round_bf16(x);
+    for (auto &x : vv) x = round_bf16(x);
 
-      /* a2: QKV projections, bf16 outputs (reading R3). */
-      gemv(Ly.wq, 0, Hq * D, d, nb, dbl, q.data());
-      gemv(Ly.wk, 0, Hkv * D, d, nb, dbl, kk.data());
-      gemv(Ly.wv, 0, Hkv * D, d, nb, dbl, vv.data());
-      for (auto &x : q) x = round_bf16(x);
-      for (auto &x : kk) x = round_bf16(x);
-      for (auto &x : vv) x = round_bf16(x);
+    /* a3: RoPE at position L_b, then append K/V there (reading R6). */
+    const int64_t pos = m->cur_len[b];
+    rope(q.data(), Hq, D, pos, dm.rope_base);
+    rope(kk.data(), Hkv, D, pos, dm.rope_base);
+    if (out->q) dump16(out->q + (row * B + b) * Hq * D, q.data(), Hq * D);
+    if (out->k) dump16(out->k + (row * B + b) * Hkv * D, kk.data(), Hkv * D);
+    if (out->v) dump16(out->v + (row * B + b) * Hkv * D, vv.data(), Hkv * D);
+    std::vector<float> &ak = m->app_k[l][b], &av = m->app_v[l][b];
+    ak.insert(ak.end(), kk.begin(), kk.end());
+    av.insert(av.end(), vv.begin(), vv.end());
 
-      /* a3: RoPE at position L_b, then append K/V there (reading R6). */
-      const int64_t pos = m->cur_len[b];
-      rope(q.data(), Hq, D, pos, dm.rope_base);
-      rope(kk.data(), Hkv, D, pos, dm.rope_base);
-      if (out->q) dump16(out->q + (l * B + b) * Hq * D, q.data(), Hq * D);
-      if (out->k) dump16(out->k + (l * B + b) * Hkv * D, kk.data(), Hkv * D);
-      if (out->v) dump16(out->v + (l * B + b) * Hkv * D, vv.data(), Hkv * D);
-      std::vector<float> &ak = m->app_k[l][b], &av = m->app_v[l][b];
-      ak.insert(ak.end(), kk.begin(), kk.end());
-      av.insert(av.end(), vv.begin(), vv.end());
-
-      /* a4+a5: attention over the pos + 1 keys (cached + the new one). */
-      const int64_t nkeys = pos + 1;
-      std::vector<float> keys(Hkv * nkeys * D), vals(Hkv * nkeys * D); /* [hk][j][D] */
+    /* a4+a5: attention over the pos + 1 keys (cached + the new one). */
+    const int64_t nkeys = pos + 1;
+    std::vector<float> keys(Hkv * nkeys * D), vals(Hkv * nkeys * D); /* [hk][j][D] */
 #pragma omp parallel for schedule(static)
-      for (int64_t j = 0; j < nkeys; ++j)
-        for (int64_t hk = 0; hk < Hkv; ++hk) {
-          m->kv_row(l, b, hk, j, false, &keys[(hk * nkeys + j) * D]);
-          m->kv_row(l, b, hk, j, true, &vals[(hk * nkeys + j) * D]);
-        }
-      /* GQA: query head i reads kv head i / G. */
+    for (int64_t j = 0; j < nkeys; ++j)
+      for (int64_t hk = 0; hk < Hkv; ++hk) {
+        m->kv_row(l, b, hk, j, false, &keys[(hk * nkeys + j) * D]);
+        m->kv_row(l, b, hk, j, true, &vals[(hk * nkeys + j) * D]);
+      }
+    /* GQA: query head i reads kv head i / G. */
 #pragma omp parallel for schedule(static)
-      for (int64_t i = 0; i < Hq; ++i) {
-        const int64_t hk = i / G;
-        attention_head(&q[i * D], &keys[hk * nkeys * D], &vals[hk * nkeys * D], nkeys, D,
-                       dbl, &o[i * D]);
-      }
-      if (out->o) dump16(out->o + (l * B + b) * Hq * D, o.data(), Hq * D);
-
-      /* a6: output projection. */
-      gemv(Ly.wo, 0, d, Hq * D, o.data(), dbl, &attn[b * d]);
-      for (int64_t i = 0; i < d; ++i) attn[b * d + i] = round_bf16(attn[b * d + i]);
-
-      /* a7: router logits (fp32, + bias), top-k, renormalised weights. */
-      gemv(Ly.wr, 0, E, d, nb, dbl, r.data());
-      if (!Ly.bias.empty())
-        for (int64_t e = 0; e < E; ++e) r[e] = r[e] + Ly.bias[e];
-      if (out->router_logits) memcpy(out->router_logits + (l * B + b) * E, r.data(), E * 4);
-      float margin;
-      route(r.data(), E, K, ids.data(), wts.data(), &margin);
-      if (out->route_margin) out->route_margin[l * B + b] = margin;
-
-      if (forced_ids) {
-        /* Adopt the other side's choice only where it differs among near ties. */
-        const int32_t *fid = forced_ids + (l * B + b) * K;
-        const float rk = r[ids[K - 1]];
-        bool same = true, ok = true;
-        std::vector<char> in_own(E, 0), in_forced(E, 0);
-        for (int64_t t = 0; t < K; ++t) in_own[ids[t]] = 1;
-        for (int64_t t = 0; t < K; ++t) {
-          if (fid[t] < 0 || fid[t] >= E || in_forced[fid[t]]) { ok = false; break; }
-          in_forced[fid[t]] = 1;
-        }
-        if (ok)
-          for (int64_t e = 0; e < E; ++e)
-            if (in_own[e] != in_forced[e]) {
-              same = false;
-              if (!(margin < tie_eps) || fabsf(r[e] - rk) >= tie_eps) ok = false;
-            }
-        if (!ok) {
-          out->route_mismatch += 1;
-        } else if (!same) {
-          /* Use the forced set, ranked by the oracle's logits (ties -> lower id). */
-          std::vector<int32_t> set(fid, fid + K);
-          std::stable_sort(set.begin(), set.end(), [&](int32_t x, int32_t z) {
-            return r[x] > r[z] || (r[x] == r[z] && x < z);
-          });
-          float mx = -std::numeric_limits<float>::infinity();
-          for (int64_t e = 0; e < E; ++e) mx = std::max(mx, r[e]);
-          float zsum = 0.0f;
-          for (int64_t e = 0; e < E; ++e) zsum += expf(r[e] - mx);
-          float st = 0.0f;
-          std::vector<float> p(K);
-          for (int64_t t = 0; t < K; ++t) {
-            p[t] = expf(r[set[t]] - mx) / zsum;
-            st += p[t];
-          }
-          for (int64_t t = 0; t < K; ++t) {
-            ids[t] = set[t];
-            wts[t] = p[t] / st;
-          }
-        }
-      }
-      if (out->route_ids) memcpy(out->route_ids + (l * B + b) * K, ids.data(), K * 4);
-      if (out->route_w) memcpy(out->route_w + (l * B + b) * K, wts.data(), K * 4);
-
-      /* a8-a10: chosen experts' SwiGLU, weighted fp32 combine, one rounding. */
-      for (int64_t i = 0; i < d; ++i) acc[i] = 0.0f;
-      for (int64_t t = 0; t < K; ++t) {
-        const int64_t e = ids[t];
-        gemv(Ly.wg, e * F, F, d, nb, dbl, g.data());
-        gemv(Ly.wu, e * F, F, d, nb, dbl, u.data());
-        for (int64_t f = 0; f < F; ++f) {
-          const float gb = round_bf16(g[f]), ub = round_bf16(u[f]);
-          a[f] = round_bf16(silu(gb) * ub);
-        }
-        gemv(Ly.wd, e * d, d, F, a.data(), dbl, y.data());
-        for (int64_t i = 0; i < d; ++i) acc[i] = acc[i] + wts[t] * y[i];
-      }
-      for (int64_t i = 0; i < d; ++i) moe[b * d + i] = round_bf16(acc[i]);
+    for (int64_t i = 0; i < Hq; ++i) {
+      const int64_t hk = i / G;
+      attention_head(&q[i * D], &keys[hk * nkeys * D], &vals[hk * nkeys * D], nkeys, D,
+                     dbl, &o[i * D]);
     }
-    if (out->attn) dump16(out->attn + (l * B) * d, attn.data(), B * d);
-    if (out->moe) dump16(out->moe + (l * B) * d, moe.data(), B * d);
+    if (out->o) dump16(out->o + (row * B + b) * Hq * D, o.data(), Hq * D);
+    if (!keep) { /* a teacher-forced evaluation leaves the state as it was */
+      ak.resize(ak.size() - Hkv * D);
+      av.resize(av.size() - Hkv * D);
+    }
 
-    /* a11: residual, h <- bf16((h + attn) + moe) (reading R10). */
-    for (int64_t i = 0; i < B * d; ++i) h[i] = round_bf16((h[i] + attn[i]) + moe[i]);
+    /* a6: output projection. */
+    gemv(Ly.wo, 0, d, Hq * D, o.data(), dbl, &attn[b * d]);
+    for (int64_t i = 0; i < d; ++i) attn[b * d + i] = round_bf16(attn[b * d + i]);
+
+    /* a7: router logits (fp32, + bias), top-k, renormalised weights. */
+    gemv(Ly.wr, 0, E, d, nb, dbl, r.data());
+    if (!Ly.bias.empty())
+      for (int64_t e = 0; e < E; ++e) r[e] = r[e] + Ly.bias[e];
+    if (out->router_logits) memcpy(out->router_logits + (row * B + b) * E, r.data(), E * 4);
+    float margin;
+    route(r.data(), E, K, ids.data(), wts.data(), &margin);
+    if (out->route_margin) out->route_margin[row * B + b] = margin;
+
+    if (forced_l) {
+      /* Adopt the other side's choice only where it differs among near ties. */
+      const int32_t *fid = forced_l + b * K;
+      const float rk = r[ids[K - 1]];
+      bool same = true, ok = true;
+      std::vector<char> in_own(E, 0), in_forced(E, 0);
+      for (int64_t t = 0; t < K; ++t) in_own[ids[t]] = 1;
+      for (int64_t t = 0; t < K; ++t) {
+        if (fid[t] < 0 || fid[t] >= E || in_forced[fid[t]]) { ok = false; break; }
+        in_forced[fid[t]] = 1;
+      }
+      if (ok)
+        for (int64_t e = 0; e < E; ++e)
+          if (in_own[e] != in_forced[e]) {
+            same = false;
+            if (!(margin < tie_eps) || fabsf(r[e] - rk) >= tie_eps) ok = false;
+          }
+      if (!ok) {
+        out->route_mismatch += 1;
+      } else if (!same) {
+        /* Use the forced set, ranked by the oracle's logits (ties -> lower id). */
+        std::vector<int32_t> set(fid, fid + K);
+        std::stable_sort(set.begin(), set.end(), [&](int32_t x, int32_t z) {
+          return r[x] > r[z] || (r[x] == r[z] && x < z);
+        });
+        float mx = -std::numeric_limits<float>::infinity();
+        for (int64_t e = 0; e < E; ++e) mx = std::max(mx, r[e]);
+        float zsum = 0.0f;
+        for (int64_t e = 0; e < E; ++e) zsum += expf(r[e] - mx);
+        float st = 0.0f;
+        std::vector<float> p(K);
+        for (int64_t t = 0; t < K; ++t) {
+          p[t] = expf(r[set[t]] - mx) / zsum;
+          st += p[t];
+        }
+        for (int64_t t = 0; t < K; ++t) {
+          ids[t] = set[t];
+          wts[t] = p[t] / st;
+        }
+      }
+    }
+    if (out->route_ids) memcpy(out->route_ids + (row * B + b) * K, ids.data(), K * 4);
+    if (out->route_w) memcpy(out->route_w + (row * B + b) * K, wts.data(), K * 4);
+
+    /* a8-a10: chosen experts' SwiGLU, weighted fp32 combine, one rounding. */
+    for (int64_t i = 0; i < d; ++i) acc[i] = 0.0f;
+    for (int64_t t = 0; t < K; ++t) {
+      const int64_t e = ids[t];
+      gemv(Ly.wg, e * F, F, d, nb, dbl, g.data());
+      gemv(Ly.wu, e * F, F, d, nb, dbl, u.data());
+      for (int64_t f = 0; f < F; ++f) {
+        const float gb = round_bf16(g[f]), ub = round_bf16(u[f]);
+        a[f] = round_bf16(silu(gb) * ub);
+      }
+      gemv(Ly.wd, e * d, d, F, a.data(), dbl, y.data());
+      for (int64_t i = 0; i < d; ++i) acc[i] = acc[i] + wts[t] * y[i];
+    }
+    for (int64_t i = 0; i < d; ++i) moe[b * d + i] = round_bf16(acc[i]);
   }
-  if (out->h) dump16(out->h + (L * B) * d, h.data(), B * d);
+  if (out->attn) dump16(out->attn + (row * B) * d, attn.data(), B * d);
+  if (out->moe) dump16(out->moe + (row * B) * d, moe.data(), B * d);
 
-  /* a12-a13: final norm, LM head (fp32 logits), greedy argmax. */
-  std::vector<float> logits(V);
+  /* a11: residual, h <- bf16((h + attn) + moe) (reading R10). */
+  for (int64_t i = 0; i < B * d; ++i) h[i] = round_bf16((h[i] + attn[i]) + moe[i]);
+}
+
+/* The final norm, LM head and greedy argmax (a12, a13) of the final
+ * residual h [B][d]. */
+void head_forward(orc_model *m, const std::vector<float> &h, orc_step_out *out) {
+  const orc_dims &dm = m->dims;
+  const int64_t B = m->B, d = dm.d_model, V = dm.vocab;
+  const int dbl = m->dbl;
+  std::vector<float> n(B * d), logits(V);
   for (int64_t b = 0; b < B; ++b) {
     rmsnorm(&h[b * d], m->final_norm, d, dm.rms_eps, dbl, &n[b * d]);
     gemv(m->lm_head, 0, V, d, &n[b * d], dbl, logits.data());
@@ -443,7 +446,82 @@ int32_t orc_step(orc_model *m, const int32_t *tokens, const int32_t *forced_ids,
     if (out->next_tokens) out->next_tokens[b] = (int32_t)best;
     if (out->argmax_margin) out->argmax_margin[b] = logits[best] - second;
   }
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t orc_step(orc_model *m, const int32_t *tokens, const int32_t *forced_ids,
+                 float tie_eps, orc_step_out *out) {
+  if (!m || !tokens) return -1;
+  const orc_dims &dm = m->dims;
+  const int64_t B = m->B, d = dm.d_model, K = dm.top_k, V = dm.vocab, L = dm.n_layers;
+  orc_step_out dummy;
+  memset(&dummy, 0, sizeof(dummy));
+  if (!out) out = &dummy;
+  out->route_mismatch = 0;
+
+  for (int64_t b = 0; b < B; ++b)
+    if (tokens[b] < 0 || tokens[b] >= V) return -2;
+
+  /* a0: embedding rows. h holds bf16 values as floats. */
+  std::vector<float> h(B * d);
+  for (int64_t b = 0; b < B; ++b) m->embed.row(tokens[b], d, &h[b * d]);
+
+  for (int64_t l = 0; l < L; ++l) {
+    if (out->h) dump16(out->h + (l * B) * d, h.data(), B * d);
+    layer_forward(m, l, h, forced_ids ? forced_ids + l * B * K : nullptr, tie_eps, out, l, true);
+  }
+  if (out->h) dump16(out->h + (L * B) * d, h.data(), B * d);
+  head_forward(m, h, out);
   for (int64_t b = 0; b < B; ++b) m->cur_len[b] += 1;
+  return 0;
+}
+
+int32_t orc_layer_step(orc_model *m, int32_t layer, const uint16_t *h_in,
+                       const int32_t *forced_ids, float tie_eps, int32_t keep, uint16_t *h_out,
+                       orc_step_out *out) {
+  if (!m || !h_in || layer < 0 || layer >= m->dims.n_layers) return -1;
+  const int64_t B = m->B, d = m->dims.d_model;
+  orc_step_out dummy;
+  memset(&dummy, 0, sizeof(dummy));
+  if (!out) out = &dummy;
+  out->route_mismatch = 0;
+  std::vector<float> h(B * d);
+  for (int64_t i = 0; i < B * d; ++i) h[i] = bf16_to_f32(h_in[i]);
+  layer_forward(m, layer, h, forced_ids, tie_eps, out, 0, keep != 0);
+  dump16(h_out, h.data(), B * d);
+  return 0;
+}
+
+int32_t orc_head(orc_model *m, const uint16_t *h_in, orc_step_out *out) {
+  if (!m || !h_in) return -1;
+  const int64_t B = m->B, d = m->dims.d_model;
+  orc_step_out dummy;
+  memset(&dummy, 0, sizeof(dummy));
+  if (!out) out = &dummy;
+  std::vector<float> h(B * d);
+  for (int64_t i = 0; i < B * d; ++i) h[i] = bf16_to_f32(h_in[i]);
+  head_forward(m, h, out);
+  return 0;
+}
+
+int32_t orc_reset_seq(orc_model *m, int32_t b, int32_t new_len, const int32_t *page_row) {
+  if (!m || b < 0 || b >= m->B || new_len < 0 || !page_row) return -1;
+  m->base_len[b] = new_len;
+  m->cur_len[b] = new_len;
+  memcpy(&m->page_table[(int64_t)b * m->max_pages], page_row, m->max_pages * sizeof(int32_t));
+  for (int64_t l = 0; l < m->dims.n_layers; ++l) {
+    m->app_k[l][b].clear();
+    m->app_v[l][b].clear();
+  }
+  return 0;
+}
+
+int32_t orc_advance(orc_model *m) {
+  if (!m) return -1;
+  for (int64_t b = 0; b < m->B; ++b) m->cur_len[b] += 1;
   return 0;
 }
 

@@ -117,6 +117,38 @@ typedef struct {
 int32_t orc_step(orc_model *m, const int32_t *tokens, const int32_t *forced_ids,
                  float tie_eps, orc_step_out *out);
 
+/* Teacher-forced evaluation, one piece of the step at a time.
+ *
+ * orc_layer_step: layer `layer` of the step (a1-a11) from a given residual input
+ * h_in [B][d] (bf16 bits) -- another implementation's residual entering that
+ * layer -- writing the residual entering the next layer to h_out [B][d].
+ * Tokens sit at the current positions L_b; the attention reads the state's
+ * K/V rows (cached, plus rows kept by earlier steps) and the new row.  With
+ * keep = 0 the state is left unchanged; with keep = 1 the new K/V row is
+ * kept (call it once per layer, then orc_advance, to replay a whole step).
+ * forced_ids: this layer's [B][k] routing of the other implementation, with
+ * the same near-tie rule as orc_step.  out: any of n, q, k, v, o, attn, moe,
+ * router_logits, route_ids, route_w, route_margin (sized for ONE layer) and
+ * route_mismatch; the other fields are ignored.
+ *
+ * orc_head: the final norm, LM head and argmax (a12, a13) of a given final
+ * residual h_in [B][d]: out's logits, next_tokens and argmax_margin.
+ *
+ * orc_advance: every L_b advances by one (the end of a replayed step).
+ *
+ * orc_step is exactly orc_layer_step(keep = 1) for every layer, orc_head, then
+ * orc_advance. */
+int32_t orc_layer_step(orc_model *m, int32_t layer, const uint16_t *h_in,
+                       const int32_t *forced_ids, float tie_eps, int32_t keep, uint16_t *h_out,
+                       orc_step_out *out);
+int32_t orc_head(orc_model *m, const uint16_t *h_in, orc_step_out *out);
+int32_t orc_advance(orc_model *m);
+
+/* Continuous batching: slot b gets a new sequence with new_len cached tokens
+ * held in the pages of page_row [max_pages]; the K/V rows the slot kept from
+ * earlier steps are dropped, the other slots are untouched. */
+int32_t orc_reset_seq(orc_model *m, int32_t b, int32_t new_len, const int32_t *page_row);
+
 /* ---- the building blocks, exposed for the pin tests ---------------------- */
 
 /* out = bf16(h * (1/sqrtf(mean_fp32(h^2) + eps)) * g); all bf16 bits. */

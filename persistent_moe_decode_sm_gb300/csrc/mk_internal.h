@@ -131,8 +131,9 @@ typedef struct {
   mk_ctrl *ctrl;
   int32_t *seq_lens;          /* [MAXB] live lengths (advanced by the kernel) */
   const int32_t *page_table;  /* [MAXB][max_pages] */
-  const float *rope;          /* [max_pos][D/2][2] (cos, sin) */
+  const float *rope;          /* [max_pos][D/2][2] (cos, sin), or [MAXB][D/2][2] */
   int32_t rope_max_pos;
+  int32_t rope_per_seq;       /* 1: rope holds one row per sequence (this step's position) */
   const int32_t *table;       /* [n_cta][tasks_per_cta][32] */
   int32_t tasks_per_cta;
   int32_t n_slots, u_max;

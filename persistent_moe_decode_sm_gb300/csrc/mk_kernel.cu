@@ -1364,7 +1364,7 @@ struct Consumer {
     float *mb = vs + D;                           /* warp merge [4][8][D + 8] */
     const int QKVD = (p.Hq + 2 * p.Hkv) * D;
     const uint16_t *qkv = p.qkv + ((size_t)layer * MK_MAX_BATCH + b) * QKVD;
-    const float *rp = p.rope + (size_t)L_now * half * 2;
+    const float *rp = p.rope + (size_t)(p.rope_per_seq ? b : L_now) * half * 2;
     for (int i = tid; i < 8 * half; i += NCT) {
       const int g = i / half, j = i % half;
       uint16_t o1 = 0, o2 = 0;
@@ -2034,9 +2034,16 @@ static void *mk_kernel_fn(int nb) {
                    : (void *)mk::decode_kernel<8>;
 }
 
+/* Sets the kernel's dynamic shared-memory limit on the current device to the
+ * largest size any plan uses (MK_SMEM_OPTIN), so that every later launch of
+ * this instantiation -- whatever model dims it was planned for, from any
+ * context or from mk_decode_step_static -- stays within the limit, and
+ * reports how many CTAs of `smem` bytes fit on an SM. */
 extern "C" cudaError_t mk_kernel_prepare(int nb, size_t smem, int *blocks_per_sm) {
   void *fn = mk_kernel_fn(nb);
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (smem > MK_SMEM_OPTIN) return cudaErrorInvalidValue;
+  cudaError_t e =
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)MK_SMEM_OPTIN);
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, fn, MK_THREADS, smem);
 }

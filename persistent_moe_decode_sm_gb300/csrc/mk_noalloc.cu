@@ -9,20 +9,24 @@
  * handed out), or a host process that only borrows device pointers from a
  * framework.  mk_decode_step_static serves them: it runs the same persistent
  * decode kernel as mk_decode_step, with every scratch buffer (activations,
- * partial sums, counters, routing, the task table, page tables, the RoPE rows
- * it needs) carved out of one file-scope device array, mk_static_scratch, of
- * MK_STATIC_SCRATCH_BYTES.  Nothing here calls cudaMalloc, cudaFree,
+ * partial sums, counters, routing, the task table, page tables, one RoPE row
+ * per sequence) carved out of one file-scope device array, mk_static_scratch,
+ * of MK_STATIC_SCRATCH_BYTES.  Nothing here calls cudaMalloc, cudaFree,
  * cudaHostAlloc or an allocating library routine.  The task table itself is
  * built in ordinary host memory of the calling thread.
  *
  * The array lives on every GPU that loads the library until the process
- * exits.  Its address is looked up once per device with cudaGetSymbolAddress
- * by the first call made on that device (with that device current), so that
- * first call should come before any stream capture.  Every call reuses the
- * same array and it keeps the previous call's contents; the counters and the
- * control block are cleared at the start of each call.  Two calls whose work
- * overlaps on the GPU (different streams, or different host threads) race on
- * the array and give wrong results: serialise them.
+ * exits.  Its device address is looked up once per device with
+ * cudaGetSymbolAddress, by the first call made on that device (with that
+ * device current).  Every call reuses the same array and it keeps the
+ * previous call's contents; the counters and the control block are cleared
+ * at the start of each call.  Two calls whose work overlaps on the GPU
+ * (different streams, or different host threads) race on the array and give
+ * wrong results: serialise them.  Each call is synchronous (it copies from
+ * pageable host memory and reads the kernel's status back), so it must not
+ * be called while its stream is being captured into a graph.  The kernel's
+ * waits give up after a fixed 1 s (MK_STATIC_WAIT_LIMIT_NS) and the call
+ * then returns MK_ERR_DEVICE_TIMEOUT.
  */
 #include <cuda_runtime.h>
 
@@ -45,6 +49,8 @@ extern "C" cudaError_t mk_launch(const mk_kparams *p, int nb, int grid, size_t s
 /* 16 MiB: enough for the tiny and mid models and for short contexts of models
  * of that size; the call rejects anything larger with MK_ERR_SCRATCH_LIMIT. */
 #define MK_STATIC_SCRATCH_BYTES (16u << 20)
+/* Every device wait of a static step gives up after this long. */
+#define MK_STATIC_WAIT_LIMIT_NS 1000000000ULL
 
 static __device__ __align__(256) unsigned char mk_static_scratch[MK_STATIC_SCRATCH_BYTES];
 
@@ -53,7 +59,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mu;
 unsigned char *g_scratch[kMaxDevices];      /* device address of mk_static_scratch */
-bool g_prepared[kMaxDevices][4];             /* kernel attributes set per batch bucket */
+bool g_prepared[kMaxDevices][4];             /* kernel attribute set per batch bucket */
 
 size_t up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -130,7 +136,6 @@ extern "C" mk_status mk_decode_step_static(const mk_model_dims *dims, const mk_w
   const int n_slots = std::max(1, plan.n_attn_slots);
   const int ctrs_per_layer = mk_ctrs_per_layer(MB, d.n_kv_heads);
   const size_t n_ctr = ((size_t)Lyr * ctrs_per_layer + GCTR_COUNT) * MK_CTR_STRIDE;
-  const int max_pos = mp * P;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t o = up(off, 256);
@@ -146,7 +151,7 @@ extern "C" mk_status mk_decode_step_static(const mk_model_dims *dims, const mk_w
   const size_t o_rt = take((size_t)Lyr * sizeof(mk_routing));
   const size_t o_act = take((size_t)Lyr * u_max * MB * d.d_ffn * 2);
   const size_t o_lm = take((size_t)plan.n_lm * MB * 2 * 4);
-  const size_t o_rope = take((size_t)max_pos * half * 2 * 4);
+  const size_t o_rope = take((size_t)MB * half * 2 * 4); /* one row per sequence */
   const size_t o_ctr = take(n_ctr * 4);
   const size_t o_ctrl = take(sizeof(mk_ctrl));
   const size_t o_len = take((size_t)MB * 4);
@@ -228,9 +233,8 @@ extern "C" mk_status mk_decode_step_static(const mk_model_dims *dims, const mk_w
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(base + o_tab, plan.table.data(), plan.table.size() * 4,
                         cudaMemcpyHostToDevice, stream);
-  for (int b = 0; b < batch && e == cudaSuccess; ++b)
-    e = cudaMemcpyAsync(base + o_rope + (size_t)seq_lens[b] * half * 2 * 4,
-                        rope_rows.data() + (size_t)b * half * 2, (size_t)half * 2 * 4,
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(base + o_rope, rope_rows.data(), rope_rows.size() * 4,
                         cudaMemcpyHostToDevice, stream);
   if (e != cudaSuccess) return MK_ERR_CUDA;
 
@@ -271,7 +275,8 @@ extern "C" mk_status mk_decode_step_static(const mk_model_dims *dims, const mk_w
   p.seq_lens = (int32_t *)(base + o_len);
   p.page_table = (const int32_t *)(base + o_pt);
   p.rope = (const float *)(base + o_rope);
-  p.rope_max_pos = max_pos;
+  p.rope_max_pos = mp * P;
+  p.rope_per_seq = 1;
   p.table = (const int32_t *)(base + o_tab);
   p.tasks_per_cta = plan.tasks_per_cta;
   p.n_slots = n_slots;
@@ -283,7 +288,7 @@ extern "C" mk_status mk_decode_step_static(const mk_model_dims *dims, const mk_w
   p.n_lm = plan.n_lm;
   p.n_attn_done = plan.n_attn_done;
   p.ctrs_per_layer = ctrs_per_layer;
-  p.wait_limit_ns = 1000000000ULL;
+  p.wait_limit_ns = MK_STATIC_WAIT_LIMIT_NS;
   p.err_host = nullptr;
   p.stage_bytes = sm.stage_bytes;
   p.kv_maps = base + o_maps;

@@ -1,52 +1,84 @@
 """GPU-vs-oracle parity harness (used by the gpu tests and by smoke()).
 
 The GPU side runs through the C ABI (persistent_moe_decode_sm_gb300); the
-oracle side is the CPU reference in oracle/.  Both read the same seeded
-inputs from synth/.  Per step:
-  1. the GPU step runs; its routing is read back;
-  2. the oracle runs the same step, adopting the GPU's routing only at an
-     (layer, token) whose top-k margin is below TIE_EPS and only if the two
-     choices differ among experts within TIE_EPS of the k-th logit;
-     anything else is a routing mismatch (must be 0);
-  3. logits must agree within LOGIT_MAX_ABS / LOGIT_REL_L2.  The reference
-     is the oracle with exact (double) sums and the method's bf16 rounding
-     points.  Two more oracle instances with plain fp32 sums -- ascending and
-     descending summation order, both faithful to the method, which fixes
-     fp32 accumulation but not the order -- run the same step with the same
-     routing; the fp32 noise floor is the largest of their deviations from
-     the exact evaluation and from each other, and where it approaches the
-     stated bound (deep models, large batch x vocabulary) the bound becomes
-     NOISE_FACTOR times that floor;
-  4. the greedy token must be identical where the oracle's top-1/top-2
-     margin exceeds TIE_EPS, else the GPU's token must be within TIE_EPS of
-     the oracle's maximum; both continue with the GPU's token.
+oracle side is the CPU reference in oracle/ with exact (double) sums and the
+method's bf16 rounding points.  Both read the same seeded inputs from synth/.
+
+Two comparisons per step:
+
+Teacher-forced, layer by layer (always).  For every layer l the oracle
+evaluates layer l from the GPU's own residual entering it (h_l, dumped by the
+library) under the GPU's routing (adopted only at near ties, see below), and
+the GPU's residual entering layer l + 1 must agree with the oracle's within
+bf16 rounding: every element within 2 * (ulp(h) + ulp(attn) + ulp(moe)) of
+the oracle's values (one rounding flip in each of the three roundings that
+make the residual), at most TF_FRAC_CHANGED of the elements changed at all,
+relative L2 at most TF_REL_L2.  The attention output o of every layer is held
+to the same kind of bound, the routing must match wherever the oracle's top-k
+margin exceeds TIE_EPS, and the logits that the oracle's LM head makes from
+the GPU's final residual must agree with the GPU's logits within the stated
+max-abs / relative-L2 bound.  This comparison is not chaotic: both sides see
+the same input at every layer, so it holds at any depth, batch and context.
+
+Free-running, end to end (ParityRun(free_steps=N) for the first N steps).
+The oracle runs the whole step from the token alone, keeping its own KV rows,
+adopting the GPU's routing only at (layer, token) pairs whose top-k margin is
+below TIE_EPS and only where the two choices differ among experts within
+TIE_EPS of the k-th logit (anything else is a routing mismatch and fails);
+its logits must agree with the GPU's within the case's fixed bound (the
+stated 3e-2 / 1e-2 unless the test names another, derived bound).  The
+greedy token must be identical where the oracle's top-1/top-2 margin exceeds
+TIE_EPS, else the GPU's token must be within TIE_EPS of the oracle's
+maximum; both continue with the GPU's token.  After the free-running steps
+the oracle's state advances by the teacher-forced replay (its own K/V rows
+computed from the GPU's residuals).
 """
 from __future__ import annotations
 
 import os
 import sys
-from typing import Dict, Optional, Sequence
+from typing import Dict, Optional, Sequence, Tuple
 
 import numpy as np
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-if ROOT not in sys.path:
-    sys.path.insert(0, ROOT)
+TESTS = os.path.dirname(os.path.abspath(__file__))
+for p in (ROOT, TESTS):
+    if p not in sys.path:
+        sys.path.insert(0, p)
 
 import oracle  # noqa: E402
 import persistent_moe_decode_sm_gb300 as mk  # noqa: E402
 import synth  # noqa: E402
+from bf16util import to_f32, ulp  # noqa: E402
 
 # The parity bar: router ids and greedy tokens bit-exact wherever the
 # oracle's margin exceeds 1e-2; logits max-abs 3e-2 and relative L2 1e-2.
 TIE_EPS = 1e-2
 LOGIT_MAX_ABS = 3e-2
 LOGIT_REL_L2 = 1e-2
-# One step's fp32 noise is a single sample of a chaotic quantity (bf16
-# rounding flips amplified layer by layer): on the 8-layer mid model the
-# fp32 deviation from the exact evaluation went 0.0197 -> 0.0352 between
-# consecutive steps, so the bound allows twice the floor measured on the step.
-NOISE_FACTOR = 2.0
+STATED_BOUND = (LOGIT_MAX_ABS, LOGIT_REL_L2)
+# Teacher-forced layer bounds.  Two faithful fp32 evaluations of a layer
+# (the oracle's two summation orders) from the same residual differ from the
+# exact one in at most ~1.4 % of the residual's elements, relative L2 <=
+# 2e-4, each element by at most one rounding flip of h, attn or moe
+# (measured on the tiny, mid and full-scale models).
+TF_FRAC_CHANGED = 0.05
+TF_REL_L2 = 2e-3
+
+# Free-running bound of the 8-layer mid model.  Faithful fp32 evaluations of
+# the method (the oracle's two summation orders) deviate from the exact
+# evaluation by 0.024-0.041 max-abs and 0.009-0.0155 relative L2 at 124 of
+# the 128 greedy steps of that workload (measured on the CPU; at the other 4
+# steps the drift flips a router choice whose margin exceeds 1e-2), so the
+# stated 3e-2 / 1e-2 sits below the method's own fp32 noise there; the bound
+# is 1.5x that floor, rounded up.
+MID_FREE_BOUND = (6e-2, 2.4e-2)
+# Free-running bound of the full-width model cut to 4 layers.  Faithful fp32
+# evaluations reach max-abs 0.032 (batch 1, 8192 cached), 0.044 (batch 8,
+# ragged, Zipf skew) and 0.031 (batch 2, 131072 cached) over 152,064 x batch
+# logits, relative L2 at most 0.0077; the bound is 1.5x that, rounded up.
+FULL4_FREE_BOUND = (7e-2, 1.2e-2)
 
 # d, F and Hq*D multiples of 64, head_dim 32, group 3: an odd small shape
 ODD = synth.Dims(2, 192, 6, 2, 32, 6, 2, 128, 300)
@@ -54,10 +86,62 @@ ODD = synth.Dims(2, 192, 6, 2, 32, 6, 2, 128, 300)
 SMALL = {"tiny": synth.TINY, "mid": synth.MID, "odd": ODD, "full": synth.FULL}
 
 
+def f64(bits) -> np.ndarray:
+    return to_f32(bits).astype(np.float64)
+
+
+def layer_check(gpu_next, gpu_o, gpu_ids, y) -> Dict[str, float]:
+    """One teacher-forced layer: the GPU's residual entering the next layer
+    and attention output against the oracle's layer evaluation y from the
+    GPU's own input (oracle.Oracle.layer with dumps o, attn, moe)."""
+    g, o = f64(gpu_next), f64(y["h_out"])
+    d = np.abs(g - o)
+    lim = 2.0 * (ulp(o) + ulp(f64(y["attn"])) + ulp(f64(y["moe"]))) + \
+        2.0 ** -16 * np.sqrt(np.mean(o * o))
+    go, oo = f64(gpu_o), f64(y["o"])
+    do = np.abs(go - oo)
+    lim_o = 2.0 * ulp(oo) + 2.0 ** -10 * np.sqrt(np.mean(oo * oo) + 1e-30)
+    clear = y["route_margin"] > TIE_EPS
+    same = np.all(np.sort(gpu_ids, -1) == np.sort(y["route_ids"], -1), -1)
+    return {"h_ratio": float((d / lim).max()), "h_frac": float(np.mean(d > 0)),
+            "h_rel": float(np.linalg.norm(d) / max(np.linalg.norm(o), 1e-30)),
+            "o_ratio": float((do / lim_o).max()), "o_frac": float(np.mean(do > 0)),
+            "route_mismatch": int(y["route_mismatch"]),
+            "route_clear_mismatch": int((clear & ~same).sum())}
+
+
+def layers_ok(s: Dict[str, float]) -> bool:
+    return (s["h_ratio"] <= 1.0 and s["h_frac"] <= TF_FRAC_CHANGED and s["h_rel"] <= TF_REL_L2
+            and s["o_ratio"] <= 1.0 and s["o_frac"] <= TF_FRAC_CHANGED
+            and s["route_mismatch"] == 0 and s["route_clear_mismatch"] == 0)
+
+
+def logit_stats(gl: np.ndarray, ol: np.ndarray) -> Tuple[float, float]:
+    return (float(np.abs(gl - ol).max()),
+            float(np.linalg.norm(gl - ol) / max(np.linalg.norm(ol), 1e-30)))
+
+
+def token_ok(gn, ol, next_tokens, margin) -> bool:
+    ok = True
+    for b in range(len(gn)):
+        if margin[b] > TIE_EPS:
+            ok &= int(gn[b]) == int(next_tokens[b])
+        else:
+            ok &= float(ol[b, gn[b]]) >= float(ol[b].max()) - TIE_EPS
+    return bool(ok)
+
+
 class ParityRun:
+    """One GPU decoder and one exact oracle on the same seeded inputs.
+
+    free_steps: how many of the first steps also run the free-running
+    end-to-end comparison (None: every step).  bound: the free-running logit
+    bound (max-abs, relative L2)."""
+
     def __init__(self, dims="tiny", seq_lens: Optional[Sequence[int]] = None, reserve_steps=9,
                  zipf_s=None, max_batch=None, materialise=None, seed=0, tokens=None,
-                 accum_double=True, noise_floor=True):
+                 free_steps: Optional[int] = None, bound: Tuple[float, float] = STATED_BOUND,
+                 layout_lens: Optional[Sequence[int]] = None):
         import torch
 
         self.torch = torch
@@ -69,36 +153,49 @@ class ParityRun:
         self.dims = dims
         self.seq_lens = list(seq_lens)
         self.B = len(self.seq_lens)
+        self.free_steps = free_steps
+        self.bound = bound
+        self.n_steps = 0
         if materialise is None:
             materialise = synth.weight_bytes_total(dims) < 2e9
-        self.dev = synth.device_inputs(dims, self.seq_lens, reserve_steps, zipf_s, seed)
+        # layout_lens: allocate pages for more sequences than are scheduled
+        # (the spare ones replace finished sequences later)
+        self.dev = synth.device_inputs(dims, list(layout_lens or self.seq_lens), reserve_steps,
+                                       zipf_s, seed)
         pl = self.dev.layout
+        self.page_tables = pl.page_tables[:self.B]
         self.dec = mk.Decoder(dims, self.dev.tensors, pl.num_pages, pl.max_pages,
                               max_batch or self.B, self.dev.bias_tensors)
-        self.dec.build_schedule(self.seq_lens, pl.page_tables)
-        host = synth.host_inputs(dims, pl, seed, materialise=materialise)
-        self.accum_double = accum_double
-        self.orc = oracle.Oracle(dims, host, self.seq_lens, pl.page_tables, self.dev.biases,
-                                 accum_double=accum_double, seed=seed)
-        self.orc32 = (oracle.Oracle(dims, host, self.seq_lens, pl.page_tables, self.dev.biases,
-                                    accum_double=False, seed=seed)
-                      if noise_floor and accum_double else None)
-        self.orc32r = (oracle.Oracle(dims, host, self.seq_lens, pl.page_tables, self.dev.biases,
-                                     accum_double=False, seed=seed, reverse=True)
-                       if noise_floor and accum_double else None)
+        self.dec.build_schedule(self.seq_lens, self.page_tables)
+        self.host = synth.host_inputs(dims, pl, seed, materialise=materialise)
+        self.seed = seed
+        self.orc = oracle.Oracle(dims, self.host, self.seq_lens, self.page_tables,
+                                 self.dev.biases, accum_double=True, seed=seed)
         self.tokens = (np.asarray(tokens, np.int32) if tokens is not None
                        else synth.first_tokens(dims, self.B, seed))
+        self.cur_lens = list(self.seq_lens)
         self.alloc_io(self.B)
 
-    def reset_oracles(self, host, seq_lens, page_tables):
-        """New oracle state(s) for a new batch (continuous batching)."""
-        self.orc = oracle.Oracle(self.dims, host, seq_lens, page_tables, self.dev.biases,
-                                 accum_double=self.accum_double)
-        if self.orc32 is not None:
-            self.orc32 = oracle.Oracle(self.dims, host, seq_lens, page_tables, self.dev.biases,
-                                       accum_double=False)
-            self.orc32r = oracle.Oracle(self.dims, host, seq_lens, page_tables, self.dev.biases,
-                                        accum_double=False, reverse=True)
+    def replace(self, slot: int, new_len: int, page_row, token: int) -> None:
+        """Continuous batching: `slot` gets a new sequence of new_len cached
+        tokens held in the pages of page_row, whose first token is `token`;
+        the library's schedule is rebuilt for the new membership, the
+        oracle's slot is reset, the other sequences continue."""
+        self.cur_lens[slot] = int(new_len)
+        pt = np.array(self.page_tables, copy=True)
+        pt[slot] = page_row
+        self.page_tables = pt
+        self.dec.build_schedule(self.cur_lens, self.page_tables)
+        self.orc.reset_seq(slot, new_len, page_row)
+        self.tokens = np.array(self.tokens, copy=True)
+        self.tokens[slot] = token
+
+    def reset_oracle(self, seq_lens, page_tables):
+        """A new oracle state for a new batch (continuous batching)."""
+        self.orc = oracle.Oracle(self.dims, self.host, seq_lens, page_tables, self.dev.biases,
+                                 accum_double=True, seed=self.seed)
+        self.cur_lens = list(seq_lens)
+        self.page_tables = np.asarray(page_tables, np.int32)
 
     def alloc_io(self, B):
         torch = self.torch
@@ -107,58 +204,79 @@ class ParityRun:
         self.next_d = torch.zeros(B, dtype=torch.int32, device="cuda")
         self.logits_d = torch.zeros(B, self.dims.vocab, dtype=torch.float32, device="cuda")
 
-    def step(self, dumps: bool = False) -> Dict:
+    def step(self) -> Dict:
         torch = self.torch
+        L = self.dims.n_layers
         self.tok_d.copy_(torch.from_numpy(self.tokens))
         self.dec.decode_step(self.tok_d, self.logits_d, self.next_d)
         self.dec.sync()
         gpu_ids, gpu_w = self.dec.routing()
+        gh, go = self.dec.dump_h(), self.dec.dump_o()
         gl = self.logits_d.cpu().numpy()
         gn = self.next_d.cpu().numpy()
-        r = self.orc.step(self.tokens, forced_ids=gpu_ids, tie_eps=TIE_EPS,
-                          dumps=("h",) if dumps else ())
-        ol = r["logits"]
-        rep = {"max_abs": float(np.abs(gl - ol).max()),
-               "rel_l2": float(np.linalg.norm(gl - ol) / max(np.linalg.norm(ol), 1e-30)),
-               "route_mismatch": int(r["route_mismatch"])}
-        rep["bound_max_abs"], rep["bound_rel_l2"] = LOGIT_MAX_ABS, LOGIT_REL_L2
-        if self.orc32 is not None:
-            a = self.orc32.step(self.tokens, forced_ids=gpu_ids, tie_eps=TIE_EPS)["logits"]
-            b = self.orc32r.step(self.tokens, forced_ids=gpu_ids, tie_eps=TIE_EPS)["logits"]
-            nol = max(np.linalg.norm(ol), 1e-30)
-            diffs = (a - ol, b - ol, a - b)
-            rep["noise_max_abs"] = float(max(np.abs(x).max() for x in diffs))
-            rep["noise_rel_l2"] = float(max(np.linalg.norm(x) for x in diffs) / nol)
-            rep["bound_max_abs"] = max(LOGIT_MAX_ABS, NOISE_FACTOR * rep["noise_max_abs"])
-            rep["bound_rel_l2"] = max(LOGIT_REL_L2, NOISE_FACTOR * rep["noise_rel_l2"])
-        clear = r["route_margin"] > TIE_EPS
-        same = np.all(np.sort(gpu_ids, -1) == np.sort(r["route_ids"], -1), axis=-1)
-        rep["route_clear"] = int(clear.sum())
-        rep["route_clear_mismatch"] = int((clear & ~same).sum())
-        rep["route_w_max_err"] = float(np.abs(np.sort(gpu_w, -1) - np.sort(r["route_w"], -1)).max())
-        ok = True
-        for b in range(self.B):
-            if r["argmax_margin"][b] > TIE_EPS:
-                ok &= int(gn[b]) == int(r["next_tokens"][b])
-            else:
-                ok &= float(ol[b, gn[b]]) >= float(ol[b].max()) - TIE_EPS
-        rep["token_ok"] = bool(ok)
+        free = self.free_steps is None or self.n_steps < self.free_steps
+        rep: Dict = {"step": self.n_steps, "free_running": free}
+        # embedding rows: the GPU's h[0] must be the embedding of the tokens
+        emb_ok = np.array_equal(gh[0], np.stack([self._embed_row(t) for t in self.tokens]))
+        # teacher-forced, layer by layer (keeps the K/V rows when the
+        # free-running oracle does not advance the state itself)
+        worst = {"h_ratio": 0.0, "h_frac": 0.0, "h_rel": 0.0, "o_ratio": 0.0, "o_frac": 0.0,
+                 "route_mismatch": 0, "route_clear_mismatch": 0}
+        per_layer = []
+        for l in range(L):
+            y = self.orc.layer(l, gh[l], forced_ids=gpu_ids[l], tie_eps=TIE_EPS, keep=not free,
+                               dumps=("o", "attn", "moe"))
+            s = layer_check(gh[l + 1], go[l], gpu_ids[l], y)
+            per_layer.append(s)
+            for k in worst:
+                worst[k] = max(worst[k], s[k]) if isinstance(worst[k], float) else worst[k] + s[k]
+        hd = self.orc.head(gh[L])
+        rep["tf"] = worst
+        rep["tf_worst_layer"] = int(np.argmax([s["h_ratio"] for s in per_layer]))
+        rep["tf_logits"] = logit_stats(gl, hd["logits"])
+        rep["tf_token_ok"] = token_ok(gn, hd["logits"], hd["next_tokens"], hd["argmax_margin"])
+        rep["embed_ok"] = bool(emb_ok)
+        if free:
+            r = self.orc.step(self.tokens, forced_ids=gpu_ids, tie_eps=TIE_EPS)
+            ol = r["logits"]
+            rep["max_abs"], rep["rel_l2"] = logit_stats(gl, ol)
+            rep["bound_max_abs"], rep["bound_rel_l2"] = self.bound
+            rep["route_mismatch"] = int(r["route_mismatch"])
+            clear = r["route_margin"] > TIE_EPS
+            same = np.all(np.sort(gpu_ids, -1) == np.sort(r["route_ids"], -1), axis=-1)
+            rep["route_clear_mismatch"] = int((clear & ~same).sum())
+            rep["route_w_max_err"] = float(np.abs(np.sort(gpu_w, -1) -
+                                                  np.sort(r["route_w"], -1)).max())
+            rep["token_ok"] = token_ok(gn, ol, r["next_tokens"], r["argmax_margin"])
+            rep["oracle_token"] = r["next_tokens"].tolist()
+        else:
+            self.orc.advance()
         rep["gpu_token"] = gn.tolist()
-        rep["oracle_token"] = r["next_tokens"].tolist()
-        rep["argmax_margin"] = r["argmax_margin"].tolist()
-        if dumps:
-            gh = self.dec.dump_h()
-            rep["h_max_abs"] = [float(np.abs(synth.bf16_bits_to_f32(gh[l]) -
-                                             synth.bf16_bits_to_f32(r["h"][l])).max())
-                                for l in range(gh.shape[0])]
         self.tokens = gn.astype(np.int32)
+        self.cur_lens = [L + 1 for L in self.cur_lens]
+        self.n_steps += 1
         return rep
+
+    def _embed_row(self, tok: int) -> np.ndarray:
+        e = self.host["embed"]
+        if isinstance(e, np.ndarray):
+            return e[int(tok)]
+        d = self.dims.d_model
+        return synth.normal_bf16(self.seed, e.tid, e.sigma, d, int(tok) * d)
+
+    @staticmethod
+    def summary(rep: Dict) -> Dict:
+        return {k: v for k, v in rep.items() if not isinstance(v, list)}
 
     @staticmethod
     def ok(rep: Dict) -> bool:
-        return (rep["route_mismatch"] == 0 and rep["route_clear_mismatch"] == 0
-                and rep["max_abs"] <= rep["bound_max_abs"]
-                and rep["rel_l2"] <= rep["bound_rel_l2"] and rep["token_ok"])
+        good = (rep["embed_ok"] and layers_ok(rep["tf"]) and rep["tf_token_ok"]
+                and rep["tf_logits"][0] <= LOGIT_MAX_ABS and rep["tf_logits"][1] <= LOGIT_REL_L2)
+        if rep["free_running"]:
+            good = good and (rep["route_mismatch"] == 0 and rep["route_clear_mismatch"] == 0
+                             and rep["max_abs"] <= rep["bound_max_abs"]
+                             and rep["rel_l2"] <= rep["bound_rel_l2"] and rep["token_ok"])
+        return bool(good)
 
     def close(self):
         self.dec.close()

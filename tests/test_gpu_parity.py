@@ -2,8 +2,12 @@
 
 Small workloads cover several tiles, ragged tails, every batch bucket of the
 kernel (1, 2, 4, 8 tokens), pages crossed mid-run, an empty cache, an
-automatic schedule rebuild and continuous batching.  The tolerance and the
-routing / greedy-token rules are the parity bar described in harness.py.
+automatic schedule rebuild and continuous batching.  Every step is checked
+layer by layer against the oracle evaluated from the GPU's own residuals
+(teacher-forced) and, end to end, against the free-running oracle at the
+stated logit bound (max-abs 3e-2, relative L2 1e-2) -- except the 8-layer
+mid model, whose free-running bound is derived from the fp32 noise floor
+(harness.MID_FREE_BOUND).  The rules are described in harness.py.
 """
 import numpy as np
 import pytest
@@ -14,11 +18,11 @@ import synth
 pytestmark = pytest.mark.gpu
 
 
-def run_steps(run, n, dumps=False):
+def run_steps(run, n):
     reps = []
     for _ in range(n):
-        rep = run.step(dumps=dumps)
-        print({k: v for k, v in rep.items() if not isinstance(v, list)})
+        rep = run.step()
+        print(run.summary(rep))
         reps.append(rep)
         assert run.ok(rep), rep
     return reps
@@ -37,7 +41,7 @@ def test_generator_device_matches_host():
 
 def test_tiny_one_step_plus_eight_greedy():
     run = harness.ParityRun("tiny")
-    run_steps(run, 9, dumps=True)
+    run_steps(run, 9)
     run.close()
 
 
@@ -61,9 +65,15 @@ def test_empty_cache_and_page_boundaries():
     run.close()
 
 
-def test_mid_workload():
-    run = harness.ParityRun("mid", reserve_steps=4)
-    run_steps(run, 3)
+def test_mid_workload_128_greedy_steps():
+    """The mid model over the workload's 128 greedy steps: every step
+    teacher-forced layer by layer; the first 3 also free-running at the
+    derived bound (beyond them the method's own fp32 drift flips router
+    choices of clear margin, so end-to-end agreement is not defined)."""
+    run = harness.ParityRun("mid", reserve_steps=130, free_steps=3, bound=harness.MID_FREE_BOUND)
+    reps = run_steps(run, 128)
+    worst = max(r["tf"]["h_frac"] for r in reps)
+    print("worst teacher-forced changed fraction over 128 steps:", worst)
     run.close()
 
 
@@ -93,7 +103,7 @@ def test_continuous_batching_rebuild():
         pt[b, :n] = free[at:at + n]
         at += n
     run.dec.build_schedule(new_lens, pt)
-    run.reset_oracles(synth.host_inputs(run.dims, pl), new_lens, pt)
+    run.reset_oracle(new_lens, pt)
     run.tokens = np.array([1, 2, 3], np.int32)
     run.alloc_io(3)
     run_steps(run, 3)

@@ -1,0 +1,85 @@
+"""The parity checker's own discrimination (CPU only).
+
+The teacher-forced layer bound of tests/harness.py must admit a faithful fp32
+evaluation of the method -- the oracle's plain fp32 mode evaluated from the
+same residual as the exact oracle -- and must reject small planted errors:
+one residual element off by a few bf16 ulps, a dropped rounding of the
+attention output, a small systematic bias.  The free-running bound of the
+mid model is checked against the noise of the same faithful evaluations.
+"""
+import numpy as np
+
+import harness
+import oracle
+import synth
+from bf16util import to_bits, to_f32, ulp
+
+
+def _pair(dims, lens, layer):
+    pl = synth.page_layout(dims, lens, 4)
+    host = synth.host_inputs(dims, pl)
+    ex = oracle.Oracle(dims, host, lens, pl.page_tables, accum_double=True)
+    fp = oracle.Oracle(dims, host, lens, pl.page_tables)
+    h = oracle.Oracle(dims, host, lens, pl.page_tables, accum_double=True).step(
+        synth.first_tokens(dims, len(lens)), dumps=("h",))["h"][layer]
+    y = ex.layer(layer, h, dumps=("o", "attn", "moe"))
+    g = fp.layer(layer, h, forced_ids=y["route_ids"], dumps=("o",))
+    return y, g
+
+
+def test_faithful_fp32_layer_passes_and_planted_errors_fail():
+    for dims, lens, layer in ((synth.TINY, [64], 1), (synth.MID, [2048], 3),
+                              (harness.ODD, [29, 3], 1)):
+        y, g = _pair(dims, lens, layer)
+        s = harness.layer_check(g["h_out"], g["o"], g["route_ids"], y)
+        assert harness.layers_ok(s), (dims, s)
+        h = to_f32(g["h_out"]).astype(np.float64)
+        # one element three ulps (of the largest of h, attn, moe) off
+        bad = h.copy()
+        i = np.unravel_index(np.argmax(np.abs(h)), h.shape)
+        big = max(ulp(h[i]), ulp(to_f32(y["attn"])[i]), ulp(to_f32(y["moe"])[i]))
+        bad[i] += 7 * big
+        assert not harness.layers_ok(harness.layer_check(to_bits(bad), g["o"], g["route_ids"], y))
+        # a systematic relative bias of 2^-8 on every element (an operand
+        # off by one rounding everywhere)
+        bias = to_bits(h * (1 + 2.0 ** -7))
+        assert not harness.layers_ok(harness.layer_check(bias, g["o"], g["route_ids"], y))
+        # the attention output not rounded the same way: o off by one ulp in
+        # a tenth of its elements
+        o = to_f32(g["o"]).astype(np.float64)
+        rng = np.random.default_rng(0)
+        flip = rng.random(o.shape) < 0.1
+        o2 = to_bits(np.where(flip, o + ulp(o), o))
+        assert not harness.layers_ok(harness.layer_check(g["h_out"], o2, g["route_ids"], y))
+        # a different expert chosen where the margin is clear
+        ids = g["route_ids"].copy()
+        clear = np.nonzero(y["route_margin"] > harness.TIE_EPS)[0]
+        if clear.size:
+            b = clear[0]
+            ids[b, -1] = next(e for e in range(dims.n_experts) if e not in ids[b])
+            assert not harness.layers_ok(harness.layer_check(g["h_out"], g["o"], ids, y))
+
+
+def test_mid_free_running_bound_sits_above_the_fp32_noise_floor():
+    """Over the first steps of the mid model, faithful fp32 evaluations of
+    the method (the oracle's two summation orders) already deviate from the
+    exact evaluation by more than the stated 3e-2 max-abs -- so a free-running
+    comparison on this model needs the derived bound MID_FREE_BOUND -- and
+    stay well inside that derived bound."""
+    dims, lens = synth.MID, [2048]
+    pl = synth.page_layout(dims, lens, 4)
+    host = synth.host_inputs(dims, pl)
+    ex = oracle.Oracle(dims, host, lens, pl.page_tables, accum_double=True)
+    fw = oracle.Oracle(dims, host, lens, pl.page_tables)
+    rv = oracle.Oracle(dims, host, lens, pl.page_tables, reverse=True)
+    tok = synth.first_tokens(dims, 1)
+    worst = 0.0
+    for _ in range(3):
+        r = ex.step(tok)
+        for o in (fw, rv):
+            a = o.step(tok, forced_ids=r["route_ids"])
+            mx, rel = harness.logit_stats(a["logits"], r["logits"])
+            worst = max(worst, mx)
+            assert mx <= harness.MID_FREE_BOUND[0] / 1.4 and rel <= harness.MID_FREE_BOUND[1] / 1.2
+        tok = r["next_tokens"]
+    assert worst > harness.LOGIT_MAX_ABS

@@ -31,8 +31,8 @@ MUTANTS = {
     "gqa_wrong_head_map": [("const int64_t hk = i / G;", "const int64_t hk = i % Hkv;")],
     "kv_wrong_slot": [("const int64_t slot = j % P;", "const int64_t slot = (j + 1) % P;")],
     "kv_cached_before_rope": [
-        ("      rope(kk.data(), Hkv, D, pos, dm.rope_base);",
-         "      std::vector<float> kpre(kk); rope(kk.data(), Hkv, D, pos, dm.rope_base);"),
+        ("    rope(kk.data(), Hkv, D, pos, dm.rope_base);",
+         "    std::vector<float> kpre(kk); rope(kk.data(), Hkv, D, pos, dm.rope_base);"),
         ("ak.insert(ak.end(), kk.begin(), kk.end());", "ak.insert(ak.end(), kpre.begin(), kpre.end());")],
     "q_not_rounded": [("for (auto &x : q) x = round_bf16(x);", "")],
     "router_no_renormalisation": [("w[t] = p[order[t]] / sum_top;", "w[t] = p[order[t]];")],

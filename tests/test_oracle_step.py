@@ -18,7 +18,7 @@ from scipy.special import softmax
 
 import oracle
 import synth
-from bf16util import rnd, to_bits, to_f32
+from bf16util import rnd, to_bits, to_f32, ulp
 
 TINY = synth.TINY
 
@@ -69,42 +69,47 @@ class BruteForce:
         x1, x2 = x[:, :half], x[:, half:]
         return rnd(np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=1))
 
-    def step(self, tokens):
+    def layer(self, l, b, h):
+        """Layer l for sequence b from the residual h (float64 holding bf16
+        values): appends the new K/V row, returns (next residual, top-k ids)."""
         d = self.d
-        D, Hq, Hkv, E, k, F = d.head_dim, d.n_q_heads, d.n_kv_heads, d.n_experts, d.top_k, d.d_ffn
+        D, Hq, Hkv, E, k = d.head_dim, d.n_q_heads, d.n_kv_heads, d.n_experts, d.top_k
         G = Hq // Hkv
+        p = f"l{l}."
+        n = self.norm(h, self.W(p + "norm"))
+        q = rnd(self.W(p + "wq") @ n).reshape(Hq, D)
+        kk = rnd(self.W(p + "wk") @ n).reshape(Hkv, D)
+        vv = rnd(self.W(p + "wv") @ n).reshape(Hkv, D)
+        pos = self.lens[b]
+        q, kk = self.rope(q, pos), self.rope(kk, pos)
+        self.K[l][b] = np.concatenate([self.K[l][b], kk[None]], 0)
+        self.V[l][b] = np.concatenate([self.V[l][b], vv[None]], 0)
+        o = np.empty((Hq, D))
+        for i in range(Hq):
+            Kh, Vh = self.K[l][b][:, i // G, :], self.V[l][b][:, i // G, :]
+            o[i] = rnd(softmax(Kh @ q[i] / math.sqrt(D)) @ Vh)
+        attn = rnd(self.W(p + "wo") @ o.ravel())
+        r = self.W(p + "wr") @ n
+        r32 = r.astype(np.float32)
+        top = np.lexsort((np.arange(E), -r32.astype(np.float64)))[:k]
+        w = softmax(r32[top].astype(np.float64))
+        acc = np.zeros(d.d_model)
+        wg, wu, wd = self.W(p + "wg"), self.W(p + "wu"), self.W(p + "wd")
+        for e, we in zip(top, w):
+            g, u = rnd(wg[e] @ n), rnd(wu[e] @ n)
+            a = rnd(g / (1 + np.exp(-g)) * u)
+            acc += we * (wd[e] @ a)
+        moe = rnd(acc)
+        return rnd(h + attn + moe), top
+
+    def step(self, tokens):
         emb = self.W("embed")
         logits_all, ids_all = [], []
         for b, tok in enumerate(tokens):
             h = emb[tok].copy()
             ids_b = []
-            for l in range(d.n_layers):
-                p = f"l{l}."
-                n = self.norm(h, self.W(p + "norm"))
-                q = rnd(self.W(p + "wq") @ n).reshape(Hq, D)
-                kk = rnd(self.W(p + "wk") @ n).reshape(Hkv, D)
-                vv = rnd(self.W(p + "wv") @ n).reshape(Hkv, D)
-                pos = self.lens[b]
-                q, kk = self.rope(q, pos), self.rope(kk, pos)
-                self.K[l][b] = np.concatenate([self.K[l][b], kk[None]], 0)
-                self.V[l][b] = np.concatenate([self.V[l][b], vv[None]], 0)
-                o = np.empty((Hq, D))
-                for i in range(Hq):
-                    Kh, Vh = self.K[l][b][:, i // G, :], self.V[l][b][:, i // G, :]
-                    o[i] = rnd(softmax(Kh @ q[i] / math.sqrt(D)) @ Vh)
-                attn = rnd(self.W(p + "wo") @ o.ravel())
-                r = self.W(p + "wr") @ n
-                r32 = r.astype(np.float32)
-                top = np.lexsort((np.arange(E), -r32.astype(np.float64)))[:k]
-                w = softmax(r32[top].astype(np.float64))
-                acc = np.zeros(d.d_model)
-                wg, wu, wd = self.W(p + "wg"), self.W(p + "wu"), self.W(p + "wd")
-                for e, we in zip(top, w):
-                    g, u = rnd(wg[e] @ n), rnd(wu[e] @ n)
-                    a = rnd(g / (1 + np.exp(-g)) * u)
-                    acc += we * (wd[e] @ a)
-                moe = rnd(acc)
-                h = rnd(h + attn + moe)
+            for l in range(self.d.n_layers):
+                h, top = self.layer(l, b, h)
                 ids_b.append(top)
             nf = self.norm(h, self.W("final_norm"))
             logits_all.append(self.W("lm_head") @ nf)
@@ -292,3 +297,82 @@ def test_forced_routing_adoption_rules():
     acc = oracle.Oracle(TINY, t, [64], pl.page_tables).step([17], forced_ids=bad, tie_eps=1e3)
     assert acc["route_mismatch"] == 0
     assert sorted(acc["route_ids"][0, 0].tolist()) == sorted(bad[0, 0].tolist())
+
+
+# ------------------------------------------------------ teacher-forced entry points
+
+
+def test_layer_by_layer_replay_equals_the_step_bit_exact():
+    """orc_layer_step (keeping the K/V rows) over every layer, orc_head and
+    orc_advance reproduce orc_step exactly, over two steps of a ragged batch;
+    a teacher-forced evaluation with keep=False in between changes nothing."""
+    lens = [29, 3]
+    t, pl = tiny_inputs(dims=ODD, seq_lens=lens, reserve=3)
+    ref = oracle.Oracle(ODD, t, lens, pl.page_tables)
+    rep = oracle.Oracle(ODD, t, lens, pl.page_tables)
+    emb = t["embed"]
+    rng = np.random.default_rng(5)
+    tok = [7, 250]
+    for _ in range(2):
+        r = ref.step(tok, dumps=("h", "o"))
+        noise = to_bits(rng.standard_normal((2, ODD.d_model)))
+        for l in range(ODD.n_layers):
+            rep.layer(l, noise, keep=False)  # must leave the state alone
+        h = emb[np.asarray(tok)]
+        for l in range(ODD.n_layers):
+            assert np.array_equal(h, r["h"][l])
+            y = rep.layer(l, h, keep=True, dumps=("o",))
+            assert np.array_equal(y["o"], r["o"][l])
+            assert np.array_equal(y["route_ids"], r["route_ids"][l])
+            h = y["h_out"]
+        assert np.array_equal(h, r["h"][ODD.n_layers])
+        hd = rep.head(h)
+        rep.advance()
+        assert np.array_equal(hd["logits"], r["logits"])
+        assert np.array_equal(hd["next_tokens"], r["next_tokens"])
+        tok = r["next_tokens"]
+
+
+def test_teacher_forced_layer_matches_brute_force_from_a_foreign_residual():
+    """One layer from a residual the model never produced (bf16 ~N(0, 1)),
+    against the float64 brute force's same layer: every output element within
+    one bf16 ulp (the double-sum oracle differs only where a sum lands within
+    rounding of a bf16 tie), routing identical where the margin is clear."""
+    lens = [29, 3]
+    t, pl = tiny_inputs(dims=ODD, seq_lens=lens, reserve=3)
+    orc = oracle.Oracle(ODD, t, lens, pl.page_tables, accum_double=True)
+    bf = BruteForce(ODD, t, lens, pl.page_tables)
+    rng = np.random.default_rng(11)
+    for l in range(ODD.n_layers):
+        h = to_bits(rng.standard_normal((2, ODD.d_model)))
+        y = orc.layer(l, h)
+        for b in range(2):
+            bf_lens = list(bf.lens)
+            hb, top = bf.layer(l, b, to_f32(h[b]).astype(np.float64))
+            bf.K[l][b], bf.V[l][b] = bf.K[l][b][:-1], bf.V[l][b][:-1]  # teacher-forced: no append
+            bf.lens = bf_lens
+            got = to_f32(y["h_out"][b]).astype(np.float64)
+            assert np.all(np.abs(got - hb) <= ulp(hb)), (l, b, np.abs(got - hb).max())
+            if y["route_margin"][b] > 1e-2:
+                assert np.array_equal(np.sort(y["route_ids"][b]), np.sort(top))
+
+
+def test_reset_slot_equals_a_fresh_state_and_leaves_other_slots():
+    """Continuous batching: after two steps, slot 1 gets a new sequence (new
+    length, pages of its own).  Its next step equals a fresh state holding
+    just that sequence; slot 0 continues exactly as if nothing happened."""
+    lens = [29, 3, 40]
+    t, pl = tiny_inputs(dims=ODD, seq_lens=lens, reserve=4)
+    cont = oracle.Oracle(ODD, t, lens[:2], pl.page_tables[:2])
+    ref0 = oracle.Oracle(ODD, t, lens[:1], pl.page_tables[:1])
+    tok = [7, 250]
+    for _ in range(2):
+        r = cont.step(tok)
+        ref0.step(tok[:1])
+        tok = list(r["next_tokens"])
+    cont.reset_seq(1, lens[2], pl.page_tables[2])
+    tok[1] = 123
+    r = cont.step(tok)
+    fresh = oracle.Oracle(ODD, t, [lens[2]], pl.page_tables[2:3]).step([123])
+    assert np.array_equal(r["logits"][1], fresh["logits"][0])
+    assert np.array_equal(r["logits"][0], ref0.step(tok[:1])["logits"][0])
