@@ -352,6 +352,12 @@ class Decoder:
         d = self.dims
         return mk_debug_dump(self.ctx, 2, (d.n_layers, self.batch, d.n_experts), np.float32)
 
+    def dump_qkv(self):
+        d = self.dims
+        return mk_debug_dump(self.ctx, 3, (d.n_layers, self.batch,
+                                           (d.n_q_heads + 2 * d.n_kv_heads) * d.head_dim),
+                             np.uint16)
+
     def stats(self):
         return mk_get_stats(self.ctx)
 

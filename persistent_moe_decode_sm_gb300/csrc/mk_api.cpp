@@ -628,6 +628,12 @@ mk_status mk_debug_dump(mk_ctx *c, int32_t what, void *host_out, uint64_t bytes)
     case 0: row = d.d_model; nl = L + 1; esz = 2; src = (const uint8_t *)c->h; break;
     case 1: row = (size_t)d.n_q_heads * d.head_dim; nl = L; esz = 2; src = (const uint8_t *)c->o; break;
     case 2: row = d.n_experts; nl = L; esz = 4; src = (const uint8_t *)c->router_logits; break;
+    case 3:
+      row = (size_t)(d.n_q_heads + 2 * d.n_kv_heads) * d.head_dim;
+      nl = L;
+      esz = 2;
+      src = (const uint8_t *)c->qkv;
+      break;
     default: return MK_ERR_INVALID_ARG;
   }
   if (bytes != nl * B * row * esz) return MK_ERR_INVALID_ARG;

@@ -12,9 +12,10 @@ library) under the GPU's routing (adopted only at near ties, see below), and
 the GPU's residual entering layer l + 1 must agree with the oracle's within
 bf16 rounding: every element within 2 * (ulp(h) + ulp(attn) + ulp(moe)) of
 the oracle's values (one rounding flip in each of the three roundings that
-make the residual), at most TF_FRAC_CHANGED of the elements changed at all,
-relative L2 at most TF_REL_L2.  The attention output o of every layer is held
-to the same kind of bound, the routing must match wherever the oracle's top-k
+make the residual) plus one bf16 ulp of the typical size of attn and moe, at
+most TF_FRAC_CHANGED of the elements changed at all, relative L2 at most
+TF_REL_L2.  The attention output o of every layer is held to two ulps of
+each element plus one ulp of the row's rms, the routing must match wherever the oracle's top-k
 margin exceeds TIE_EPS, and the logits that the oracle's LM head makes from
 the GPU's final residual must agree with the GPU's logits within the stated
 max-abs / relative-L2 bound.  This comparison is not chaotic: both sides see
@@ -62,8 +63,11 @@ STATED_BOUND = (LOGIT_MAX_ABS, LOGIT_REL_L2)
 # (the oracle's two summation orders) from the same residual differ from the
 # exact one in at most ~1.4 % of the residual's elements, relative L2 <=
 # 2e-4, each element by at most one rounding flip of h, attn or moe
-# (measured on the tiny, mid and full-scale models).
-TF_FRAC_CHANGED = 0.05
+# (measured on the tiny, mid and full-scale models).  The changed fraction
+# is coarse at d = 256 (one flipped attention output moves ~10 residual
+# elements across a rounding boundary); an error present in every element
+# changes about half of them.
+TF_FRAC_CHANGED = 0.10
 TF_REL_L2 = 2e-3
 
 # Free-running bound of the 8-layer mid model.  Faithful fp32 evaluations of
@@ -94,13 +98,22 @@ def layer_check(gpu_next, gpu_o, gpu_ids, y) -> Dict[str, float]:
     """One teacher-forced layer: the GPU's residual entering the next layer
     and attention output against the oracle's layer evaluation y from the
     GPU's own input (oracle.Oracle.layer with dumps o, attn, moe)."""
+    def rms(x):
+        return np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + 1e-60)
+
     g, o = f64(gpu_next), f64(y["h_out"])
+    at, mo = f64(y["attn"]), f64(y["moe"])
     d = np.abs(g - o)
-    lim = 2.0 * (ulp(o) + ulp(f64(y["attn"])) + ulp(f64(y["moe"]))) + \
-        2.0 ** -16 * np.sqrt(np.mean(o * o))
+    # one rounding flip in each of h, attn and moe, twice over, plus one bf16
+    # ulp at the typical size of attn and moe (what an upstream flip moves a
+    # near-zero element by)
+    lim = 2.0 * (ulp(o) + ulp(at) + ulp(mo)) + 2.0 ** -8 * (rms(at) + rms(mo))
     go, oo = f64(gpu_o), f64(y["o"])
     do = np.abs(go - oo)
-    lim_o = 2.0 * ulp(oo) + 2.0 ** -10 * np.sqrt(np.mean(oo * oo) + 1e-30)
+    # two ulps of the element plus one bf16 ulp of its row's rms (a flipped
+    # query element moves every score of the head: near-zero outputs move by
+    # many ulps of their own)
+    lim_o = 2.0 * ulp(oo) + 2.0 ** -8 * rms(oo)
     clear = y["route_margin"] > TIE_EPS
     same = np.all(np.sort(gpu_ids, -1) == np.sort(y["route_ids"], -1), -1)
     return {"h_ratio": float((d / lim).max()), "h_frac": float(np.mean(d > 0)),
@@ -169,6 +182,11 @@ class ParityRun:
         self.dec.build_schedule(self.seq_lens, self.page_tables)
         self.host = synth.host_inputs(dims, pl, seed, materialise=materialise)
         self.seed = seed
+        # two exact oracle states: `tf` follows the GPU (each step replayed
+        # teacher-forced from the GPU's residuals, keeping the K/V rows that
+        # makes), `orc` runs free from the tokens alone
+        self.tf = oracle.Oracle(dims, self.host, self.seq_lens, self.page_tables,
+                                self.dev.biases, accum_double=True, seed=seed)
         self.orc = oracle.Oracle(dims, self.host, self.seq_lens, self.page_tables,
                                  self.dev.biases, accum_double=True, seed=seed)
         self.tokens = (np.asarray(tokens, np.int32) if tokens is not None
@@ -187,6 +205,7 @@ class ParityRun:
         self.page_tables = pt
         self.dec.build_schedule(self.cur_lens, self.page_tables)
         self.orc.reset_seq(slot, new_len, page_row)
+        self.tf.reset_seq(slot, new_len, page_row)
         self.tokens = np.array(self.tokens, copy=True)
         self.tokens[slot] = token
 
@@ -194,6 +213,8 @@ class ParityRun:
         """A new oracle state for a new batch (continuous batching)."""
         self.orc = oracle.Oracle(self.dims, self.host, seq_lens, page_tables, self.dev.biases,
                                  accum_double=True, seed=self.seed)
+        self.tf = oracle.Oracle(self.dims, self.host, seq_lens, page_tables, self.dev.biases,
+                                accum_double=True, seed=self.seed)
         self.cur_lens = list(seq_lens)
         self.page_tables = np.asarray(page_tables, np.int32)
 
@@ -218,20 +239,21 @@ class ParityRun:
         rep: Dict = {"step": self.n_steps, "free_running": free}
         # embedding rows: the GPU's h[0] must be the embedding of the tokens
         emb_ok = np.array_equal(gh[0], np.stack([self._embed_row(t) for t in self.tokens]))
-        # teacher-forced, layer by layer (keeps the K/V rows when the
-        # free-running oracle does not advance the state itself)
+        # teacher-forced, layer by layer
         worst = {"h_ratio": 0.0, "h_frac": 0.0, "h_rel": 0.0, "o_ratio": 0.0, "o_frac": 0.0,
                  "route_mismatch": 0, "route_clear_mismatch": 0}
         per_layer = []
         for l in range(L):
-            y = self.orc.layer(l, gh[l], forced_ids=gpu_ids[l], tie_eps=TIE_EPS, keep=not free,
-                               dumps=("o", "attn", "moe"))
+            y = self.tf.layer(l, gh[l], forced_ids=gpu_ids[l], tie_eps=TIE_EPS, keep=True,
+                              dumps=("o", "attn", "moe"))
             s = layer_check(gh[l + 1], go[l], gpu_ids[l], y)
             per_layer.append(s)
             for k in worst:
                 worst[k] = max(worst[k], s[k]) if isinstance(worst[k], float) else worst[k] + s[k]
-        hd = self.orc.head(gh[L])
+        hd = self.tf.head(gh[L])
+        self.tf.advance()
         rep["tf"] = worst
+        rep["tf_layers_over"] = [(l, s) for l, s in enumerate(per_layer) if not layers_ok(s)][:6]
         rep["tf_worst_layer"] = int(np.argmax([s["h_ratio"] for s in per_layer]))
         rep["tf_logits"] = logit_stats(gl, hd["logits"])
         rep["tf_token_ok"] = token_ok(gn, hd["logits"], hd["next_tokens"], hd["argmax_margin"])
@@ -249,8 +271,6 @@ class ParityRun:
                                                   np.sort(r["route_w"], -1)).max())
             rep["token_ok"] = token_ok(gn, ol, r["next_tokens"], r["argmax_margin"])
             rep["oracle_token"] = r["next_tokens"].tolist()
-        else:
-            self.orc.advance()
         rep["gpu_token"] = gn.tolist()
         self.tokens = gn.astype(np.int32)
         self.cur_lens = [L + 1 for L in self.cur_lens]

@@ -45,10 +45,10 @@ def test_faithful_fp32_layer_passes_and_planted_errors_fail():
         bias = to_bits(h * (1 + 2.0 ** -7))
         assert not harness.layers_ok(harness.layer_check(bias, g["o"], g["route_ids"], y))
         # the attention output not rounded the same way: o off by one ulp in
-        # a tenth of its elements
+        # a quarter of its elements
         o = to_f32(g["o"]).astype(np.float64)
         rng = np.random.default_rng(0)
-        flip = rng.random(o.shape) < 0.1
+        flip = rng.random(o.shape) < 0.25
         o2 = to_bits(np.where(flip, o + ulp(o), o))
         assert not harness.layers_ok(harness.layer_check(g["h_out"], o2, g["route_ids"], y))
         # a different expert chosen where the margin is clear
