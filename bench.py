@@ -239,10 +239,16 @@ def run_mk(args, rank, world):
         from persistent_moe_decode_sm_gb300 import trace as mktrace
 
         mk.mk_set_trace(dec.ctx, dims.n_layers * 16 + 16)
+        mk.mk_set_stage_trace_cta(dec.ctx, args.trace_cta)
         dec.decode_step(tok[0], logits, tok[1])
         tr, stages = mk.mk_get_trace(dec.ctx)
         trace_summary = mktrace.summarize(tr, dims.n_layers)
-        trace_summary["stages_cta0"] = mktrace.stage_summary(stages)
+        trace_summary["stages_cta"] = args.trace_cta
+        trace_summary["stages"] = mktrace.stage_summary(stages)
+        if args.trace_raw:
+            import numpy as np
+
+            np.savez_compressed(args.trace_raw, tasks=tr, stages=stages)
         with open(args.trace, "w") as f:
             json.dump(trace_summary, f, indent=1)
         mk.mk_set_trace(dec.ctx, 0)
@@ -405,6 +411,9 @@ def main():
     ap.add_argument("--batches", default="2,4,8",
                     help="also time these batch sizes at 8192 cached tokens ('' to skip)")
     ap.add_argument("--trace", default="", help="write a per-task trace summary (JSON) here")
+    ap.add_argument("--trace-cta", type=int, default=0,
+                    help="the CTA whose ring stages the trace records")
+    ap.add_argument("--trace-raw", default="", help="also save the raw trace (npz) here")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: cut the model to its first N layers")
     args = ap.parse_args()

@@ -176,7 +176,10 @@ mk_status mk_debug_routing(mk_ctx *ctx, int32_t *ids, float *w);
  * what: 0 = residual h [n_layers+1][batch][d] bf16 (h[0] is the embedding),
  *       1 = attention output o [n_layers][batch][Hq*D] bf16,
  *       2 = router logits [n_layers][batch][E] fp32,
- *       3 = q, k, v before RoPE [n_layers][batch][(Hq + 2 Hkv) D] bf16.
+ *       3 = q, k, v before RoPE [n_layers][batch][(Hq + 2 Hkv) D] bf16,
+ *       4 = the attention term of the residual, attn = bf16(o Wo^T)
+ *           [n_layers][batch][d] bf16,
+ *       5 = the MoE term of the residual [n_layers][batch][d] bf16.
  * bytes must equal the buffer size. */
 mk_status mk_debug_dump(mk_ctx *ctx, int32_t what, void *host_out, uint64_t bytes);
 

@@ -358,6 +358,11 @@ class Decoder:
                                            (d.n_q_heads + 2 * d.n_kv_heads) * d.head_dim),
                              np.uint16)
 
+    def dump_attn_moe(self):
+        d = self.dims
+        shp = (d.n_layers, self.batch, d.d_model)
+        return (mk_debug_dump(self.ctx, 4, shp, np.uint16), mk_debug_dump(self.ctx, 5, shp, np.uint16))
+
     def stats(self):
         return mk_get_stats(self.ctx)
 

@@ -51,7 +51,7 @@ struct mk_ctx {
   /* workspace */
   uint8_t *ws = nullptr;
   size_t ws_bytes = 0;
-  uint16_t *h = nullptr, *qkv = nullptr, *o = nullptr, *act = nullptr;
+  uint16_t *h = nullptr, *qkv = nullptr, *o = nullptr, *act = nullptr, *am = nullptr;
   float *attn_part = nullptr, *attn_part2 = nullptr, *router_logits = nullptr, *lm_part = nullptr,
         *rope = nullptr;
   mk_routing *routing = nullptr;
@@ -276,6 +276,7 @@ mk_status mk_create(const mk_model_dims *dims, const mk_weights *w, void *stream
   const size_t o_h = cv.take((size_t)(L + 1) * MB * d.d_model * 2);
   const size_t o_qkv = cv.take((size_t)L * MB * QKVD * 2);
   const size_t o_o = cv.take((size_t)L * MB * HqD * 2);
+  const size_t o_am = cv.take((size_t)L * 2 * MB * d.d_model * 2);
   const size_t o_part = cv.take((size_t)c->n_slots_max * G * (d.head_dim + 4) * 4);
   const size_t o_part2 = cv.take((size_t)c->n_slots_max * G * (d.head_dim + 4) * 4);
   const size_t o_rl = cv.take((size_t)L * MB * d.n_experts * 4);
@@ -299,6 +300,7 @@ mk_status mk_create(const mk_model_dims *dims, const mk_weights *w, void *stream
   c->h = (uint16_t *)(c->ws + o_h);
   c->qkv = (uint16_t *)(c->ws + o_qkv);
   c->o = (uint16_t *)(c->ws + o_o);
+  c->am = (uint16_t *)(c->ws + o_am);
   c->attn_part = (float *)(c->ws + o_part);
   c->attn_part2 = (float *)(c->ws + o_part2);
   c->router_logits = (float *)(c->ws + o_rl);
@@ -475,6 +477,7 @@ mk_status mk_decode_step(mk_ctx *c, const int32_t *token_ids, float *out_logits,
   p.h = c->h;
   p.qkv = c->qkv;
   p.o = c->o;
+  p.am = c->am;
   p.attn_part = c->attn_part;
   p.attn_part2 = c->attn_part2;
   p.router_logits = c->router_logits;
@@ -634,11 +637,20 @@ mk_status mk_debug_dump(mk_ctx *c, int32_t what, void *host_out, uint64_t bytes)
       esz = 2;
       src = (const uint8_t *)c->qkv;
       break;
+    case 4: row = d.d_model; nl = L; esz = 2; src = (const uint8_t *)c->am; break;
+    case 5:
+      row = d.d_model;
+      nl = L;
+      esz = 2;
+      src = (const uint8_t *)(c->am + (size_t)MK_MAX_BATCH * d.d_model);
+      break;
     default: return MK_ERR_INVALID_ARG;
   }
   if (bytes != nl * B * row * esz) return MK_ERR_INVALID_ARG;
+  /* per layer: [MAXB][row], or [2][MAXB][row] for the attn / moe terms */
+  const size_t lstride = (what >= 4 ? 2 : 1) * (size_t)MK_MAX_BATCH * row * esz;
   for (size_t l = 0; l < nl; ++l)
-    if (cudaMemcpy((uint8_t *)host_out + l * B * row * esz, src + l * MK_MAX_BATCH * row * esz,
+    if (cudaMemcpy((uint8_t *)host_out + l * B * row * esz, src + l * lstride,
                    B * row * esz, cudaMemcpyDeviceToHost) != cudaSuccess)
       return MK_ERR_CUDA;
   return MK_OK;

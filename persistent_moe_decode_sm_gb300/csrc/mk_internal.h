@@ -17,8 +17,9 @@
 /* ---- opcodes ---------------------------------------------------------------- */
 enum {
   OP_HEADER = 100, /* [1] n_layer_tasks, [2] n_final_tasks */
-  OP_QKV = 1,      /* [1] mat (0 q, 1 k, 2 v), [2] row0, [3] nrows */
-  OP_ROUTER = 2,   /* [2] row0 (expert), [3] nrows */
+  OP_QKV = 1,      /* [1] mat (0 q, 1 k, 2 v), [2] row0, [3] nrows (may be 0),
+                      [4] router row0 (expert), [5] router rows (0: none) -- the router
+                      rows stream first and each stage's warp signals its rows at once */
   OP_ATTN = 3,     /* [1] b, [2] kvh, [3] page0, [4] page1 (-1: up to the live length),
                       [5] slot (partial slot), [6] slot0 of (b,kvh), [7] n_splits,
                       [8] is_last (handles and appends the new token),
@@ -38,12 +39,11 @@ enum {
 #define MK_CTR_STRIDE 8 /* int32s per counter */
 enum {
   CTR_QKV_DONE = 0,
-  CTR_ROUTER_TICKET = 1,
-  CTR_ROUTED = 2,
-  CTR_ATTN_DONE = 3,
-  CTR_UP_DONE = 4,
-  CTR_OUT_DONE = 5,
-  CTR_ATTN_TICKET0 = 6 /* + (b * n_kv_heads + kvh) * (1 + MK_MAX_MERGE_GROUPS):
+  CTR_ROUTER_DONE = 1, /* router logits written (counts rows: E per step) */
+  CTR_ATTN_DONE = 2,
+  CTR_UP_DONE = 3,
+  CTR_OUT_DONE = 4,
+  CTR_ATTN_TICKET0 = 5 /* + (b * n_kv_heads + kvh) * (1 + MK_MAX_MERGE_GROUPS):
                           the final merge ticket, then one ticket per merge group */
 };
 /* after the per-layer blocks: */
@@ -77,7 +77,8 @@ static inline int mk_ctrs_per_layer(int max_batch, int n_kv_heads) {
 #define MK_SMEM_STATIC 1024     /* slack to align the ring to 1024 bytes */
 #define MK_SMEM_TASKS 32        /* task descriptors of a CTA kept in shared memory (more: read from global) */
 
-/* Routing result of one layer, written by the last router task. */
+/* Routing result of one layer (for the diagnostics: every CTA takes the
+ * top-k itself; CTA 0 records it here). */
 typedef struct {
   int32_t U;                               /* distinct experts chosen */
   int32_t pad[3];
@@ -121,6 +122,7 @@ typedef struct {
   uint16_t *h;                /* [L+1][MAXB][d]  (h[0] holds the embedding rows for dumps) */
   uint16_t *qkv;              /* [L][MAXB][(Hq+2Hkv)D] pre-RoPE q, k, v */
   uint16_t *o;                /* [L][MAXB][Hq D] */
+  uint16_t *am;               /* [L][2][MAXB][d] the rounded attn and moe terms of the residual */
   float *attn_part;           /* [n_slots][G][D + 4] (m, l, -, -, o[D]), reused by every layer */
   float *attn_part2;          /* [n_slots][G][D + 4] merge-group partials */
   float *router_logits;       /* [L][MAXB][E] */
@@ -138,7 +140,7 @@ typedef struct {
   int32_t tasks_per_cta;
   int32_t n_slots, u_max;
   /* per-step increments of each counter */
-  int32_t n_qkv, n_router, n_up, n_out, n_lm, n_attn_done;
+  int32_t n_qkv, n_router, n_up, n_out, n_lm, n_attn_done; /* n_router: E (rows) */
   int32_t ctrs_per_layer;
   unsigned long long wait_limit_ns;
   int32_t *err_host;          /* host-mapped mirror: [code, cta, task, op, layer, ctr, seen, target] */

@@ -55,6 +55,9 @@
 namespace mk {
 
 constexpr int NC = MK_NC_WARPS;
+/* Batch 1 on the CUDA cores (packed fp32x2 FMAs) or, like batch 2..8, on the
+ * tensor cores (one token in the M rows of m16n8k16). */
+constexpr bool kB1CudaCores = true;
 constexpr int NCT = NC * 32;
 static_assert(NC % MK_NP_WARPS == 0, "each ring slot must have one producer");
 #define NEG_INF (-INFINITY)
@@ -111,6 +114,34 @@ __device__ __forceinline__ int ld_acquire(const int32_t *p) {
 
 __device__ __forceinline__ int ld_volatile(const int32_t *p) {
   return *(const volatile int32_t *)p;
+}
+
+/* A poll of a counter other CTAs update: relaxed, so that the spin does not
+ * order (and slow) anything; the successful poll is followed by one acquire
+ * fence. */
+__device__ __forceinline__ int ld_relaxed(const int32_t *p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void fence_acquire_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
+/* CTA-scope release / acquire on a shared-memory word. */
+__device__ __forceinline__ void st_release_cta(int32_t *p, int v) {
+  asm volatile("st.release.cta.shared.b32 [%0], %1;" ::"r"((uint32_t)__cvta_generic_to_shared(p)),
+               "r"(v)
+               : "memory");
+}
+__device__ __forceinline__ int ld_acquire_cta(const int32_t *p) {
+  int v;
+  asm volatile("ld.acquire.cta.shared.b32 %0, [%1];"
+               : "=r"(v)
+               : "r"((uint32_t)__cvta_generic_to_shared(p))
+               : "memory");
+  return v;
 }
 
 __device__ __forceinline__ void red_release_add(int32_t *p, int v) {
@@ -509,16 +540,22 @@ struct Misc {
   uint64_t empty[NC];
   /* each producer warp's planned stage descriptors (offset independent of NB) */
   QDesc qd[MK_NP_WARPS][MK_QBATCH];
+  /* each producer warp's routing of its current layer: slot -> expert, U */
+  int32_t pexp[MK_NP_WARPS][128];
+  int32_t pU[MK_NP_WARPS];
+  int32_t prouted; /* last layer whose router logits producer warp 0 saw complete */
   int32_t norm_layer; /* layer whose normed input sits in xbuf (-2: none) */
   int32_t ok;         /* 0 once a consumer stopped early */
-  int32_t pad0[2];
+  int32_t route_layer; /* layer whose routing the consumers hold (-1: none) */
+  int32_t route_U;
+  int32_t route_expert[128];        /* slot -> expert id, ascending */
+  float route_w[128][NB];           /* weight of slot u for token b (0: not chosen) */
   float red[NC][MK_MAX_BATCH];
   float rsum[MK_MAX_BATCH];
   float am[NC / 2][8], al[NC / 2][8]; /* attention warp-merge exchange */
   int32_t tasks[MK_SMEM_TASKS][MK_DESC_INTS]; /* this CTA's task-table row */
   union {
     struct {
-      float slot_w[128][NB];
       float hres[MK_MAX_OUT_ROWS][NB];          /* the layer input h at the task's rows */
       float acc_o[MK_MAX_OUT_ROWS][NB];         /* Wo rows (one writer each) */
       float acc_w[NC][MK_MAX_OUT_ROWS][NB];     /* per-warp expert-down sums */
@@ -526,12 +563,6 @@ struct Misc {
     struct {
       float best[NC][MK_MAX_BATCH][2];
     } lm;
-    struct {
-      uint32_t used[4];
-      int32_t ids[MK_MAX_BATCH][MK_MAX_TOPK];
-      float w[MK_MAX_BATCH][MK_MAX_TOPK];
-      int32_t rank_of[128];
-    } rt;
   } u;
 };
 
@@ -592,25 +623,40 @@ __device__ void raise_error(const mk_kparams &p, int code, int cta, int task, in
   atomicExch(&p.ctrl->abort, 1);
 }
 
-/* Waits until (int)(*c - target) >= 0.  Bounded: gives up after the wait
- * limit (recording MK_ERR_DEVICE_TIMEOUT) or as soon as another CTA raised
- * the abort flag.  Returns false then. */
-__device__ bool wait_counter(const Ctx &cx, int32_t *c, int target, int task, int op, int layer,
-                             int ctr_kind) {
+/* Waits until (int)(*c - target) >= 0.  Called by all 32 lanes of a warp
+ * together: lane 0 polls and broadcasts, and every lane sleeps between
+ * polls, so the warp never sits split between a spinning lane and lanes
+ * parked at a convergence point (measured on GB300: a lone lane spinning
+ * that way saw a completed counter ~15 us after other warps did).  Bounded:
+ * gives up after the wait limit (recording MK_ERR_DEVICE_TIMEOUT) or as soon
+ * as another CTA raised the abort flag.  Returns false then (on every lane). */
+__device__ bool wait_counter_warp(const Ctx &cx, int32_t *c, int target, int task, int op,
+                                  int layer, int ctr_kind) {
   const mk_kparams &p = *cx.p;
-  int v = ld_acquire(c);
+  const int lane = threadIdx.x & 31;
+  int v = lane == 0 ? ld_acquire(c) : 0;
+  v = __shfl_sync(0xFFFFFFFFu, v, 0);
   if ((int)(v - target) >= 0) return true;
   const uint64_t t0 = gtimer();
   uint32_t spins = 0;
   while (true) {
-    v = ld_acquire(c);
-    if ((int)(v - target) >= 0) return true;
+    v = lane == 0 ? ld_relaxed(c) : 0;
+    v = __shfl_sync(0xFFFFFFFFu, v, 0);
+    if ((int)(v - target) >= 0) {
+      fence_acquire_gpu();
+      return true;
+    }
     if ((++spins & 31) == 0) {
-      if (ld_volatile(&p.ctrl->abort)) return false;
-      if (gtimer() - t0 > p.wait_limit_ns) {
-        raise_error(p, MK_ERR_DEVICE_TIMEOUT, cx.cta, task, op, layer, ctr_kind, v, target);
-        return false;
+      int stop = 0;
+      if (lane == 0) {
+        if (ld_volatile(&p.ctrl->abort)) {
+          stop = 1;
+        } else if (gtimer() - t0 > p.wait_limit_ns) {
+          raise_error(p, MK_ERR_DEVICE_TIMEOUT, cx.cta, task, op, layer, ctr_kind, v, target);
+          stop = 1;
+        }
       }
+      if (__shfl_sync(0xFFFFFFFFu, stop, 0)) return false;
     }
     __nanosleep(20);
   }
@@ -630,6 +676,126 @@ __device__ bool wait_mbar(const Ctx &cx, uint64_t *bar, uint32_t parity, int tas
     }
   }
   return true;
+}
+
+/* ================================================================ routing
+ * Every warp that needs a layer's routing takes it from the router logits
+ * itself (the router pieces are spread over the grid and signal one
+ * counter), so no CTA computes it for the others and no result has to be
+ * published and polled before the expert weights can be fetched.
+ *
+ * route_warp: one warp, the NT <= 8 tokens' selections interleaved so that
+ * their shuffle chains overlap.  Per token: K rounds of a warp argmax over
+ * the E <= 128 fp32 logits (lane l holds experts l, l + 32, l + 64, l + 96),
+ * ties to the lower expert id; the weights are the softmax over the chosen
+ * logits (the softmax over all E renormalised over the chosen k).  Then the
+ * distinct experts of the batch in ascending id: expert[slot], *U, and --
+ * if slot_w is given -- the weight of each slot for each token (0 where the
+ * token did not choose it).  publish (or NULL): the per-token ids and
+ * weights for the diagnostics. */
+template <int NT>
+__device__ void route_warp(const float *lg, int E, int B, int K, int lane, int32_t *expert,
+                           int32_t *U_out, float (*slot_w)[NT], mk_routing *publish) {
+  float v[NT][4];
+  uint32_t taken[NT];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    taken[t] = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = lane + 32 * i;
+      v[t][i] = (t < B && e < E) ? __ldcg(lg + (size_t)t * E + e) : NEG_INF;
+      if (!(t < B && e < E)) taken[t] |= 1u << i;
+    }
+  }
+  int pick[NT];
+  float pv[NT];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    pick[t] = 0;
+    pv[t] = NEG_INF;
+  }
+  for (int k = 0; k < K; ++k) {
+    float bv[NT];
+    int bi[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      bv[t] = NEG_INF;
+      bi[t] = 0x7FFFFFFF;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (!((taken[t] >> i) & 1u) && (v[t][i] > bv[t] || bi[t] == 0x7FFFFFFF)) {
+          bv[t] = v[t][i];
+          bi[t] = lane + 32 * i;
+        }
+    }
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1)
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv[t], s);
+        const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi[t], s);
+        if (oi != 0x7FFFFFFF && (bi[t] == 0x7FFFFFFF || ov > bv[t] || (ov == bv[t] && oi < bi[t]))) {
+          bv[t] = ov;
+          bi[t] = oi;
+        }
+      }
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      if (lane == k) {
+        pick[t] = bi[t];
+        pv[t] = bv[t];
+      }
+      if ((bi[t] & 31) == lane && bi[t] != 0x7FFFFFFF) taken[t] |= 1u << (bi[t] >> 5);
+    }
+  }
+  /* weights: softmax over the chosen logits; the union of the chosen sets */
+  float w[NT];
+  uint32_t words[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    const float v0 = __shfl_sync(0xFFFFFFFFu, pv[t], 0);
+    const float ex = (lane < K && t < B) ? expf(pv[t] - v0) : 0.0f;
+    float z = ex;
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, s);
+    w[t] = z > 0.0f ? ex / z : 0.0f;
+    if (lane < K && t < B) words[pick[t] >> 5] |= 1u << (pick[t] & 31);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) words[i] = __reduce_or_sync(0xFFFFFFFFu, words[i]);
+  const int U = __popc(words[0]) + __popc(words[1]) + __popc(words[2]) + __popc(words[3]);
+  /* slot of expert e: the chosen experts below it */
+  auto rank = [&](int e) {
+    int r = __popc(words[e >> 5] & ((1u << (e & 31)) - 1u));
+#pragma unroll
+    for (int i = 0; i < 3; ++i) r += (i < (e >> 5)) ? __popc(words[i]) : 0;
+    return r;
+  };
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int e = lane + 32 * i;
+    if ((words[i] >> lane) & 1u) expert[rank(e)] = e;
+  }
+  if (lane == 0) *U_out = U;
+  if (slot_w) {
+    for (int j = lane; j < U * NT; j += 32) slot_w[j / NT][j % NT] = 0.0f;
+    __syncwarp();
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+      if (lane < K && t < B) slot_w[rank(pick[t])][t] = w[t];
+  }
+  if (publish) {
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+      if (lane < K && t < B) {
+        publish->ids[t][lane] = pick[t];
+        publish->w[t][lane] = w[t];
+      }
+    for (int u = lane; u < U; u += 32) publish->expert[u] = expert[u];
+    if (lane == 0) publish->U = U;
+  }
+  __syncwarp();
 }
 
 /* ============================================================== producer
@@ -659,23 +825,65 @@ __device__ bool wait_mbar(const Ctx &cx, uint64_t *bar, uint32_t parity, int tas
  * free.  Issuing a copy costs the issuing thread tens of nanoseconds, which
  * is why there are several producer warps; planning in parallel keeps the
  * issuing thread free of everything else. */
+template <int NB>
 struct Producer {
   Ctx cx;
   uint64_t policy;
   int k, lane;
   QDesc *buf; /* this warp's MK_QBATCH planned descriptors (shared memory) */
+  int32_t *pexp; /* this warp's slot -> expert list (shared memory) */
+  int32_t *pU;
+  int32_t *prouted; /* shared: the last layer whose logits warp 0 saw complete */
+  int r_layer;   /* layer of the routing in pexp (-1: none) */
+  uint64_t t_task, t_plan; /* stage trace: the current task's start, its plan ready */
   int last_slot[NC];
   unsigned long long *strc;
 
-  /* bounded wait for the layer's routing, on lane 0; false on timeout/abort */
-  __device__ bool routed(int layer) const {
+  /* The layer's routing for this warp's expert stages: a bounded wait (lane
+   * 0) for every router piece's logits, then the warp's own top-k.  Only
+   * producer warp 0 polls the global counter (hundreds of pollers on one
+   * line slow every poll and the router pieces' own signals); it passes the
+   * news on through a shared word the other producer warps wait on.
+   * Returns U, or -1 on timeout / abort. */
+  __device__ int routed(int layer) {
+    const mk_kparams &p = *cx.p;
+    if (r_layer == layer) return *(volatile int32_t *)pU;
     int ok = 1;
-    if (lane == 0) {
-      int32_t *c = lctr(*cx.p, layer, CTR_ROUTED);
-      if ((int)(ld_acquire(c) - (int)(cx.epoch + 1)) < 0)
-        ok = wait_counter(cx, c, (int)(cx.epoch + 1), -1, OP_UP, layer, CTR_ROUTED) ? 1 : 0;
+    if (k == 0) { /* the whole warp waits, lane 0 polls */
+      int32_t *c = lctr(p, layer, CTR_ROUTER_DONE);
+      const int target = (int)((cx.epoch + 1) * (uint32_t)p.n_router);
+      ok = wait_counter_warp(cx, c, target, -1, OP_UP, layer, CTR_ROUTER_DONE) ? 1 : 0;
+      if (ok && lane == 0) st_release_cta(prouted, layer);
+    } else {
+      const uint64_t t0 = gtimer();
+      uint32_t spins = 0;
+      while (true) {
+        int seen = lane == 0 ? ld_acquire_cta(prouted) : 0;
+        if (__shfl_sync(0xFFFFFFFFu, seen, 0) >= layer) break;
+        if ((++spins & 31) == 0) {
+          int stop = 0;
+          if (lane == 0) {
+            if (ld_volatile(&p.ctrl->abort)) {
+              stop = 1;
+            } else if (gtimer() - t0 > p.wait_limit_ns) {
+              raise_error(p, MK_ERR_DEVICE_TIMEOUT, cx.cta, -1, OP_UP, layer, CTR_ROUTER_DONE, -1,
+                          layer);
+              stop = 1;
+            }
+          }
+          if (__shfl_sync(0xFFFFFFFFu, stop, 0)) {
+            ok = 0;
+            break;
+          }
+        }
+        __nanosleep(20);
+      }
     }
-    return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+    if (!ok) return -1;
+    route_warp<NB>(p.router_logits + (size_t)layer * MK_MAX_BATCH * p.E, p.E, p.B, p.K, lane,
+                   pexp, pU, nullptr, nullptr);
+    r_layer = layer;
+    return *(volatile int32_t *)pU;
   }
 
   /* issues one planned stage (lane 0); false on a failed wait */
@@ -712,8 +920,8 @@ struct Producer {
     last_slot[slot] = i;
     if (strc && i < MK_STAGE_TRACE_EVENTS - 1) {
       unsigned long long *e = strc + (size_t)i * 8;
-      e[1] = ta;
-      e[2] = ta;
+      e[1] = t_task ? t_task : ta;
+      e[2] = t_plan ? t_plan : ta;
       e[3] = tb;
       e[4] = sclock();
     }
@@ -759,19 +967,28 @@ struct Producer {
         const int32_t *t = row + MK_DESC_INTS * (1 + (layer < p.L ? kt : nl + kt));
         const mk_layer_dev *ly = p.layers + (layer < p.L ? layer : p.L - 1);
         const int op = t[0];
-        if (op == OP_QKV || op == OP_ROUTER || op == OP_LM) {
-          const uint16_t *w = op == OP_LM       ? p.lm_head
-                              : op == OP_ROUTER ? ly->wr
-                              : t[1] == 0       ? ly->wq
-                              : t[1] == 1       ? ly->wk
-                                                : ly->wv;
+        t_task = strc ? sclock() : 0;
+        t_plan = 0;
+        if (op == OP_QKV || op == OP_LM) {
+          /* QKV: the router rows first, then the q / k / v rows */
+          const uint16_t *w = op == OP_LM ? p.lm_head
+                              : t[1] == 0 ? ly->wq
+                              : t[1] == 1 ? ly->wk
+                                          : ly->wv;
           const uint16_t *src = w + (size_t)t[2] * d;
           const int nrows = t[3], rps = mk_rows_per_stage(d, SB);
-          const int n_st = (nrows + rps - 1) / rps;
+          const int rn = op == OP_QKV ? t[5] : 0;
+          const uint16_t *rsrc = ly->wr + (size_t)(op == OP_QKV ? t[4] : 0) * d;
+          const int n_rst = (rn + rps - 1) / rps, n_st = n_rst + (nrows + rps - 1) / rps;
           ok = run_stages(base, 0, n_st, [&](int j, QDesc &q) {
             q.kind = SK_ROWS;
-            q.n = min(rps, nrows - j * rps);
-            q.a = (const uint8_t *)(src + (size_t)j * rps * d);
+            if (j < n_rst) {
+              q.n = min(rps, rn - j * rps);
+              q.a = (const uint8_t *)(rsrc + (size_t)j * rps * d);
+            } else {
+              q.n = min(rps, nrows - (j - n_rst) * rps);
+              q.a = (const uint8_t *)(src + (size_t)(j - n_rst) * rps * d);
+            }
             q.row_bytes = (uint32_t)d * 2;
           });
           base += n_st;
@@ -789,12 +1006,13 @@ struct Producer {
           });
           base += n_st;
         } else if (op == OP_UP) {
-          if (!routed(layer)) {
+          const int U = routed(layer);
+          if (U < 0) {
             ok = false;
             break;
           }
-          const mk_routing *rt = p.routing + layer;
-          const int U = __ldcg(&rt->U), pps = mk_pairs_per_stage(d, SB);
+          t_plan = strc ? sclock() : 0;
+          const int pps = mk_pairs_per_stage(d, SB);
           const int64_t T = (int64_t)U * F;
           const int64_t v = T * t[1] / t[2], v1 = T * (t[1] + 1) / t[2];
           /* stages per expert segment, as the consumers walk them */
@@ -816,7 +1034,7 @@ struct Producer {
             }
             const int f0 = (int)(lo - (int64_t)u * F) + jr * pps;
             const int cnt = min(pps, (int)(hi - (int64_t)u * F) - f0);
-            const int e = __ldcg(&rt->expert[u]);
+            const int e = pexp[u];
             const size_t eo = ((size_t)e * F + f0) * d;
             q.kind = SK_PAIRS;
             q.n = cnt;
@@ -829,12 +1047,12 @@ struct Producer {
           /* the chosen experts' down rows first (their activations are
            * ready before the attention output), then the Wo rows */
           const int r0 = t[2], nr = t[3];
-          if (!routed(layer)) {
+          const int U = routed(layer);
+          if (U < 0) {
             ok = false;
             break;
           }
-          const mk_routing *rt = p.routing + layer;
-          const int U = __ldcg(&rt->U);
+          t_plan = strc ? sclock() : 0;
           const int rps_f = mk_rows_per_stage(F, SB), n_se = (nr + rps_f - 1) / rps_f;
           const int n_dn = U * n_se;
           const int rps_o = mk_rows_per_stage(HqD, SB), n_wo = (nr + rps_o - 1) / rps_o;
@@ -843,7 +1061,7 @@ struct Producer {
             q.kind = SK_ROWS;
             if (j < n_dn) {
               const int u = j / n_se, jj = j % n_se;
-              const int e = __ldcg(&rt->expert[u]);
+              const int e = pexp[u];
               q.n = min(rps_f, nr - jj * rps_f);
               q.a = (const uint8_t *)(ly->wd + ((size_t)e * d + r0 + (size_t)jj * rps_f) * F);
               q.row_bytes = (uint32_t)F * 2;
@@ -877,14 +1095,21 @@ struct Producer {
 
 /* A producer warp's whole life, out of line so that its registers are
  * allocated apart from the consumers', with its state passed by value. */
-__device__ __noinline__ void produce(const Ctx cx, int k, int lane, QDesc *buf,
-                                     unsigned long long *strc, const int32_t *row) {
-  Producer pr;
+template <int NB>
+__device__ __noinline__ void produce(const Ctx cx, int k, int lane, QDesc *buf, int32_t *pexp,
+                                     int32_t *pU, int32_t *prouted, unsigned long long *strc,
+                                     const int32_t *row) {
+  Producer<NB> pr;
   pr.cx = cx;
   pr.policy = evict_first_policy();
   pr.k = k;
   pr.lane = lane;
   pr.buf = buf;
+  pr.pexp = pexp;
+  pr.pU = pU;
+  pr.prouted = prouted;
+  pr.r_layer = -1;
+  pr.t_task = pr.t_plan = 0;
   pr.strc = strc;
   pr.run(row);
 }
@@ -912,13 +1137,13 @@ struct Consumer {
 
   __device__ __forceinline__ Misc<NB> *M() const { return (Misc<NB> *)(mk_smem + cx.misc_off); }
 
-  /* Thread 0 waits on a counter; every consumer learns whether the CTA goes
+  /* Warp 0 waits on a counter; every consumer learns whether the CTA goes
    * on (false also when any warp has failed a stage wait). */
   __device__ bool cwait(int32_t *c, int target, int task, int op, int layer, int kind) {
     bool fail = wfail;
-    if (tid == 0) {
-      fail |= !wait_counter(cx, c, target, task, op, layer, kind);
-      if (tr && !t_ready) t_ready = gtimer();
+    if (warp == 0) {
+      fail |= !wait_counter_warp(cx, c, target, task, op, layer, kind);
+      if (tr && tid == 0 && !t_ready) t_ready = gtimer();
     }
     return !bar_any(fail);
   }
@@ -1016,18 +1241,24 @@ struct Consumer {
     uint16_t *raw = (uint16_t *)cx.xbuf();
     const int n8 = p.d / 8;
     float ss[NB];
+    /* every load of the first pass (all tokens' h and this thread's first
+     * piece of the gain) is issued before any is used: one round trip */
+    const uint4 g_first = tid < n8 ? __ldg((const uint4 *)g + tid) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-    for (int b = 0; b < NB; ++b) {
-      ss[b] = 0.0f;
-      if (b < p.B)
-        for (int i = tid; i < n8; i += NCT) {
-          const uint4 v = __ldcg((const uint4 *)hrows[b] + i);
-          *(uint4 *)(raw + (size_t)b * p.d + 8 * i) = v;
-          float f[8];
-          unpack8(v, f);
+    for (int b = 0; b < NB; ++b) ss[b] = 0.0f;
+    for (int i = tid; i < n8; i += NCT) {
+      uint4 v[NB];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) ss[b] = fmaf(f[k], f[k], ss[b]);
-        }
+      for (int b = 0; b < NB; ++b)
+        v[b] = b < p.B ? __ldcg((const uint4 *)hrows[b] + i) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        *(uint4 *)(raw + (size_t)b * p.d + 8 * i) = v[b];
+        float f[8];
+        unpack8(v[b], f);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) ss[b] = fmaf(f[k], f[k], ss[b]);
+      }
     }
     block_sum(ss);
 #pragma unroll
@@ -1038,7 +1269,7 @@ struct Consumer {
         if (b < p.B) {
           float hf[8], gf[8];
           unpack8(*(const uint4 *)(raw + (size_t)b * p.d + 8 * i), hf);
-          unpack8(__ldg((const uint4 *)g + i), gf);
+          unpack8(i == tid ? g_first : __ldg((const uint4 *)g + i), gf);
 #pragma unroll
           for (int k = 0; k < 8; ++k) o[k] = f2bf(__fmul_rn(__fmul_rn(hf[k], r), gf[k]));
         } else {
@@ -1099,34 +1330,47 @@ struct Consumer {
   /* nrows streamed rows of K elements against the activations x (pitch
    * K + 32); each stage is computed by the warp that owns it and row r
    * (index within the task) handed to epi(r, b, value). */
+  /* The cnt rows of one ring stage (K elements each) against the
+   * activations x (pitch K); row r of the stage handed to epi(r, b, value). */
+  template <class Epi>
+  __device__ __forceinline__ void gemv_stage(const uint8_t *st, int cnt, int K, const uint16_t *x,
+                                             Epi &&epi) {
+    const int pitch = mk_row_pitch(K), xp = mk_x_pitch(K);
+    if (NB == 1 && kB1CudaCores) {
+      cc_rows(st, cnt, pitch, K, x, lane, 0,
+              [&](int n0, float sum, int nr) {
+                if ((lane & 3) == 0 && (lane >> 2) < nr) epi(n0 + (lane >> 2), 0, sum);
+              });
+    } else {
+      mma_rows<NB>(st, cnt, pitch, K, x, xp, lane, [](int v) { return v; },
+                   [&](int n0, const float(&a)[4], const float(&b)[4], bool two) {
+                     take_out<NB>(n0, a, cnt, lane, epi);
+                     if (two) take_out<NB>(n0 + 8, b, cnt, lane, epi);
+                   });
+    }
+  }
+
   template <class Epi>
   __device__ void gemv_rows(int nrows, int K, const uint16_t *x, int task, int op, int layer,
                             Epi &&epi) {
-    const int rps = mk_rows_per_stage(K, cx.SB), pitch = mk_row_pitch(K), xp = mk_x_pitch(K);
+    const int rps = mk_rows_per_stage(K, cx.SB);
     const int n_st = (nrows + rps - 1) / rps;
     for (int j = first_mine(); j < n_st; j += NC) {
       uint8_t *st;
       if (!stage_wait(si + j, st, task, op, layer)) break;
       const int r0 = j * rps, cnt = min(rps, nrows - r0);
-      if (NB == 1) {
-        cc_rows(st, cnt, pitch, K, x, lane, 0,
-                [&](int n0, float sum, int nr) {
-                  if ((lane & 3) == 0 && (lane >> 2) < nr) epi(r0 + n0 + (lane >> 2), 0, sum);
-                });
-      } else {
-        mma_rows<NB>(st, cnt, pitch, K, x, xp, lane, [](int v) { return v; },
-                     [&](int n0, const float(&a)[4], const float(&b)[4], bool two) {
-                       auto f = [&](int r, int bb, float v) { epi(r0 + r, bb, v); };
-                       take_out<NB>(n0, a, cnt, lane, f);
-                       if (two) take_out<NB>(n0 + 8, b, cnt, lane, f);
-                     });
-      }
+      gemv_stage(st, cnt, K, x, [&](int r, int bb, float v) { epi(r0 + r, bb, v); });
       stage_release(si + j);
     }
     si += n_st;
   }
 
-  /* ---------------------------------------------------------------- QKV */
+  /* ---------------------------------------------------------------- QKV
+   * The CTA's router rows (if any) stream first: the warp that computes a
+   * router stage writes its fp32 logits (+ bias) and at once adds its rows
+   * to the layer's router counter (E per step), so the routing every expert
+   * stage waits for does not wait for the q / k / v rows.  Then the q, k or v
+   * rows (bf16 outputs). */
   __device__ bool op_qkv(const int32_t *t, int task, int layer) {
     const mk_kparams &p = *cx.p;
     if (layer > 0 && !cwait(lctr(p, layer - 1, CTR_OUT_DONE), (int)((cx.epoch + 1) * p.n_out),
@@ -1136,130 +1380,66 @@ struct Consumer {
     const int QKVD = (p.Hq + 2 * p.Hkv) * p.D;
     const int base = (t[1] == 0 ? 0 : t[1] == 1 ? p.Hq * p.D : (p.Hq + p.Hkv) * p.D) + t[2];
     uint16_t *out = p.qkv + (size_t)layer * MK_MAX_BATCH * QKVD;
-    const int B = p.B;
-    gemv_rows(t[3], p.d, cx.xn(), task, OP_QKV, layer,
-              [&](int r, int b, float v) {
-                if (b < B) out[(size_t)b * QKVD + base + r] = f2bf(v);
-              });
+    const int B = p.B, E = p.E, d = p.d, e0 = t[4], rn = t[5], nrows = t[3];
+    float *lg = p.router_logits + (size_t)layer * MK_MAX_BATCH * E;
+    const float *bias = p.layers[layer].bias;
+    int32_t *rctr = lctr(p, layer, CTR_ROUTER_DONE);
+    const int rps = mk_rows_per_stage(d, cx.SB);
+    const int n_rst = (rn + rps - 1) / rps, n_st = n_rst + (nrows + rps - 1) / rps;
+    const uint16_t *x = cx.xn();
+    for (int j = first_mine(); j < n_st; j += NC) {
+      uint8_t *st;
+      if (!stage_wait(si + j, st, task, OP_QKV, layer)) break;
+      if (j < n_rst) {
+        const int r0 = j * rps, cnt = min(rps, rn - r0);
+        gemv_stage(st, cnt, d, x, [&](int r, int b, float v) {
+          const int e = e0 + r0 + r;
+          if (b < B) lg[(size_t)b * E + e] = bias ? v + __ldg(bias + e) : v;
+        });
+        stage_release(si + j); /* ends with __syncwarp: the warp's logits are written */
+        if (lane == 0) {
+          __threadfence();
+          red_release_add(rctr, cnt);
+        }
+      } else {
+        const int r0 = (j - n_rst) * rps, cnt = min(rps, nrows - r0);
+        gemv_stage(st, cnt, d, x, [&](int r, int b, float v) {
+          if (b < B) out[(size_t)b * QKVD + base + r0 + r] = f2bf(v);
+        });
+        stage_release(si + j);
+      }
+    }
+    si += n_st;
     if (!task_end()) return false;
     signal(lctr(p, layer, CTR_QKV_DONE));
     return true;
   }
 
-  /* ------------------------------------------------------------- router */
-  __device__ bool op_router(const int32_t *t, int task, int layer) {
+  /* The layer's routing in shared memory (route_expert, route_w, route_U):
+   * once every router piece's logits are written, warp 0 takes the top-k of
+   * every token (route_warp); CTA 0 also records it for the diagnostics.
+   * Called by every consumer thread at the start of a task that needs it
+   * (while the out union is not live).  False on timeout / abort. */
+  __device__ bool route_local(int layer, int task, int op) {
     const mk_kparams &p = *cx.p;
-    if (layer > 0 && !cwait(lctr(p, layer - 1, CTR_OUT_DONE), (int)((cx.epoch + 1) * p.n_out),
-                            task, OP_ROUTER, layer, CTR_OUT_DONE))
+    Misc<NB> *m = M();
+    if (*(volatile int32_t *)&m->route_layer == layer) return true;
+    bar_consumers(); /* everyone has read the tag before it can change */
+    if (!cwait(lctr(p, layer, CTR_ROUTER_DONE), (int)((cx.epoch + 1) * (uint32_t)p.n_router),
+               task, op, layer, CTR_ROUTER_DONE))
       return false;
-    ensure_norm(layer);
-    const int e0 = t[2];
-    float *lg = p.router_logits + (size_t)layer * MK_MAX_BATCH * p.E;
-    const float *bias = p.layers[layer].bias;
-    const int B = p.B, E = p.E;
-    gemv_rows(t[3], p.d, cx.xn(), task, OP_ROUTER, layer,
-              [&](int r, int b, float v) {
-                if (b < B) lg[(size_t)b * E + e0 + r] = bias ? v + __ldg(bias + e0 + r) : v;
-              });
-    if (!task_end()) return false;
-    if (!ticket(lctr(p, layer, CTR_ROUTER_TICKET), p.n_router)) return true;
-    route(layer);
-    bar_consumers();
-    if (tid == 0) {
-      __threadfence();
-      st_release(lctr(p, layer, CTR_ROUTED), (int)(cx.epoch + 1));
-      /* the statistic after the release: off the experts' critical path */
-      auto &R = M()->u.rt;
-      const int U = __popc(R.used[0]) + __popc(R.used[1]) + __popc(R.used[2]) + __popc(R.used[3]);
-      atomicAdd(&p.ctrl->sum_experts, (unsigned long long)U);
+    if (warp == 0) {
+      route_warp<NB>(p.router_logits + (size_t)layer * MK_MAX_BATCH * p.E, p.E, p.B, p.K, lane,
+                     m->route_expert, &m->route_U, m->route_w,
+                     cx.cta == 0 ? p.routing + layer : nullptr);
+      if (lane == 0) {
+        m->route_layer = layer;
+        if (cx.cta == 0) atomicAdd(&p.ctrl->sum_experts, (unsigned long long)m->route_U);
+      }
     }
+    bar_consumers();
     return true;
   }
-
-  /* The last router task: top-k per token (warp b), ties -> lower id;
-   * weights = softmax over the chosen logits (the same as the softmax over
-   * all E renormalised over the chosen k); then the distinct-expert slots in
-   * ascending expert id. */
-  __device__ void route(int layer) {
-    const mk_kparams &p = *cx.p;
-    mk_routing *rt = p.routing + layer;
-    const float *lg = p.router_logits + (size_t)layer * MK_MAX_BATCH * p.E;
-    auto &R = M()->u.rt;
-    if (tid < 4) R.used[tid] = 0;
-    bar_consumers();
-    if (warp < p.B) {
-      const int b = warp;
-      float v[4];
-      int id[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        id[i] = lane + 32 * i;
-        v[i] = id[i] < p.E ? __ldcg(lg + (size_t)b * p.E + id[i]) : NEG_INF;
-        if (id[i] >= p.E) id[i] = 0x40000000;
-      }
-      /* k rounds of a warp argmax; lane k keeps the k-th pick */
-      float my_v = NEG_INF, v0 = 0.0f, z = 0.0f;
-      int my_i = 0;
-      for (int k = 0; k < p.K; ++k) {
-        float bv = NEG_INF;
-        int bi = 0x7FFFFFFF;
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          if (id[i] < 0x40000000 && (v[i] > bv || (v[i] == bv && id[i] < bi))) {
-            bv = v[i];
-            bi = id[i];
-          }
-#pragma unroll
-        for (int s = 16; s >= 1; s >>= 1) {
-          const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, s);
-          const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, s);
-          if (ov > bv || (ov == bv && oi < bi)) {
-            bv = ov;
-            bi = oi;
-          }
-        }
-        if (k == 0) v0 = bv;
-        z += expf(bv - v0);
-        if (lane == k) {
-          my_v = bv;
-          my_i = bi;
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          if (id[i] == bi) id[i] = 0x40000000; /* taken */
-      }
-      if (lane < p.K) {
-        const float w = expf(my_v - v0) / z;
-        R.ids[b][lane] = my_i;
-        R.w[b][lane] = w;
-        rt->ids[b][lane] = my_i;
-        rt->w[b][lane] = w;
-        atomicOr(&R.used[my_i >> 5], 1u << (my_i & 31));
-      }
-    }
-    bar_consumers();
-    /* slots in ascending expert id; every slot's weights start at zero */
-    if (tid < p.E) {
-      const int e = tid;
-      if ((R.used[e >> 5] >> (e & 31)) & 1u) {
-        int rank = __popc(R.used[e >> 5] & ((1u << (e & 31)) - 1u));
-        for (int w = 0; w < (e >> 5); ++w) rank += __popc(R.used[w]);
-        R.rank_of[e] = rank;
-        rt->expert[rank] = e;
-#pragma unroll
-        for (int b = 0; b < MK_MAX_BATCH; ++b) rt->slot_w[rank][b] = 0.0f;
-      }
-    }
-    bar_consumers();
-    /* then each (token, pick) sets its slot's weight */
-    if (tid < p.B * p.K) {
-      const int b = tid / p.K, k = tid % p.K;
-      rt->slot_w[R.rank_of[R.ids[b][k]]][b] = R.w[b][k];
-    }
-    if (tid == 0)
-      rt->U = __popc(R.used[0]) + __popc(R.used[1]) + __popc(R.used[2]) + __popc(R.used[3]);
-  }
-
 
   /* Merges n attention partials (consecutive slots at `parts`; per head
    * [m, l, -, -, o[D]] with o unnormalised): M = max_s m_s, L = sum_s
@@ -1630,11 +1810,9 @@ struct Consumer {
    * 2j + 1 and applies SwiGLU directly. */
   __device__ bool op_up(const int32_t *t, int task, int layer) {
     const mk_kparams &p = *cx.p;
-    if (!cwait(lctr(p, layer, CTR_ROUTED), (int)(cx.epoch + 1), task, OP_UP, layer, CTR_ROUTED))
-      return false;
+    if (!route_local(layer, task, OP_UP)) return false;
     ensure_norm(layer);
-    const mk_routing *rt = p.routing + layer;
-    const int U = __ldcg(&rt->U);
+    const int U = M()->route_U;
     const int d = p.d, F = p.F, B = p.B;
     const int64_t T = (int64_t)U * F;
     int64_t v = T * t[1] / t[2];
@@ -1659,7 +1837,7 @@ struct Consumer {
           }
         };
         auto pairmap = [cnt](int vr) { return (vr & 1) ? cnt + (vr >> 1) : (vr >> 1); };
-        if (NB == 1) {
+        if (NB == 1 && kB1CudaCores) {
           /* virtual row 2j is gate row j, 2j + 1 up row j: lanes 8j'..8j'+3
            * hold the gate sum, the next four lanes the up sum */
           cc_rows(st, 2 * cnt, pitch, d, x, lane, cnt, [&](int n0, float sum, int nr) {
@@ -1706,19 +1884,15 @@ struct Consumer {
     const int target = (int)((cx.epoch + 1) * p.n_attn_done) +
                        (layer == p.poison_layer ? p.poison_delta : 0);
     auto &O = M()->u.out;
-    /* before waiting on the outputs: the residual input rows (final since
-     * the layer began), then -- once the layer's routing is known, which it
-     * normally is by now -- the routing weights */
-    const mk_routing *rt = p.routing + layer;
+    /* the layer's routing (normally known long before), then the residual
+     * input rows (final since the layer began) */
+    if (!route_local(layer, task, OP_OUT)) return false;
+    const int U = M()->route_U;
+    const float(*slot_w)[NB] = M()->route_w;
     for (int i = tid; i < nr * B; i += NCT) {
       const int r = i / B, bb = i % B;
       O.hres[r][bb] = bf2f(__ldcg(h_row(layer, bb) + r0 + r));
     }
-    if (!cwait(lctr(p, layer, CTR_ROUTED), (int)(cx.epoch + 1), task, OP_OUT, layer, CTR_ROUTED))
-      return false;
-    const int U = __ldcg(&rt->U);
-    for (int i = tid; i < U * NB; i += NCT)
-      O.slot_w[i / NB][i % NB] = __ldcg(&rt->slot_w[i / NB][i % NB]);
     uint16_t *x = (uint16_t *)cx.xbuf();
     for (int i = tid; i < NC * MK_MAX_OUT_ROWS * NB; i += NCT) (&O.acc_w[0][0][0])[i] = 0.0f;
     /* the experts' down rows first: their activations are complete once
@@ -1748,15 +1922,15 @@ struct Consumer {
           const int rb0 = jj * rps, cnt = min(rps, nr - rb0);
           auto acc = [&](int r, int bb, float v) {
             float &a = O.acc_w[warp][rb0 + r][bb];
-            a = fmaf(O.slot_w[u][bb], v, a);
+            a = fmaf(slot_w[u][bb], v, a);
           };
-          if (NB == 1) {
+          if (NB == 1 && kB1CudaCores) {
             /* branch-free: every lane updates a valid row's accumulator
              * value, the lane that owns the row stores it */
             cc_rows(st, cnt, pitch, F, xa, lane, 0, [&](int n0, float sum, int nr) {
               const int r = n0 + min(lane >> 2, nr - 1);
               float *a = &O.acc_w[warp][rb0 + r][0];
-              sts32_if(a, fmaf(O.slot_w[u][0], sum, *a), (lane & 3) == 0 && (lane >> 2) < nr);
+              sts32_if(a, fmaf(slot_w[u][0], sum, *a), (lane & 3) == 0 && (lane >> 2) < nr);
             });
           } else {
             mma_rows<NB>(st, cnt, pitch, F, xa, xpf, lane, [](int vr) { return vr; },
@@ -1786,12 +1960,16 @@ struct Consumer {
     for (int i = tid; i < nr * B; i += NCT) {
       const int r = i / B, bb = i % B;
       const float hv = O.hres[r][bb];
-      const float at = rbf(O.acc_o[r][bb]);
+      const uint16_t at = f2bf(O.acc_o[r][bb]);
       float mo = 0.0f;
 #pragma unroll
       for (int w = 0; w < NC; ++w) mo += O.acc_w[w][r][bb];
+      const uint16_t mb = f2bf(mo);
       p.h[((size_t)(layer + 1) * MK_MAX_BATCH + bb) * d + r0 + r] =
-          f2bf(__fadd_rn(__fadd_rn(hv, at), rbf(mo)));
+          f2bf(__fadd_rn(__fadd_rn(hv, bf2f(at)), bf2f(mb)));
+      uint16_t *am = p.am + ((size_t)layer * 2 * MK_MAX_BATCH + bb) * d + r0 + r;
+      am[0] = at;
+      am[(size_t)MK_MAX_BATCH * d] = mb;
       if (layer == 0) p.h[(size_t)bb * d + r0 + r] = f2bf(hv);
     }
     bar_consumers();
@@ -1834,7 +2012,7 @@ struct Consumer {
     /* the lanes holding a token's rows (all 32 for one token on the CUDA
      * cores; lanes 8b..8b+7 on the tensor cores), then the warps */
     auto &LM = M()->u.lm;
-    constexpr int LANES = NB == 1 ? 32 : 8;
+    constexpr int LANES = (NB == 1 && kB1CudaCores) ? 32 : 8;
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
 #pragma unroll
@@ -1896,7 +2074,6 @@ struct Consumer {
     bool ok;
     switch (t[0]) {
       case OP_QKV: ok = op_qkv(t, task, layer); break;
-      case OP_ROUTER: ok = op_router(t, task, layer); break;
       case OP_ATTN:
         ok = cx.p->D == 128 ? op_attn<128>(t, task, layer)
              : cx.p->D == 64 ? op_attn<64>(t, task, layer)
@@ -1960,6 +2137,8 @@ __global__ void __launch_bounds__(MK_THREADS, 1) decode_kernel(const __grid_cons
       mbar_init(&misc->empty[s], 1);
     }
     misc->norm_layer = -2;
+    misc->route_layer = -1;
+    misc->prouted = -1;
     misc->ok = 1;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -1985,8 +2164,9 @@ __global__ void __launch_bounds__(MK_THREADS, 1) decode_kernel(const __grid_cons
   const bool header_ok = row[0] == OP_HEADER;
   if (header_ok) {
     if (warp >= NC) {
-      produce(cx, warp - NC, lane, misc->qd[warp - NC],
-              (int)blockIdx.x == p.stage_trace_cta ? p.stage_trace : nullptr, row);
+      produce<NB>(cx, warp - NC, lane, misc->qd[warp - NC], misc->pexp[warp - NC],
+                  &misc->pU[warp - NC], &misc->prouted,
+                  (int)blockIdx.x == p.stage_trace_cta ? p.stage_trace : nullptr, row);
     } else {
       Consumer<NB> c;
       c.cx = cx;

@@ -145,6 +145,7 @@ extern "C" mk_status mk_decode_step_static(const mk_model_dims *dims, const mk_w
   const size_t o_h = take((size_t)(Lyr + 1) * MB * d.d_model * 2);
   const size_t o_qkv = take((size_t)Lyr * MB * QKVD * 2);
   const size_t o_o = take((size_t)Lyr * MB * HqD * 2);
+  const size_t o_am = take((size_t)Lyr * 2 * MB * d.d_model * 2);
   const size_t o_part = take((size_t)n_slots * G * (d.head_dim + 4) * 4);
   const size_t o_part2 = take((size_t)n_slots * G * (d.head_dim + 4) * 4);
   const size_t o_rl = take((size_t)Lyr * MB * d.n_experts * 4);
@@ -264,6 +265,7 @@ extern "C" mk_status mk_decode_step_static(const mk_model_dims *dims, const mk_w
   p.h = (uint16_t *)(base + o_h);
   p.qkv = (uint16_t *)(base + o_qkv);
   p.o = (uint16_t *)(base + o_o);
+  p.am = (uint16_t *)(base + o_am);
   p.attn_part = (float *)(base + o_part);
   p.attn_part2 = (float *)(base + o_part2);
   p.router_logits = (float *)(base + o_rl);

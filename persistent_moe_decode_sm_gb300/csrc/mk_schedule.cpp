@@ -13,10 +13,9 @@
  * stays small (a few hundred descriptors) for any depth.
  *
  * Per-layer phases, in the order every CTA runs them:
- *   QKV     (the [Wq | Wk | Wv | Wrouter] rows cut into one contiguous
- *   ROUTER   piece per CTA; the router rows of a piece form a ROUTER task,
- *            after the CTA's QKV rows; the last router task to finish runs
- *            the top-k)
+ *   QKV     (the [Wq | Wk | Wv] rows cut per matrix into one contiguous
+ *            piece per CTA, preceded by about E / n_cta router rows; every
+ *            consumer of the routing takes the top-k itself from the logits)
  *   ATTN    (split-K attention: the CTAs are shared out among the
  *            (sequence, kv head) pairs in proportion to their pages, one
  *            split of about equal size per CTA)
@@ -147,91 +146,67 @@ mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int
 
   const int Hq = d.n_q_heads, Hkv = d.n_kv_heads, D = d.head_dim, P = d.page_size;
   std::vector<std::vector<Desc>> lt(n_cta), ft(n_cta);
-  std::vector<std::vector<Desc>> router_t(n_cta), qkv_t(n_cta), attn_t(n_cta), up_t(n_cta),
-      out_t(n_cta);
+  std::vector<std::vector<Desc>> qkv_t(n_cta), attn_t(n_cta), up_t(n_cta), out_t(n_cta);
   MkPlan &p = *out;
   p = MkPlan();
 
-  /* QKV + ROUTER.  With enough CTAs the router rows go to the last n_rc
-   * CTAs alone, sized like a QKV piece: the last of them to finish runs the
-   * top-k, and since those CTAs get no attention split, that serial step
-   * delays no split (and so no attention merge).  The [q | k | v] rows are
-   * cut into equal contiguous pieces over the other CTAs, split again at
-   * matrix boundaries.  With few CTAs the router rows simply continue the
-   * concatenated row space. */
-  int n_rc = 0; /* router-only CTAs (no QKV rows, no attention split) */
+  /* QKV with the router rows.  The [q | k | v] rows are cut per matrix over
+   * all CTAs in proportion to its rows (largest remainder, at least one CTA
+   * each), each CTA one contiguous piece (with fewer CTAs than matrices the
+   * pieces wrap around the grid).  The router rows are spread over the CTAs,
+   * about E / n_cta per CTA, and stream first in the CTA's first QKV task:
+   * the warp that computes a router stage signals its rows at once, so the
+   * logits are complete one norm and one short GEMV after the layer's input
+   * is, while the other warps go on with the QKV rows.  Every consumer of the
+   * routing (producers and consumers of the expert stages alike) then takes
+   * the top-k itself from the logits -- no CTA does it for the others, so no
+   * further hop. */
   {
-    const int64_t rows[4] = {(int64_t)Hq * D, (int64_t)Hkv * D, (int64_t)Hkv * D,
-                             (int64_t)d.n_experts};
+    const int64_t rows[3] = {(int64_t)Hq * D, (int64_t)Hkv * D, (int64_t)Hkv * D};
     const int64_t Rq = rows[0] + rows[1] + rows[2];
-    if (n_cta >= 16) {
-      const double per = (double)(Rq + rows[3]) / n_cta;
-      n_rc = (int)std::max<int64_t>(1, std::min<int64_t>(n_cta / 8, (int64_t)(rows[3] / per + 0.5)));
+    const int E = d.n_experts;
+    int nq = 0;
+    int share[3];
+    double rem[3];
+    int used = 0;
+    for (int m = 0; m < 3; ++m) {
+      const double q = (double)rows[m] * n_cta / (double)Rq;
+      share[m] = std::max(1, (int)q);
+      rem[m] = q - share[m];
+      used += share[m];
     }
-    int nq = 0, nr = 0;
-    auto cut = [&](int64_t R, int c0, int pieces, int m_lo, int m_hi) {
+    while (used < n_cta) {
+      const int m = (int)(std::max_element(rem, rem + 3) - rem);
+      ++share[m];
+      rem[m] -= 1.0;
+      ++used;
+    }
+    int c0 = 0;
+    for (int m = 0; m < 3; ++m) {
+      const int pieces = (int)std::min<int64_t>(share[m], rows[m]);
       for (int c = 0; c < pieces; ++c) {
-        const int64_t a = R * c / pieces, b = R * (c + 1) / pieces;
-        int64_t base = 0;
-        for (int m = 0; m < 4; ++m) {
-          if (m < m_lo || m > m_hi) continue;
-          const int64_t lo = std::max(a, base), hi = std::min(b, base + rows[m]);
-          if (lo < hi) {
-            Desc t = desc(m < 3 ? OP_QKV : OP_ROUTER);
-            t[1] = m;
-            t[2] = (int32_t)(lo - base);
-            t[3] = (int32_t)(hi - lo);
-            if (m < 3) {
-              qkv_t[c0 + c].push_back(t);
-              ++nq;
-            } else {
-              router_t[c0 + c].push_back(t);
-              ++nr;
-            }
-          }
-          base += rows[m];
-        }
+        Desc t = desc(OP_QKV);
+        t[1] = m;
+        t[2] = (int32_t)(rows[m] * c / pieces);
+        t[3] = (int32_t)(rows[m] * (c + 1) / pieces - t[2]);
+        qkv_t[(c0 + c) % n_cta].push_back(t);
+        ++nq;
       }
-    };
-    if (n_rc > 0) {
-      /* CTAs to each of q, k, v in proportion to its rows (largest
-       * remainder, at least one each), each matrix cut evenly: one QKV task
-       * per CTA, none straddling a matrix boundary */
-      const int nq_cta = n_cta - n_rc;
-      int share[3];
-      double rem[3];
-      int used = 0;
-      for (int m = 0; m < 3; ++m) {
-        const double q = (double)rows[m] * nq_cta / (double)Rq;
-        share[m] = std::max(1, (int)q);
-        rem[m] = q - share[m];
-        used += share[m];
+      c0 += share[m];
+    }
+    const int n_rp = std::min(n_cta, E);
+    for (int c = 0; c < n_rp; ++c) {
+      const int cta = (int)((int64_t)c * n_cta / n_rp); /* spread over the grid */
+      if (qkv_t[cta].empty()) {
+        qkv_t[cta].push_back(desc(OP_QKV)); /* a router piece alone */
+        ++nq;
       }
-      while (used < nq_cta) {
-        const int m = (int)(std::max_element(rem, rem + 3) - rem);
-        ++share[m];
-        rem[m] -= 1.0;
-        ++used;
-      }
-      int c0 = 0;
-      for (int m = 0; m < 3; ++m) {
-        const int pieces = (int)std::min<int64_t>(share[m], rows[m]);
-        for (int c = 0; c < pieces; ++c) {
-          Desc t = desc(OP_QKV);
-          t[1] = m;
-          t[2] = (int32_t)(rows[m] * c / pieces);
-          t[3] = (int32_t)(rows[m] * (c + 1) / pieces - t[2]);
-          qkv_t[c0 + c].push_back(t);
-          ++nq;
-        }
-        c0 += share[m];
-      }
-      cut(rows[3], n_cta - n_rc, (int)std::min<int64_t>(n_rc, rows[3]), 3, 3);
-    } else {
-      cut(Rq + rows[3], 0, (int)std::min<int64_t>(n_cta, Rq + rows[3]), 0, 3);
+      Desc &t = qkv_t[cta].front();
+      t[4] = (int32_t)((int64_t)E * c / n_rp);
+      t[5] = (int32_t)((int64_t)E * (c + 1) / n_rp - t[4]);
     }
     p.n_qkv = nq;
-    p.n_router = nr;
+    p.n_router = E;
   }
   /* Roles.  With enough CTAs, attention and the experts run side by side on
    * different SMs, as the pages run them from the same normed input
@@ -242,8 +217,8 @@ mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int
    * bytes, weighted by the attention stage's higher compute per byte, against
    * the expected distinct experts' gate/up bytes.  With few CTAs every CTA
    * does everything. */
-  int n_acta = n_cta - n_rc;
-  if (n_rc > 0) {
+  int n_acta = n_cta;
+  if (n_cta >= 16) {
     double kv = 0.0;
     for (int b = 0; b < batch; ++b) kv += (double)seq_lens[b] * Hkv * D * 2 * 2;
     const double E = d.n_experts, K = d.top_k;
@@ -255,10 +230,10 @@ mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int
      * the attention side */
     constexpr double kAttnCostPerByte = 1.6;
     const double frac = kAttnCostPerByte * kv / std::max(kAttnCostPerByte * kv + up, 1.0);
-    const int lo = std::min(batch * Hkv, n_cta - n_rc - 1), hi = n_cta - n_rc - 1;
+    const int lo = std::min(batch * Hkv, n_cta - 1), hi = n_cta - 1;
     n_acta = std::max(std::max(lo, 1), std::min(hi, (int)std::lround(n_cta * frac)));
   }
-  const bool roles = n_acta < n_cta - n_rc; /* attention CTAs take no expert share */
+  const bool roles = n_acta < n_cta; /* attention CTAs take no expert share */
 
   /* ATTN: split-K over pages. */
   {
@@ -419,7 +394,7 @@ mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int
 
   int width = 0, lmax = 0;
   for (int c = 0; c < n_cta; ++c) {
-    for (auto *v : {&qkv_t[c], &router_t[c], &attn_t[c], &up_t[c], &out_t[c]})
+    for (auto *v : {&qkv_t[c], &attn_t[c], &up_t[c], &out_t[c]})
       lt[c].insert(lt[c].end(), v->begin(), v->end());
     width = std::max<int>(width, 1 + (int)lt[c].size() + (int)ft[c].size());
     lmax = std::max<int>(lmax, (int)lt[c].size());

@@ -94,7 +94,7 @@ def f64(bits) -> np.ndarray:
     return to_f32(bits).astype(np.float64)
 
 
-def layer_check(gpu_next, gpu_o, gpu_ids, y) -> Dict[str, float]:
+def layer_check(gpu_next, gpu_o, gpu_ids, y, gpu_attn=None, gpu_moe=None) -> Dict[str, float]:
     """One teacher-forced layer: the GPU's residual entering the next layer
     and attention output against the oracle's layer evaluation y from the
     GPU's own input (oracle.Oracle.layer with dumps o, attn, moe)."""
@@ -116,7 +116,11 @@ def layer_check(gpu_next, gpu_o, gpu_ids, y) -> Dict[str, float]:
     lim_o = 2.0 * ulp(oo) + 2.0 ** -8 * rms(oo)
     clear = y["route_margin"] > TIE_EPS
     same = np.all(np.sort(gpu_ids, -1) == np.sort(y["route_ids"], -1), -1)
-    return {"h_ratio": float((d / lim).max()), "h_frac": float(np.mean(d > 0)),
+    extra = {}
+    if gpu_attn is not None:
+        extra["attn_frac"] = float(np.mean(gpu_attn != y["attn"]))
+        extra["moe_frac"] = float(np.mean(gpu_moe != y["moe"]))
+    return {**extra, "h_ratio": float((d / lim).max()), "h_frac": float(np.mean(d > 0)),
             "h_rel": float(np.linalg.norm(d) / max(np.linalg.norm(o), 1e-30)),
             "o_ratio": float((do / lim_o).max()), "o_frac": float(np.mean(do > 0)),
             "route_mismatch": int(y["route_mismatch"]),
@@ -233,6 +237,7 @@ class ParityRun:
         self.dec.sync()
         gpu_ids, gpu_w = self.dec.routing()
         gh, go = self.dec.dump_h(), self.dec.dump_o()
+        ga, gm = self.dec.dump_attn_moe()
         gl = self.logits_d.cpu().numpy()
         gn = self.next_d.cpu().numpy()
         free = self.free_steps is None or self.n_steps < self.free_steps
@@ -241,12 +246,12 @@ class ParityRun:
         emb_ok = np.array_equal(gh[0], np.stack([self._embed_row(t) for t in self.tokens]))
         # teacher-forced, layer by layer
         worst = {"h_ratio": 0.0, "h_frac": 0.0, "h_rel": 0.0, "o_ratio": 0.0, "o_frac": 0.0,
-                 "route_mismatch": 0, "route_clear_mismatch": 0}
+                 "attn_frac": 0.0, "moe_frac": 0.0, "route_mismatch": 0, "route_clear_mismatch": 0}
         per_layer = []
         for l in range(L):
             y = self.tf.layer(l, gh[l], forced_ids=gpu_ids[l], tie_eps=TIE_EPS, keep=True,
                               dumps=("o", "attn", "moe"))
-            s = layer_check(gh[l + 1], go[l], gpu_ids[l], y)
+            s = layer_check(gh[l + 1], go[l], gpu_ids[l], y, ga[l], gm[l])
             per_layer.append(s)
             for k in worst:
                 worst[k] = max(worst[k], s[k]) if isinstance(worst[k], float) else worst[k] + s[k]
@@ -286,7 +291,8 @@ class ParityRun:
 
     @staticmethod
     def summary(rep: Dict) -> Dict:
-        return {k: v for k, v in rep.items() if not isinstance(v, list)}
+        return {k: v for k, v in rep.items()
+                if not isinstance(v, list) or (k == "tf_layers_over" and v)}
 
     @staticmethod
     def ok(rep: Dict) -> bool:

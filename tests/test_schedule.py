@@ -13,7 +13,7 @@ import pytest
 import persistent_moe_decode_sm_gb300 as mk
 import synth
 
-OP_QKV, OP_ROUTER, OP_ATTN, OP_UP, OP_OUT, OP_LM, OP_HEADER = 1, 2, 3, 4, 5, 6, 100
+OP_QKV, OP_ATTN, OP_UP, OP_OUT, OP_LM, OP_HEADER = 1, 3, 4, 5, 6, 100
 
 
 def cdims(d, max_batch, max_pages):
@@ -34,8 +34,7 @@ def simulate(d, info, rows, batch, rng):
     """Runs one step's worth of tasks; raises on deadlock."""
     L, Hkv = d.n_layers, d.n_kv_heads
     qkv_done = [0] * L
-    router_ticket = [0] * L
-    routed = [False] * L
+    router_done = [0] * L
     attn_ticket = {}
     group_ticket = {}
     attn_done = [0] * L
@@ -47,25 +46,24 @@ def simulate(d, info, rows, batch, rng):
 
     def ready(l, t):
         op = t[0]
-        if op in (OP_QKV, OP_ROUTER):
+        if op == OP_QKV:
             return l == 0 or out_done[l - 1] == info.n_out
         if op == OP_ATTN:
             return qkv_done[l] == info.n_qkv
-        if op == OP_UP:
-            return routed[l]
+        if op == OP_UP:  # every consumer takes the top-k from the complete logits
+            return router_done[l] == info.n_router
         if op == OP_OUT:
-            return attn_done[l] == batch * Hkv and up_done[l] == info.n_up
+            return (router_done[l] == info.n_router and attn_done[l] == batch * Hkv
+                    and up_done[l] == info.n_up)
         if op == OP_LM:
             return out_done[L - 1] == info.n_out
         raise AssertionError(op)
 
     def run(l, t):
         op = t[0]
-        if op == OP_QKV:
+        if op == OP_QKV:  # its router rows (first in the task), then q / k / v
+            router_done[l] += int(t[5])
             qkv_done[l] += 1
-        elif op == OP_ROUTER:
-            router_ticket[l] += 1
-            routed[l] = router_ticket[l] == info.n_router
         elif op == OP_ATTN:
             # two-level merge: the last split of a group merges the group,
             # the last group merger merges the groups
@@ -97,7 +95,7 @@ def simulate(d, info, rows, batch, rng):
                 progressed = True
         assert progressed, "deadlock: no CTA can run its next task"
     assert all(x == info.n_qkv for x in qkv_done)
-    assert all(routed)
+    assert all(x == info.n_router for x in router_done)
     assert all(x == batch * Hkv for x in attn_done)
     assert all(x == info.n_up for x in up_done)
     assert all(x == info.n_out for x in out_done)
@@ -116,8 +114,8 @@ def check_coverage(d, info, rows, seq_lens):
         assert np.all(cov == 1), mat
     cov = np.zeros(d.n_experts, int)
     for t in lt_all:
-        if t[0] == OP_ROUTER:
-            cov[t[2]:t[2] + t[3]] += 1
+        if t[0] == OP_QKV:
+            cov[t[4]:t[4] + t[5]] += 1
     assert np.all(cov == 1)
     slots = []
     slots2 = []
@@ -173,7 +171,7 @@ def check_coverage(d, info, rows, seq_lens):
 
 
 def phase_rank(t):
-    return {OP_ROUTER: 0, OP_QKV: 0, OP_ATTN: 1, OP_UP: 2, OP_OUT: 3}[int(t[0])]
+    return {OP_QKV: 0, OP_ATTN: 1, OP_UP: 2, OP_OUT: 3}[int(t[0])]
 
 
 CASES = [
@@ -240,15 +238,21 @@ def test_roles_balance_streamed_bytes():
         assert 0.45 < kv / up < 1.1, (lens[:2], kv, up)
 
 
-def test_router_rows_sit_on_ctas_without_attention_splits():
+def test_router_rows_are_spread_and_lead_the_qkv_task():
+    """The router rows are spread over the grid, at most ceil(E / n_cta) per
+    CTA, and ride at the front of the CTA's first QKV task (so the routing
+    every expert stage waits for is complete one norm and one short GEMV
+    after the layer's input); the counter expects E rows per step."""
     d = synth.FULL
-    info, table = mk.mk_plan(cdims(d, 8, 600), 152, 1, [8192])
-    rows = decode(table)
-    router_ctas = {c for c, (lt, _) in enumerate(rows) if any(t[0] == OP_ROUTER for t in lt)}
-    assert 1 <= len(router_ctas) <= 152 // 8
-    for c in router_ctas:
-        ops = {int(t[0]) for t in rows[c][0]}
-        assert OP_ATTN not in ops and OP_QKV not in ops, (c, ops)
+    for n_sm in (152, 148, 16, 7):
+        info, table = mk.mk_plan(cdims(d, 8, 600), n_sm, 1, [8192])
+        rows = decode(table)
+        per = [sum(int(t[5]) for t in lt if t[0] == OP_QKV) for lt, _ in rows]
+        assert sum(per) == d.n_experts and max(per) <= -(-d.n_experts // n_sm)
+        assert info.n_router == d.n_experts
+        for lt, _ in rows:
+            qk = [t for t in lt if t[0] == OP_QKV]
+            assert all(int(t[5]) == 0 for t in qk[1:])
 
 
 def test_out_tasks_fit_the_per_task_row_cap():
