@@ -52,6 +52,9 @@ struct mk_ctx {
   uint8_t *ws = nullptr;
   size_t ws_bytes = 0;
   uint16_t *h = nullptr, *qkv = nullptr, *o = nullptr, *act = nullptr, *am = nullptr;
+  float *moe_part = nullptr;
+  void *wd_maps = nullptr;             /* device [n_layers] tensor maps of the down weights */
+  int fold_rows = 0;
   float *attn_part = nullptr, *attn_part2 = nullptr, *router_logits = nullptr, *lm_part = nullptr,
         *rope = nullptr;
   mk_routing *routing = nullptr;
@@ -189,6 +192,26 @@ mk_status mk_encode_kv_maps(const mk_model_dims *dm, const void *const *k_pools,
   return MK_OK;
 }
 
+mk_status mk_encode_wd_maps(const mk_model_dims *dm, const void *const *w_down, int box_rows,
+                            void *host_out) {
+  const mk_model_dims &d = *dm;
+  EncodeTiledFn enc = tensor_map_encoder();
+  if (!enc) return MK_ERR_CUDA;
+  /* [E * d rows][F columns], row-major; one box = MK_FOLD_COLS columns (128
+   * bytes, swizzled) of box_rows consecutive rows */
+  const cuuint64_t dims[2] = {(cuuint64_t)d.d_ffn, (cuuint64_t)d.n_experts * d.d_model};
+  const cuuint64_t strides[1] = {(cuuint64_t)d.d_ffn * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)MK_FOLD_COLS, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUtensorMap *out = (CUtensorMap *)host_out;
+  for (int l = 0; l < d.n_layers; ++l)
+    if (enc(&out[l], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(w_down[l]), dims,
+            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return MK_ERR_INVALID_ARG;
+  return MK_OK;
+}
+
 extern "C" {
 
 const char *mk_status_string(mk_status s) {
@@ -290,6 +313,9 @@ mk_status mk_create(const mk_model_dims *dims, const mk_weights *w, void *stream
   const size_t o_pt = cv.take((size_t)MB * d.max_pages_per_seq * 4);
   const size_t o_ly = cv.take((size_t)L * sizeof(mk_layer_dev));
   const size_t o_maps = cv.take((size_t)L * 2 * 128);
+  const size_t o_wdm = cv.take((size_t)L * 128);
+  const size_t o_mp =
+      cv.take((size_t)std::min(d.n_experts, d.top_k) * (d.d_ffn / MK_FOLD_COLS) * d.d_model * 4);
   c->ws_bytes = cv.off;
 
   cudaError_t e = cudaMalloc(&c->ws, c->ws_bytes);
@@ -314,14 +340,23 @@ mk_status mk_create(const mk_model_dims *dims, const mk_weights *w, void *stream
   c->page_table_dev = (int32_t *)(c->ws + o_pt);
   c->layers_dev = (mk_layer_dev *)(c->ws + o_ly);
   c->kv_maps = c->ws + o_maps;
-  std::vector<uint8_t> maps((size_t)L * 2 * 128);
+  c->wd_maps = c->ws + o_wdm;
+  c->moe_part = (float *)(c->ws + o_mp);
+  c->fold_rows = mk_fold_rows(&d);
+  std::vector<uint8_t> maps((size_t)L * 2 * 128), wdmaps;
   {
     std::vector<const void *> kp(L), vp(L);
     for (int l = 0; l < L; ++l) {
       kp[l] = w->layers[l].k_cache;
       vp[l] = w->layers[l].v_cache;
     }
-    const mk_status ms = mk_encode_kv_maps(&d, kp.data(), vp.data(), maps.data());
+    mk_status ms = mk_encode_kv_maps(&d, kp.data(), vp.data(), maps.data());
+    if (ms == MK_OK) {
+      std::vector<const void *> wd(L);
+      for (int l = 0; l < L; ++l) wd[l] = w->layers[l].w_down;
+      wdmaps.resize((size_t)L * 128);
+      ms = mk_encode_wd_maps(&d, wd.data(), c->fold_rows, wdmaps.data());
+    }
     if (ms != MK_OK) {
       cudaFree(c->ws);
       delete c;
@@ -351,6 +386,9 @@ mk_status mk_create(const mk_model_dims *dims, const mk_weights *w, void *stream
                         cudaMemcpyHostToDevice, c->stream);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(c->kv_maps, maps.data(), maps.size(), cudaMemcpyHostToDevice, c->stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(c->wd_maps, wdmaps.data(), wdmaps.size(), cudaMemcpyHostToDevice,
+                        c->stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
   if (e == cudaSuccess) e = cudaHostAlloc(&c->err_host, 16 * sizeof(int32_t), cudaHostAllocMapped);
   if (e == cudaSuccess) {
@@ -507,6 +545,10 @@ mk_status mk_decode_step(mk_ctx *c, const int32_t *token_ids, float *out_logits,
   p.kv_maps = c->kv_maps;
   p.xbuf_bytes = (int32_t)sm.xbuf;
   p.xn_bytes = (int32_t)sm.xn;
+  p.fold = c->plan.fold;
+  p.fold_rows = c->fold_rows;
+  p.moe_part = c->moe_part;
+  p.wd_maps = c->wd_maps;
   p.poison_layer = c->poison_layer;
   p.poison_delta = c->poison_delta;
   p.trace = c->trace;

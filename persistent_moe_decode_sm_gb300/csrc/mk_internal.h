@@ -26,7 +26,10 @@ enum {
                       [9] merge group, [10] splits in the group, [11] groups of (b,kvh),
                       [12] first split slot of the group, [13] the group's level-2 slot,
                       [14] first level-2 slot of (b,kvh) */
-  OP_UP = 4,       /* [1] share, [2] n_shares */
+  OP_UP = 4,       /* [1] share, [2] n_shares.  With the down projection folded in
+                      (batch 1), a share is a range of 64-column blocks of the chosen
+                      experts' F: their gate and up rows, then the down matrix's 64
+                      columns of every row of d, giving one partial down vector per block */
   OP_OUT = 5,      /* [2] row0, [3] nrows */
   OP_LM = 6        /* [2] row0, [3] nrows, [4] lm task index */
 };
@@ -63,6 +66,7 @@ static inline int mk_ctrs_per_layer(int max_batch, int n_kv_heads) {
 }
 
 /* ---- limits ----------------------------------------------------------------- */
+#define MK_FOLD_COLS 64  /* f columns per folded block (one 128-byte swizzled box row) */
 #define MK_MAX_BATCH 8
 #define MK_MAX_TOPK 16
 #define MK_MAX_GROUP 8          /* q heads per kv head */
@@ -149,6 +153,10 @@ typedef struct {
   int32_t xbuf_bytes;         /* shared scratch buffer */
   int32_t xn_bytes;           /* shared normed-input buffer (kept across a layer's tasks) */
   int32_t poison_layer, poison_delta; /* test hook: see mk_debug_poison_wait */
+  int32_t fold;               /* 1: each gate/up share also computes its blocks' down partials */
+  int32_t fold_rows;          /* rows of d per down box (the tensor maps' box height) */
+  float *moe_part;            /* [Umax * F / 64][d] partial down vectors of the folded blocks */
+  const void *wd_maps;        /* [L] CUtensorMap of each layer's down weights [E*d][F] */
   unsigned long long *trace;  /* NULL, or [n_cta][trace_cap][MK_TRACE_WORDS] task timestamps */
   int32_t trace_cap;
   unsigned long long *stage_trace; /* NULL, or one CTA's [MK_STAGE_TRACE_EVENTS][8] stage timestamps */

@@ -70,6 +70,33 @@ __device__ __forceinline__ uint32_t saddr(const void *p) {
 
 __device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 
+/* Knuth's TwoSum: s = fl(a + b) and e with s + e == a + b exactly (round to
+ * nearest, no overflow).  The _rn intrinsics keep the compiler from
+ * reassociating. */
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+/* (hi, lo) += x: hi takes the rounded sum, lo collects the errors */
+__device__ __forceinline__ void pair_add(float &hi, float &lo, float x) {
+  float s, e;
+  two_sum(hi, x, s, e);
+  hi = s;
+  lo = __fadd_rn(lo, e);
+}
+
+/* (hi, lo) += (h2, l2), renormalised with Dekker's Fast2Sum so that
+ * hi == fl(hi + lo) */
+__device__ __forceinline__ void pair_merge(float &hi, float &lo, float h2, float l2) {
+  float s, e;
+  two_sum(hi, h2, s, e);
+  e = __fadd_rn(e, __fadd_rn(lo, l2));
+  hi = __fadd_rn(s, e);
+  lo = __fsub_rn(e, __fsub_rn(hi, s));
+}
+
 __device__ __forceinline__ uint16_t f2bf(float f) {
   uint32_t u = __float_as_uint(f);
   if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0x7FC0;
@@ -251,6 +278,16 @@ __device__ __forceinline__ void tensor_g2s_3d(void *dst, const void *tmap, int z
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(saddr(dst)),
       "l"(tmap), "r"(0), "r"(0), "r"(z), "r"(saddr(bar)), "l"(policy)
+      : "memory");
+}
+
+/* 2-D TMA tensor-map box global -> shared at coordinates {x, y}. */
+__device__ __forceinline__ void tensor_g2s_2d(void *dst, const void *tmap, int x, int y,
+                                              uint64_t *bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(saddr(dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(saddr(bar)), "l"(policy)
       : "memory");
 }
 
@@ -519,11 +556,12 @@ __device__ __forceinline__ void cc_rows(const uint8_t *st, int R, int pitch, int
 
 /* ----------------------------------------------------------- shared layout */
 
-enum { SK_ROWS = 0, SK_PAIRS = 1, SK_PAGES = 2 };
+enum { SK_ROWS = 0, SK_PAIRS = 1, SK_PAGES = 2, SK_BOX = 3 };
 
 /* One stage's copies: ROWS n rows of row_bytes at a (one copy); PAIRS n gate
  * rows at a and n up rows at b (two copies); PAGES n pages of one (layer, kv
- * head) (two tensor boxes each). */
+ * head) (two tensor boxes each); BOX one 2-D tensor-map box of row_bytes
+ * bytes, map a, coordinates {pages[0], pages[1]}. */
 struct QDesc {
   const uint8_t *a, *b;
   int32_t kind, n;
@@ -550,7 +588,7 @@ struct Misc {
   int32_t route_U;
   int32_t route_expert[128];        /* slot -> expert id, ascending */
   float route_w[128][NB];           /* weight of slot u for token b (0: not chosen) */
-  float red[NC][MK_MAX_BATCH];
+  float red[NC][MK_MAX_BATCH], red_lo[NC][MK_MAX_BATCH];
   float rsum[MK_MAX_BATCH];
   float am[NC / 2][8], al[NC / 2][8]; /* attention warp-merge exchange */
   int32_t tasks[MK_SMEM_TASKS][MK_DESC_INTS]; /* this CTA's task-table row */
@@ -900,6 +938,9 @@ struct Producer {
       const uint32_t bytes = d.n * d.row_bytes;
       mbar_expect_tx(bar, bytes);
       bulk_g2s(dst, d.a, bytes, bar, policy);
+    } else if (d.kind == SK_BOX) {
+      mbar_expect_tx(bar, d.row_bytes);
+      tensor_g2s_2d(dst, d.a, d.pages[0], d.pages[1], bar, policy);
     } else if (d.kind == SK_PAIRS) {
       const uint32_t bytes = d.n * d.row_bytes;
       mbar_expect_tx(bar, 2 * bytes);
@@ -1005,6 +1046,42 @@ struct Producer {
             for (int jj = 0; jj < cnt; ++jj) q.pages[jj] = __ldg(p.page_table + b * p.max_pages + q0 + jj);
           });
           base += n_st;
+        } else if (op == OP_UP && NB == 1 && p.fold) {
+          /* a range of 64-column blocks of the chosen experts' F: every
+           * block's 64 gate rows and 64 up rows, then its down boxes (the
+           * block's 64 columns of fold_rows rows of d each) */
+          const int U = routed(layer);
+          if (U < 0) {
+            ok = false;
+            break;
+          }
+          t_plan = strc ? sclock() : 0;
+          const int nbf = F / MK_FOLD_COLS, T64 = U * nbf;
+          const int b0 = (int)((int64_t)T64 * t[1] / t[2]);
+          const int b1 = (int)((int64_t)T64 * (t[1] + 1) / t[2]);
+          const int rps = mk_rows_per_stage(d, SB), ng = (MK_FOLD_COLS + rps - 1) / rps;
+          const int BR = p.fold_rows, nrb = d / BR;
+          const int nA = (b1 - b0) * 2 * ng, nB = (b1 - b0) * nrb;
+          ok = run_stages(base, 0, nA + nB, [&](int j, QDesc &q) {
+            if (j < nA) {
+              const int blk = b0 + j / (2 * ng), jj = j % (2 * ng);
+              const int up = jj >= ng, c = up ? jj - ng : jj;
+              const int f0 = (blk % nbf) * MK_FOLD_COLS + c * rps;
+              q.kind = SK_ROWS;
+              q.n = min(rps, MK_FOLD_COLS - c * rps);
+              q.a = (const uint8_t *)((up ? ly->wu : ly->wg) + ((size_t)pexp[blk / nbf] * F + f0) * d);
+              q.row_bytes = (uint32_t)d * 2;
+            } else {
+              const int jb = j - nA, blk = b0 + jb / nrb, rb = jb % nrb;
+              q.kind = SK_BOX;
+              q.n = 1;
+              q.a = (const uint8_t *)p.wd_maps + (size_t)layer * 128;
+              q.pages[0] = (blk % nbf) * MK_FOLD_COLS;
+              q.pages[1] = pexp[blk / nbf] * d + rb * BR;
+              q.row_bytes = (uint32_t)(MK_FOLD_COLS * BR * 2);
+            }
+          });
+          base += nA + nB;
         } else if (op == OP_UP) {
           const int U = routed(layer);
           if (U < 0) {
@@ -1054,7 +1131,7 @@ struct Producer {
           }
           t_plan = strc ? sclock() : 0;
           const int rps_f = mk_rows_per_stage(F, SB), n_se = (nr + rps_f - 1) / rps_f;
-          const int n_dn = U * n_se;
+          const int n_dn = (NB == 1 && p.fold) ? 0 : U * n_se; /* folded: in the gate/up shares */
           const int rps_o = mk_rows_per_stage(HqD, SB), n_wo = (nr + rps_o - 1) / rps_o;
           const uint16_t *wo = ly->wo + (size_t)r0 * HqD;
           ok = run_stages(base, 0, n_dn + n_wo, [&](int j, QDesc &q) {
@@ -1211,19 +1288,25 @@ struct Consumer {
     return p.h + ((size_t)layer * MK_MAX_BATCH + b) * p.d;
   }
 
-  __device__ void block_sum(float (&v)[NB]) {
+  /* The block-wide sum of every thread's (hi, lo) pair per token, exact up
+   * to the pairs' own rounding; v[b] = the sum rounded once to fp32. */
+  __device__ void block_sum_pair(float (&hi)[NB], float (&lo)[NB], float (&v)[NB]) {
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
-      float s = v[b];
+      float h = hi[b], l = lo[b];
 #pragma unroll
-      for (int k = 16; k >= 1; k >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, k);
-      if (lane == 0) M()->red[warp][b] = s;
+      for (int k = 16; k >= 1; k >>= 1)
+        pair_merge(h, l, __shfl_xor_sync(0xFFFFFFFFu, h, k), __shfl_xor_sync(0xFFFFFFFFu, l, k));
+      if (lane == 0) {
+        M()->red[warp][b] = h;
+        M()->red_lo[warp][b] = l;
+      }
     }
     bar_consumers();
     if (tid < NB) {
-      float s = 0.0f;
-      for (int w = 0; w < NC; ++w) s += M()->red[w][tid];
-      M()->rsum[tid] = s;
+      float h = 0.0f, l = 0.0f;
+      for (int w = 0; w < NC; ++w) pair_merge(h, l, M()->red[w][tid], M()->red_lo[w][tid]);
+      M()->rsum[tid] = __fadd_rn(h, l);
     }
     bar_consumers();
 #pragma unroll
@@ -1233,19 +1316,23 @@ struct Consumer {
 
   /* xn[b][0..d) = bf16((h * (1/sqrtf(mean_fp32(h^2) + eps))) * g); rows
    * b >= B zero.  h is read once with 16-byte loads and staged in the
-   * scratch buffer. */
+   * scratch buffer.  The sum of squares is carried as an unevaluated pair of
+   * floats (each square of a bf16 value is exact in fp32, and TwoSum keeps
+   * every addition's error), so the fp32 mean is the exact sum rounded once:
+   * the same fp32 value in any summation order, hence the same normed input
+   * as any other evaluation that rounds the exact mean once. */
   __device__ void norm_into_xbuf(int layer_tag, const uint16_t *const *hrows, const uint16_t *g) {
     const mk_kparams &p = *cx.p;
     const int xp = mk_x_pitch(p.d);
     uint16_t *x = cx.xn();
     uint16_t *raw = (uint16_t *)cx.xbuf();
     const int n8 = p.d / 8;
-    float ss[NB];
+    float ss[NB], sh[NB], sl[NB];
     /* every load of the first pass (all tokens' h and this thread's first
      * piece of the gain) is issued before any is used: one round trip */
     const uint4 g_first = tid < n8 ? __ldg((const uint4 *)g + tid) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-    for (int b = 0; b < NB; ++b) ss[b] = 0.0f;
+    for (int b = 0; b < NB; ++b) sh[b] = sl[b] = 0.0f;
     for (int i = tid; i < n8; i += NCT) {
       uint4 v[NB];
 #pragma unroll
@@ -1257,10 +1344,10 @@ struct Consumer {
         float f[8];
         unpack8(v[b], f);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) ss[b] = fmaf(f[k], f[k], ss[b]);
+        for (int k = 0; k < 8; ++k) pair_add(sh[b], sl[b], __fmul_rn(f[k], f[k]));
       }
     }
-    block_sum(ss);
+    block_sum_pair(sh, sl, ss);
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
       const float r = 1.0f / sqrtf(ss[b] / (float)p.d + p.eps);
@@ -1808,8 +1895,87 @@ struct Consumer {
    * A share of the (expert slot, ffn index) pairs; each stage holds gate and
    * up rows interleaved, so the thread holding gate row 2j also holds up row
    * 2j + 1 and applies SwiGLU directly. */
+  /* Batch 1 with the down projection folded in: the share's blocks of 64
+   * f-columns.  First every block's gate and up rows (g and u rounded to
+   * bf16, kept in the scratch buffer), then a = bf16(silu(g) u), then the
+   * block's down boxes: rows r of the down matrix against a over the block's
+   * 64 columns, the partial written to moe_part[block][r] for the OUT tasks,
+   * which weight and add the blocks in order. */
+  __device__ bool op_up_fold(const int32_t *t, int task, int layer) {
+    const mk_kparams &p = *cx.p;
+    if (!route_local(layer, task, OP_UP)) return false;
+    ensure_norm(layer);
+    const int U = M()->route_U, d = p.d;
+    const int nbf = p.F / MK_FOLD_COLS, T64 = U * nbf;
+    const int b0 = (int)((int64_t)T64 * t[1] / t[2]);
+    const int b1 = (int)((int64_t)T64 * (t[1] + 1) / t[2]);
+    const int rps = mk_rows_per_stage(d, cx.SB), ng = (MK_FOLD_COLS + rps - 1) / rps;
+    const int BR = p.fold_rows, nrb = d / BR;
+    const int nA = (b1 - b0) * 2 * ng, nB = (b1 - b0) * nrb;
+    float *gsm = (float *)cx.xbuf();
+    float *usm = gsm + (b1 - b0) * MK_FOLD_COLS;
+    const uint16_t *x = cx.xn();
+    const int pitch = mk_row_pitch(d);
+    for (int j = first_mine(); j < nA; j += NC) {
+      uint8_t *st;
+      if (!stage_wait(si + j, st, task, OP_UP, layer)) break;
+      const int kb = j / (2 * ng), jj = j % (2 * ng), up = jj >= ng, c = up ? jj - ng : jj;
+      float *dst = (up ? usm : gsm) + kb * MK_FOLD_COLS + c * rps;
+      cc_rows(st, min(rps, MK_FOLD_COLS - c * rps), pitch, d, x, lane, 0,
+              [&](int n0, float sum, int nr) {
+                if ((lane & 3) == 0 && (lane >> 2) < nr) dst[n0 + (lane >> 2)] = rbf(sum);
+              });
+      stage_release(si + j);
+    }
+    if (!task_end()) return false; /* every g and u of the share is in */
+    for (int i = tid; i < (b1 - b0) * MK_FOLD_COLS; i += NCT) {
+      const float g = gsm[i];
+      gsm[i] = rbf((g / (1.0f + expf(-g))) * usm[i]);
+    }
+    bar_consumers();
+    const int sB = si + nA;
+    for (int jb = (warp - sB % NC + NC) % NC; jb < nB; jb += NC) {
+      uint8_t *st;
+      if (!stage_wait(sB + jb, st, task, OP_UP, layer)) break;
+      const int kb = jb / nrb, r0 = (jb % nrb) * BR;
+      /* the block's 64 activations as fp32 pairs, the same on every lane */
+      unsigned long long a2[MK_FOLD_COLS / 2];
+      const float4 *a4 = (const float4 *)(gsm + kb * MK_FOLD_COLS);
+#pragma unroll
+      for (int i = 0; i < MK_FOLD_COLS / 4; ++i) {
+        const float4 v = a4[i];
+        a2[2 * i] = pack2(__float_as_uint(v.x), __float_as_uint(v.y));
+        a2[2 * i + 1] = pack2(__float_as_uint(v.z), __float_as_uint(v.w));
+      }
+      /* box row r: 128 bytes, 16-byte chunk c stored at (c ^ (r & 7)) */
+      const uint32_t sb = saddr(st);
+      float *part = p.moe_part + (size_t)(b0 + kb) * d + r0;
+      for (int r = lane; r < BR; r += 32) {
+        unsigned long long acc0 = 0ULL, acc1 = 0ULL;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          uint4 w;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                       : "r"(sb + (uint32_t)(r * 128 + ((ch ^ (r & 7)) << 4))));
+          acc0 = ffma2(bf2_f2(w.x), a2[4 * ch], acc0);
+          acc1 = ffma2(bf2_f2(w.y), a2[4 * ch + 1], acc1);
+          acc0 = ffma2(bf2_f2(w.z), a2[4 * ch + 2], acc0);
+          acc1 = ffma2(bf2_f2(w.w), a2[4 * ch + 3], acc1);
+        }
+        part[r] = sum2(acc0) + sum2(acc1);
+      }
+      stage_release(sB + jb);
+    }
+    si += nA + nB;
+    if (!task_end()) return false;
+    signal(lctr(p, layer, CTR_UP_DONE));
+    return true;
+  }
+
   __device__ bool op_up(const int32_t *t, int task, int layer) {
     const mk_kparams &p = *cx.p;
+    if (NB == 1 && p.fold) return op_up_fold(t, task, layer);
     if (!route_local(layer, task, OP_UP)) return false;
     ensure_norm(layer);
     const int U = M()->route_U;
@@ -1904,8 +2070,9 @@ struct Consumer {
     const int xpf = mk_x_pitch(F), per = NB * xpf;
     const int fit = max(1, (int)min((int64_t)U, (int64_t)p.xbuf_bytes / ((int64_t)2 * per)));
     const int rps = mk_rows_per_stage(F, cx.SB), pitch = mk_row_pitch(F);
-    const int n_se = (nr + rps - 1) / rps; /* stages per expert */
-    for (int u0 = 0; u0 < U; u0 += fit) {
+    const bool fold = NB == 1 && p.fold; /* down rows done by the gate/up shares */
+    const int n_se = fold ? 0 : (nr + rps - 1) / rps; /* stages per expert */
+    for (int u0 = 0; u0 < (fold ? 0 : U); u0 += fit) {
       const int u1 = min(U, u0 + fit);
       if (u0 > 0) bar_consumers(); /* the previous experts' activations are consumed */
       for (int u = u0; u < u1; ++u)
@@ -1957,13 +2124,27 @@ struct Consumer {
     bar_consumers();
     gemv_rows(nr, HqD, xo, task, OP_OUT, layer, [&](int r, int bb, float v) { O.acc_o[r][bb] = v; });
     if (!task_end()) return false;
+    /* folded: every block's partial of this task's rows, staged in the
+     * scratch buffer (free again: Wo is done), added in block order */
+    const int T64 = U * (F / MK_FOLD_COLS);
+    float *ps = (float *)cx.xbuf();
+    if (fold) {
+      for (int i = tid; i < T64 * nr; i += NCT)
+        ps[i] = __ldcg(p.moe_part + (size_t)(i / nr) * d + r0 + i % nr);
+      bar_consumers();
+    }
     for (int i = tid; i < nr * B; i += NCT) {
       const int r = i / B, bb = i % B;
       const float hv = O.hres[r][bb];
       const uint16_t at = f2bf(O.acc_o[r][bb]);
       float mo = 0.0f;
+      if (fold) {
+        for (int blk = 0; blk < T64; ++blk)
+          mo = fmaf(slot_w[blk / (F / MK_FOLD_COLS)][0], ps[blk * nr + r], mo);
+      } else {
 #pragma unroll
-      for (int w = 0; w < NC; ++w) mo += O.acc_w[w][r][bb];
+        for (int w = 0; w < NC; ++w) mo += O.acc_w[w][r][bb];
+      }
       const uint16_t mb = f2bf(mo);
       p.h[((size_t)(layer + 1) * MK_MAX_BATCH + bb) * d + r0 + r] =
           f2bf(__fadd_rn(__fadd_rn(hv, bf2f(at)), bf2f(mb)));

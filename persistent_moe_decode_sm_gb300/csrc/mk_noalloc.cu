@@ -160,6 +160,9 @@ extern "C" mk_status mk_decode_step_static(const mk_model_dims *dims, const mk_w
   const size_t o_ly = take((size_t)Lyr * sizeof(mk_layer_dev));
   const size_t o_tab = take(plan.table.size() * sizeof(int32_t));
   const size_t o_maps = take((size_t)Lyr * 2 * 128);
+  const size_t o_wdm = take((size_t)Lyr * 128);
+  const size_t o_mp =
+      take((size_t)std::min(d.n_experts, d.top_k) * (d.d_ffn / MK_FOLD_COLS) * d.d_model * 4);
   if (off > MK_STATIC_SCRATCH_BYTES) return MK_ERR_SCRATCH_LIMIT;
 
   /* ---- shared memory plan (as for mk_decode_step) ---- */
@@ -206,6 +209,14 @@ extern "C" mk_status mk_decode_step_static(const mk_model_dims *dims, const mk_w
     st = mk_encode_kv_maps(dims, kp.data(), vp.data(), maps.data());
     if (st != MK_OK) return st;
   }
+  const int fold_rows = mk_fold_rows(dims);
+  std::vector<uint8_t> wdmaps((size_t)Lyr * 128);
+  {
+    std::vector<const void *> wd(Lyr);
+    for (int l = 0; l < Lyr; ++l) wd[l] = w->layers[l].w_down;
+    st = mk_encode_wd_maps(dims, wd.data(), fold_rows, wdmaps.data());
+    if (st != MK_OK) return st;
+  }
   std::vector<int32_t> lens(MB, 0), pt((size_t)MB * mp, -1);
   std::copy(seq_lens, seq_lens + batch, lens.begin());
   std::memcpy(pt.data(), page_tables, (size_t)batch * mp * sizeof(int32_t));
@@ -227,6 +238,9 @@ extern "C" mk_status mk_decode_step_static(const mk_model_dims *dims, const mk_w
                         cudaMemcpyHostToDevice, stream);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(base + o_maps, maps.data(), maps.size(), cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(base + o_wdm, wdmaps.data(), wdmaps.size(), cudaMemcpyHostToDevice,
+                        stream);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(base + o_len, lens.data(), MB * 4, cudaMemcpyHostToDevice, stream);
   if (e == cudaSuccess)
@@ -296,6 +310,10 @@ extern "C" mk_status mk_decode_step_static(const mk_model_dims *dims, const mk_w
   p.kv_maps = base + o_maps;
   p.xbuf_bytes = (int32_t)sm.xbuf;
   p.xn_bytes = (int32_t)sm.xn;
+  p.fold = plan.fold;
+  p.fold_rows = fold_rows;
+  p.moe_part = (float *)(base + o_mp);
+  p.wd_maps = base + o_wdm;
   p.poison_layer = -1;
   p.poison_delta = 0;
 

@@ -12,6 +12,7 @@ struct MkPlan {
   int n_cta = 0, tasks_per_cta = 0, n_layer_tasks_max = 0, batch = 0;
   int n_qkv = 0, n_router = 0, n_attn = 0, n_up = 0, n_out = 0, n_lm = 0;
   int n_attn_slots = 0, n_attn_done = 0;
+  int fold = 0; /* the down projection is folded into the gate/up shares (batch 1) */
   std::vector<int32_t> table;      /* [n_cta][tasks_per_cta][32] */
   std::vector<int32_t> built_lens; /* lengths the attention splits were cut for */
 };
@@ -36,6 +37,15 @@ int mk_nb_for(int batch);
  * head_dim >= 64. */
 mk_status mk_encode_kv_maps(const mk_model_dims *d, const void *const *k_pools,
                             const void *const *v_pools, void *host_out);
+
+/* Encodes a 2-D TMA tensor map per layer over the down weights viewed as
+ * [n_experts * d_model rows][d_ffn columns] into host_out ([n_layers] maps of
+ * 128 bytes): box {MK_FOLD_COLS columns, box_rows rows}, 128-byte swizzle. */
+mk_status mk_encode_wd_maps(const mk_model_dims *d, const void *const *w_down, int box_rows,
+                            void *host_out);
+/* Rows of d per down box for the batch-1 ring stages (a multiple of 8, at
+ * most 256). */
+int mk_fold_rows(const mk_model_dims *d);
 
 mk_status mk_validate_dims(const mk_model_dims *d);
 mk_status mk_build_plan(const mk_model_dims *d, int n_cta, int batch, const int32_t *seq_lens,

@@ -106,6 +106,17 @@ bool mk_smem_plan(const mk_model_dims *dm, int nb, MkSmem *out) {
   return true;
 }
 
+int mk_fold_rows(const mk_model_dims *d) {
+  MkSmem sm;
+  int lim = 64;
+  if (mk_smem_plan(d, 1, &sm)) lim = std::min(256, sm.stage_bytes / (MK_FOLD_COLS * 2));
+  /* the largest multiple of 8 that fits a stage and divides d (d is a
+   * multiple of 64), so that a box never reaches into the next expert */
+  for (int r = lim / 8 * 8; r >= 8; r -= 8)
+    if (d->d_model % r == 0) return r;
+  return 8;
+}
+
 mk_status mk_validate_dims(const mk_model_dims *dm) {
   if (!dm) return MK_ERR_INVALID_ARG;
   const mk_model_dims &d = *dm;
@@ -217,13 +228,20 @@ mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int
    * bytes, weighted by the attention stage's higher compute per byte, against
    * the expected distinct experts' gate/up bytes.  With few CTAs every CTA
    * does everything. */
+  /* Batch 1 folds the down projection into the gate/up shares: a share is a
+   * range of 64-column blocks of the chosen experts' F, whose g and u are
+   * kept in shared memory and whose down partials have one slot per block --
+   * so the expert path has no second phase behind a grid-wide wait.  It needs
+   * the largest share's g and u to fit the scratch buffer. */
+  const int fold_blocks = std::min(d.n_experts, d.top_k) * (d.d_ffn / MK_FOLD_COLS);
   int n_acta = n_cta;
   if (n_cta >= 16) {
     double kv = 0.0;
     for (int b = 0; b < batch; ++b) kv += (double)seq_lens[b] * Hkv * D * 2 * 2;
     const double E = d.n_experts, K = d.top_k;
     const double u_exp = E * (1.0 - std::pow(1.0 - K / E, (double)batch));
-    const double up = u_exp * 2.0 * d.d_ffn * d.d_model * 2;
+    const bool fold = mk_nb_for(batch) == 1;
+    const double up = u_exp * (fold ? 3.0 : 2.0) * d.d_ffn * d.d_model * 2;
     /* SM cycles of a 24 KB attention stage (48 keys x 8 query heads, both
      * products and the online softmax) over those of a gate/up stage of the
      * same bytes (~1.5, measured on GB300), plus the merge at the end of
@@ -232,8 +250,20 @@ mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int
     const double frac = kAttnCostPerByte * kv / std::max(kAttnCostPerByte * kv + up, 1.0);
     const int lo = std::min(batch * Hkv, n_cta - 1), hi = n_cta - 1;
     n_acta = std::max(std::max(lo, 1), std::min(hi, (int)std::lround(n_cta * frac)));
+    /* folded blocks are whole: more expert CTAs than blocks would idle */
+    if (fold) n_acta = std::max(n_acta, std::min(hi, n_cta - fold_blocks));
   }
   const bool roles = n_acta < n_cta; /* attention CTAs take no expert share */
+  {
+    const int n_up = n_cta - (roles ? n_acta : 0);
+    const int max_blocks = (fold_blocks + n_up - 1) / n_up;
+    MkSmem sm;
+    /* a share's g and u, and an OUT task's rows of every block's partial,
+     * staged in the scratch buffer */
+    p.fold = mk_nb_for(batch) == 1 && mk_smem_plan(&d, 1, &sm) &&
+             (size_t)2 * max_blocks * MK_FOLD_COLS * sizeof(float) <= sm.xbuf &&
+             (size_t)fold_blocks * MK_MAX_OUT_ROWS * sizeof(float) <= sm.xbuf;
+  }
 
   /* ATTN: split-K over pages. */
   {
