@@ -506,6 +506,7 @@ mk_status mk_decode_step(mk_ctx *c, const int32_t *token_ids, float *out_logits,
   p.eps = d.rms_eps;
   p.attn_scale = (float)(1.0 / std::sqrt((double)d.head_dim));
   p.layers = c->layers_dev;
+  mk_param_layers(&p, c->layers.data(), d.n_layers);
   p.embed = c->embed;
   p.final_norm = c->final_norm;
   p.lm_head = c->lm_head;
@@ -542,6 +543,7 @@ mk_status mk_decode_step(mk_ctx *c, const int32_t *token_ids, float *out_logits,
   p.wait_limit_ns = c->wait_limit_ns;
   p.err_host = c->err_host_dev;
   p.stage_bytes = sm.stage_bytes;
+  p.ring_slots = sm.ring_slots;
   p.kv_maps = c->kv_maps;
   p.xbuf_bytes = (int32_t)sm.xbuf;
   p.xn_bytes = (int32_t)sm.xn;

@@ -75,7 +75,9 @@ static inline int mk_ctrs_per_layer(int max_batch, int n_kv_heads) {
 #define MK_NP_WARPS 4           /* producer warps; producer k fills the ring slots = k mod 4 */
 #define MK_THREADS ((MK_NC_WARPS + MK_NP_WARPS) * 32)
 #define MK_MAX_STAGE_ROWS 64
+#ifndef MK_MAX_STAGE_BYTES
 #define MK_MAX_STAGE_BYTES 32768
+#endif
 #define MK_MAX_STAGE_PAGES 8
 #define MK_SMEM_OPTIN 232448    /* opt-in shared memory per block on sm_100-class parts */
 #define MK_SMEM_STATIC 1024     /* slack to align the ring to 1024 bytes */
@@ -102,6 +104,8 @@ typedef struct {
   unsigned long long sum_experts; /* sum of U over layers and steps */
 } mk_ctrl;
 
+#define MK_PARAM_LAYERS 64
+
 /* Per-layer device pointers (a device array of n_layers of these). */
 typedef struct {
   const uint16_t *norm, *wq, *wk, *wv, *wo, *wr;
@@ -117,6 +121,12 @@ typedef struct {
   float eps, attn_scale;
   /* model */
   const mk_layer_dev *layers;
+  /* the first MK_PARAM_LAYERS layers' norm gains, router biases and K/V
+   * pools again, in the parameter space: read from the constant cache, with
+   * no dependent global load at a layer's start (later layers: `layers`) */
+  const uint16_t *l_norm[MK_PARAM_LAYERS];
+  const float *l_bias[MK_PARAM_LAYERS];
+  uint16_t *l_kc[MK_PARAM_LAYERS], *l_vc[MK_PARAM_LAYERS];
   const uint16_t *embed, *final_norm, *lm_head;
   /* step io */
   const int32_t *tokens;
@@ -149,6 +159,7 @@ typedef struct {
   unsigned long long wait_limit_ns;
   int32_t *err_host;          /* host-mapped mirror: [code, cta, task, op, layer, ctr, seen, target] */
   int32_t stage_bytes;        /* bytes of one ring slot (a multiple of 1024) */
+  int32_t ring_slots;         /* MK_NC_WARPS: stage i -> slot i % ring_slots */
   const void *kv_maps;        /* [L][2] CUtensorMap of the K and V pools (64-byte aligned) */
   int32_t xbuf_bytes;         /* shared scratch buffer */
   int32_t xn_bytes;           /* shared normed-input buffer (kept across a layer's tasks) */
@@ -162,6 +173,17 @@ typedef struct {
   unsigned long long *stage_trace; /* NULL, or one CTA's [MK_STAGE_TRACE_EVENTS][8] stage timestamps */
   int32_t stage_trace_cta;         /* the CTA that records them */
 } mk_kparams;
+
+/* Copies the first MK_PARAM_LAYERS layers' pointers into the parameter
+ * space (host side, when the parameters are filled in). */
+static inline void mk_param_layers(mk_kparams *p, const mk_layer_dev *ly, int n_layers) {
+  for (int l = 0; l < n_layers && l < MK_PARAM_LAYERS; ++l) {
+    p->l_norm[l] = ly[l].norm;
+    p->l_bias[l] = ly[l].bias;
+    p->l_kc[l] = ly[l].kc;
+    p->l_vc[l] = ly[l].vc;
+  }
+}
 
 /* One trace event (per executed task, written by consumer thread 0):
  * [0] op | layer << 8 | task << 20, [1] entry, [2] dependency satisfied,

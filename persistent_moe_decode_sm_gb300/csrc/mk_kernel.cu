@@ -291,6 +291,19 @@ __device__ __forceinline__ void tensor_g2s_2d(void *dst, const void *tmap, int x
       : "memory");
 }
 
+/* a layer's norm gain, from the parameter space when it is there */
+__device__ __forceinline__ const uint16_t *lnorm(const mk_kparams &p, int layer) {
+  return layer < MK_PARAM_LAYERS ? p.l_norm[layer] : p.layers[layer].norm;
+}
+
+#ifndef MK_PROD_SLEEP
+#define MK_PROD_SLEEP 20
+#endif
+
+__device__ __forceinline__ void prefetch_tensormap(const void *map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
@@ -615,6 +628,7 @@ struct Ctx {
   uint32_t epoch;
   int cta;
   int SB; /* bytes of one ring slot */
+  int NS; /* ring slots: stage i uses slot i % NS and belongs to consumer warp i % NC */
   __device__ __forceinline__ uint8_t *ring() const { return mk_smem + ring_off; }
   __device__ __forceinline__ uint8_t *xbuf() const { return mk_smem + xbuf_off; }
   /* the normed layer input [NB][d] bf16, kept while the layer's QKV, router
@@ -723,29 +737,38 @@ __device__ bool wait_mbar(const Ctx &cx, uint64_t *bar, uint32_t parity, int tas
  * published and polled before the expert weights can be fetched.
  *
  * route_warp: one warp, the NT <= 8 tokens' selections interleaved so that
- * their shuffle chains overlap.  Per token: K rounds of a warp argmax over
+ * their reduction chains overlap.  Per token: K rounds of a warp argmax over
  * the E <= 128 fp32 logits (lane l holds experts l, l + 32, l + 64, l + 96),
- * ties to the lower expert id; the weights are the softmax over the chosen
- * logits (the softmax over all E renormalised over the chosen k).  Then the
- * distinct experts of the batch in ascending id: expert[slot], *U, and --
- * if slot_w is given -- the weight of each slot for each token (0 where the
- * token did not choose it).  publish (or NULL): the per-token ids and
- * weights for the diagnostics. */
+ * ties to the lower expert id.  A round is two single-instruction warp
+ * reductions: the largest of the lanes' best keys (an order-preserving
+ * unsigned image of the float), then the lowest expert id among the lanes
+ * holding it.  The weights are the softmax over the chosen logits (the
+ * softmax over all E renormalised over the chosen k).  Then the distinct
+ * experts of the batch in ascending id: expert[slot], *U, and -- if slot_w
+ * is given -- the weight of each slot for each token (0 where the token did
+ * not choose it).  publish (or NULL): the per-token ids and weights for the
+ * diagnostics. */
+/* Unsigned keys in the order of the floats (-0 taken as +0, which compares
+ * equal to it); 0 marks an expert out of the running. */
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t u = __float_as_uint(__fadd_rn(f, 0.0f));
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 template <int NT>
 __device__ void route_warp(const float *lg, int E, int B, int K, int lane, int32_t *expert,
                            int32_t *U_out, float (*slot_w)[NT], mk_routing *publish) {
-  float v[NT][4];
-  uint32_t taken[NT];
+  uint32_t key[NT][4];
 #pragma unroll
-  for (int t = 0; t < NT; ++t) {
-    taken[t] = 0;
+  for (int t = 0; t < NT; ++t)
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int e = lane + 32 * i;
-      v[t][i] = (t < B && e < E) ? __ldcg(lg + (size_t)t * E + e) : NEG_INF;
-      if (!(t < B && e < E)) taken[t] |= 1u << i;
+      key[t][i] = (t < B && e < E) ? order_key(__ldcg(lg + (size_t)t * E + e)) : 0u;
     }
-  }
   int pick[NT];
   float pv[NT];
 #pragma unroll
@@ -754,37 +777,39 @@ __device__ void route_warp(const float *lg, int E, int B, int K, int lane, int32
     pv[t] = NEG_INF;
   }
   for (int k = 0; k < K; ++k) {
-    float bv[NT];
-    int bi[NT];
+    uint32_t best[NT], bi[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-      bv[t] = NEG_INF;
-      bi[t] = 0x7FFFFFFF;
+      best[t] = key[t][0];
+      bi[t] = 0;
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (!((taken[t] >> i) & 1u) && (v[t][i] > bv[t] || bi[t] == 0x7FFFFFFF)) {
-          bv[t] = v[t][i];
-          bi[t] = lane + 32 * i;
+      for (int i = 1; i < 4; ++i)
+        if (key[t][i] > best[t]) {
+          best[t] = key[t][i];
+          bi[t] = i;
         }
     }
+    uint32_t top[NT];
 #pragma unroll
-    for (int s = 16; s >= 1; s >>= 1)
+    for (int t = 0; t < NT; ++t) top[t] = __reduce_max_sync(0xFFFFFFFFu, best[t]);
+    uint32_t win[NT];
 #pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv[t], s);
-        const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi[t], s);
-        if (oi != 0x7FFFFFFF && (bi[t] == 0x7FFFFFFF || ov > bv[t] || (ov == bv[t] && oi < bi[t]))) {
-          bv[t] = ov;
-          bi[t] = oi;
-        }
-      }
+    for (int t = 0; t < NT; ++t)
+      win[t] = __reduce_min_sync(0xFFFFFFFFu, (best[t] == top[t] && top[t] != 0u)
+                                                  ? bi[t] * 32u + (uint32_t)lane
+                                                  : 0xFFFFFFFFu);
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
+      if (win[t] == 0xFFFFFFFFu) continue; /* no expert left (rows of absent tokens) */
       if (lane == k) {
-        pick[t] = bi[t];
-        pv[t] = bv[t];
+        pick[t] = (int)win[t];
+        pv[t] = key_value(top[t]);
       }
-      if ((bi[t] & 31) == lane && bi[t] != 0x7FFFFFFF) taken[t] |= 1u << (bi[t] >> 5);
+      if ((int)(win[t] & 31u) == lane) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if ((uint32_t)i == (win[t] >> 5)) key[t][i] = 0u;
+      }
     }
   }
   /* weights: softmax over the chosen logits; the union of the chosen sets */
@@ -872,54 +897,72 @@ struct Producer {
   int32_t *pexp; /* this warp's slot -> expert list (shared memory) */
   int32_t *pU;
   int32_t *prouted; /* shared: the last layer whose logits warp 0 saw complete */
+  /* the consumers' routing in shared memory: its layer, U, slot -> expert */
+  const int32_t *c_layer, *c_U, *c_expert;
   int r_layer;   /* layer of the routing in pexp (-1: none) */
   uint64_t t_task, t_plan; /* stage trace: the current task's start, its plan ready */
   int last_slot[NC];
   unsigned long long *strc;
 
-  /* The layer's routing for this warp's expert stages: a bounded wait (lane
-   * 0) for every router piece's logits, then the warp's own top-k.  Only
-   * producer warp 0 polls the global counter (hundreds of pollers on one
-   * line slow every poll and the router pieces' own signals); it passes the
-   * news on through a shared word the other producer warps wait on.
+  /* The layer's routing for this warp's expert stages.  For a gate/up
+   * share (from_consumers) it is the consumers' routing of the layer, which
+   * consumer warp 0 publishes in shared memory as soon as the consumers have
+   * taken it (they start the share right after the CTA's QKV task); it stays
+   * valid while a producer warp copies it, as the consumers cannot leave the
+   * share before every producer warp has issued its stages of it.  For
+   * expert down rows in an OUT task (whose consumers take the routing only
+   * after their attention splits) each producer warp takes the top-k itself
+   * once every router piece is in: producer warp 0 alone polls the global
+   * counter (hundreds of pollers on one line slow every poll and the router
+   * pieces' own signals) and passes the news on through a shared word.
    * Returns U, or -1 on timeout / abort. */
-  __device__ int routed(int layer) {
+  __device__ int routed(int layer, bool from_consumers) {
     const mk_kparams &p = *cx.p;
     if (r_layer == layer) return *(volatile int32_t *)pU;
-    int ok = 1;
-    if (k == 0) { /* the whole warp waits, lane 0 polls */
-      int32_t *c = lctr(p, layer, CTR_ROUTER_DONE);
-      const int target = (int)((cx.epoch + 1) * (uint32_t)p.n_router);
-      ok = wait_counter_warp(cx, c, target, -1, OP_UP, layer, CTR_ROUTER_DONE) ? 1 : 0;
-      if (ok && lane == 0) st_release_cta(prouted, layer);
-    } else {
-      const uint64_t t0 = gtimer();
-      uint32_t spins = 0;
-      while (true) {
-        int seen = lane == 0 ? ld_acquire_cta(prouted) : 0;
-        if (__shfl_sync(0xFFFFFFFFu, seen, 0) >= layer) break;
-        if ((++spins & 31) == 0) {
-          int stop = 0;
-          if (lane == 0) {
-            if (ld_volatile(&p.ctrl->abort)) {
-              stop = 1;
-            } else if (gtimer() - t0 > p.wait_limit_ns) {
-              raise_error(p, MK_ERR_DEVICE_TIMEOUT, cx.cta, -1, OP_UP, layer, CTR_ROUTER_DONE, -1,
-                          layer);
-              stop = 1;
-            }
+    int32_t *c = lctr(p, layer, CTR_ROUTER_DONE);
+    const int target = (int)((cx.epoch + 1) * (uint32_t)p.n_router);
+    const uint64_t t0 = gtimer();
+    uint32_t spins = 0;
+    while (true) {
+      int seen = 0;
+      if (lane == 0) {
+        if (from_consumers) {
+          seen = ld_acquire_cta(c_layer) == layer;
+        } else if (k == 0) {
+          if ((int)(ld_relaxed(c) - target) >= 0) {
+            fence_acquire_gpu();
+            seen = 1;
           }
-          if (__shfl_sync(0xFFFFFFFFu, stop, 0)) {
-            ok = 0;
-            break;
+        } else {
+          seen = ld_acquire_cta(prouted) >= layer;
+        }
+      }
+      if (__shfl_sync(0xFFFFFFFFu, seen, 0)) break;
+      if ((++spins & 31) == 0) {
+        int stop = 0;
+        if (lane == 0) {
+          if (ld_volatile(&p.ctrl->abort)) {
+            stop = 1;
+          } else if (gtimer() - t0 > p.wait_limit_ns) {
+            raise_error(p, MK_ERR_DEVICE_TIMEOUT, cx.cta, -1, OP_UP, layer, CTR_ROUTER_DONE, -1,
+                        layer);
+            stop = 1;
           }
         }
-        __nanosleep(20);
+        if (__shfl_sync(0xFFFFFFFFu, stop, 0)) return -1;
       }
+      __nanosleep(MK_PROD_SLEEP);
     }
-    if (!ok) return -1;
-    route_warp<NB>(p.router_logits + (size_t)layer * MK_MAX_BATCH * p.E, p.E, p.B, p.K, lane,
-                   pexp, pU, nullptr, nullptr);
+    if (from_consumers) {
+      const int U = *(volatile const int32_t *)c_U;
+      for (int i = lane; i < U; i += 32) pexp[i] = c_expert[i];
+      if (lane == 0) *pU = U;
+      __syncwarp();
+    } else {
+      if (k == 0 && lane == 0) st_release_cta(prouted, layer);
+      route_warp<NB>(p.router_logits + (size_t)layer * MK_MAX_BATCH * p.E, p.E, p.B, p.K, lane,
+                     pexp, pU, nullptr, nullptr);
+    }
     r_layer = layer;
     return *(volatile int32_t *)pU;
   }
@@ -928,8 +971,8 @@ struct Producer {
   __device__ bool issue(const QDesc &d, int i) {
     const mk_kparams &p = *cx.p;
     const uint64_t ta = strc ? sclock() : 0;
-    const int slot = i % NC;
-    if (i >= NC && !wait_mbar(cx, &cx.empty()[slot], (uint32_t)(((i / NC) - 1) & 1), -1, -1, -1))
+    const int NS = cx.NS, slot = i % NS;
+    if (i >= NS && !wait_mbar(cx, &cx.empty()[slot], (uint32_t)(((i / NS) - 1) & 1), -1, -1, -1))
       return false;
     const uint64_t tb = strc ? sclock() : 0;
     uint8_t *dst = cx.ring() + (size_t)slot * cx.SB;
@@ -1002,11 +1045,26 @@ struct Producer {
     const int d = p.d, F = p.F, HqD = p.Hq * p.D, P = p.P;
     int base = 0;
     bool ok = true;
+    /* the layer's weight pointers, loaded one layer ahead (a dependent L2
+     * round trip before the first stage of every task otherwise); the final
+     * tasks keep the last layer's */
+    mk_layer_dev cur = p.layers[0], nxt = p.layers[p.L > 1 ? 1 : 0];
     for (int layer = 0; layer <= p.L && ok; ++layer) {
       const int ntask = layer < p.L ? nl : nf;
+      if (layer > 0 && layer < p.L) {
+        cur = nxt;
+        nxt = p.layers[min(layer + 1, p.L - 1)];
+      }
+      if (k == 0 && lane == 0 && layer + 1 < p.L) {
+        /* the next layer's tensor maps into the descriptor cache */
+        const uint8_t *kmap = (const uint8_t *)p.kv_maps + (size_t)(layer + 1) * 2 * 128;
+        prefetch_tensormap(kmap);
+        prefetch_tensormap(kmap + 128);
+        if (NB == 1 && p.fold) prefetch_tensormap((const uint8_t *)p.wd_maps + (size_t)(layer + 1) * 128);
+      }
       for (int kt = 0; kt < ntask && ok; ++kt) {
         const int32_t *t = row + MK_DESC_INTS * (1 + (layer < p.L ? kt : nl + kt));
-        const mk_layer_dev *ly = p.layers + (layer < p.L ? layer : p.L - 1);
+        const mk_layer_dev *ly = &cur;
         const int op = t[0];
         t_task = strc ? sclock() : 0;
         t_plan = 0;
@@ -1050,7 +1108,7 @@ struct Producer {
           /* a range of 64-column blocks of the chosen experts' F: every
            * block's 64 gate rows and 64 up rows, then its down boxes (the
            * block's 64 columns of fold_rows rows of d each) */
-          const int U = routed(layer);
+          const int U = routed(layer, true);
           if (U < 0) {
             ok = false;
             break;
@@ -1083,7 +1141,7 @@ struct Producer {
           });
           base += nA + nB;
         } else if (op == OP_UP) {
-          const int U = routed(layer);
+          const int U = routed(layer, true);
           if (U < 0) {
             ok = false;
             break;
@@ -1124,14 +1182,15 @@ struct Producer {
           /* the chosen experts' down rows first (their activations are
            * ready before the attention output), then the Wo rows */
           const int r0 = t[2], nr = t[3];
-          const int U = routed(layer);
+          const bool fold = NB == 1 && p.fold; /* down rows in the gate/up shares */
+          const int U = fold ? 0 : routed(layer, false);
           if (U < 0) {
             ok = false;
             break;
           }
           t_plan = strc ? sclock() : 0;
           const int rps_f = mk_rows_per_stage(F, SB), n_se = (nr + rps_f - 1) / rps_f;
-          const int n_dn = (NB == 1 && p.fold) ? 0 : U * n_se; /* folded: in the gate/up shares */
+          const int n_dn = fold ? 0 : U * n_se;
           const int rps_o = mk_rows_per_stage(HqD, SB), n_wo = (nr + rps_o - 1) / rps_o;
           const uint16_t *wo = ly->wo + (size_t)r0 * HqD;
           ok = run_stages(base, 0, n_dn + n_wo, [&](int j, QDesc &q) {
@@ -1158,10 +1217,10 @@ struct Producer {
     /* Every copy issued must land before the CTA exits (normally the
      * consumers have waited for all of them already). */
     if (lane == 0)
-      for (int s = 0; s < NC; ++s) {
+      for (int s = 0; s < c.NS; ++s) {
         const int kk = last_slot[s];
         if (kk < 0) continue;
-        const uint32_t parity = (uint32_t)((kk / NC) & 1);
+        const uint32_t parity = (uint32_t)((kk / c.NS) & 1);
         const uint64_t t0 = gtimer();
         while (!mbar_test(&c.full()[s], parity) && gtimer() - t0 < p.wait_limit_ns) {
         }
@@ -1185,6 +1244,12 @@ __device__ __noinline__ void produce(const Ctx cx, int k, int lane, QDesc *buf, 
   pr.pexp = pexp;
   pr.pU = pU;
   pr.prouted = prouted;
+  {
+    const Misc<NB> *m = (const Misc<NB> *)(mk_smem + cx.misc_off);
+    pr.c_layer = &m->route_layer;
+    pr.c_U = &m->route_U;
+    pr.c_expert = m->route_expert;
+  }
   pr.r_layer = -1;
   pr.t_task = pr.t_plan = 0;
   pr.strc = strc;
@@ -1240,8 +1305,8 @@ struct Consumer {
    * per lane group. */
   __device__ bool stage_wait(int i, uint8_t *&st, int task, int op, int layer) {
     if (wfail) return false;
-    const int slot = i % NC;
-    const uint32_t parity = (uint32_t)((i / NC) & 1);
+    const int slot = i % cx.NS;
+    const uint32_t parity = (uint32_t)((i / cx.NS) & 1);
     const bool trace = tr && warp == 0;
     const bool sev = tr && cx.cta == cx.p->stage_trace_cta && i < MK_STAGE_TRACE_EVENTS - 1;
     const uint64_t w0 = trace ? gtimer() : 0, c0 = sev ? sclock() : 0;
@@ -1268,7 +1333,7 @@ struct Consumer {
 
   __device__ void stage_release(int i) {
     __syncwarp(); /* every lane's reads of the slot precede the release */
-    mbar_arrive_if(&cx.empty()[i % NC], lane == 0);
+    mbar_arrive_if(&cx.empty()[i % cx.NS], lane == 0);
     if (tr && cx.cta == cx.p->stage_trace_cta && i < MK_STAGE_TRACE_EVENTS - 1)
       st64_if(cx.p->stage_trace + (size_t)i * 8 + 7, sclock(), lane == 0);
   }
@@ -1378,7 +1443,7 @@ struct Consumer {
     const uint16_t *hr[NB];
 #pragma unroll
     for (int b = 0; b < NB; ++b) hr[b] = b < cx.p->B ? h_row(layer, b) : nullptr;
-    norm_into_xbuf(layer, hr, cx.p->layers[layer].norm);
+    norm_into_xbuf(layer, hr, lnorm(*cx.p, layer));
     if (tr && tid == 0) t_mark = gtimer();
   }
 
@@ -1469,7 +1534,7 @@ struct Consumer {
     uint16_t *out = p.qkv + (size_t)layer * MK_MAX_BATCH * QKVD;
     const int B = p.B, E = p.E, d = p.d, e0 = t[4], rn = t[5], nrows = t[3];
     float *lg = p.router_logits + (size_t)layer * MK_MAX_BATCH * E;
-    const float *bias = p.layers[layer].bias;
+    const float *bias = layer < MK_PARAM_LAYERS ? p.l_bias[layer] : p.layers[layer].bias;
     int32_t *rctr = lctr(p, layer, CTR_ROUTER_DONE);
     const int rps = mk_rows_per_stage(d, cx.SB);
     const int n_rst = (rn + rps - 1) / rps, n_st = n_rst + (nrows + rps - 1) / rps;
@@ -1502,11 +1567,99 @@ struct Consumer {
     return true;
   }
 
-  /* The layer's routing in shared memory (route_expert, route_w, route_U):
-   * once every router piece's logits are written, warp 0 takes the top-k of
-   * every token (route_warp); CTA 0 also records it for the diagnostics.
-   * Called by every consumer thread at the start of a task that needs it
-   * (while the out union is not live).  False on timeout / abort. */
+  /* The layer's routing from the router logits, taken by all consumer
+   * threads at once: each (token, expert) pair counts the token's logits
+   * that rank above it (larger, or equal with a lower id), so the pairs of
+   * rank < k are the token's choices in descending order -- the same
+   * selection as k rounds of argmax with ties to the lower id.  The weights
+   * are the softmax over the chosen logits (warp t for token t); the batch's
+   * distinct experts get the slots in ascending id.  Writes route_expert,
+   * route_U and route_w, and the diagnostics record when publish is set.
+   * Uses the scratch buffer; ends with a consumer barrier. */
+  __device__ void route_block(const float *lg, mk_routing *publish) {
+    const mk_kparams &p = *cx.p;
+    Misc<NB> *m = M();
+    const int E = p.E, B = p.B, K = p.K, E4 = (E + 3) & ~3;
+    uint32_t *key = (uint32_t *)cx.xbuf();                  /* [NB][128] */
+    int32_t *pick = (int32_t *)(key + NB * 128);             /* [NB][MK_MAX_TOPK] */
+    uint32_t *flag = (uint32_t *)(pick + NB * MK_MAX_TOPK);  /* [128]: chosen by a token */
+    for (int i = tid; i < NB * 128; i += NCT) {
+      const int t = i >> 7, e = i & 127;
+      key[i] = (t < B && e < E) ? order_key(__ldcg(lg + (size_t)t * E + e)) : 0u;
+    }
+    for (int i = tid; i < 128; i += NCT) flag[i] = 0u;
+    bar_consumers();
+    for (int i = tid; i < NB * 128; i += NCT) {
+      const int t = i >> 7, e = i & 127;
+      if (t >= B || e >= E) continue;
+      const uint32_t ke = key[i];
+      const uint32_t *kt = key + t * 128;
+      int r = 0;
+      for (int j = 0; j < E4; j += 4) {
+        const uint4 q = *(const uint4 *)(kt + j);
+        r += (q.x > ke) + (q.y > ke) + (q.z > ke) + (q.w > ke);
+        r += (q.x == ke && j < e) + (q.y == ke && j + 1 < e) + (q.z == ke && j + 2 < e) +
+             (q.w == ke && j + 3 < e);
+      }
+      if (r < K) {
+        pick[t * MK_MAX_TOPK + r] = e;
+        flag[e] = 1u;
+      }
+    }
+    bar_consumers();
+    /* the slots: experts chosen by any token, ascending */
+    uint32_t words[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) words[i] = __ballot_sync(0xFFFFFFFFu, flag[lane + 32 * i] != 0u);
+    const int U = __popc(words[0]) + __popc(words[1]) + __popc(words[2]) + __popc(words[3]);
+    auto slot_of = [&](int e) {
+      int r = __popc(words[e >> 5] & ((1u << (e & 31)) - 1u));
+#pragma unroll
+      for (int i = 0; i < 3; ++i) r += (i < (e >> 5)) ? __popc(words[i]) : 0;
+      return r;
+    };
+    if (warp == 0) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if ((words[i] >> lane) & 1u) m->route_expert[slot_of(lane + 32 * i)] = lane + 32 * i;
+      if (lane == 0) m->route_U = U;
+      if (publish) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if ((words[i] >> lane) & 1u) publish->expert[slot_of(lane + 32 * i)] = lane + 32 * i;
+        if (lane == 0) publish->U = U;
+      }
+    }
+    for (int i = tid; i < U * NB; i += NCT) (&m->route_w[0][0])[i] = 0.0f;
+    bar_consumers();
+    /* token t's weights: warp t, lane k for its k-th choice */
+    if (warp < B) {
+      const int t = warp;
+      const int e = lane < K ? pick[t * MK_MAX_TOPK + lane] : 0;
+      const float v = lane < K ? key_value(key[t * 128 + e]) : 0.0f;
+      const float v0 = __shfl_sync(0xFFFFFFFFu, v, 0);
+      const float ex = lane < K ? expf(v - v0) : 0.0f;
+      float z = ex;
+#pragma unroll
+      for (int sh = 16; sh >= 1; sh >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, sh);
+      const float w = z > 0.0f ? ex / z : 0.0f;
+      if (lane < K) {
+        m->route_w[slot_of(e)][t] = w;
+        if (publish) {
+          publish->ids[t][lane] = e;
+          publish->w[t][lane] = w;
+        }
+      }
+    }
+    bar_consumers();
+  }
+
+  /* The layer's routing in shared memory (route_expert, route_w, route_U),
+   * taken once every router piece's logits are written; CTA 0 also records
+   * it for the diagnostics, and consumer thread 0 then publishes it to the
+   * producer warps.  Called by every consumer thread at the start of a task
+   * that needs it (while the out union is not live).  False on timeout /
+   * abort. */
   __device__ bool route_local(int layer, int task, int op) {
     const mk_kparams &p = *cx.p;
     Misc<NB> *m = M();
@@ -1515,14 +1668,13 @@ struct Consumer {
     if (!cwait(lctr(p, layer, CTR_ROUTER_DONE), (int)((cx.epoch + 1) * (uint32_t)p.n_router),
                task, op, layer, CTR_ROUTER_DONE))
       return false;
-    if (warp == 0) {
-      route_warp<NB>(p.router_logits + (size_t)layer * MK_MAX_BATCH * p.E, p.E, p.B, p.K, lane,
-                     m->route_expert, &m->route_U, m->route_w,
-                     cx.cta == 0 ? p.routing + layer : nullptr);
-      if (lane == 0) {
-        m->route_layer = layer;
-        if (cx.cta == 0) atomicAdd(&p.ctrl->sum_experts, (unsigned long long)m->route_U);
-      }
+    route_block(p.router_logits + (size_t)layer * MK_MAX_BATCH * p.E,
+                cx.cta == 0 ? p.routing + layer : nullptr);
+    if (tid == 0) {
+      if (cx.cta == 0) atomicAdd(&p.ctrl->sum_experts, (unsigned long long)m->route_U);
+      if (tr && !t_mark) t_mark = gtimer();
+      __threadfence_block();
+      st_release_cta(&m->route_layer, layer); /* the producer warps may take it from here */
     }
     bar_consumers();
     return true;
@@ -1650,7 +1802,8 @@ struct Consumer {
       const uint16_t *vsrc = qkv + (size_t)(p.Hq + p.Hkv + kvh) * D;
       const int page = __ldg(p.page_table + b * p.max_pages + L_now / P);
       const size_t row = (((size_t)page * p.Hkv + kvh) * P + (L_now % P)) * D;
-      uint16_t *kc = p.layers[layer].kc + row, *vc = p.layers[layer].vc + row;
+      uint16_t *kc = (layer < MK_PARAM_LAYERS ? p.l_kc[layer] : p.layers[layer].kc) + row;
+      uint16_t *vc = (layer < MK_PARAM_LAYERS ? p.l_vc[layer] : p.layers[layer].vc) + row;
       for (int j = tid; j < half; j += NCT) {
         const float x1 = bf2f(__ldcg(ksrc + j)), x2 = bf2f(__ldcg(ksrc + j + half));
         const float c = __ldg(rp + 2 * j), s = __ldg(rp + 2 * j + 1);
@@ -2071,6 +2224,33 @@ struct Consumer {
     const int fit = max(1, (int)min((int64_t)U, (int64_t)p.xbuf_bytes / ((int64_t)2 * per)));
     const int rps = mk_rows_per_stage(F, cx.SB), pitch = mk_row_pitch(F);
     const bool fold = NB == 1 && p.fold; /* down rows done by the gate/up shares */
+    static_assert(MK_MAX_OUT_ROWS >= 32, "a lane per row of an OUT task");
+    if (fold) {
+      /* the gate/up shares' down partials of this task's rows: warp w adds
+       * blocks w, w + NC, ... in that order (lane r for row r0 + r, every
+       * load of a batch in flight at once), the warps' sums are added in
+       * warp order with the residual below */
+      const int nbf = F / MK_FOLD_COLS, T64 = U * nbf;
+      constexpr int BAT = 16;
+      float s = 0.0f;
+      if (lane < nr) {
+        const float *src = p.moe_part + r0 + lane;
+        for (int b0 = warp; b0 < T64; b0 += BAT * NC) {
+          float v[BAT];
+#pragma unroll
+          for (int i = 0; i < BAT; ++i) {
+            const int blk = b0 + i * NC;
+            v[i] = blk < T64 ? __ldcg(src + (size_t)blk * d) : 0.0f;
+          }
+#pragma unroll
+          for (int i = 0; i < BAT; ++i) {
+            const int blk = b0 + i * NC;
+            if (blk < T64) s = fmaf(slot_w[blk / nbf][0], v[i], s);
+          }
+        }
+      }
+      O.acc_w[warp][lane][0] = s; /* rows nr.. of the task: 0 */
+    }
     const int n_se = fold ? 0 : (nr + rps - 1) / rps; /* stages per expert */
     for (int u0 = 0; u0 < (fold ? 0 : U); u0 += fit) {
       const int u1 = min(U, u0 + fit);
@@ -2124,27 +2304,13 @@ struct Consumer {
     bar_consumers();
     gemv_rows(nr, HqD, xo, task, OP_OUT, layer, [&](int r, int bb, float v) { O.acc_o[r][bb] = v; });
     if (!task_end()) return false;
-    /* folded: every block's partial of this task's rows, staged in the
-     * scratch buffer (free again: Wo is done), added in block order */
-    const int T64 = U * (F / MK_FOLD_COLS);
-    float *ps = (float *)cx.xbuf();
-    if (fold) {
-      for (int i = tid; i < T64 * nr; i += NCT)
-        ps[i] = __ldcg(p.moe_part + (size_t)(i / nr) * d + r0 + i % nr);
-      bar_consumers();
-    }
     for (int i = tid; i < nr * B; i += NCT) {
       const int r = i / B, bb = i % B;
       const float hv = O.hres[r][bb];
       const uint16_t at = f2bf(O.acc_o[r][bb]);
       float mo = 0.0f;
-      if (fold) {
-        for (int blk = 0; blk < T64; ++blk)
-          mo = fmaf(slot_w[blk / (F / MK_FOLD_COLS)][0], ps[blk * nr + r], mo);
-      } else {
 #pragma unroll
-        for (int w = 0; w < NC; ++w) mo += O.acc_w[w][r][bb];
-      }
+      for (int w = 0; w < NC; ++w) mo += O.acc_w[w][r][bb];
       const uint16_t mb = f2bf(mo);
       p.h[((size_t)(layer + 1) * MK_MAX_BATCH + bb) * d + r0 + r] =
           f2bf(__fadd_rn(__fadd_rn(hv, bf2f(at)), bf2f(mb)));
@@ -2304,8 +2470,9 @@ __global__ void __launch_bounds__(MK_THREADS, 1) decode_kernel(const __grid_cons
   Ctx cx;
   cx.p = &p;
   cx.SB = p.stage_bytes;
+  cx.NS = p.ring_slots;
   cx.ring_off = (1024u - (saddr(mk_smem) & 1023u)) & 1023u;
-  cx.xn_off = cx.ring_off + (uint32_t)NC * p.stage_bytes;
+  cx.xn_off = cx.ring_off + (uint32_t)p.ring_slots * p.stage_bytes;
   cx.xbuf_off = cx.xn_off + (uint32_t)p.xn_bytes;
   cx.misc_off = cx.xbuf_off + (uint32_t)p.xbuf_bytes;
   Misc<NB> *misc = (Misc<NB> *)(mk_smem + cx.misc_off);
@@ -2387,6 +2554,7 @@ extern "C" size_t mk_misc_bytes(int nb) {
          : nb == 4 ? sizeof(mk::Misc<4>)
                    : sizeof(mk::Misc<8>);
 }
+
 
 static void *mk_kernel_fn(int nb) {
   return nb == 1   ? (void *)mk::decode_kernel<1>

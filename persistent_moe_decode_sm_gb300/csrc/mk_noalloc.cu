@@ -270,6 +270,7 @@ extern "C" mk_status mk_decode_step_static(const mk_model_dims *dims, const mk_w
   p.eps = d.rms_eps;
   p.attn_scale = (float)(1.0 / std::sqrt((double)d.head_dim));
   p.layers = (const mk_layer_dev *)(base + o_ly);
+  mk_param_layers(&p, layers.data(), Lyr);
   p.embed = (const uint16_t *)w->embed;
   p.final_norm = (const uint16_t *)w->final_norm;
   p.lm_head = (const uint16_t *)w->lm_head;
@@ -307,6 +308,7 @@ extern "C" mk_status mk_decode_step_static(const mk_model_dims *dims, const mk_w
   p.wait_limit_ns = MK_STATIC_WAIT_LIMIT_NS;
   p.err_host = nullptr;
   p.stage_bytes = sm.stage_bytes;
+  p.ring_slots = sm.ring_slots;
   p.kv_maps = base + o_maps;
   p.xbuf_bytes = (int32_t)sm.xbuf;
   p.xn_bytes = (int32_t)sm.xn;

@@ -17,12 +17,13 @@ struct MkPlan {
   std::vector<int32_t> built_lens; /* lengths the attention splits were cut for */
 };
 
-/* Dynamic shared memory of the nb-token kernel: NC ring slots of stage_bytes,
+/* Dynamic shared memory of the nb-token kernel: ring_slots slots of stage_bytes,
  * the normed-input buffer, the scratch buffer, the control block (total),
  * plus MK_SMEM_STATIC bytes of slack to align the ring to 1024 bytes (dyn,
  * the launch size). */
 struct MkSmem {
   int stage_bytes = 0;
+  int ring_slots = 0; /* one per consumer warp */
   size_t xn = 0, xbuf = 0, misc = 0, total = 0, dyn = 0;
 };
 /* false if the model does not fit (a row, a row pair or a KV page larger

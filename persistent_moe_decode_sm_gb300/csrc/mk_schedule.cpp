@@ -95,6 +95,7 @@ bool mk_smem_plan(const mk_model_dims *dm, int nb, MkSmem *out) {
   size_t sb = (MK_SMEM_OPTIN - fixed) / MK_NC_WARPS / 1024 * 1024;
   sb = std::min<size_t>(sb, MK_MAX_STAGE_BYTES);
   s.stage_bytes = (int)sb;
+  s.ring_slots = MK_NC_WARPS;
   const int HqD = d.n_q_heads * d.head_dim;
   if (mk_rows_per_stage(d.d_model, s.stage_bytes) < 2 || mk_rows_per_stage(HqD, s.stage_bytes) < 1 ||
       mk_rows_per_stage(d.d_ffn, s.stage_bytes) < 1 ||
@@ -258,11 +259,9 @@ mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int
     const int n_up = n_cta - (roles ? n_acta : 0);
     const int max_blocks = (fold_blocks + n_up - 1) / n_up;
     MkSmem sm;
-    /* a share's g and u, and an OUT task's rows of every block's partial,
-     * staged in the scratch buffer */
+    /* a share's g and u are staged in the scratch buffer */
     p.fold = mk_nb_for(batch) == 1 && mk_smem_plan(&d, 1, &sm) &&
-             (size_t)2 * max_blocks * MK_FOLD_COLS * sizeof(float) <= sm.xbuf &&
-             (size_t)fold_blocks * MK_MAX_OUT_ROWS * sizeof(float) <= sm.xbuf;
+             (size_t)2 * max_blocks * MK_FOLD_COLS * sizeof(float) <= sm.xbuf;
   }
 
   /* ATTN: split-K over pages. */
