@@ -53,6 +53,8 @@ struct mk_ctx {
   size_t ws_bytes = 0;
   uint16_t *h = nullptr, *qkv = nullptr, *o = nullptr, *act = nullptr, *am = nullptr;
   float *moe_part = nullptr;
+  int moe_part_stride = 0;
+  uint64_t *h_tag = nullptr, *lg_tag = nullptr;
   void *wd_maps = nullptr;             /* device [n_layers] tensor maps of the down weights */
   int fold_rows = 0;
   float *attn_part = nullptr, *attn_part2 = nullptr, *router_logits = nullptr, *lm_part = nullptr,
@@ -83,6 +85,7 @@ struct mk_ctx {
   uint64_t wait_limit_ns = 1000000000ULL;
   int poison_layer = -1, poison_delta = 0;
   uint64_t steps = 0, rebuilds = 0;
+  uint32_t tag_serial = 0; /* the last step tag used (never reset) */
   mk_status sticky = MK_OK;
   bool prepared[4] = {false, false, false, false}; /* kernel attributes set per batch bucket */
   unsigned long long *trace = nullptr; /* [n_sm][trace_cap][MK_TRACE_WORDS] */
@@ -300,8 +303,8 @@ mk_status mk_create(const mk_model_dims *dims, const mk_weights *w, void *stream
   const size_t o_qkv = cv.take((size_t)L * MB * QKVD * 2);
   const size_t o_o = cv.take((size_t)L * MB * HqD * 2);
   const size_t o_am = cv.take((size_t)L * 2 * MB * d.d_model * 2);
-  const size_t o_part = cv.take((size_t)c->n_slots_max * G * (d.head_dim + 4) * 4);
-  const size_t o_part2 = cv.take((size_t)c->n_slots_max * G * (d.head_dim + 4) * 4);
+  const size_t o_part = cv.take((size_t)2 * c->n_slots_max * G * (d.head_dim + 4) * 4);
+  const size_t o_part2 = cv.take((size_t)2 * c->n_slots_max * G * (d.head_dim + 4) * 4);
   const size_t o_rl = cv.take((size_t)L * MB * d.n_experts * 4);
   const size_t o_rt = cv.take((size_t)L * sizeof(mk_routing));
   const size_t o_act = cv.take((size_t)L * c->u_max * MB * d.d_ffn * 2);
@@ -314,8 +317,10 @@ mk_status mk_create(const mk_model_dims *dims, const mk_weights *w, void *stream
   const size_t o_ly = cv.take((size_t)L * sizeof(mk_layer_dev));
   const size_t o_maps = cv.take((size_t)L * 2 * 128);
   const size_t o_wdm = cv.take((size_t)L * 128);
-  const size_t o_mp =
-      cv.take((size_t)std::min(d.n_experts, d.top_k) * (d.d_ffn / MK_FOLD_COLS) * d.d_model * 4);
+  c->moe_part_stride = std::min(d.n_experts, d.top_k) * (d.d_ffn / MK_FOLD_COLS) * d.d_model;
+  const size_t o_mp = cv.take((size_t)2 * c->moe_part_stride * 4);
+  const size_t o_htag = cv.take((size_t)(L + 1) * MB * (d.d_model / 2) * 8);
+  const size_t o_lgtag = cv.take((size_t)L * MB * d.n_experts * 8);
   c->ws_bytes = cv.off;
 
   cudaError_t e = cudaMalloc(&c->ws, c->ws_bytes);
@@ -342,6 +347,8 @@ mk_status mk_create(const mk_model_dims *dims, const mk_weights *w, void *stream
   c->kv_maps = c->ws + o_maps;
   c->wd_maps = c->ws + o_wdm;
   c->moe_part = (float *)(c->ws + o_mp);
+  c->h_tag = (uint64_t *)(c->ws + o_htag);
+  c->lg_tag = (uint64_t *)(c->ws + o_lgtag);
   c->fold_rows = mk_fold_rows(&d);
   std::vector<uint8_t> maps((size_t)L * 2 * 128), wdmaps;
   {
@@ -550,6 +557,11 @@ mk_status mk_decode_step(mk_ctx *c, const int32_t *token_ids, float *out_logits,
   p.fold = c->plan.fold;
   p.fold_rows = c->fold_rows;
   p.moe_part = c->moe_part;
+  p.moe_part_stride = c->moe_part_stride;
+  p.h_tag = c->h_tag;
+  p.lg_tag = c->lg_tag;
+  c->tag_serial = c->tag_serial == 0xFFFFFFFFu ? 1u : c->tag_serial + 1u;
+  p.step_tag = c->tag_serial;
   p.wd_maps = c->wd_maps;
   p.poison_layer = c->poison_layer;
   p.poison_delta = c->poison_delta;

@@ -138,7 +138,8 @@ typedef struct {
   uint16_t *o;                /* [L][MAXB][Hq D] */
   uint16_t *am;               /* [L][2][MAXB][d] the rounded attn and moe terms of the residual */
   float *attn_part;           /* [n_slots][G][D + 4] (m, l, -, -, o[D]), reused by every layer */
-  float *attn_part2;          /* [n_slots][G][D + 4] merge-group partials */
+  float *attn_part2;          /* [n_slots][G][D + 4] merge-group partials (both by layer
+                               * parity: [2][n_slots]...) */
   float *router_logits;       /* [L][MAXB][E] */
   mk_routing *routing;        /* [L] */
   uint16_t *act;              /* [L][Umax][MAXB][F] */
@@ -166,7 +167,16 @@ typedef struct {
   int32_t poison_layer, poison_delta; /* test hook: see mk_debug_poison_wait */
   int32_t fold;               /* 1: each gate/up share also computes its blocks' down partials */
   int32_t fold_rows;          /* rows of d per down box (the tensor maps' box height) */
-  float *moe_part;            /* [Umax * F / 64][d] partial down vectors of the folded blocks */
+  float *moe_part;            /* [2][Umax * F / 64][d] partial down vectors of the folded blocks
+                               * (layer parity: a layer's writers never meet the previous
+                               * layer's readers) */
+  int32_t moe_part_stride;    /* floats per parity half of moe_part */
+  /* Values that carry their own validity: 64-bit words {payload, step_tag}
+   * written with one relaxed store and polled by their readers, so that no
+   * counter round trip or release fence stands between writer and reader. */
+  uint32_t step_tag;          /* this step's tag (never 0, never reused) */
+  uint64_t *h_tag;            /* [L+1][MAXB][d/2]: {bf16 h[2i], bf16 h[2i+1]} */
+  uint64_t *lg_tag;           /* [L][MAXB][E]: {fp32 router logit} */
   const void *wd_maps;        /* [L] CUtensorMap of each layer's down weights [E*d][F] */
   unsigned long long *trace;  /* NULL, or [n_cta][trace_cap][MK_TRACE_WORDS] task timestamps */
   int32_t trace_cap;

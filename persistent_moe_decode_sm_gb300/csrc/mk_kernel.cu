@@ -152,6 +152,21 @@ __device__ __forceinline__ int ld_relaxed(const int32_t *p) {
   return v;
 }
 
+/* Tagged words: {payload, tag} in one 64-bit relaxed store / load.  A word
+ * read with this step's tag is this step's value: no fence or counter is
+ * needed between the writer and the reader. */
+__device__ __forceinline__ void st_tag(uint64_t *a, uint32_t payload, uint32_t tag) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(a),
+               "l"(((unsigned long long)tag << 32) | payload)
+               : "memory");
+}
+__device__ __forceinline__ uint64_t ld_tag(const uint64_t *a) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ bool tag_ok(uint64_t w, uint32_t tag) { return (uint32_t)(w >> 32) == tag; }
+
 __device__ __forceinline__ void fence_acquire_gpu() {
   asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }
@@ -295,10 +310,6 @@ __device__ __forceinline__ void tensor_g2s_2d(void *dst, const void *tmap, int x
 __device__ __forceinline__ const uint16_t *lnorm(const mk_kparams &p, int layer) {
   return layer < MK_PARAM_LAYERS ? p.l_norm[layer] : p.layers[layer].norm;
 }
-
-#ifndef MK_PROD_SLEEP
-#define MK_PROD_SLEEP 20
-#endif
 
 __device__ __forceinline__ void prefetch_tensormap(const void *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
@@ -594,7 +605,6 @@ struct Misc {
   /* each producer warp's routing of its current layer: slot -> expert, U */
   int32_t pexp[MK_NP_WARPS][128];
   int32_t pU[MK_NP_WARPS];
-  int32_t prouted; /* last layer whose router logits producer warp 0 saw complete */
   int32_t norm_layer; /* layer whose normed input sits in xbuf (-2: none) */
   int32_t ok;         /* 0 once a consumer stopped early */
   int32_t route_layer; /* layer whose routing the consumers hold (-1: none) */
@@ -675,6 +685,43 @@ __device__ void raise_error(const mk_kparams &p, int code, int cta, int task, in
   atomicExch(&p.ctrl->abort, 1);
 }
 
+/* Polls the n <= 8 words at a[0], a[stride], ... (all loads of a round in
+ * flight at once) until each carries `tag`; payloads to v.  Bounded: false
+ * once the wait limit passes (recording MK_ERR_DEVICE_TIMEOUT with `op`,
+ * `layer`) or another CTA raised the abort flag. */
+__device__ bool poll_tagged(const mk_kparams &p, int cta, const uint64_t *a, int stride, int n,
+                            uint32_t tag, uint32_t *v, int op, int layer) {
+  uint64_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    if (i < n) w[i] = ld_tag(a + (size_t)i * stride);
+  uint64_t t0 = 0;
+  while (true) {
+    bool all = true;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (i < n && !tag_ok(w[i], tag)) all = false;
+    if (all) break;
+    if (!t0) {
+      t0 = gtimer();
+    } else if (gtimer() - t0 > p.wait_limit_ns) {
+      raise_error(p, MK_ERR_DEVICE_TIMEOUT, cta, -1, op, layer, -1, 0, (int)tag);
+      return false;
+    } else if (ld_volatile(&p.ctrl->abort)) {
+      return false;
+    }
+    __nanosleep(32);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (i < n && !tag_ok(w[i], tag)) w[i] = ld_tag(a + (size_t)i * stride);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    if (i < n) v[i] = (uint32_t)w[i];
+  return true;
+}
+
+
 /* Waits until (int)(*c - target) >= 0.  Called by all 32 lanes of a warp
  * together: lane 0 polls and broadcasts, and every lane sleeps between
  * polls, so the warp never sits split between a spinning lane and lanes
@@ -736,18 +783,17 @@ __device__ bool wait_mbar(const Ctx &cx, uint64_t *bar, uint32_t parity, int tas
  * counter), so no CTA computes it for the others and no result has to be
  * published and polled before the expert weights can be fetched.
  *
- * route_warp: one warp, the NT <= 8 tokens' selections interleaved so that
- * their reduction chains overlap.  Per token: K rounds of a warp argmax over
- * the E <= 128 fp32 logits (lane l holds experts l, l + 32, l + 64, l + 96),
- * ties to the lower expert id.  A round is two single-instruction warp
+ * route_warp: the batch's distinct chosen experts for a producer warp that
+ * needs them before its CTA's consumers take the routing (expert down rows
+ * in an OUT task).  One warp, the NT <= 8 tokens' selections interleaved so
+ * that their reduction chains overlap.  Per token: K rounds of a warp argmax
+ * over the E <= 128 fp32 logits (lane l holds experts l, l + 32, l + 64,
+ * l + 96), ties to the lower expert id -- the same selection as the
+ * consumers' rank count.  A round is two single-instruction warp
  * reductions: the largest of the lanes' best keys (an order-preserving
  * unsigned image of the float), then the lowest expert id among the lanes
- * holding it.  The weights are the softmax over the chosen logits (the
- * softmax over all E renormalised over the chosen k).  Then the distinct
- * experts of the batch in ascending id: expert[slot], *U, and -- if slot_w
- * is given -- the weight of each slot for each token (0 where the token did
- * not choose it).  publish (or NULL): the per-token ids and weights for the
- * diagnostics. */
+ * holding it.  Writes expert[slot] (ascending id) and *U; false on timeout
+ * or abort while waiting for the logits. */
 /* Unsigned keys in the order of the floats (-0 taken as +0, which compares
  * equal to it); 0 marks an expert out of the running. */
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -759,23 +805,26 @@ __device__ __forceinline__ float key_value(uint32_t k) {
 }
 
 template <int NT>
-__device__ void route_warp(const float *lg, int E, int B, int K, int lane, int32_t *expert,
-                           int32_t *U_out, float (*slot_w)[NT], mk_routing *publish) {
+__device__ bool route_warp(const mk_kparams &p, int cta, int layer, int lane, int32_t *expert,
+                           int32_t *U_out) {
+  const int E = p.E, B = p.B, K = p.K;
+  const uint64_t *lgt = p.lg_tag + (size_t)layer * MK_MAX_BATCH * E;
+  /* the logits as their router pieces write them (tagged words) */
+  const int n = max(0, min(4, (E - lane + 31) / 32));
   uint32_t key[NT][4];
-#pragma unroll
-  for (int t = 0; t < NT; ++t)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int e = lane + 32 * i;
-      key[t][i] = (t < B && e < E) ? order_key(__ldcg(lg + (size_t)t * E + e)) : 0u;
-    }
-  int pick[NT];
-  float pv[NT];
+  bool ok = true;
 #pragma unroll
   for (int t = 0; t < NT; ++t) {
-    pick[t] = 0;
-    pv[t] = NEG_INF;
+    uint32_t v[8];
+    if (ok && t < B && n > 0)
+      ok = poll_tagged(p, cta, lgt + (size_t)t * E + lane, 32, n, p.step_tag, v, OP_UP, layer);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) key[t][i] = (ok && t < B && i < n) ? order_key(__uint_as_float(v[i])) : 0u;
   }
+  if (!__all_sync(0xFFFFFFFFu, ok)) return false;
+  int pick[NT];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) pick[t] = 0;
   for (int k = 0; k < K; ++k) {
     uint32_t best[NT], bi[NT];
 #pragma unroll
@@ -801,10 +850,7 @@ __device__ void route_warp(const float *lg, int E, int B, int K, int lane, int32
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       if (win[t] == 0xFFFFFFFFu) continue; /* no expert left (rows of absent tokens) */
-      if (lane == k) {
-        pick[t] = (int)win[t];
-        pv[t] = key_value(top[t]);
-      }
+      if (lane == k) pick[t] = (int)win[t];
       if ((int)(win[t] & 31u) == lane) {
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -812,19 +858,11 @@ __device__ void route_warp(const float *lg, int E, int B, int K, int lane, int32
       }
     }
   }
-  /* weights: softmax over the chosen logits; the union of the chosen sets */
-  float w[NT];
+  /* the union of the chosen sets */
   uint32_t words[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-  for (int t = 0; t < NT; ++t) {
-    const float v0 = __shfl_sync(0xFFFFFFFFu, pv[t], 0);
-    const float ex = (lane < K && t < B) ? expf(pv[t] - v0) : 0.0f;
-    float z = ex;
-#pragma unroll
-    for (int s = 16; s >= 1; s >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, s);
-    w[t] = z > 0.0f ? ex / z : 0.0f;
+  for (int t = 0; t < NT; ++t)
     if (lane < K && t < B) words[pick[t] >> 5] |= 1u << (pick[t] & 31);
-  }
 #pragma unroll
   for (int i = 0; i < 4; ++i) words[i] = __reduce_or_sync(0xFFFFFFFFu, words[i]);
   const int U = __popc(words[0]) + __popc(words[1]) + __popc(words[2]) + __popc(words[3]);
@@ -841,24 +879,8 @@ __device__ void route_warp(const float *lg, int E, int B, int K, int lane, int32
     if ((words[i] >> lane) & 1u) expert[rank(e)] = e;
   }
   if (lane == 0) *U_out = U;
-  if (slot_w) {
-    for (int j = lane; j < U * NT; j += 32) slot_w[j / NT][j % NT] = 0.0f;
-    __syncwarp();
-#pragma unroll
-    for (int t = 0; t < NT; ++t)
-      if (lane < K && t < B) slot_w[rank(pick[t])][t] = w[t];
-  }
-  if (publish) {
-#pragma unroll
-    for (int t = 0; t < NT; ++t)
-      if (lane < K && t < B) {
-        publish->ids[t][lane] = pick[t];
-        publish->w[t][lane] = w[t];
-      }
-    for (int u = lane; u < U; u += 32) publish->expert[u] = expert[u];
-    if (lane == 0) publish->U = U;
-  }
   __syncwarp();
+  return true;
 }
 
 /* ============================================================== producer
@@ -896,7 +918,6 @@ struct Producer {
   QDesc *buf; /* this warp's MK_QBATCH planned descriptors (shared memory) */
   int32_t *pexp; /* this warp's slot -> expert list (shared memory) */
   int32_t *pU;
-  int32_t *prouted; /* shared: the last layer whose logits warp 0 saw complete */
   /* the consumers' routing in shared memory: its layer, U, slot -> expert */
   const int32_t *c_layer, *c_U, *c_expert;
   int r_layer;   /* layer of the routing in pexp (-1: none) */
@@ -906,62 +927,43 @@ struct Producer {
 
   /* The layer's routing for this warp's expert stages.  For a gate/up
    * share (from_consumers) it is the consumers' routing of the layer, which
-   * consumer warp 0 publishes in shared memory as soon as the consumers have
-   * taken it (they start the share right after the CTA's QKV task); it stays
-   * valid while a producer warp copies it, as the consumers cannot leave the
-   * share before every producer warp has issued its stages of it.  For
-   * expert down rows in an OUT task (whose consumers take the routing only
-   * after their attention splits) each producer warp takes the top-k itself
-   * once every router piece is in: producer warp 0 alone polls the global
-   * counter (hundreds of pollers on one line slow every poll and the router
-   * pieces' own signals) and passes the news on through a shared word.
-   * Returns U, or -1 on timeout / abort. */
+   * consumer thread 0 publishes in shared memory as soon as the consumers
+   * have taken it (they start the share right after the CTA's QKV task); it
+   * stays valid while a producer warp copies it, as the consumers cannot
+   * leave the share before every producer warp has issued its stages of it.
+   * For expert down rows in an OUT task (whose consumers take the routing
+   * only after their attention splits) the warp takes the top-k itself from
+   * the tagged logits.  Returns U, or -1 on timeout / abort. */
   __device__ int routed(int layer, bool from_consumers) {
     const mk_kparams &p = *cx.p;
     if (r_layer == layer) return *(volatile int32_t *)pU;
-    int32_t *c = lctr(p, layer, CTR_ROUTER_DONE);
-    const int target = (int)((cx.epoch + 1) * (uint32_t)p.n_router);
-    const uint64_t t0 = gtimer();
-    uint32_t spins = 0;
-    while (true) {
-      int seen = 0;
-      if (lane == 0) {
-        if (from_consumers) {
-          seen = ld_acquire_cta(c_layer) == layer;
-        } else if (k == 0) {
-          if ((int)(ld_relaxed(c) - target) >= 0) {
-            fence_acquire_gpu();
-            seen = 1;
-          }
-        } else {
-          seen = ld_acquire_cta(prouted) >= layer;
-        }
-      }
-      if (__shfl_sync(0xFFFFFFFFu, seen, 0)) break;
-      if ((++spins & 31) == 0) {
-        int stop = 0;
-        if (lane == 0) {
-          if (ld_volatile(&p.ctrl->abort)) {
-            stop = 1;
-          } else if (gtimer() - t0 > p.wait_limit_ns) {
-            raise_error(p, MK_ERR_DEVICE_TIMEOUT, cx.cta, -1, OP_UP, layer, CTR_ROUTER_DONE, -1,
-                        layer);
-            stop = 1;
-          }
-        }
-        if (__shfl_sync(0xFFFFFFFFu, stop, 0)) return -1;
-      }
-      __nanosleep(MK_PROD_SLEEP);
-    }
     if (from_consumers) {
+      const uint64_t t0 = gtimer();
+      uint32_t spins = 0;
+      while (true) {
+        const int seen = lane == 0 ? ld_acquire_cta(c_layer) == layer : 0;
+        if (__shfl_sync(0xFFFFFFFFu, seen, 0)) break;
+        if ((++spins & 31) == 0) {
+          int stop = 0;
+          if (lane == 0) {
+            if (ld_volatile(&p.ctrl->abort)) {
+              stop = 1;
+            } else if (gtimer() - t0 > p.wait_limit_ns) {
+              raise_error(p, MK_ERR_DEVICE_TIMEOUT, cx.cta, -1, OP_UP, layer, CTR_ROUTER_DONE,
+                          -1, layer);
+              stop = 1;
+            }
+          }
+          if (__shfl_sync(0xFFFFFFFFu, stop, 0)) return -1;
+        }
+        __nanosleep(20);
+      }
       const int U = *(volatile const int32_t *)c_U;
       for (int i = lane; i < U; i += 32) pexp[i] = c_expert[i];
       if (lane == 0) *pU = U;
       __syncwarp();
-    } else {
-      if (k == 0 && lane == 0) st_release_cta(prouted, layer);
-      route_warp<NB>(p.router_logits + (size_t)layer * MK_MAX_BATCH * p.E, p.E, p.B, p.K, lane,
-                     pexp, pU, nullptr, nullptr);
+    } else if (!route_warp<NB>(p, cx.cta, layer, lane, pexp, pU)) {
+      return -1;
     }
     r_layer = layer;
     return *(volatile int32_t *)pU;
@@ -1233,7 +1235,7 @@ struct Producer {
  * allocated apart from the consumers', with its state passed by value. */
 template <int NB>
 __device__ __noinline__ void produce(const Ctx cx, int k, int lane, QDesc *buf, int32_t *pexp,
-                                     int32_t *pU, int32_t *prouted, unsigned long long *strc,
+                                     int32_t *pU, unsigned long long *strc,
                                      const int32_t *row) {
   Producer<NB> pr;
   pr.cx = cx;
@@ -1243,7 +1245,6 @@ __device__ __noinline__ void produce(const Ctx cx, int k, int lane, QDesc *buf, 
   pr.buf = buf;
   pr.pexp = pexp;
   pr.pU = pU;
-  pr.prouted = prouted;
   {
     const Misc<NB> *m = (const Misc<NB> *)(mk_smem + cx.misc_off);
     pr.c_layer = &m->route_layer;
@@ -1386,13 +1387,14 @@ struct Consumer {
    * every addition's error), so the fp32 mean is the exact sum rounded once:
    * the same fp32 value in any summation order, hence the same normed input
    * as any other evaluation that rounds the exact mean once. */
-  __device__ void norm_into_xbuf(int layer_tag, const uint16_t *const *hrows, const uint16_t *g) {
+  __device__ bool norm_into_xbuf(int src, const uint16_t *g) {
     const mk_kparams &p = *cx.p;
-    const int xp = mk_x_pitch(p.d);
+    const int xp = mk_x_pitch(p.d), B = p.B;
     uint16_t *x = cx.xn();
     uint16_t *raw = (uint16_t *)cx.xbuf();
-    const int n8 = p.d / 8;
+    const int n8 = p.d / 8, dw = p.d / 2;
     float ss[NB], sh[NB], sl[NB];
+    bool fail = false;
     /* every load of the first pass (all tokens' h and this thread's first
      * piece of the gain) is issued before any is used: one round trip */
     const uint4 g_first = tid < n8 ? __ldg((const uint4 *)g + tid) : make_uint4(0, 0, 0, 0);
@@ -1400,9 +1402,49 @@ struct Consumer {
     for (int b = 0; b < NB; ++b) sh[b] = sl[b] = 0.0f;
     for (int i = tid; i < n8; i += NCT) {
       uint4 v[NB];
+      if (src == 0) {
 #pragma unroll
-      for (int b = 0; b < NB; ++b)
-        v[b] = b < p.B ? __ldcg((const uint4 *)hrows[b] + i) : make_uint4(0, 0, 0, 0);
+        for (int b = 0; b < NB; ++b)
+          v[b] = b < B ? __ldcg((const uint4 *)h_row(0, b) + i) : make_uint4(0, 0, 0, 0);
+      } else {
+        /* the residual as the OUT tasks write it: 4 tagged words (8 values)
+         * per token, polled until every word carries this step's tag */
+        const uint64_t *hw = p.h_tag + (size_t)src * MK_MAX_BATCH * dw + 4 * i;
+        uint64_t w[NB][4];
+#pragma unroll
+        for (int b = 0; b < NB; ++b)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) w[b][k] = b < B ? ld_tag(hw + (size_t)b * dw + k) : 0ULL;
+        uint64_t t0 = 0;
+        while (!fail) {
+          bool all = true;
+#pragma unroll
+          for (int b = 0; b < NB; ++b)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              if (b < B && !tag_ok(w[b][k], p.step_tag)) all = false;
+          if (all) break;
+          if (!t0) {
+            t0 = gtimer();
+          } else if (gtimer() - t0 > p.wait_limit_ns) {
+            raise_error(p, MK_ERR_DEVICE_TIMEOUT, cx.cta, -1, OP_QKV, src, -1, 0, (int)p.step_tag);
+            fail = true;
+          } else if (ld_volatile(&p.ctrl->abort)) {
+            fail = true;
+          }
+          __nanosleep(32);
+#pragma unroll
+          for (int b = 0; b < NB; ++b)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              if (b < B && !tag_ok(w[b][k], p.step_tag)) w[b][k] = ld_tag(hw + (size_t)b * dw + k);
+        }
+#pragma unroll
+        for (int b = 0; b < NB; ++b)
+          v[b] = b < B ? make_uint4((uint32_t)w[b][0], (uint32_t)w[b][1], (uint32_t)w[b][2],
+                                    (uint32_t)w[b][3])
+                       : make_uint4(0, 0, 0, 0);
+      }
 #pragma unroll
       for (int b = 0; b < NB; ++b) {
         *(uint4 *)(raw + (size_t)b * p.d + 8 * i) = v[b];
@@ -1418,7 +1460,7 @@ struct Consumer {
       const float r = 1.0f / sqrtf(ss[b] / (float)p.d + p.eps);
       for (int i = tid; i < n8; i += NCT) {
         uint16_t o[8];
-        if (b < p.B) {
+        if (b < B) {
           float hf[8], gf[8];
           unpack8(*(const uint4 *)(raw + (size_t)b * p.d + 8 * i), hf);
           unpack8(i == tid ? g_first : __ldg((const uint4 *)g + i), gf);
@@ -1433,18 +1475,18 @@ struct Consumer {
                        pack_bf16(o[6], o[7]));
       }
     }
-    if (tid == 0) M()->norm_layer = layer_tag;
-    bar_consumers();
+    if (tid == 0) M()->norm_layer = src;
+    return !bar_any(fail);
   }
 
-  __device__ void ensure_norm(int layer) {
-    if (*(volatile int32_t *)&M()->norm_layer == layer) return;
+  /* The normed input of `layer` in xn (computed unless it is there already);
+   * false on timeout / abort. */
+  __device__ bool ensure_norm(int layer) {
+    if (*(volatile int32_t *)&M()->norm_layer == layer) return true;
     bar_consumers(); /* everyone has read the tag before it can change */
-    const uint16_t *hr[NB];
-#pragma unroll
-    for (int b = 0; b < NB; ++b) hr[b] = b < cx.p->B ? h_row(layer, b) : nullptr;
-    norm_into_xbuf(layer, hr, lnorm(*cx.p, layer));
+    const bool ok = norm_into_xbuf(layer, lnorm(*cx.p, layer));
     if (tr && tid == 0) t_mark = gtimer();
+    return ok;
   }
 
   /* Copies NB vectors of n bf16 (global, row stride gstride) into xbuf at
@@ -1525,17 +1567,15 @@ struct Consumer {
    * rows (bf16 outputs). */
   __device__ bool op_qkv(const int32_t *t, int task, int layer) {
     const mk_kparams &p = *cx.p;
-    if (layer > 0 && !cwait(lctr(p, layer - 1, CTR_OUT_DONE), (int)((cx.epoch + 1) * p.n_out),
-                            task, OP_QKV, layer, CTR_OUT_DONE))
-      return false;
-    ensure_norm(layer);
+    /* the layer's input: the previous layer's OUT tasks' tagged residual */
+    if (!ensure_norm(layer)) return false;
     const int QKVD = (p.Hq + 2 * p.Hkv) * p.D;
     const int base = (t[1] == 0 ? 0 : t[1] == 1 ? p.Hq * p.D : (p.Hq + p.Hkv) * p.D) + t[2];
     uint16_t *out = p.qkv + (size_t)layer * MK_MAX_BATCH * QKVD;
     const int B = p.B, E = p.E, d = p.d, e0 = t[4], rn = t[5], nrows = t[3];
     float *lg = p.router_logits + (size_t)layer * MK_MAX_BATCH * E;
+    uint64_t *lgt = p.lg_tag + (size_t)layer * MK_MAX_BATCH * E;
     const float *bias = layer < MK_PARAM_LAYERS ? p.l_bias[layer] : p.layers[layer].bias;
-    int32_t *rctr = lctr(p, layer, CTR_ROUTER_DONE);
     const int rps = mk_rows_per_stage(d, cx.SB);
     const int n_rst = (rn + rps - 1) / rps, n_st = n_rst + (nrows + rps - 1) / rps;
     const uint16_t *x = cx.xn();
@@ -1546,13 +1586,13 @@ struct Consumer {
         const int r0 = j * rps, cnt = min(rps, rn - r0);
         gemv_stage(st, cnt, d, x, [&](int r, int b, float v) {
           const int e = e0 + r0 + r;
-          if (b < B) lg[(size_t)b * E + e] = bias ? v + __ldg(bias + e) : v;
+          if (b < B) {
+            const float l = bias ? v + __ldg(bias + e) : v;
+            lg[(size_t)b * E + e] = l; /* for the diagnostics */
+            st_tag(lgt + (size_t)b * E + e, __float_as_uint(l), p.step_tag);
+          }
         });
-        stage_release(si + j); /* ends with __syncwarp: the warp's logits are written */
-        if (lane == 0) {
-          __threadfence();
-          red_release_add(rctr, cnt);
-        }
+        stage_release(si + j);
       } else {
         const int r0 = (j - n_rst) * rps, cnt = min(rps, nrows - r0);
         gemv_stage(st, cnt, d, x, [&](int r, int b, float v) {
@@ -1576,19 +1616,32 @@ struct Consumer {
    * distinct experts get the slots in ascending id.  Writes route_expert,
    * route_U and route_w, and the diagnostics record when publish is set.
    * Uses the scratch buffer; ends with a consumer barrier. */
-  __device__ void route_block(const float *lg, mk_routing *publish) {
+  __device__ bool route_block(int layer, mk_routing *publish) {
     const mk_kparams &p = *cx.p;
     Misc<NB> *m = M();
     const int E = p.E, B = p.B, K = p.K, E4 = (E + 3) & ~3;
+    const uint64_t *lgt = p.lg_tag + (size_t)layer * MK_MAX_BATCH * E;
     uint32_t *key = (uint32_t *)cx.xbuf();                  /* [NB][128] */
     int32_t *pick = (int32_t *)(key + NB * 128);             /* [NB][MK_MAX_TOPK] */
     uint32_t *flag = (uint32_t *)(pick + NB * MK_MAX_TOPK);  /* [128]: chosen by a token */
-    for (int i = tid; i < NB * 128; i += NCT) {
-      const int t = i >> 7, e = i & 127;
-      key[i] = (t < B && e < E) ? order_key(__ldcg(lg + (size_t)t * E + e)) : 0u;
+    /* the logits as their router pieces write them: thread i polls the
+     * words (t, e) = i, i + 256, ... (all in flight at once) */
+    static_assert(NB * 128 <= 4 * NCT, "four logit words per thread at most");
+    bool fail = false;
+    {
+      const int t0 = tid >> 7, e = tid & 127, n = (B - t0 + 1) / 2;
+      uint32_t v[8];
+      if (e < E && n > 0)
+        fail = !poll_tagged(p, cx.cta, lgt + (size_t)t0 * E + e, 2 * E, n, p.step_tag, v, OP_UP,
+                            layer);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int t = t0 + 2 * k;
+        if (t < NB) key[t * 128 + e] = (!fail && k < n && e < E) ? order_key(__uint_as_float(v[k])) : 0u;
+      }
     }
     for (int i = tid; i < 128; i += NCT) flag[i] = 0u;
-    bar_consumers();
+    if (bar_any(fail)) return false;
     for (int i = tid; i < NB * 128; i += NCT) {
       const int t = i >> 7, e = i & 127;
       if (t >= B || e >= E) continue;
@@ -1652,6 +1705,7 @@ struct Consumer {
       }
     }
     bar_consumers();
+    return true;
   }
 
   /* The layer's routing in shared memory (route_expert, route_w, route_U),
@@ -1665,11 +1719,8 @@ struct Consumer {
     Misc<NB> *m = M();
     if (*(volatile int32_t *)&m->route_layer == layer) return true;
     bar_consumers(); /* everyone has read the tag before it can change */
-    if (!cwait(lctr(p, layer, CTR_ROUTER_DONE), (int)((cx.epoch + 1) * (uint32_t)p.n_router),
-               task, op, layer, CTR_ROUTER_DONE))
-      return false;
-    route_block(p.router_logits + (size_t)layer * MK_MAX_BATCH * p.E,
-                cx.cta == 0 ? p.routing + layer : nullptr);
+    if (tr && tid == 0 && !t_ready) t_ready = gtimer();
+    if (!route_block(layer, cx.cta == 0 ? p.routing + layer : nullptr)) return false;
     if (tid == 0) {
       if (cx.cta == 0) atomicAdd(&p.ctrl->sum_experts, (unsigned long long)m->route_U);
       if (tr && !t_mark) t_mark = gtimer();
@@ -2008,10 +2059,11 @@ struct Consumer {
     }
     /* warp 0 holds this split's partial: per head [m, l, -, -, o[D]] */
     const int PS = D + 4;
-    /* one layer's slots serve every layer: a layer's partials are merged
-     * before its attention-done count completes, which every later layer
-     * waits for */
-    float *part = p.attn_part + (size_t)t[5] * G * PS;
+    /* the split partials by layer parity: the next layer's splits never
+     * overwrite slots this layer's merges still read (two layers apart, the
+     * attention-done count of the layer between orders them) */
+    const size_t par = (size_t)(layer & 1) * p.n_slots * G * PS;
+    float *part = p.attn_part + par + (size_t)t[5] * G * PS;
     if (warp == 0 && g < G) {
       if (tq == 0) {
         part[(size_t)g * PS] = m_run;
@@ -2028,8 +2080,8 @@ struct Consumer {
     const int ng = t[11], bh = b * p.Hkv + kvh;
     const int tk0 = CTR_ATTN_TICKET0 + bh * (1 + MK_MAX_MERGE_GROUPS);
     uint16_t *ob = p.o + ((size_t)layer * MK_MAX_BATCH + b) * p.Hq * D + (size_t)kvh * G * D;
-    const float *part1 = p.attn_part;
-    float *part2 = p.attn_part2;
+    const float *part1 = p.attn_part + par;
+    float *part2 = p.attn_part2 + par;
     if (ng <= 1) {
       if (!ticket(lctr(p, layer, tk0), t[7])) return true;
       merge_parts(part1 + (size_t)t[6] * G * PS, t[7], G, D, nullptr, ob);
@@ -2057,7 +2109,7 @@ struct Consumer {
   __device__ bool op_up_fold(const int32_t *t, int task, int layer) {
     const mk_kparams &p = *cx.p;
     if (!route_local(layer, task, OP_UP)) return false;
-    ensure_norm(layer);
+    if (!ensure_norm(layer)) return false;
     const int U = M()->route_U, d = p.d;
     const int nbf = p.F / MK_FOLD_COLS, T64 = U * nbf;
     const int b0 = (int)((int64_t)T64 * t[1] / t[2]);
@@ -2102,7 +2154,7 @@ struct Consumer {
       }
       /* box row r: 128 bytes, 16-byte chunk c stored at (c ^ (r & 7)) */
       const uint32_t sb = saddr(st);
-      float *part = p.moe_part + (size_t)(b0 + kb) * d + r0;
+      float *part = p.moe_part + (size_t)(layer & 1) * p.moe_part_stride + (size_t)(b0 + kb) * d + r0;
       for (int r = lane; r < BR; r += 32) {
         unsigned long long acc0 = 0ULL, acc1 = 0ULL;
 #pragma unroll
@@ -2130,7 +2182,7 @@ struct Consumer {
     const mk_kparams &p = *cx.p;
     if (NB == 1 && p.fold) return op_up_fold(t, task, layer);
     if (!route_local(layer, task, OP_UP)) return false;
-    ensure_norm(layer);
+    if (!ensure_norm(layer)) return false;
     const int U = M()->route_U;
     const int d = p.d, F = p.F, B = p.B;
     const int64_t T = (int64_t)U * F;
@@ -2208,14 +2260,27 @@ struct Consumer {
     if (!route_local(layer, task, OP_OUT)) return false;
     const int U = M()->route_U;
     const float(*slot_w)[NB] = M()->route_w;
+    bool hfail = false;
     for (int i = tid; i < nr * B; i += NCT) {
       const int r = i / B, bb = i % B;
-      O.hres[r][bb] = bf2f(__ldcg(h_row(layer, bb) + r0 + r));
+      if (layer == 0) {
+        O.hres[r][bb] = bf2f(__ldcg(h_row(0, bb) + r0 + r));
+      } else {
+        /* the tagged residual (its words are valid by now: this CTA's norm
+         * saw them, or the poll waits for them) */
+        uint32_t w;
+        if (!poll_tagged(p, cx.cta,
+                         p.h_tag + ((size_t)layer * MK_MAX_BATCH + bb) * (d / 2) + (r0 + r) / 2, 1,
+                         1, p.step_tag, &w, OP_OUT, layer))
+          hfail = true;
+        O.hres[r][bb] = bf2f((uint16_t)(((r0 + r) & 1) ? (w >> 16) : (w & 0xFFFFu)));
+      }
     }
     uint16_t *x = (uint16_t *)cx.xbuf();
     for (int i = tid; i < NC * MK_MAX_OUT_ROWS * NB; i += NCT) (&O.acc_w[0][0][0])[i] = 0.0f;
     /* the experts' down rows first: their activations are complete once
      * every gate/up share is, normally before the attention output */
+    if (bar_any(hfail)) return false;
     if (!cwait(lctr(p, layer, CTR_UP_DONE), (int)((cx.epoch + 1) * p.n_up), task, OP_OUT, layer,
                CTR_UP_DONE))
       return false;
@@ -2234,7 +2299,7 @@ struct Consumer {
       constexpr int BAT = 16;
       float s = 0.0f;
       if (lane < nr) {
-        const float *src = p.moe_part + r0 + lane;
+        const float *src = p.moe_part + (size_t)(layer & 1) * p.moe_part_stride + r0 + lane;
         for (int b0 = warp; b0 < T64; b0 += BAT * NC) {
           float v[BAT];
 #pragma unroll
@@ -2304,23 +2369,31 @@ struct Consumer {
     bar_consumers();
     gemv_rows(nr, HqD, xo, task, OP_OUT, layer, [&](int r, int bb, float v) { O.acc_o[r][bb] = v; });
     if (!task_end()) return false;
-    for (int i = tid; i < nr * B; i += NCT) {
-      const int r = i / B, bb = i % B;
-      const float hv = O.hres[r][bb];
-      const uint16_t at = f2bf(O.acc_o[r][bb]);
-      float mo = 0.0f;
+    /* the residual entering the next layer, a pair of rows per thread: one
+     * tagged word for the next layer's readers, plain copies (and the two
+     * terms) for the diagnostics.  r0 and nr are even. */
+    for (int i = tid; i < (nr / 2) * B; i += NCT) {
+      const int r = 2 * (i / B), bb = i % B;
+      uint16_t hn[2];
 #pragma unroll
-      for (int w = 0; w < NC; ++w) mo += O.acc_w[w][r][bb];
-      const uint16_t mb = f2bf(mo);
-      p.h[((size_t)(layer + 1) * MK_MAX_BATCH + bb) * d + r0 + r] =
-          f2bf(__fadd_rn(__fadd_rn(hv, bf2f(at)), bf2f(mb)));
-      uint16_t *am = p.am + ((size_t)layer * 2 * MK_MAX_BATCH + bb) * d + r0 + r;
-      am[0] = at;
-      am[(size_t)MK_MAX_BATCH * d] = mb;
-      if (layer == 0) p.h[(size_t)bb * d + r0 + r] = f2bf(hv);
+      for (int q = 0; q < 2; ++q) {
+        const float hv = O.hres[r + q][bb];
+        const uint16_t at = f2bf(O.acc_o[r + q][bb]);
+        float mo = 0.0f;
+#pragma unroll
+        for (int w = 0; w < NC; ++w) mo += O.acc_w[w][r + q][bb];
+        const uint16_t mb = f2bf(mo);
+        hn[q] = f2bf(__fadd_rn(__fadd_rn(hv, bf2f(at)), bf2f(mb)));
+        p.h[((size_t)(layer + 1) * MK_MAX_BATCH + bb) * d + r0 + r + q] = hn[q];
+        uint16_t *am = p.am + ((size_t)layer * 2 * MK_MAX_BATCH + bb) * d + r0 + r + q;
+        am[0] = at;
+        am[(size_t)MK_MAX_BATCH * d] = mb;
+        if (layer == 0) p.h[(size_t)bb * d + r0 + r + q] = f2bf(hv);
+      }
+      st_tag(p.h_tag + ((size_t)(layer + 1) * MK_MAX_BATCH + bb) * (d / 2) + (r0 + r) / 2,
+             (uint32_t)hn[0] | ((uint32_t)hn[1] << 16), p.step_tag);
     }
-    bar_consumers();
-    signal(lctr(p, layer, CTR_OUT_DONE));
+    bar_consumers(); /* the out union is read before the next task reuses it */
     return true;
   }
 
@@ -2328,16 +2401,10 @@ struct Consumer {
   __device__ bool op_lm(const int32_t *t, int task) {
     const mk_kparams &p = *cx.p;
     const int L = p.L, B = p.B;
-    if (!cwait(lctr(p, L - 1, CTR_OUT_DONE), (int)((cx.epoch + 1) * p.n_out), task, OP_LM, L,
-               CTR_OUT_DONE))
-      return false;
+    /* the final residual (tagged, as the last OUT tasks write it) */
     if (*(volatile int32_t *)&M()->norm_layer != L) {
       bar_consumers();
-      const uint16_t *hr[NB];
-#pragma unroll
-      for (int bb = 0; bb < NB; ++bb)
-        hr[bb] = bb < B ? p.h + ((size_t)L * MK_MAX_BATCH + bb) * p.d : nullptr;
-      norm_into_xbuf(L, hr, p.final_norm);
+      if (!norm_into_xbuf(L, p.final_norm)) return false;
     }
     const int v0 = t[2];
     /* each lane keeps the best of the rows it computed for its two tokens
@@ -2486,7 +2553,6 @@ __global__ void __launch_bounds__(MK_THREADS, 1) decode_kernel(const __grid_cons
     }
     misc->norm_layer = -2;
     misc->route_layer = -1;
-    misc->prouted = -1;
     misc->ok = 1;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -2513,7 +2579,7 @@ __global__ void __launch_bounds__(MK_THREADS, 1) decode_kernel(const __grid_cons
   if (header_ok) {
     if (warp >= NC) {
       produce<NB>(cx, warp - NC, lane, misc->qd[warp - NC], misc->pexp[warp - NC],
-                  &misc->pU[warp - NC], &misc->prouted,
+                  &misc->pU[warp - NC],
                   (int)blockIdx.x == p.stage_trace_cta ? p.stage_trace : nullptr, row);
     } else {
       Consumer<NB> c;

@@ -31,6 +31,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstddef>
 #include <cstdint>
@@ -146,8 +147,8 @@ extern "C" mk_status mk_decode_step_static(const mk_model_dims *dims, const mk_w
   const size_t o_qkv = take((size_t)Lyr * MB * QKVD * 2);
   const size_t o_o = take((size_t)Lyr * MB * HqD * 2);
   const size_t o_am = take((size_t)Lyr * 2 * MB * d.d_model * 2);
-  const size_t o_part = take((size_t)n_slots * G * (d.head_dim + 4) * 4);
-  const size_t o_part2 = take((size_t)n_slots * G * (d.head_dim + 4) * 4);
+  const size_t o_part = take((size_t)2 * n_slots * G * (d.head_dim + 4) * 4);
+  const size_t o_part2 = take((size_t)2 * n_slots * G * (d.head_dim + 4) * 4);
   const size_t o_rl = take((size_t)Lyr * MB * d.n_experts * 4);
   const size_t o_rt = take((size_t)Lyr * sizeof(mk_routing));
   const size_t o_act = take((size_t)Lyr * u_max * MB * d.d_ffn * 2);
@@ -161,8 +162,10 @@ extern "C" mk_status mk_decode_step_static(const mk_model_dims *dims, const mk_w
   const size_t o_tab = take(plan.table.size() * sizeof(int32_t));
   const size_t o_maps = take((size_t)Lyr * 2 * 128);
   const size_t o_wdm = take((size_t)Lyr * 128);
-  const size_t o_mp =
-      take((size_t)std::min(d.n_experts, d.top_k) * (d.d_ffn / MK_FOLD_COLS) * d.d_model * 4);
+  const int moe_stride = std::min(d.n_experts, d.top_k) * (d.d_ffn / MK_FOLD_COLS) * d.d_model;
+  const size_t o_mp = take((size_t)2 * moe_stride * 4);
+  const size_t o_htag = take((size_t)(Lyr + 1) * MB * (d.d_model / 2) * 8);
+  const size_t o_lgtag = take((size_t)Lyr * MB * d.n_experts * 8);
   if (off > MK_STATIC_SCRATCH_BYTES) return MK_ERR_SCRATCH_LIMIT;
 
   /* ---- shared memory plan (as for mk_decode_step) ---- */
@@ -232,6 +235,9 @@ extern "C" mk_status mk_decode_step_static(const mk_model_dims *dims, const mk_w
 
   /* pageable sources: each copy returns once the host data is consumed */
   cudaError_t e = cudaMemsetAsync(base + o_ctr, 0, n_ctr * 4, stream);
+  /* the tagged words: another call may have left any bytes there */
+  if (e == cudaSuccess) e = cudaMemsetAsync(base + o_htag, 0, o_lgtag - o_htag, stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(base + o_lgtag, 0, (size_t)Lyr * MB * d.n_experts * 8, stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(base + o_ctrl, 0, sizeof(mk_ctrl), stream);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(base + o_ly, layers.data(), Lyr * sizeof(mk_layer_dev),
@@ -315,6 +321,16 @@ extern "C" mk_status mk_decode_step_static(const mk_model_dims *dims, const mk_w
   p.fold = plan.fold;
   p.fold_rows = fold_rows;
   p.moe_part = (float *)(base + o_mp);
+  p.moe_part_stride = moe_stride;
+  p.h_tag = (uint64_t *)(base + o_htag);
+  p.lg_tag = (uint64_t *)(base + o_lgtag);
+  {
+    /* a tag no earlier call used on this scratch (it starts zeroed) */
+    static std::atomic<uint32_t> serial{0};
+    uint32_t t = serial.fetch_add(1u) + 1u;
+    if (t == 0u) t = serial.fetch_add(1u) + 1u;
+    p.step_tag = t;
+  }
   p.wd_maps = base + o_wdm;
   p.poison_layer = -1;
   p.poison_delta = 0;

@@ -393,13 +393,15 @@ mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int
     p.n_up = n;
   }
 
-  /* OUT: rows of d. */
+  /* OUT: rows of d, in units of 8 rows (the residual is published as
+   * tagged pairs of rows). */
   {
-    int n = std::min(n_cta, d.d_model);
-    if (ceil_div(d.d_model, n) > MK_MAX_OUT_ROWS) n = (int)ceil_div(d.d_model, MK_MAX_OUT_ROWS);
+    const int u8 = d.d_model / 8;
+    int n = std::min(n_cta, u8);
+    if (ceil_div(u8, n) * 8 > MK_MAX_OUT_ROWS) n = (int)ceil_div(u8, MK_MAX_OUT_ROWS / 8);
     for (int i = 0; i < n; ++i) {
       Desc t = desc(OP_OUT);
-      const int a = (int)((int64_t)d.d_model * i / n), b = (int)((int64_t)d.d_model * (i + 1) / n);
+      const int a = 8 * (int)((int64_t)u8 * i / n), b = 8 * (int)((int64_t)u8 * (i + 1) / n);
       t[2] = a;
       t[3] = b - a;
       out_t[i % n_cta].push_back(t);
