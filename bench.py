@@ -40,6 +40,18 @@ METRIC = "decode tok/s at batch 1/8 and % of HBM speed-of-light (bytes/step ÷ p
 PEAK_FALLBACK_GBS = 6800.0
 
 
+HEADLINE_WORKLOAD = ("full-scale synthetic MoE, batch 1 at 8192 cached tokens (48 layers, d 2048, "
+                     "32/4 heads x 128, 128 experts top-8, F 768, vocab 152064)")
+
+
+def headline_config(lens, steps, world=1):
+    """The config dict of the headline line (both arms print the same one)."""
+    return {"workload": HEADLINE_WORKLOAD, "batch": len(lens), "cached_tokens": list(lens),
+            "decode_steps": steps,
+            "l2": "inputs larger than L2 (6.9 GB streamed per step), no flush",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -253,6 +265,7 @@ def run_mk(args, rank, world):
             json.dump(trace_summary, f, indent=1)
         mk.mk_set_trace(dec.ctx, 0)
     dec.close()
+    weights = {n: inp.tensors[n] for n in synth.weight_specs(dims)}
     del inp
 
     out = {
@@ -260,12 +273,7 @@ def run_mk(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded bf16 N(0,0.02) weights, N(0,1) KV; no trained weights)",
-        "config": {"workload": "full-scale synthetic MoE, batch 1 at 8192 cached tokens "
-                               "(48 layers, d 2048, 32/4 heads x 128, 128 experts top-8, "
-                               "F 768, vocab 152064)",
-                   "batch": B, "cached_tokens": lens, "decode_steps": args.steps,
-                   "l2": "inputs larger than L2 (6.9 GB streamed per step), no flush",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "config": headline_config(lens, args.steps, world),
         "sol": {"bytes_per_step": round(bytes_per_step), "weight_bytes_per_step":
                 round(w_bytes / args.steps), "kv_bytes_per_step": round(kv_bytes / args.steps),
                 "sol_tok_s": round(sol_tok_s, 1), "fraction": round(tok_s / world / sol_tok_s, 4),
@@ -284,14 +292,16 @@ def run_mk(args, rank, world):
         out["trace"] = {k: trace_summary[k] for k in ("step_us", "layer_us_median", "cta_time_split")}
     batches = [int(x) for x in args.batches.split(",") if x.strip()]
     if batches and world == 1 and not args.layers:
-        out["batches"] = batch_sweep(dims, dev, stream, batches)
+        out["batches"] = batch_sweep(dims, dev, stream, batches, weights)
+    if args.workloads and world == 1 and not args.layers:
+        out["workloads"] = other_workloads(dev, stream, weights, args.workloads.split(","))
     return out
 
 
-def batch_sweep(dims, dev, stream, batches, steps=16, warmup=4):
+def batch_sweep(dims, dev, stream, batches, weights, steps=64, warmup=4):
     """Decode tok/s and speed-of-light fraction of the same full-scale model
-    at other batch sizes, every sequence at 8192 cached tokens (short
-    CUDA-event-timed runs after the headline measurement)."""
+    at other batch sizes, every sequence at 8192 cached tokens (CUDA-event
+    timed runs after the headline measurement)."""
     import torch
 
     import persistent_moe_decode_sm_gb300 as mk
@@ -300,7 +310,7 @@ def batch_sweep(dims, dev, stream, batches, steps=16, warmup=4):
     if not batches:
         return []
     lens_all = [8192] * max(batches)
-    inp = synth.device_inputs(dims, lens_all, warmup + steps + 8, None, seed=0)
+    inp = synth.device_inputs(dims, lens_all, warmup + steps + 8, None, seed=0, weights=weights)
     pl = inp.layout
     peak, _ = load_peaks()
     res = []
@@ -340,6 +350,129 @@ def batch_sweep(dims, dev, stream, batches, steps=16, warmup=4):
                     "steps": steps, "warmup": warmup})
         dec.close()
     del inp
+    return res
+
+
+def timed_decode(dec, dims, dev, stream, lens0, tokens0, steps, warmup, events=(), spare=None):
+    """Greedy decode: `warmup` untimed steps, then `steps` steps between two
+    CUDA events.  events: (step, slot) replacements inside the timed region
+    (continuous batching): the slot takes the next spare sequence (length,
+    page row, first token) and the schedule is rebuilt -- host work that the
+    events' interval includes.  Returns (ms, sum of U over the timed steps,
+    KV bytes read over the timed steps, replacements done)."""
+    import numpy as np
+    import torch
+
+    B = len(lens0)
+    lens = list(lens0)
+    pt = np.array(spare["page_rows"][:B], copy=True) if spare else None
+    tok = [torch.tensor(tokens0, dtype=torch.int32, device=dev),
+           torch.zeros(B, dtype=torch.int32, device=dev)]
+    logits = torch.empty(B, dims.vocab, dtype=torch.float32, device=dev)
+    cur = 0
+    for _ in range(warmup):
+        dec.decode_step(tok[cur], logits, tok[cur ^ 1])
+        cur ^= 1
+        lens = [L + 1 for L in lens]
+    dec.sync()
+    st0 = dec.stats()
+    ev = sorted(events)
+    at, used, kv = 0, 0, 0.0
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for k in range(steps):
+        changed = False
+        while at < len(ev) and ev[at][0] == k:
+            slot = ev[at][1]
+            j = B + used
+            lens[slot] = spare["lens"][j]
+            pt[slot] = spare["page_rows"][j]
+            tok[cur][slot] = int(spare["tokens"][used])
+            used += 1
+            at += 1
+            changed = True
+        if changed:
+            dec.build_schedule(lens, pt)
+        kv += kv_bytes_step(dims, lens)
+        dec.decode_step(tok[cur], logits, tok[cur ^ 1])
+        cur ^= 1
+        lens = [L + 1 for L in lens]
+    b.record(stream)
+    torch.cuda.synchronize()
+    dec.sync()
+    return a.elapsed_time(b), float(dec.stats().sum_experts - st0.sum_experts), kv, used
+
+
+def other_workloads(dev, stream, weights, names):
+    """The other workloads, each on its own KV pool (the full-scale ones
+    reuse the headline's weights):
+      mid: the 8-layer mid model, batch 1 at 2048 cached tokens, 128 steps
+           (its 225 MB partly fit L2, so its SOL fraction is informational);
+      full_b8: batch 8, ragged U[1024, 16384] contexts, Zipf(1.1) router
+           bias, 256 steps with continuous batching: each slot's sequence
+           has a budget ~U[16, 128] steps, then the slot takes a fresh
+           sequence (fresh context and KV pages) and the schedule is
+           rebuilt inside the timed region;
+      long_b1 / long_b2: 262144 cached tokens at batch 1, 131072 at batch 2,
+           64 steps."""
+    import numpy as np
+    import torch
+
+    import persistent_moe_decode_sm_gb300 as mk
+    import synth
+
+    peak, _ = load_peaks()
+    wl = synth.workloads()
+    res = {}
+    for name in names:
+        name = name.strip()
+        if name not in wl or name in ("full", "tiny"):
+            continue
+        w = wl[name]
+        dims = w.dims
+        lens0 = list(w.seq_lens)
+        B = len(lens0)
+        steps = w.steps
+        warmup = 4
+        events, spare = (), None
+        layout_lens = list(lens0)
+        if name == "full_b8":
+            events = synth.replacement_events(0, B, steps)
+            spare_lens = synth.ragged_lens(0, len(events), 1024, 16384, gen=1)
+            layout_lens = lens0 + spare_lens
+        inp = synth.device_inputs(dims, layout_lens, warmup + steps + 8, w.zipf_s, seed=0,
+                                  weights=weights if dims == synth.FULL else None)
+        pl = inp.layout
+        if events:
+            spare = {"lens": layout_lens, "page_rows": pl.page_tables,
+                     "tokens": synth.first_tokens(dims, len(events), gen=1)}
+        dec = mk.Decoder(dims, inp.tensors, pl.num_pages, pl.max_pages, B, inp.bias_tensors,
+                         stream)
+        dec.build_schedule(lens0, pl.page_tables[:B])
+        ms, sum_u, kv, n_rep = timed_decode(dec, dims, dev, stream, lens0,
+                                            synth.first_tokens(dims, B), steps, warmup, events,
+                                            spare)
+        dec.close()
+        del inp
+        torch.cuda.empty_cache()
+        wb = steps * weight_bytes_step(dims, 0.0, B) + 2.0 * sum_u * 3 * dims.d_model * dims.d_ffn
+        per_step = (wb + kv) / steps
+        tok_s = B * steps / (ms / 1e3)
+        sol = sol_formula(per_step, peak, B)
+        r = {"batch": B, "cached_tokens": lens0 if B <= 2 else "ragged U[1024, 16384]",
+             "steps": steps, "warmup": warmup, "tok_s": round(tok_s, 2),
+             "ms_per_step": round(ms / steps, 4), "bytes_per_step": round(per_step),
+             "bytes_basis": "active weights from the observed routing + KV read",
+             "sol_tok_s": round(sol, 1), "sol_fraction": round(tok_s / sol, 4)}
+        if name == "mid":
+            r["sol_informational"] = "225 MB per step, partly L2-resident"
+        if events:
+            r["replacements"] = n_rep
+            r["router_bias"] = "Zipf(1.1) per expert"
+            r["schedule_rebuilds_in_timed_region"] = True
+        res[name] = r
     return res
 
 
@@ -394,7 +527,7 @@ def run_reference(args):
             "ms_per_step": round(1e3 * sum(times) / len(times), 1), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32-accumulate over bf16",
             "data": "synthetic",
-            "config": {"workload": "full-scale synthetic MoE, batch 1 at 8192 cached tokens"},
+            "config": headline_config([8192], max(1, args.steps)),
             "cpu_baseline": cb,
             "e2e": {"value": round(v, 4), "unit": "tok/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -414,6 +547,8 @@ def main():
     ap.add_argument("--trace-cta", type=int, default=0,
                     help="the CTA whose ring stages the trace records")
     ap.add_argument("--trace-raw", default="", help="also save the raw trace (npz) here")
+    ap.add_argument("--workloads", default="mid,full_b8,long_b1,long_b2",
+                    help="also time these workloads ('' to skip)")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: cut the model to its first N layers")
     args = ap.parse_args()

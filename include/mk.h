@@ -93,7 +93,10 @@ typedef struct {
 
 typedef struct mk_ctx mk_ctx;
 
-/* Validates dims and pointers, queries the device, allocates the workspace.
+/* The model and its paged KV cache ("Cohere speeds up North Mini Code with
+ * new megakernel", paragraphs 1 and 3: a BF16 MoE model, paged attention,
+ * ragged sequence lengths).
+ * Validates dims and pointers, queries the device, allocates the workspace.
  * stream: a cudaStream_t (NULL = legacy default stream).  Supported: head_dim
  * in {32, 64, 128}; n_q_heads / n_kv_heads <= 8; top_k <= 16; n_experts <=
  * 128; d_model, d_ffn and n_q_heads*head_dim multiples of 64; max_batch <= 8.
@@ -101,7 +104,11 @@ typedef struct mk_ctx mk_ctx;
  * MK_ERR_CUDA; *out is set only on MK_OK. */
 mk_status mk_create(const mk_model_dims *dims, const mk_weights *w, void *stream, mk_ctx **out);
 
-/* Builds the task table for `batch` sequences: seq_lens (HOST [batch]) =
+/* The host-built task table ("Cohere Packs the Entire Decoding Step Into a
+ * Single CUDA Megakernel", paragraph 2: GEMM tiles and attention splits
+ * assigned to the SMs in advance; continuous batching: "Cohere speeds up
+ * North Mini Code with new megakernel", paragraph 3).
+ * Builds the task table for `batch` sequences: seq_lens (HOST [batch]) =
  * cached tokens L_b before the next step; page_tables (HOST
  * [batch][max_pages_per_seq]) = physical page ids, -1 where unallocated.
  * Copies both to the device, resets the counters, uploads the table.
@@ -109,7 +116,11 @@ mk_status mk_create(const mk_model_dims *dims, const mk_weights *w, void *stream
 mk_status mk_build_schedule(mk_ctx *ctx, int32_t batch, const int32_t *seq_lens,
                             const int32_t *page_tables);
 
-/* One decode step for the scheduled batch.  token_ids: DEVICE int32 [batch];
+/* The decode step as one persistent kernel ("Cohere speeds up North Mini
+ * Code with new megakernel", paragraph 2; "Cohere megakernel serves 30B MoE
+ * 1.58x faster than vLLM", paragraphs 2-3: every operation of the step in
+ * one kernel, dependencies through counters in global memory).
+ * One decode step for the scheduled batch.  token_ids: DEVICE int32 [batch];
  * out_logits: DEVICE fp32 [batch][vocab] or NULL; out_next_tokens: DEVICE
  * int32 [batch] (greedy argmax, ties -> lowest id).  A token id outside
  * [0, vocab) fails the step with MK_ERR_BAD_TOKEN (sticky; the kernel reads
@@ -122,11 +133,16 @@ mk_status mk_build_schedule(mk_ctx *ctx, int32_t batch, const int32_t *seq_lens,
 mk_status mk_decode_step(mk_ctx *ctx, const int32_t *token_ids, float *out_logits,
                          int32_t *out_next_tokens);
 
-/* Waits for the stream and returns the sticky device status. */
+/* Library plumbing (no operation of the pages): waits for the stream and
+ * returns the sticky device status. */
 mk_status mk_sync(mk_ctx *ctx);
 
+/* Library plumbing: releases what mk_create allocated (never the caller's
+ * weights or KV pools). */
 void mk_destroy(mk_ctx *ctx);
 
+/* Library plumbing: a static name for a status code ("unknown status" for
+ * any other value). */
 const char *mk_status_string(mk_status s);
 
 /* One decode step that allocates no memory of its own: no cudaMalloc,
@@ -163,16 +179,24 @@ mk_status mk_decode_step_static(const mk_model_dims *dims, const mk_weights *w, 
 
 /* ---- diagnostics (tests / benchmark) ------------------------------------- */
 
-/* Device wait limit in nanoseconds (default 1e9).  Every counter / mbarrier
+/* The bound on the counter barriers ("Cohere megakernel serves 30B MoE
+ * 1.58x faster than vLLM", paragraph 3).
+ * Device wait limit in nanoseconds (default 1e9).  Every counter / mbarrier
  * wait in the kernel gives up after this long and reports
  * MK_ERR_DEVICE_TIMEOUT instead of hanging. */
 mk_status mk_set_wait_limit_ns(mk_ctx *ctx, uint64_t ns);
 
-/* Routing of the last step (synchronises): ids / w HOST [n_layers][batch][top_k]
+/* The router's top-k of the last step ("Cohere megakernel serves 30B MoE
+ * 1.58x faster than vLLM", paragraph 2: MoE routing).  The oracle replays
+ * this routing at near ties instead of the library accepting a forced one.
+ * Routing of the last step (synchronises): ids / w HOST [n_layers][batch][top_k]
  * in descending-logit order; either may be NULL. */
 mk_status mk_debug_routing(mk_ctx *ctx, int32_t *ids, float *w);
 
-/* Copies a workspace buffer of the last step to HOST memory (synchronises).
+/* The intermediate values of the step's operations ("Cohere Packs the Entire
+ * Decoding Step Into a Single CUDA Megakernel", paragraph 1: RMSNorm, QKV,
+ * attention, MoE), for layer-by-layer comparison with the oracle.
+ * Copies a workspace buffer of the last step to HOST memory (synchronises).
  * what: 0 = residual h [n_layers+1][batch][d] bf16 (h[0] is the embedding),
  *       1 = attention output o [n_layers][batch][Hq*D] bf16,
  *       2 = router logits [n_layers][batch][E] fp32,
@@ -183,7 +207,9 @@ mk_status mk_debug_routing(mk_ctx *ctx, int32_t *ids, float *w);
  * bytes must equal the buffer size. */
 mk_status mk_debug_dump(mk_ctx *ctx, int32_t what, void *host_out, uint64_t bytes);
 
-/* Running totals since mk_build_schedule (synchronises). */
+/* Running totals since mk_build_schedule (synchronises): the distinct
+ * experts streamed, which fix the step's bytes ("Cohere megakernel serves
+ * 30B MoE 1.58x faster than vLLM", paragraph 4: weights streamed per step). */
 typedef struct {
   uint64_t steps;          /* decode steps launched */
   uint64_t sum_experts;    /* sum over steps and layers of distinct experts U */
@@ -191,12 +217,16 @@ typedef struct {
 } mk_stats;
 mk_status mk_get_stats(mk_ctx *ctx, mk_stats *out);
 
-/* Test only: adds `delta` to the target of layer `layer`'s attention-done
+/* Failure detection of the counter barriers ("Cohere megakernel serves 30B
+ * MoE 1.58x faster than vLLM", paragraph 3).
+ * Test only: adds `delta` to the target of layer `layer`'s attention-done
  * counter in the next launch, making that wait unsatisfiable so that the
  * bounded-wait path (MK_ERR_DEVICE_TIMEOUT) can be exercised without a hang. */
 mk_status mk_debug_poison_wait(mk_ctx *ctx, int32_t layer, int32_t delta);
 
-/* Per-task timing trace of the following steps (diagnostic; each step
+/* Where the SMs idle ("Cohere megakernel serves 30B MoE 1.58x faster than
+ * vLLM", paragraph 4: idle SMs, dataflow start and weight prefetch).
+ * Per-task timing trace of the following steps (diagnostic; each step
  * overwrites the previous one).  events_per_cta = 0 turns it off; otherwise
  * a buffer of n_sm * events_per_cta task events plus 4096 stage events is
  * allocated.  Consumer thread 0 of every CTA records, for each task it runs:
@@ -221,7 +251,10 @@ mk_status mk_set_stage_trace_cta(mk_ctx *ctx, int32_t cta);
 mk_status mk_get_trace(mk_ctx *ctx, uint64_t *host_out, uint64_t n_words, int32_t *n_cta,
                        int32_t *events_per_cta);
 
-/* Host-only schedule planning (no GPU needed): the task table that
+/* The task table ("Cohere Packs the Entire Decoding Step Into a Single CUDA
+ * Megakernel", paragraph 2; 32-int32 descriptors: "Cohere megakernel serves
+ * 30B MoE 1.58x faster than vLLM", paragraph 2).
+ * Host-only schedule planning (no GPU needed): the task table that
  * mk_build_schedule would upload for n_sm SMs.  Writes at most cap int32s of
  * [n_cta][tasks_per_cta][32] descriptors into table (may be NULL to query)
  * and the table geometry into info.  Returns MK_ERR_INVALID_ARG /

@@ -19,7 +19,7 @@ import ctypes
 import os
 import subprocess
 from dataclasses import dataclass
-from typing import Dict, List, Optional, Sequence
+from typing import Tuple, Dict, List, Optional, Sequence
 
 import numpy as np
 
@@ -186,6 +186,24 @@ def ragged_lens(seed: int, batch: int, lo: int, hi: int, gen: int = 0) -> List[i
     return [int(lo + x) for x in u]
 
 
+def replacement_events(seed: int, batch: int, steps: int, lo: int = 16,
+                       hi: int = 128) -> List[Tuple[int, int]]:
+    """Continuous batching: every slot's sequence gets a generation budget
+    ~U[lo, hi] (seeded per slot and generation); when it is spent the slot
+    takes a fresh sequence.  Returns the (step, slot) replacements within
+    `steps` steps, in order (step k: before the k-th step)."""
+    ev = []
+    for b in range(batch):
+        t, g = 0, 0
+        while True:
+            t += lo + int(uniform_int(seed, tensor_id(K_BUDGET, layer=b, gen=g), hi - lo + 1, 1)[0])
+            if t >= steps:
+                break
+            ev.append((t, b))
+            g += 1
+    return sorted(ev)
+
+
 def workloads() -> Dict[str, Workload]:
     """The five workloads: tiny, mid, full-scale (B=1 at 8K), full-scale B=8
     ragged with Zipf router skew, and long context."""
@@ -340,13 +358,18 @@ class DeviceInputs:
 
 def device_inputs(dims: Dims, seq_lens: Sequence[int], reserve_steps: int,
                   zipf_s: Optional[float] = None, seed: int = 0, gen: int = 0,
-                  shuffle: bool = True, device="cuda") -> DeviceInputs:
+                  shuffle: bool = True, device="cuda", weights=None) -> DeviceInputs:
+    """Weights, KV pools (laid out for seq_lens plus reserve_steps tokens)
+    and router biases on the device.  weights: the weight tensors of an
+    earlier DeviceInputs of the same dims and seed, reused as they are."""
     import torch
 
     layout = page_layout(dims, seq_lens, reserve_steps, seed, gen, shuffle)
-    specs = dict(weight_specs(dims))
+    specs = {} if weights is not None else dict(weight_specs(dims))
     specs.update(kv_specs(dims, layout.num_pages, gen))
     tensors = {n: device_tensor(s, seed, device) for n, s in specs.items()}
+    if weights is not None:
+        tensors.update({n: weights[n] for n in weight_specs(dims)})
     biases = [router_bias(dims, l, zipf_s, seed) for l in range(dims.n_layers)]
     bias_t = [None if b is None else torch.from_numpy(b).to(device) for b in biases]
     return DeviceInputs(dims, tensors, layout, biases, bias_t, seed)
