@@ -166,7 +166,7 @@ def run_mk(args, rank, world):
     if args.layers:
         # profiling captures only: the same model cut to its first layers
         dims = dataclasses.replace(dims, n_layers=args.layers)
-    lens = list(wl.seq_lens)
+    lens = list(wl.seq_lens) * args.batch
     B = len(lens)
     e2e_steps = args.e2e_steps
     reserve = args.warmup + args.steps + e2e_steps + 8
@@ -280,7 +280,8 @@ def run_mk(args, rank, world):
                 "bw_gbs": peak, "bw_kind": peak_kind},
         "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved_gbs / peak, 4),
-                     "traffic": profiled_traffic(), "kernel": "mk::decode_kernel<1>",
+                     "traffic": profiled_traffic() if B == 1 else None,
+                     "kernel": f"mk::decode_kernel<{1 if B <= 1 else 2 if B <= 2 else 4 if B <= 4 else 8}>",
                      "peak_kind": f"{peak_kind} (copy bandwidth)",
                      "mean_launch_ms": round(mean_launch_s * 1e3, 4)},
         "e2e": {"value": e2e_tok_s and round(e2e_tok_s, 2), "unit": "tok/s", "h2d_bytes_per_step": 4 * B,
@@ -549,6 +550,8 @@ def main():
     ap.add_argument("--trace-raw", default="", help="also save the raw trace (npz) here")
     ap.add_argument("--workloads", default="mid,full_b8,long_b1,long_b2",
                     help="also time these workloads ('' to skip)")
+    ap.add_argument("--batch", type=int, default=1,
+                    help="profiling only: the headline step at this batch (8192 cached each)")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: cut the model to its first N layers")
     args = ap.parse_args()
