@@ -2278,9 +2278,29 @@ struct Consumer {
     }
     uint16_t *x = (uint16_t *)cx.xbuf();
     for (int i = tid; i < NC * MK_MAX_OUT_ROWS * NB; i += NCT) (&O.acc_w[0][0][0])[i] = 0.0f;
-    /* the experts' down rows first: their activations are complete once
-     * every gate/up share is, normally before the attention output */
     if (bar_any(hfail)) return false;
+    /* Wo against the attention output (its rows are in the ring already).
+     * Wo's input spans the normed-input buffer and the scratch buffer after
+     * it (the normed input is dead: this is the CTA's last task of the
+     * layer); the next norm must recompute it. */
+    auto wo = [&]() -> bool {
+      if (!cwait(lctr(p, layer, CTR_ATTN_DONE), target, task, OP_OUT, layer, CTR_ATTN_DONE))
+        return false;
+      bar_consumers(); /* every warp is done with xbuf */
+      uint16_t *xo = cx.xn();
+      if (tid == 0) M()->norm_layer = -2;
+      load_x(xo, p.o + (size_t)layer * MK_MAX_BATCH * HqD, HqD, HqD);
+      bar_consumers();
+      gemv_rows(nr, HqD, xo, task, OP_OUT, layer,
+                [&](int r, int bb, float v) { O.acc_o[r][bb] = v; });
+      return task_end();
+    };
+    const bool fold = NB == 1 && p.fold; /* down rows done by the gate/up shares */
+    /* Folded (batch 1): the expert shares are the long path, so Wo runs
+     * first, while they finish; otherwise the experts' down rows come first:
+     * their activations are complete once every gate/up share is, normally
+     * before the attention output. */
+    if (fold && !wo()) return false;
     if (!cwait(lctr(p, layer, CTR_UP_DONE), (int)((cx.epoch + 1) * p.n_up), task, OP_OUT, layer,
                CTR_UP_DONE))
       return false;
@@ -2288,7 +2308,6 @@ struct Consumer {
     const int xpf = mk_x_pitch(F), per = NB * xpf;
     const int fit = max(1, (int)min((int64_t)U, (int64_t)p.xbuf_bytes / ((int64_t)2 * per)));
     const int rps = mk_rows_per_stage(F, cx.SB), pitch = mk_row_pitch(F);
-    const bool fold = NB == 1 && p.fold; /* down rows done by the gate/up shares */
     static_assert(MK_MAX_OUT_ROWS >= 32, "a lane per row of an OUT task");
     if (fold) {
       /* the gate/up shares' down partials of this task's rows: warp w adds
@@ -2315,6 +2334,7 @@ struct Consumer {
         }
       }
       O.acc_w[warp][lane][0] = s; /* rows nr.. of the task: 0 */
+      bar_consumers();              /* every warp's sums before the residual */
     }
     const int n_se = fold ? 0 : (nr + rps - 1) / rps; /* stages per expert */
     for (int u0 = 0; u0 < (fold ? 0 : U); u0 += fit) {
@@ -2356,19 +2376,7 @@ struct Consumer {
       }
     }
     si += U * n_se;
-    /* then Wo against the attention output */
-    if (!cwait(lctr(p, layer, CTR_ATTN_DONE), target, task, OP_OUT, layer, CTR_ATTN_DONE))
-      return false;
-    bar_consumers(); /* every warp is done with the activations in xbuf */
-    /* Wo's input spans the normed-input buffer and the scratch buffer after
-     * it (the normed input is dead: this is the CTA's last task of the
-     * layer); the next norm must recompute it */
-    uint16_t *xo = cx.xn();
-    if (tid == 0) M()->norm_layer = -2;
-    load_x(xo, p.o + (size_t)layer * MK_MAX_BATCH * HqD, HqD, HqD);
-    bar_consumers();
-    gemv_rows(nr, HqD, xo, task, OP_OUT, layer, [&](int r, int bb, float v) { O.acc_o[r][bb] = v; });
-    if (!task_end()) return false;
+    if (!fold && !wo()) return false;
     /* the residual entering the next layer, a pair of rows per thread: one
      * tagged word for the next layer's readers, plain copies (and the two
      * terms) for the diagnostics.  r0 and nr are even. */
