@@ -264,6 +264,7 @@ typedef struct {
   int32_t n_layer_tasks_max;          /* per-CTA tasks of one layer (template) */
   int32_t n_qkv, n_router, n_attn, n_up, n_out, n_lm; /* tasks per layer (lm: per step) */
   int32_t n_attn_slots;               /* attention partial slots per layer */
+  int32_t n_down;                     /* expert down-row shares per layer (0: folded) */
 } mk_plan_info;
 mk_status mk_plan(const mk_model_dims *dims, int32_t n_sm, int32_t batch, const int32_t *seq_lens,
                   mk_plan_info *info, int32_t *table, int64_t cap);

@@ -100,7 +100,7 @@ class mk_stats(ctypes.Structure):
 class mk_plan_info(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("n_cta", "tasks_per_cta", "n_layer_tasks_max", "n_qkv", "n_router", "n_attn",
-                 "n_up", "n_out", "n_lm", "n_attn_slots")]
+                 "n_up", "n_out", "n_lm", "n_attn_slots", "n_down")]
 
 
 EXPORTS = ["mk_create", "mk_build_schedule", "mk_decode_step", "mk_sync", "mk_destroy",

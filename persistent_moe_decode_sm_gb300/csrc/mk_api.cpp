@@ -53,6 +53,7 @@ struct mk_ctx {
   size_t ws_bytes = 0;
   uint16_t *h = nullptr, *qkv = nullptr, *o = nullptr, *act = nullptr, *am = nullptr;
   float *moe_part = nullptr;
+  float *dpart = nullptr;
   int moe_part_stride = 0;
   uint64_t *h_tag = nullptr, *lg_tag = nullptr;
   void *wd_maps = nullptr;             /* device [n_layers] tensor maps of the down weights */
@@ -308,6 +309,7 @@ mk_status mk_create(const mk_model_dims *dims, const mk_weights *w, void *stream
   const size_t o_rl = cv.take((size_t)L * MB * d.n_experts * 4);
   const size_t o_rt = cv.take((size_t)L * sizeof(mk_routing));
   const size_t o_act = cv.take((size_t)L * c->u_max * MB * d.d_ffn * 2);
+  const size_t o_dp = cv.take((size_t)2 * c->u_max * MB * d.d_model * 4);
   const size_t o_lm = cv.take((size_t)c->n_sm * MB * 2 * 4);
   const size_t o_rope = cv.take((size_t)c->rope_max_pos * (d.head_dim / 2) * 2 * 4);
   const size_t o_ctr = cv.take(c->n_ctr * 4);
@@ -337,6 +339,7 @@ mk_status mk_create(const mk_model_dims *dims, const mk_weights *w, void *stream
   c->router_logits = (float *)(c->ws + o_rl);
   c->routing = (mk_routing *)(c->ws + o_rt);
   c->act = (uint16_t *)(c->ws + o_act);
+  c->dpart = (float *)(c->ws + o_dp);
   c->lm_part = (float *)(c->ws + o_lm);
   c->rope = (float *)(c->ws + o_rope);
   c->ctr = (int32_t *)(c->ws + o_ctr);
@@ -540,6 +543,8 @@ mk_status mk_decode_step(mk_ctx *c, const int32_t *token_ids, float *out_logits,
   p.tasks_per_cta = c->plan.tasks_per_cta;
   p.n_slots = c->n_slots_max;
   p.u_max = c->u_max;
+  p.n_down = c->plan.n_down;
+  p.dpart = c->dpart;
   p.n_qkv = c->plan.n_qkv;
   p.n_router = c->plan.n_router;
   p.n_up = c->plan.n_up;

@@ -31,7 +31,10 @@ enum {
                       experts' F: their gate and up rows, then the down matrix's 64
                       columns of every row of d, giving one partial down vector per block */
   OP_OUT = 5,      /* [2] row0, [3] nrows */
-  OP_LM = 6        /* [2] row0, [3] nrows, [4] lm task index */
+  OP_LM = 6,       /* [2] row0, [3] nrows, [4] lm task index */
+  OP_DOWN = 7      /* [1] share, [2] n_shares (unfolded, batch >= 2): a range of the
+                      chosen experts' down rows (U x d of them, in slot order), each
+                      giving the weighted-free row dot products of every token */
 };
 
 /* ---- counters ----------------------------------------------------------------
@@ -45,7 +48,7 @@ enum {
   CTR_ROUTER_DONE = 1, /* router logits written (counts rows: E per step) */
   CTR_ATTN_DONE = 2,
   CTR_UP_DONE = 3,
-  CTR_OUT_DONE = 4,
+  CTR_DOWN_DONE = 4, /* unfolded expert down rows done (the OUT sums wait) */
   CTR_ATTN_TICKET0 = 5 /* + (b * n_kv_heads + kvh) * (1 + MK_MAX_MERGE_GROUPS):
                           the final merge ticket, then one ticket per merge group */
 };
@@ -156,6 +159,9 @@ typedef struct {
   int32_t n_slots, u_max;
   /* per-step increments of each counter */
   int32_t n_qkv, n_router, n_up, n_out, n_lm, n_attn_done; /* n_router: E (rows) */
+  int32_t n_down;             /* down-row shares per layer (0 when folded) */
+  float *dpart;               /* [2][u_max][MAXB][d] the down rows' dot products, by layer
+                               * parity (unfolded) */
   int32_t ctrs_per_layer;
   unsigned long long wait_limit_ns;
   int32_t *err_host;          /* host-mapped mirror: [code, cta, task, op, layer, ctr, seen, target] */

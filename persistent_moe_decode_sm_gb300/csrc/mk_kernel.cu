@@ -696,19 +696,23 @@ __device__ bool poll_tagged(const mk_kparams &p, int cta, const uint64_t *a, int
   for (int i = 0; i < 8; ++i)
     if (i < n) w[i] = ld_tag(a + (size_t)i * stride);
   uint64_t t0 = 0;
+  uint32_t spins = 0;
   while (true) {
     bool all = true;
 #pragma unroll
     for (int i = 0; i < 8; ++i)
       if (i < n && !tag_ok(w[i], tag)) all = false;
     if (all) break;
+    /* the limit and the abort flag every 16 rounds: a global load each
+     * round would put a second round trip between the data and its reader */
     if (!t0) {
       t0 = gtimer();
-    } else if (gtimer() - t0 > p.wait_limit_ns) {
-      raise_error(p, MK_ERR_DEVICE_TIMEOUT, cta, -1, op, layer, -1, 0, (int)tag);
-      return false;
-    } else if (ld_volatile(&p.ctrl->abort)) {
-      return false;
+    } else if ((++spins & 15) == 0) {
+      if (gtimer() - t0 > p.wait_limit_ns) {
+        raise_error(p, MK_ERR_DEVICE_TIMEOUT, cta, -1, op, layer, -1, 0, (int)tag);
+        return false;
+      }
+      if (ld_volatile(&p.ctrl->abort)) return false;
     }
     __nanosleep(32);
 #pragma unroll
@@ -1180,37 +1184,57 @@ struct Producer {
             q.row_bytes = (uint32_t)d * 2;
           });
           base += n_st;
-        } else if (op == OP_OUT) {
-          /* the chosen experts' down rows first (their activations are
-           * ready before the attention output), then the Wo rows */
-          const int r0 = t[2], nr = t[3];
-          const bool fold = NB == 1 && p.fold; /* down rows in the gate/up shares */
-          const int U = fold ? 0 : routed(layer, false);
+        } else if (op == OP_DOWN) {
+          /* a range of the chosen experts' down rows (U x d of them, slot
+           * order), per expert segment in stages of whole rows of F; the
+           * routing is taken here if the CTA had no gate/up share, so that
+           * the rows stream while its consumers still run attention */
+          const int U = routed(layer, false);
           if (U < 0) {
             ok = false;
             break;
           }
           t_plan = strc ? sclock() : 0;
-          const int rps_f = mk_rows_per_stage(F, SB), n_se = (nr + rps_f - 1) / rps_f;
-          const int n_dn = fold ? 0 : U * n_se;
+          const int rps = mk_rows_per_stage(F, SB);
+          const int64_t T = (int64_t)U * d;
+          const int64_t v = T * t[1] / t[2], v1 = T * (t[1] + 1) / t[2];
+          const int u0 = (int)(v / d), u1 = v1 > v ? (int)((v1 - 1) / d) : u0 - 1;
+          int n_st = 0;
+          for (int u = u0; u <= u1; ++u) {
+            const int64_t lo = max(v, (int64_t)u * d), hi = min(v1, (int64_t)(u + 1) * d);
+            n_st += (int)((hi - lo + rps - 1) / rps);
+          }
+          ok = run_stages(base, 0, n_st, [&](int j, QDesc &q) {
+            int u = u0, jr = j;
+            int64_t lo = 0, hi = 0;
+            for (; u <= u1; ++u) {
+              lo = max(v, (int64_t)u * d);
+              hi = min(v1, (int64_t)(u + 1) * d);
+              const int ns = (int)((hi - lo + rps - 1) / rps);
+              if (jr < ns) break;
+              jr -= ns;
+            }
+            const int r0 = (int)(lo - (int64_t)u * d) + jr * rps;
+            q.kind = SK_ROWS;
+            q.n = min(rps, (int)(hi - (int64_t)u * d) - r0);
+            q.a = (const uint8_t *)(ly->wd + ((size_t)pexp[u] * d + r0) * F);
+            q.row_bytes = (uint32_t)F * 2;
+          });
+          base += n_st;
+        } else if (op == OP_OUT) {
+          /* the Wo rows (the experts' down rows are DOWN tasks, or folded
+           * into the gate/up shares at batch 1) */
+          const int r0 = t[2], nr = t[3];
+          t_plan = strc ? sclock() : 0;
           const int rps_o = mk_rows_per_stage(HqD, SB), n_wo = (nr + rps_o - 1) / rps_o;
           const uint16_t *wo = ly->wo + (size_t)r0 * HqD;
-          ok = run_stages(base, 0, n_dn + n_wo, [&](int j, QDesc &q) {
+          ok = run_stages(base, 0, n_wo, [&](int jw, QDesc &q) {
             q.kind = SK_ROWS;
-            if (j < n_dn) {
-              const int u = j / n_se, jj = j % n_se;
-              const int e = pexp[u];
-              q.n = min(rps_f, nr - jj * rps_f);
-              q.a = (const uint8_t *)(ly->wd + ((size_t)e * d + r0 + (size_t)jj * rps_f) * F);
-              q.row_bytes = (uint32_t)F * 2;
-            } else {
-              const int jw = j - n_dn;
-              q.n = min(rps_o, nr - jw * rps_o);
-              q.a = (const uint8_t *)(wo + (size_t)jw * rps_o * HqD);
-              q.row_bytes = (uint32_t)HqD * 2;
-            }
+            q.n = min(rps_o, nr - jw * rps_o);
+            q.a = (const uint8_t *)(wo + (size_t)jw * rps_o * HqD);
+            q.row_bytes = (uint32_t)HqD * 2;
           });
-          base += n_dn + n_wo;
+          base += n_wo;
         } else {
           ok = false; /* the consumers report the bad opcode */
         }
@@ -1298,6 +1322,8 @@ struct Consumer {
   /* The first stage index j >= 0 of a task (stream stage si + j) that this
    * warp owns. */
   __device__ int first_mine() const { return (warp - si % NC + NC) % NC; }
+  /* the same for a run of stages that starts at stream stage s */
+  __device__ int first_mine_at(int s) const { return (warp - s % NC + NC) % NC; }
 
   /* Every lane of the warp waits for the stage itself, and the stage
    * bookkeeping below is branch-free (predicated single stores and
@@ -1416,6 +1442,7 @@ struct Consumer {
 #pragma unroll
           for (int k = 0; k < 4; ++k) w[b][k] = b < B ? ld_tag(hw + (size_t)b * dw + k) : 0ULL;
         uint64_t t0 = 0;
+        uint32_t spins = 0;
         while (!fail) {
           bool all = true;
 #pragma unroll
@@ -1426,11 +1453,14 @@ struct Consumer {
           if (all) break;
           if (!t0) {
             t0 = gtimer();
-          } else if (gtimer() - t0 > p.wait_limit_ns) {
-            raise_error(p, MK_ERR_DEVICE_TIMEOUT, cx.cta, -1, OP_QKV, src, -1, 0, (int)p.step_tag);
-            fail = true;
-          } else if (ld_volatile(&p.ctrl->abort)) {
-            fail = true;
+          } else if ((++spins & 15) == 0) { /* as in poll_tagged */
+            if (gtimer() - t0 > p.wait_limit_ns) {
+              raise_error(p, MK_ERR_DEVICE_TIMEOUT, cx.cta, -1, OP_QKV, src, -1, 0,
+                          (int)p.step_tag);
+              fail = true;
+            } else if (ld_volatile(&p.ctrl->abort)) {
+              fail = true;
+            }
           }
           __nanosleep(32);
 #pragma unroll
@@ -2248,6 +2278,52 @@ struct Consumer {
     return true;
   }
 
+  /* ------------------------------------------------ expert down rows (batch >= 2)
+   * A share of the chosen experts' U x d down rows, per expert segment: the
+   * expert's activations (every token's a = silu(g) u, once the gate/up
+   * shares are in) staged in the scratch buffer, then its rows of F against
+   * them; each row's dot product per token goes to dpart for the OUT tasks,
+   * which weight and add them in slot order. */
+  __device__ bool op_down(const int32_t *t, int task, int layer) {
+    const mk_kparams &p = *cx.p;
+    if (!route_local(layer, task, OP_DOWN)) return false;
+    if (!cwait(lctr(p, layer, CTR_UP_DONE), (int)((cx.epoch + 1) * p.n_up), task, OP_DOWN, layer,
+               CTR_UP_DONE))
+      return false;
+    const int U = M()->route_U, d = p.d, F = p.F, B = p.B;
+    const int64_t T = (int64_t)U * d;
+    int64_t v = T * t[1] / t[2];
+    const int64_t v1 = T * (t[1] + 1) / t[2];
+    const int rps = mk_rows_per_stage(F, cx.SB), pitch = mk_row_pitch(F), xpf = mk_x_pitch(F);
+    uint16_t *xa = (uint16_t *)cx.xbuf();
+    float *dp = p.dpart + (size_t)(layer & 1) * p.u_max * MK_MAX_BATCH * d;
+    int j = 0; /* stage index within the task */
+    while (v < v1) {
+      const int u = (int)(v / d), r0 = (int)(v % d);
+      const int r1 = (int)min((int64_t)d, r0 + (v1 - v));
+      if (j > 0) bar_consumers(); /* the previous expert's activations are consumed */
+      load_x(xa, p.act + (((size_t)layer * p.u_max + u) * MK_MAX_BATCH) * F, F, F);
+      bar_consumers();
+      float *out = dp + (size_t)u * MK_MAX_BATCH * d;
+      const int nst = (r1 - r0 + rps - 1) / rps;
+      for (int jj = first_mine_at(si + j); jj < nst; jj += NC) {
+        uint8_t *st;
+        if (!stage_wait(si + j + jj, st, task, OP_DOWN, layer)) break;
+        const int rb = r0 + jj * rps, cnt = min(rps, r1 - rb);
+        gemv_stage(st, cnt, F, xa, [&](int r, int bb, float val) {
+          if (bb < B) out[(size_t)bb * d + rb + r] = val;
+        });
+        stage_release(si + j + jj);
+      }
+      j += nst;
+      v += r1 - r0;
+    }
+    si += j;
+    if (!task_end()) return false;
+    signal(lctr(p, layer, CTR_DOWN_DONE));
+    return true;
+  }
+
   /* ---------------------------------- Wo, expert down + combine, residual */
   __device__ bool op_out(const int32_t *t, int task, int layer) {
     const mk_kparams &p = *cx.p;
@@ -2276,7 +2352,6 @@ struct Consumer {
         O.hres[r][bb] = bf2f((uint16_t)(((r0 + r) & 1) ? (w >> 16) : (w & 0xFFFFu)));
       }
     }
-    uint16_t *x = (uint16_t *)cx.xbuf();
     for (int i = tid; i < NC * MK_MAX_OUT_ROWS * NB; i += NCT) (&O.acc_w[0][0][0])[i] = 0.0f;
     if (bar_any(hfail)) return false;
     /* Wo against the attention output (its rows are in the ring already).
@@ -2296,20 +2371,15 @@ struct Consumer {
       return task_end();
     };
     const bool fold = NB == 1 && p.fold; /* down rows done by the gate/up shares */
-    /* Folded (batch 1): the expert shares are the long path, so Wo runs
-     * first, while they finish; otherwise the experts' down rows come first:
-     * their activations are complete once every gate/up share is, normally
-     * before the attention output. */
-    if (fold && !wo()) return false;
-    if (!cwait(lctr(p, layer, CTR_UP_DONE), (int)((cx.epoch + 1) * p.n_up), task, OP_OUT, layer,
-               CTR_UP_DONE))
-      return false;
-    /* the experts' activations, as many experts at a time as xbuf holds */
-    const int xpf = mk_x_pitch(F), per = NB * xpf;
-    const int fit = max(1, (int)min((int64_t)U, (int64_t)p.xbuf_bytes / ((int64_t)2 * per)));
-    const int rps = mk_rows_per_stage(F, cx.SB), pitch = mk_row_pitch(F);
+    /* Wo first (its rows are in the ring; the attention output is normally
+     * complete before the experts' results), then the experts' results of
+     * this task's rows, added into acc_w[warp][row][token] in a fixed order. */
+    if (!wo()) return false;
     static_assert(MK_MAX_OUT_ROWS >= 32, "a lane per row of an OUT task");
     if (fold) {
+      if (!cwait(lctr(p, layer, CTR_UP_DONE), (int)((cx.epoch + 1) * p.n_up), task, OP_OUT,
+                 layer, CTR_UP_DONE))
+        return false;
       /* the gate/up shares' down partials of this task's rows: warp w adds
        * blocks w, w + NC, ... in that order (lane r for row r0 + r, every
        * load of a batch in flight at once), the warps' sums are added in
@@ -2334,49 +2404,35 @@ struct Consumer {
         }
       }
       O.acc_w[warp][lane][0] = s; /* rows nr.. of the task: 0 */
-      bar_consumers();              /* every warp's sums before the residual */
-    }
-    const int n_se = fold ? 0 : (nr + rps - 1) / rps; /* stages per expert */
-    for (int u0 = 0; u0 < (fold ? 0 : U); u0 += fit) {
-      const int u1 = min(U, u0 + fit);
-      if (u0 > 0) bar_consumers(); /* the previous experts' activations are consumed */
-      for (int u = u0; u < u1; ++u)
-        load_x(x + (size_t)(u - u0) * per,
-               p.act + (((size_t)layer * p.u_max + u) * MK_MAX_BATCH) * F, F, F);
-      bar_consumers();
-      for (int u = u0; u < u1; ++u) {
-        const uint16_t *xa = x + (size_t)(u - u0) * per;
-        for (int jj = 0; jj < n_se; ++jj) {
-          const int j = u * n_se + jj;
-          if ((si + j) % NC != warp) continue;
-          uint8_t *st;
-          if (!stage_wait(si + j, st, task, OP_OUT, layer)) continue;
-          const int rb0 = jj * rps, cnt = min(rps, nr - rb0);
-          auto acc = [&](int r, int bb, float v) {
-            float &a = O.acc_w[warp][rb0 + r][bb];
-            a = fmaf(slot_w[u][bb], v, a);
-          };
-          if (NB == 1 && kB1CudaCores) {
-            /* branch-free: every lane updates a valid row's accumulator
-             * value, the lane that owns the row stores it */
-            cc_rows(st, cnt, pitch, F, xa, lane, 0, [&](int n0, float sum, int nr) {
-              const int r = n0 + min(lane >> 2, nr - 1);
-              float *a = &O.acc_w[warp][rb0 + r][0];
-              sts32_if(a, fmaf(slot_w[u][0], sum, *a), (lane & 3) == 0 && (lane >> 2) < nr);
-            });
-          } else {
-            mma_rows<NB>(st, cnt, pitch, F, xa, xpf, lane, [](int vr) { return vr; },
-                         [&](int n0, const float(&a)[4], const float(&b)[4], bool two) {
-                           take_out<NB>(n0, a, cnt, lane, acc);
-                           if (two) take_out<NB>(n0 + 8, b, cnt, lane, acc);
-                         });
+    } else {
+      if (!cwait(lctr(p, layer, CTR_DOWN_DONE), (int)((cx.epoch + 1) * p.n_down), task, OP_OUT,
+                 layer, CTR_DOWN_DONE))
+        return false;
+      /* the DOWN tasks' dot products of this task's rows: warp w adds slots
+       * w, w + NC, ... (weighted by the token's routing weight) in that
+       * order, lane l for (row, token) pairs l, l + 32, ... */
+      const float *dp = p.dpart + (size_t)(layer & 1) * p.u_max * MK_MAX_BATCH * d + r0;
+      constexpr int BAT = 8;
+      for (int q = lane; q < nr * B; q += 32) {
+        const int r = q / B, bb = q % B;
+        float s = 0.0f;
+        for (int u0 = warp; u0 < U; u0 += BAT * NC) {
+          float vv[BAT];
+#pragma unroll
+          for (int i = 0; i < BAT; ++i) {
+            const int u = u0 + i * NC;
+            vv[i] = u < U ? __ldcg(dp + ((size_t)u * MK_MAX_BATCH + bb) * d + r) : 0.0f;
           }
-          stage_release(si + j);
+#pragma unroll
+          for (int i = 0; i < BAT; ++i) {
+            const int u = u0 + i * NC;
+            if (u < U) s = fmaf(slot_w[u][bb], vv[i], s);
+          }
         }
+        O.acc_w[warp][r][bb] = s;
       }
     }
-    si += U * n_se;
-    if (!fold && !wo()) return false;
+    bar_consumers(); /* every warp's sums before the residual */
     /* the residual entering the next layer, a pair of rows per thread: one
      * tagged word for the next layer's readers, plain copies (and the two
      * terms) for the diagnostics.  r0 and nr are even. */
@@ -2503,6 +2559,7 @@ struct Consumer {
         break;
       case OP_UP: ok = op_up(t, task, layer); break;
       case OP_OUT: ok = op_out(t, task, layer); break;
+      case OP_DOWN: ok = op_down(t, task, layer); break;
       case OP_LM: ok = op_lm(t, task); break;
       default:
         if (tid == 0) raise_error(*cx.p, MK_ERR_BAD_TASK, cx.cta, task, t[0], layer, -1, 0, 0);

@@ -152,6 +152,7 @@ extern "C" mk_status mk_decode_step_static(const mk_model_dims *dims, const mk_w
   const size_t o_rl = take((size_t)Lyr * MB * d.n_experts * 4);
   const size_t o_rt = take((size_t)Lyr * sizeof(mk_routing));
   const size_t o_act = take((size_t)Lyr * u_max * MB * d.d_ffn * 2);
+  const size_t o_dp = take((size_t)2 * u_max * MB * d.d_model * 4);
   const size_t o_lm = take((size_t)plan.n_lm * MB * 2 * 4);
   const size_t o_rope = take((size_t)MB * half * 2 * 4); /* one row per sequence */
   const size_t o_ctr = take(n_ctr * 4);
@@ -304,6 +305,8 @@ extern "C" mk_status mk_decode_step_static(const mk_model_dims *dims, const mk_w
   p.tasks_per_cta = plan.tasks_per_cta;
   p.n_slots = n_slots;
   p.u_max = u_max;
+  p.n_down = plan.n_down;
+  p.dpart = (float *)(base + o_dp);
   p.n_qkv = plan.n_qkv;
   p.n_router = plan.n_router;
   p.n_up = plan.n_up;

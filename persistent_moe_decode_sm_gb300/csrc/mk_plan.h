@@ -10,7 +10,7 @@
 
 struct MkPlan {
   int n_cta = 0, tasks_per_cta = 0, n_layer_tasks_max = 0, batch = 0;
-  int n_qkv = 0, n_router = 0, n_attn = 0, n_up = 0, n_out = 0, n_lm = 0;
+  int n_qkv = 0, n_router = 0, n_attn = 0, n_up = 0, n_out = 0, n_lm = 0, n_down = 0;
   int n_attn_slots = 0, n_attn_done = 0;
   int fold = 0; /* the down projection is folded into the gate/up shares (batch 1) */
   std::vector<int32_t> table;      /* [n_cta][tasks_per_cta][32] */

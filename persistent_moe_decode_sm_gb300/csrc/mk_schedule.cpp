@@ -20,8 +20,10 @@
  *            (sequence, kv head) pairs in proportion to their pages, one
  *            split of about equal size per CTA)
  *   UP      (one share per CTA of the gate/up rows of the experts the
- *            router chose; the share is resolved on the device)
- *   OUT     (rows of d: Wo rows, then the chosen experts' down rows, then
+ *            router chose; the share is resolved on the device; at batch 1
+ *            the share also takes its columns of the down rows)
+ *   DOWN    (batch >= 2: one share per CTA of the chosen experts' down rows)
+ *   OUT     (rows of d: Wo rows, the experts' weighted down results, then
  *            the residual; this produces the next layer's input)
  * then the LM head rows, one piece per CTA.
  *
@@ -158,7 +160,8 @@ mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int
 
   const int Hq = d.n_q_heads, Hkv = d.n_kv_heads, D = d.head_dim, P = d.page_size;
   std::vector<std::vector<Desc>> lt(n_cta), ft(n_cta);
-  std::vector<std::vector<Desc>> qkv_t(n_cta), attn_t(n_cta), up_t(n_cta), out_t(n_cta);
+  std::vector<std::vector<Desc>> qkv_t(n_cta), attn_t(n_cta), up_t(n_cta), down_t(n_cta),
+      out_t(n_cta);
   MkPlan &p = *out;
   p = MkPlan();
 
@@ -393,6 +396,21 @@ mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int
     p.n_up = n;
   }
 
+  /* DOWN (unfolded): the chosen experts' down rows, U x d of them, one share
+   * per CTA (every CTA: the attention CTAs take theirs after their splits),
+   * resolved on the device once the routing is known.  Each share streams
+   * its rows against its experts' activations and leaves the dot products
+   * for the OUT tasks to weight and add. */
+  if (!p.fold) {
+    for (int c = 0; c < n_cta; ++c) {
+      Desc t = desc(OP_DOWN);
+      t[1] = c;
+      t[2] = n_cta;
+      down_t[c].push_back(t);
+    }
+    p.n_down = n_cta;
+  }
+
   /* OUT: rows of d, in units of 8 rows (the residual is published as
    * tagged pairs of rows). */
   {
@@ -425,7 +443,7 @@ mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int
 
   int width = 0, lmax = 0;
   for (int c = 0; c < n_cta; ++c) {
-    for (auto *v : {&qkv_t[c], &attn_t[c], &up_t[c], &out_t[c]})
+    for (auto *v : {&qkv_t[c], &attn_t[c], &up_t[c], &down_t[c], &out_t[c]})
       lt[c].insert(lt[c].end(), v->begin(), v->end());
     width = std::max<int>(width, 1 + (int)lt[c].size() + (int)ft[c].size());
     lmax = std::max<int>(lmax, (int)lt[c].size());
@@ -467,6 +485,7 @@ extern "C" mk_status mk_plan(const mk_model_dims *dims, int32_t n_sm, int32_t ba
     info->n_out = p.n_out;
     info->n_lm = p.n_lm;
     info->n_attn_slots = p.n_attn_slots;
+    info->n_down = p.n_down;
   }
   if (table) {
     if (cap < (int64_t)p.table.size()) return MK_ERR_INVALID_ARG;

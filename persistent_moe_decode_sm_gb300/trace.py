@@ -12,7 +12,7 @@ from collections import defaultdict
 
 import numpy as np
 
-OPS = {1: "qkv", 2: "router", 3: "attn", 4: "up", 5: "out", 6: "lm"}
+OPS = {1: "qkv", 2: "router", 3: "attn", 4: "up", 5: "out", 6: "lm", 7: "down"}
 
 
 def events(trace: np.ndarray):

@@ -13,7 +13,7 @@ import pytest
 import persistent_moe_decode_sm_gb300 as mk
 import synth
 
-OP_QKV, OP_ATTN, OP_UP, OP_OUT, OP_LM, OP_HEADER = 1, 3, 4, 5, 6, 100
+OP_QKV, OP_ATTN, OP_UP, OP_OUT, OP_LM, OP_DOWN, OP_HEADER = 1, 3, 4, 5, 6, 7, 100
 
 
 def cdims(d, max_batch, max_pages):
@@ -39,6 +39,7 @@ def simulate(d, info, rows, batch, rng):
     group_ticket = {}
     attn_done = [0] * L
     up_done = [0] * L
+    down_done = [0] * L
     out_done = [0] * L
     lm_ticket = [0]
     queues = [[(l, t) for l in range(L) for t in lt] + [(L, t) for t in ft] for lt, ft in rows]
@@ -52,9 +53,11 @@ def simulate(d, info, rows, batch, rng):
             return qkv_done[l] == info.n_qkv
         if op == OP_UP:  # every consumer takes the top-k from the complete logits
             return router_done[l] == info.n_router
+        if op == OP_DOWN:  # the experts' activations are complete
+            return router_done[l] == info.n_router and up_done[l] == info.n_up
         if op == OP_OUT:
             return (router_done[l] == info.n_router and attn_done[l] == batch * Hkv
-                    and up_done[l] == info.n_up)
+                    and up_done[l] == info.n_up and down_done[l] == info.n_down)
         if op == OP_LM:
             return out_done[L - 1] == info.n_out
         raise AssertionError(op)
@@ -79,6 +82,8 @@ def simulate(d, info, rows, batch, rng):
                 attn_done[l] += 1
         elif op == OP_UP:
             up_done[l] += 1
+        elif op == OP_DOWN:
+            down_done[l] += 1
         elif op == OP_OUT:
             out_done[l] += 1
         elif op == OP_LM:
@@ -98,6 +103,7 @@ def simulate(d, info, rows, batch, rng):
     assert all(x == info.n_router for x in router_done)
     assert all(x == batch * Hkv for x in attn_done)
     assert all(x == info.n_up for x in up_done)
+    assert all(x == info.n_down for x in down_done)
     assert all(x == info.n_out for x in out_done)
     assert lm_ticket[0] == info.n_lm
 
@@ -155,6 +161,8 @@ def check_coverage(d, info, rows, seq_lens):
     assert s2 == list(range(len(s2)))  # level-2 slots distinct and dense
     ups = sorted((int(t[1]), int(t[2])) for t in lt_all if t[0] == OP_UP)
     assert ups == [(i, info.n_up) for i in range(info.n_up)]
+    downs = sorted((int(t[1]), int(t[2])) for t in lt_all if t[0] == OP_DOWN)
+    assert downs == [(i, info.n_down) for i in range(info.n_down)]
     cov = np.zeros(d.d_model, int)
     for t in lt_all:
         if t[0] == OP_OUT:
@@ -171,7 +179,7 @@ def check_coverage(d, info, rows, seq_lens):
 
 
 def phase_rank(t):
-    return {OP_QKV: 0, OP_ATTN: 1, OP_UP: 2, OP_OUT: 3}[int(t[0])]
+    return {OP_QKV: 0, OP_ATTN: 1, OP_UP: 2, OP_DOWN: 3, OP_OUT: 4}[int(t[0])]
 
 
 CASES = [
