@@ -219,22 +219,31 @@ static inline void mk_param_layers(mk_kparams *p, const mk_layer_dev *ly, int n_
 #endif
 
 /* ---- ring stage geometry (the producer and the consumers must agree) -------
- * A stage of streamed rows holds whole rows of K bf16, contiguous as in
- * memory (pitch 2K bytes), so that one bulk copy fills it.  The tensor-core
- * operand loads stay free of bank conflicts by reading the two halves of
- * each 128-byte block in opposite order on even and odd rows (see
- * mma_rows).  Activation vectors in shared memory use pitch K. */
-static inline MK_HD int mk_row_pitch(int K) { return 2 * K; }
-static inline MK_HD int mk_x_pitch(int K) { return K; }
+ * A stage of streamed rows holds whole rows of K bf16 (K a multiple of 64,
+ * so a row is a multiple of 128 bytes): n plain rows as two runs, rows
+ * [0, h) then [h, n) with h = (n + 1) / 2; gate/up pairs as the gate rows,
+ * then the up rows.  Below batch MK_RUN_GAP_MIN_NB the runs are contiguous
+ * as in memory (one bulk copy per stage, two for pairs).  From it on, the
+ * second run starts 64 bytes past the end of the first (two copies) and the
+ * token vectors of the activations sit K + 32 elements apart: the two rows
+ * (one from each run) or two tokens that a quarter-warp reads in one 16-byte
+ * operand load of the tensor-core GEMV then fall in opposite halves of the
+ * 128-byte bank window, so no token has to be entered twice (see mma_rows).
+ * The gap costs a copy that does not start on a 128-byte line, which only
+ * pays where the activation loads dominate the stage's shared-memory reads
+ * (eight tokens). */
+#define MK_RUN_GAP_MIN_NB 8
+static inline MK_HD int mk_run_gap(int nb) { return nb >= MK_RUN_GAP_MIN_NB ? 64 : 0; }
+static inline MK_HD int mk_x_pitch(int K, int nb) { return nb >= MK_RUN_GAP_MIN_NB ? K + 32 : K; }
 
-static inline MK_HD int mk_rows_per_stage(int K, int stage_bytes) {
-  int r = stage_bytes / mk_row_pitch(K);
+static inline MK_HD int mk_rows_per_stage(int K, int stage_bytes, int nb) {
+  int r = (stage_bytes - mk_run_gap(nb)) / (2 * K);
   return r > MK_MAX_STAGE_ROWS ? MK_MAX_STAGE_ROWS : r;
 }
 
 /* Gate/up row pairs per stage: the n gate rows, then the n up rows. */
-static inline MK_HD int mk_pairs_per_stage(int K, int stage_bytes) {
-  return mk_rows_per_stage(K, stage_bytes) / 2;
+static inline MK_HD int mk_pairs_per_stage(int K, int stage_bytes, int nb) {
+  return mk_rows_per_stage(K, stage_bytes, nb) / 2;
 }
 
 /* KV pages: one tensor-map box per page and pool covers min(D, 64) head dims

@@ -354,41 +354,50 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
 }
 
 /* -------------------------------------------------------- skinny GEMV tile
- * out[v][b] = W_rm(v) . x_b for the R (virtual) rows v of one ring stage --
- * stage row rm(v) at byte rm(v) * pitch -- and the NB token vectors x_b
- * (pitch xp elements), on the tensor cores.  Eight weight rows are the N
- * side of an m16n8k16 tile, the tokens the M side, and the fp32 sums come
- * out of the accumulator already reduced over K.
- *
- * Bank conflicts without padding: each thread reads 16-byte pieces; a
- * quarter-warp reads two rows (B columns g = 2i, 2i + 1) at the same
- * offsets, which rows 2K bytes apart put in the same banks.  So odd-g
- * threads read the upper half of each 128-byte block first.  That changes
- * which columns feed which k slot on odd threads, so token b is entered
- * twice on the M side: row 2b with the even order (A rows 0..7 hold tokens
- * 0..3, rows 8..15 tokens 4..7), row 2b + 1 with the odd order, and C[m][n]
- * is valid where m and n have the same parity -- thread (g, t) ends with
- * column 2t + (g & 1) for tokens g / 2 (c0 or c1) and 4 + g / 2 (c2 or c3).
- * Within a 64-column block the k order is a permutation of the columns,
- * the same for A and B of a valid pair, so each sum is over all columns.
+ * out[v][b] = W(v) . x_b for the R (virtual) rows v of one ring stage --
+ * virtual row v at byte ro(v) of the stage -- and the NB token vectors x_b
+ * (pitch xp elements), on the tensor cores: the tokens are the M side of an
+ * m16n8k16 tile, eight weight rows the N side, and the fp32 sums come out of
+ * the accumulator already reduced over K.  Each thread reads 16-byte pieces
+ * of A and B at the same column offsets of each 64-column block, so the k
+ * order inside a block is a permutation of its columns, the same on both
+ * sides of every product that is kept, and each sum is over all columns.
  * Four accumulators (one per k step) keep the mma chains independent.
  * epi(n0, sums of the n-tile at rows n0.., sums of the n-tile at n0 + 8..,
- * whether that second tile exists) runs on every lane; see take_out. */
+ * whether that second tile exists) runs on every lane; see take_out.
+ *
+ * A quarter-warp's load covers B columns (virtual rows) 2i and 2i + 1 at the
+ * same offsets.  Two layouts keep those loads free of bank conflicts:
+ *
+ * - Eight tokens (the stage's second run 64 bytes out of line, activations
+ *   at pitch K + 32): the two rows, and the two tokens, already sit in
+ *   opposite halves of the bank window.  Token g is A row g (rows 8..15
+ *   zero); thread (g, t) reads columns 8t.. and 32 + 8t.. and ends with
+ *   token g against rows n0 + 2t (c0) and n0 + 2t + 1 (c1).
+ * - Fewer tokens (contiguous runs, all rows in the same banks): odd-g
+ *   threads read the upper half of each 128-byte block first.  That changes
+ *   which columns feed which k slot on odd threads, so token b is entered
+ *   twice on the M side, row 2b with the even order and row 2b + 1 with the
+ *   odd one, and C[m][n] is valid where m and n have the same parity: thread
+ *   (g, t) ends with row n0 + 2t + (g & 1) for token g / 2 (c0 or c1). */
 template <int NB, class RowMap, class Epi>
-__device__ __forceinline__ void mma_rows(const uint8_t *st, int R, int pitch, int K,
-                                         const uint16_t *x, int xp, int lane, RowMap &&rm,
-                                         Epi &&epi) {
-  const int g = lane >> 2, t = lane & 3, q = g & 1;
-  const int ta = g >> 1, tb = 4 + (g >> 1);
-  const bool ha = ta < NB, hb = NB > 4 && tb < NB;
-  const int f0 = 8 * t + 32 * q;  /* first piece of each 64-column block */
-  const int sd = q ? -32 : 32;    /* the second piece, relative to the first */
-  const uint16_t *xa = x + (size_t)(ha ? ta : 0) * xp + f0;
-  const uint16_t *xb = x + (size_t)(hb ? tb : 0) * xp + f0;
+__device__ __forceinline__ void mma_rows(const uint8_t *st, int R, int K, const uint16_t *x,
+                                         int xp, int lane, RowMap &&ro, Epi &&epi) {
+  static_assert(NB >= MK_RUN_GAP_MIN_NB || NB <= 4, "duplicated tokens fill at most 8 A rows");
+  const int g = lane >> 2, t = lane & 3;
+  constexpr bool kGap = NB >= MK_RUN_GAP_MIN_NB;
+  const int q = kGap ? 0 : (g & 1);
+  const int tok = kGap ? g : (g >> 1);
+  const bool hx = tok < NB;
+  const int f0 = 8 * t + 32 * q; /* first piece of each 64-column block */
+  const int sd = q ? -32 : 32;   /* the second piece, relative to the first */
+  const uint16_t *xa = x + (size_t)(hx ? tok : 0) * xp + f0;
   for (int n0 = 0; n0 < R; n0 += 16) {
     const bool two = n0 + 8 < R;
-    const uint16_t *wa = (const uint16_t *)(st + (size_t)rm(min(n0 + g, R - 1)) * pitch) + f0;
-    const uint16_t *wb = (const uint16_t *)(st + (size_t)rm(min(n0 + 8 + g, R - 1)) * pitch) + f0;
+    /* rows past R: nothing loaded (eight tokens) or the last row again */
+    const bool ra = !kGap || n0 + g < R, rb = !kGap || n0 + 8 + g < R;
+    const uint16_t *wa = (const uint16_t *)(st + ro(min(n0 + g, R - 1))) + f0;
+    const uint16_t *wb = (const uint16_t *)(st + ro(min(n0 + 8 + g, R - 1))) + f0;
     float ca[4][4], cb[4][4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -396,26 +405,29 @@ __device__ __forceinline__ void mma_rows(const uint8_t *st, int R, int pitch, in
       for (int k = 0; k < 4; ++k) ca[i][k] = cb[i][k] = 0.0f;
 #pragma unroll 2
     for (int c0 = 0; c0 < K; c0 += 64) {
-      uint4 af = make_uint4(0, 0, 0, 0), as = af, bf = af, bs = af;
-      if (ha) {
+      uint4 af = make_uint4(0, 0, 0, 0), as = af, wf = af, ws = af;
+      if (hx) {
         af = *(const uint4 *)(xa + c0);
         as = *(const uint4 *)(xa + c0 + sd);
       }
-      if (hb) {
-        bf = *(const uint4 *)(xb + c0);
-        bs = *(const uint4 *)(xb + c0 + sd);
+      if (ra) {
+        wf = *(const uint4 *)(wa + c0);
+        ws = *(const uint4 *)(wa + c0 + sd);
       }
-      const uint4 wf = *(const uint4 *)(wa + c0), ws = *(const uint4 *)(wa + c0 + sd);
-      mma16816(ca[0], af.x, bf.x, af.y, bf.y, wf.x, wf.y);
-      mma16816(ca[1], af.z, bf.z, af.w, bf.w, wf.z, wf.w);
-      mma16816(ca[2], as.x, bs.x, as.y, bs.y, ws.x, ws.y);
-      mma16816(ca[3], as.z, bs.z, as.w, bs.w, ws.z, ws.w);
+      mma16816(ca[0], af.x, 0u, af.y, 0u, wf.x, wf.y);
+      mma16816(ca[1], af.z, 0u, af.w, 0u, wf.z, wf.w);
+      mma16816(ca[2], as.x, 0u, as.y, 0u, ws.x, ws.y);
+      mma16816(ca[3], as.z, 0u, as.w, 0u, ws.z, ws.w);
       if (two) {
-        const uint4 vf = *(const uint4 *)(wb + c0), vs = *(const uint4 *)(wb + c0 + sd);
-        mma16816(cb[0], af.x, bf.x, af.y, bf.y, vf.x, vf.y);
-        mma16816(cb[1], af.z, bf.z, af.w, bf.w, vf.z, vf.w);
-        mma16816(cb[2], as.x, bs.x, as.y, bs.y, vs.x, vs.y);
-        mma16816(cb[3], as.z, bs.z, as.w, bs.w, vs.z, vs.w);
+        uint4 vf = make_uint4(0, 0, 0, 0), vs = vf;
+        if (rb) {
+          vf = *(const uint4 *)(wb + c0);
+          vs = *(const uint4 *)(wb + c0 + sd);
+        }
+        mma16816(cb[0], af.x, 0u, af.y, 0u, vf.x, vf.y);
+        mma16816(cb[1], af.z, 0u, af.w, 0u, vf.z, vf.w);
+        mma16816(cb[2], as.x, 0u, as.y, 0u, vs.x, vs.y);
+        mma16816(cb[3], as.z, 0u, as.w, 0u, vs.z, vs.w);
       }
     }
     float sa[4], sb[4];
@@ -428,15 +440,21 @@ __device__ __forceinline__ void mma_rows(const uint8_t *st, int R, int pitch, in
   }
 }
 
-/* The valid outputs of one n-tile of mma_rows on this lane: f(v, b, value)
- * for virtual row v = n0 + 2t + (g & 1) (< R) and tokens g / 2 and
- * 4 + g / 2 (< NB). */
+/* The valid outputs of one n-tile of mma_rows on this lane, f(v, b, value):
+ * eight tokens, token g against virtual rows n0 + 2t and n0 + 2t + 1; fewer,
+ * token g / 2 against row n0 + 2t + (g & 1).  Rows < R, tokens < NB. */
 template <int NB, class F>
 __device__ __forceinline__ void take_out(int n0, const float (&c)[4], int R, int lane, F &&f) {
-  const int g = lane >> 2, t = lane & 3, q = g & 1, v = n0 + 2 * t + q;
-  if (v < R) {
-    if ((g >> 1) < NB) f(v, g >> 1, q ? c[1] : c[0]);
-    if (NB > 4 && 4 + (g >> 1) < NB) f(v, 4 + (g >> 1), q ? c[3] : c[2]);
+  const int g = lane >> 2, t = lane & 3;
+  if (NB >= MK_RUN_GAP_MIN_NB) {
+    const int v = n0 + 2 * t;
+    if (g < NB) {
+      if (v < R) f(v, g, c[0]);
+      if (v + 1 < R) f(v + 1, g, c[1]);
+    }
+  } else {
+    const int q = g & 1, v = n0 + 2 * t + q;
+    if (v < R && (g >> 1) < NB) f(v, g >> 1, q ? c[1] : c[0]);
   }
 }
 
@@ -983,18 +1001,26 @@ struct Producer {
     const uint64_t tb = strc ? sclock() : 0;
     uint8_t *dst = cx.ring() + (size_t)slot * cx.SB;
     uint64_t *bar = &cx.full()[slot];
-    if (d.kind == SK_ROWS) {
-      const uint32_t bytes = d.n * d.row_bytes;
-      mbar_expect_tx(bar, bytes);
-      bulk_g2s(dst, d.a, bytes, bar, policy);
+    if (d.kind == SK_ROWS || d.kind == SK_PAIRS) {
+      /* two runs, the second mk_run_gap bytes past the first (one copy for
+       * plain rows where the gap is 0) */
+      const int nr = d.kind == SK_PAIRS ? 2 * d.n : d.n;
+      const uint32_t rb = d.row_bytes;
+      mbar_expect_tx(bar, (uint32_t)nr * rb);
+      if (d.kind == SK_PAIRS) {
+        bulk_g2s(dst, d.a, d.n * rb, bar, policy);
+        bulk_g2s(dst + d.n * rb + mk_run_gap(NB), d.b, d.n * rb, bar, policy);
+      } else if (mk_run_gap(NB) == 0) {
+        bulk_g2s(dst, d.a, d.n * rb, bar, policy);
+      } else {
+        const uint32_t h = (uint32_t)(d.n + 1) / 2;
+        bulk_g2s(dst, d.a, h * rb, bar, policy);
+        if ((uint32_t)d.n > h)
+          bulk_g2s(dst + h * rb + mk_run_gap(NB), d.a + (size_t)h * rb, (d.n - h) * rb, bar, policy);
+      }
     } else if (d.kind == SK_BOX) {
       mbar_expect_tx(bar, d.row_bytes);
       tensor_g2s_2d(dst, d.a, d.pages[0], d.pages[1], bar, policy);
-    } else if (d.kind == SK_PAIRS) {
-      const uint32_t bytes = d.n * d.row_bytes;
-      mbar_expect_tx(bar, 2 * bytes);
-      bulk_g2s(dst, d.a, bytes, bar, policy);
-      bulk_g2s(dst + bytes, d.b, bytes, bar, policy);
     } else {
       const int P = p.P, layer = d.layer_kvh >> 8, kvh = d.layer_kvh & 0xFF;
       const uint32_t half = (uint32_t)P * p.D * 2, pgb = 2 * half;
@@ -1081,7 +1107,7 @@ struct Producer {
                               : t[1] == 1 ? ly->wk
                                           : ly->wv;
           const uint16_t *src = w + (size_t)t[2] * d;
-          const int nrows = t[3], rps = mk_rows_per_stage(d, SB);
+          const int nrows = t[3], rps = mk_rows_per_stage(d, SB, NB);
           const int rn = op == OP_QKV ? t[5] : 0;
           const uint16_t *rsrc = ly->wr + (size_t)(op == OP_QKV ? t[4] : 0) * d;
           const int n_rst = (rn + rps - 1) / rps, n_st = n_rst + (nrows + rps - 1) / rps;
@@ -1123,7 +1149,7 @@ struct Producer {
           const int nbf = F / MK_FOLD_COLS, T64 = U * nbf;
           const int b0 = (int)((int64_t)T64 * t[1] / t[2]);
           const int b1 = (int)((int64_t)T64 * (t[1] + 1) / t[2]);
-          const int rps = mk_rows_per_stage(d, SB), ng = (MK_FOLD_COLS + rps - 1) / rps;
+          const int rps = mk_rows_per_stage(d, SB, NB), ng = (MK_FOLD_COLS + rps - 1) / rps;
           const int BR = p.fold_rows, nrb = d / BR;
           const int nA = (b1 - b0) * 2 * ng, nB = (b1 - b0) * nrb;
           ok = run_stages(base, 0, nA + nB, [&](int j, QDesc &q) {
@@ -1153,7 +1179,7 @@ struct Producer {
             break;
           }
           t_plan = strc ? sclock() : 0;
-          const int pps = mk_pairs_per_stage(d, SB);
+          const int pps = mk_pairs_per_stage(d, SB, NB);
           const int64_t T = (int64_t)U * F;
           const int64_t v = T * t[1] / t[2], v1 = T * (t[1] + 1) / t[2];
           /* stages per expert segment, as the consumers walk them */
@@ -1195,7 +1221,7 @@ struct Producer {
             break;
           }
           t_plan = strc ? sclock() : 0;
-          const int rps = mk_rows_per_stage(F, SB);
+          const int rps = mk_rows_per_stage(F, SB, NB);
           const int64_t T = (int64_t)U * d;
           const int64_t v = T * t[1] / t[2], v1 = T * (t[1] + 1) / t[2];
           const int u0 = (int)(v / d), u1 = v1 > v ? (int)((v1 - 1) / d) : u0 - 1;
@@ -1226,7 +1252,7 @@ struct Producer {
            * into the gate/up shares at batch 1) */
           const int r0 = t[2], nr = t[3];
           t_plan = strc ? sclock() : 0;
-          const int rps_o = mk_rows_per_stage(HqD, SB), n_wo = (nr + rps_o - 1) / rps_o;
+          const int rps_o = mk_rows_per_stage(HqD, SB, NB), n_wo = (nr + rps_o - 1) / rps_o;
           const uint16_t *wo = ly->wo + (size_t)r0 * HqD;
           ok = run_stages(base, 0, n_wo, [&](int jw, QDesc &q) {
             q.kind = SK_ROWS;
@@ -1415,7 +1441,7 @@ struct Consumer {
    * as any other evaluation that rounds the exact mean once. */
   __device__ bool norm_into_xbuf(int src, const uint16_t *g) {
     const mk_kparams &p = *cx.p;
-    const int xp = mk_x_pitch(p.d), B = p.B;
+    const int xp = mk_x_pitch(p.d, NB), B = p.B;
     uint16_t *x = cx.xn();
     uint16_t *raw = (uint16_t *)cx.xbuf();
     const int n8 = p.d / 8, dw = p.d / 2;
@@ -1519,10 +1545,10 @@ struct Consumer {
     return ok;
   }
 
-  /* Copies NB vectors of n bf16 (global, row stride gstride) into xbuf at
-   * pitch n + 32; rows b >= B zero.  No barrier. */
+  /* Copies NB vectors of n bf16 (global, row stride gstride) into dst at
+   * the activation pitch mk_x_pitch(n); rows b >= B zero.  No barrier. */
   __device__ void load_x(uint16_t *dst, const uint16_t *src, size_t gstride, int n) {
-    const int xp = mk_x_pitch(n), n8 = n / 8, B = cx.p->B;
+    const int xp = mk_x_pitch(n, NB), n8 = n / 8, B = cx.p->B;
     for (int i = tid; i < NB * n8; i += NCT) {
       const int b = i / n8, c = i % n8;
       const uint4 v = b < B ? __ldcg((const uint4 *)(src + (size_t)b * gstride) + c)
@@ -1551,33 +1577,37 @@ struct Consumer {
     return bar_any(last);
   }
 
-  /* nrows streamed rows of K elements against the activations x (pitch
-   * K + 32); each stage is computed by the warp that owns it and row r
-   * (index within the task) handed to epi(r, b, value). */
   /* The cnt rows of one ring stage (K elements each) against the
-   * activations x (pitch K); row r of the stage handed to epi(r, b, value). */
+   * activations x (pitch mk_x_pitch(K)); row r of the stage handed to
+   * epi(r, b, value). */
   template <class Epi>
   __device__ __forceinline__ void gemv_stage(const uint8_t *st, int cnt, int K, const uint16_t *x,
                                              Epi &&epi) {
-    const int pitch = mk_row_pitch(K), xp = mk_x_pitch(K);
     if (NB == 1 && kB1CudaCores) {
-      cc_rows(st, cnt, pitch, K, x, lane, 0,
+      cc_rows(st, cnt, 2 * K, K, x, lane, 0,
               [&](int n0, float sum, int nr) {
                 if ((lane & 3) == 0 && (lane >> 2) < nr) epi(n0 + (lane >> 2), 0, sum);
               });
     } else {
-      mma_rows<NB>(st, cnt, pitch, K, x, xp, lane, [](int v) { return v; },
+      /* virtual row 2i is row i of the first run, 2i + 1 row h + i */
+      const int rb = 2 * K, h = (cnt + 1) >> 1, hb = h * rb + mk_run_gap(NB);
+      auto f = [&](int v, int bb, float val) { epi((v & 1) ? h + (v >> 1) : (v >> 1), bb, val); };
+      mma_rows<NB>(st, cnt, K, x, mk_x_pitch(K, NB), lane,
+                   [=](int v) { return (v & 1) ? hb + (v >> 1) * rb : (v >> 1) * rb; },
                    [&](int n0, const float(&a)[4], const float(&b)[4], bool two) {
-                     take_out<NB>(n0, a, cnt, lane, epi);
-                     if (two) take_out<NB>(n0 + 8, b, cnt, lane, epi);
+                     take_out<NB>(n0, a, cnt, lane, f);
+                     if (two) take_out<NB>(n0 + 8, b, cnt, lane, f);
                    });
     }
   }
 
+  /* nrows streamed rows of K elements against the activations x; each
+   * stage is computed by the warp that owns it and row r (index within the
+   * task) handed to epi(r, b, value). */
   template <class Epi>
   __device__ void gemv_rows(int nrows, int K, const uint16_t *x, int task, int op, int layer,
                             Epi &&epi) {
-    const int rps = mk_rows_per_stage(K, cx.SB);
+    const int rps = mk_rows_per_stage(K, cx.SB, NB);
     const int n_st = (nrows + rps - 1) / rps;
     for (int j = first_mine(); j < n_st; j += NC) {
       uint8_t *st;
@@ -1606,7 +1636,7 @@ struct Consumer {
     float *lg = p.router_logits + (size_t)layer * MK_MAX_BATCH * E;
     uint64_t *lgt = p.lg_tag + (size_t)layer * MK_MAX_BATCH * E;
     const float *bias = layer < MK_PARAM_LAYERS ? p.l_bias[layer] : p.layers[layer].bias;
-    const int rps = mk_rows_per_stage(d, cx.SB);
+    const int rps = mk_rows_per_stage(d, cx.SB, NB);
     const int n_rst = (rn + rps - 1) / rps, n_st = n_rst + (nrows + rps - 1) / rps;
     const uint16_t *x = cx.xn();
     for (int j = first_mine(); j < n_st; j += NC) {
@@ -2144,13 +2174,13 @@ struct Consumer {
     const int nbf = p.F / MK_FOLD_COLS, T64 = U * nbf;
     const int b0 = (int)((int64_t)T64 * t[1] / t[2]);
     const int b1 = (int)((int64_t)T64 * (t[1] + 1) / t[2]);
-    const int rps = mk_rows_per_stage(d, cx.SB), ng = (MK_FOLD_COLS + rps - 1) / rps;
+    const int rps = mk_rows_per_stage(d, cx.SB, NB), ng = (MK_FOLD_COLS + rps - 1) / rps;
     const int BR = p.fold_rows, nrb = d / BR;
     const int nA = (b1 - b0) * 2 * ng, nB = (b1 - b0) * nrb;
     float *gsm = (float *)cx.xbuf();
     float *usm = gsm + (b1 - b0) * MK_FOLD_COLS;
     const uint16_t *x = cx.xn();
-    const int pitch = mk_row_pitch(d);
+    const int pitch = 2 * d; /* batch 1: contiguous rows */
     for (int j = first_mine(); j < nA; j += NC) {
       uint8_t *st;
       if (!stage_wait(si + j, st, task, OP_UP, layer)) break;
@@ -2219,7 +2249,7 @@ struct Consumer {
     int64_t v = T * t[1] / t[2];
     const int64_t v1 = T * (t[1] + 1) / t[2];
     const uint16_t *x = cx.xn();
-    const int pps = mk_pairs_per_stage(d, cx.SB), pitch = mk_row_pitch(d), xp = mk_x_pitch(d);
+    const int pps = mk_pairs_per_stage(d, cx.SB, NB), rb = 2 * d, xp = mk_x_pitch(d, NB);
     int j = 0; /* stage index within the task */
     while (v < v1) {
       const int u = (int)(v / F), f0 = (int)(v % F);
@@ -2237,33 +2267,37 @@ struct Consumer {
             out[(size_t)bb * F + f + pr] = f2bf(silu * ub);
           }
         };
-        auto pairmap = [cnt](int vr) { return (vr & 1) ? cnt + (vr >> 1) : (vr >> 1); };
         if (NB == 1 && kB1CudaCores) {
           /* virtual row 2j is gate row j, 2j + 1 up row j: lanes 8j'..8j'+3
            * hold the gate sum, the next four lanes the up sum */
-          cc_rows(st, 2 * cnt, pitch, d, x, lane, cnt, [&](int n0, float sum, int nr) {
+          cc_rows(st, 2 * cnt, rb, d, x, lane, cnt, [&](int n0, float sum, int nr) {
             const float up = __shfl_xor_sync(0xFFFFFFFFu, sum, 4);
             const int r = lane >> 2;
             if ((lane & 7) == 0 && r + 1 < nr) swiglu(0, (n0 + r) >> 1, sum, up);
           });
         } else {
-          /* the lanes of a token hold gate (even g) and up (odd g) of the
-           * same pair four lanes apart */
+          /* virtual rows 2j (gate) and 2j + 1 (up) of pair j, the up rows
+           * being the stage's second run.  Eight tokens: both on one lane
+           * (c0, c1 of token g, pair n0 / 2 + t); fewer: gate on even g,
+           * up on odd g, four lanes apart. */
+          const int ub = cnt * rb + mk_run_gap(NB);
           mma_rows<NB>(
-              st, 2 * cnt, pitch, d, x, xp, lane, pairmap,
+              st, 2 * cnt, d, x, xp, lane,
+              [=](int vr) { return (vr & 1) ? ub + (vr >> 1) * rb : (vr >> 1) * rb; },
               [&](int n0, const float(&a)[4], const float(&b)[4], bool two) {
-                const int g = lane >> 2, tq = lane & 3, q = g & 1;
+                const int g = lane >> 2, tq = lane & 3;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                  if (h == 1 && !two) break;
-                  const float(&c)[4] = h ? b : a;
-                  const float va = q ? c[1] : c[0], vb = q ? c[3] : c[2];
-                  const float oa = __shfl_xor_sync(0xFFFFFFFFu, va, 4);
-                  const float ob = __shfl_xor_sync(0xFFFFFFFFu, vb, 4);
-                  const int pr = ((n0 + 8 * h) >> 1) + tq; /* pair within the stage */
-                  if (q == 0 && pr < cnt) {
-                    if ((g >> 1) < NB) swiglu(g >> 1, pr, va, oa);
-                    if (NB > 4 && 4 + (g >> 1) < NB) swiglu(4 + (g >> 1), pr, vb, ob);
+                for (int hh = 0; hh < 2; ++hh) {
+                  if (hh == 1 && !two) break;
+                  const float(&c)[4] = hh ? b : a;
+                  const int pr = ((n0 + 8 * hh) >> 1) + tq; /* pair within the stage */
+                  if (NB >= MK_RUN_GAP_MIN_NB) {
+                    if (g < NB && pr < cnt) swiglu(g, pr, c[0], c[1]);
+                  } else {
+                    const int q = g & 1;
+                    const float va = q ? c[1] : c[0];
+                    const float oa = __shfl_xor_sync(0xFFFFFFFFu, va, 4);
+                    if (q == 0 && pr < cnt && (g >> 1) < NB) swiglu(g >> 1, pr, va, oa);
                   }
                 }
               });
@@ -2294,7 +2328,7 @@ struct Consumer {
     const int64_t T = (int64_t)U * d;
     int64_t v = T * t[1] / t[2];
     const int64_t v1 = T * (t[1] + 1) / t[2];
-    const int rps = mk_rows_per_stage(F, cx.SB), pitch = mk_row_pitch(F), xpf = mk_x_pitch(F);
+    const int rps = mk_rows_per_stage(F, cx.SB, NB), xpf = mk_x_pitch(F, NB);
     uint16_t *xa = (uint16_t *)cx.xbuf();
     float *dp = p.dpart + (size_t)(layer & 1) * p.u_max * MK_MAX_BATCH * d;
     int j = 0; /* stage index within the task */
@@ -2473,39 +2507,39 @@ struct Consumer {
     const int v0 = t[2];
     /* each lane keeps the best of the rows it computed for its two tokens
      * (g / 2 and 4 + g / 2) */
-    float best_v[2] = {NEG_INF, NEG_INF};
-    int best_i[2] = {0x7FFFFFFF, 0x7FFFFFFF};
+    /* each lane sees the rows of one token: token 0 on every lane on the
+     * CUDA cores; on the tensor cores token lane / 4 with eight tokens,
+     * lane / 8 with fewer */
+    float best_v = NEG_INF;
+    int best_i = 0x7FFFFFFF;
     float *logits = p.out_logits;
     const int V = p.V;
     gemv_rows(t[3], p.d, cx.xn(), task, OP_LM, L, [&](int r, int bb, float v) {
       if (bb < B) {
         if (logits) logits[(size_t)bb * V + v0 + r] = v;
-        const int k = bb >= 4;
-        if (v > best_v[k] || (v == best_v[k] && v0 + r < best_i[k])) {
-          best_v[k] = v;
-          best_i[k] = v0 + r;
+        if (v > best_v || (v == best_v && v0 + r < best_i)) {
+          best_v = v;
+          best_i = v0 + r;
         }
       }
     });
-    /* the lanes holding a token's rows (all 32 for one token on the CUDA
-     * cores; lanes 8b..8b+7 on the tensor cores), then the warps */
+    /* the lanes holding a token's rows, then the warps */
     auto &LM = M()->u.lm;
-    constexpr int LANES = (NB == 1 && kB1CudaCores) ? 32 : 8;
+    constexpr int LANES = (NB == 1 && kB1CudaCores) ? 32 : NB >= MK_RUN_GAP_MIN_NB ? 4 : 8;
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-#pragma unroll
-      for (int s = 1; s < LANES; s <<= 1) {
-        const float ov = __shfl_xor_sync(0xFFFFFFFFu, best_v[k], s);
-        const int oi = __shfl_xor_sync(0xFFFFFFFFu, best_i[k], s);
-        if (ov > best_v[k] || (ov == best_v[k] && oi < best_i[k])) {
-          best_v[k] = ov;
-          best_i[k] = oi;
-        }
+    for (int s = 1; s < LANES; s <<= 1) {
+      const float ov = __shfl_xor_sync(0xFFFFFFFFu, best_v, s);
+      const int oi = __shfl_xor_sync(0xFFFFFFFFu, best_i, s);
+      if (ov > best_v || (ov == best_v && oi < best_i)) {
+        best_v = ov;
+        best_i = oi;
       }
-      const int bb = 4 * k + lane / LANES;
+    }
+    {
+      const int bb = lane / LANES;
       if (lane % LANES == 0 && bb < NB) {
-        LM.best[warp][bb][0] = best_v[k];
-        LM.best[warp][bb][1] = __int_as_float(best_i[k]);
+        LM.best[warp][bb][0] = best_v;
+        LM.best[warp][bb][1] = __int_as_float(best_i);
       }
     }
     if (!task_end()) return false;

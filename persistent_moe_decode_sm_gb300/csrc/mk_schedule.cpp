@@ -67,7 +67,7 @@ int mk_nb_for(int batch) { return batch <= 1 ? 1 : batch <= 2 ? 2 : batch <= 4 ?
 /* The scratch buffer: the largest of what the task types stage there (bf16
  * vectors at pitch K). */
 static size_t xn_bytes_for(const mk_model_dims &d, int nb) {
-  return align_up((size_t)nb * 2 * mk_x_pitch(d.d_model), 128);
+  return align_up((size_t)nb * 2 * mk_x_pitch(d.d_model, nb), 128);
 }
 
 static size_t xbuf_bytes_for(const mk_model_dims &d, int nb) {
@@ -75,9 +75,9 @@ static size_t xbuf_bytes_for(const mk_model_dims &d, int nb) {
   size_t x = (size_t)nb * 2 * d.d_model;                         /* staged h of the norm */
   /* the attention output (Wo's input) is staged across the normed-input
    * buffer and this one, which follows it: the normed input is dead by then */
-  const size_t wo_in = (size_t)nb * 2 * mk_x_pitch((int)HqD), xn = xn_bytes_for(d, nb);
+  const size_t wo_in = (size_t)nb * 2 * mk_x_pitch((int)HqD, nb), xn = xn_bytes_for(d, nb);
   x = std::max(x, wo_in > xn ? wo_in - xn : (size_t)0);
-  x = std::max(x, (size_t)nb * 2 * mk_x_pitch(d.d_ffn));          /* one expert's activations */
+  x = std::max(x, (size_t)nb * 2 * mk_x_pitch(d.d_ffn, nb));          /* one expert's activations */
   /* attention: q (bf16 [8][D + 8]), new k and v (fp32 [D] each), merge
    * scratch fp32 [4][8][D + 8] */
   x = std::max(x, 8 * (D + 8) * 2 + 2 * D * 4 + 4 * 8 * (D + 8) * 4);
@@ -99,8 +99,9 @@ bool mk_smem_plan(const mk_model_dims *dm, int nb, MkSmem *out) {
   s.stage_bytes = (int)sb;
   s.ring_slots = MK_NC_WARPS;
   const int HqD = d.n_q_heads * d.head_dim;
-  if (mk_rows_per_stage(d.d_model, s.stage_bytes) < 2 || mk_rows_per_stage(HqD, s.stage_bytes) < 1 ||
-      mk_rows_per_stage(d.d_ffn, s.stage_bytes) < 1 ||
+  if (mk_rows_per_stage(d.d_model, s.stage_bytes, nb) < 2 ||
+      mk_rows_per_stage(HqD, s.stage_bytes, nb) < 1 ||
+      mk_rows_per_stage(d.d_ffn, s.stage_bytes, nb) < 1 ||
       mk_pages_per_stage(d.page_size, d.head_dim, s.stage_bytes) < 1)
     return false;
   s.total = (size_t)MK_NC_WARPS * sb + s.xn + s.xbuf + s.misc;
