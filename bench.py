@@ -273,7 +273,10 @@ def run_mk(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded bf16 N(0,0.02) weights, N(0,1) KV; no trained weights)",
-        "config": headline_config(lens, args.steps, world),
+        "config": (headline_config(lens, args.steps, world) if not args.layers and B == 1 else
+                   {**headline_config(lens, args.steps, world),
+                    "workload": f"profiling cut of the full-scale synthetic MoE: {dims.n_layers} layers, "
+                                f"batch {B} at {lens[0]} cached tokens (not a bench line)"}),
         "sol": {"bytes_per_step": round(bytes_per_step), "weight_bytes_per_step":
                 round(w_bytes / args.steps), "kv_bytes_per_step": round(kv_bytes / args.steps),
                 "sol_tok_s": round(sol_tok_s, 1), "fraction": round(tok_s / world / sol_tok_s, 4),
