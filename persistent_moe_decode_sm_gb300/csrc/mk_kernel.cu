@@ -806,8 +806,9 @@ __device__ bool wait_mbar(const Ctx &cx, uint64_t *bar, uint32_t parity, int tas
  * published and polled before the expert weights can be fetched.
  *
  * route_warp: the batch's distinct chosen experts for a producer warp that
- * needs them before its CTA's consumers take the routing (expert down rows
- * in an OUT task).  One warp, the NT <= 8 tokens' selections interleaved so
+ * needs them before its CTA's consumers take the routing (a share of
+ * expert down rows on a CTA whose consumers are still in attention).  One
+ * warp, the NT <= 8 tokens' selections interleaved so
  * that their reduction chains overlap.  Per token: K rounds of a warp argmax
  * over the E <= 128 fp32 logits (lane l holds experts l, l + 32, l + 64,
  * l + 96), ties to the lower expert id -- the same selection as the
@@ -953,9 +954,9 @@ struct Producer {
    * have taken it (they start the share right after the CTA's QKV task); it
    * stays valid while a producer warp copies it, as the consumers cannot
    * leave the share before every producer warp has issued its stages of it.
-   * For expert down rows in an OUT task (whose consumers take the routing
-   * only after their attention splits) the warp takes the top-k itself from
-   * the tagged logits.  Returns U, or -1 on timeout / abort. */
+   * For a share of expert down rows (whose consumers take the routing only
+   * after their attention splits) the warp takes the top-k itself from the
+   * tagged logits.  Returns U, or -1 on timeout / abort. */
   __device__ int routed(int layer, bool from_consumers) {
     const mk_kparams &p = *cx.p;
     if (r_layer == layer) return *(volatile int32_t *)pU;
@@ -2505,8 +2506,6 @@ struct Consumer {
       if (!norm_into_xbuf(L, p.final_norm)) return false;
     }
     const int v0 = t[2];
-    /* each lane keeps the best of the rows it computed for its two tokens
-     * (g / 2 and 4 + g / 2) */
     /* each lane sees the rows of one token: token 0 on every lane on the
      * CUDA cores; on the tensor cores token lane / 4 with eight tokens,
      * lane / 8 with fewer */
