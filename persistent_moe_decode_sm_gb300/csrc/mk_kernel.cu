@@ -55,8 +55,8 @@
 namespace mk {
 
 constexpr int NC = MK_NC_WARPS;
-/* Batch 1 on the CUDA cores (packed fp32x2 FMAs) or, like batch 2..8, on the
- * tensor cores (one token in the M rows of m16n8k16). */
+/* Batch 1 on the CUDA cores (fp32 FMAs straight on the bf16 halves) or, like
+ * batch 2..8, on the tensor cores (one token in the M rows of m16n8k16). */
 constexpr bool kB1CudaCores = true;
 constexpr int NCT = NC * 32;
 static_assert(NC % MK_NP_WARPS == 0, "each ring slot must have one producer");
@@ -479,29 +479,24 @@ __device__ __forceinline__ float transpose_reduce8(float (&v)[8], int lane) {
   return s;
 }
 
-__device__ __forceinline__ unsigned long long pack2(uint32_t lo, uint32_t hi) {
-  unsigned long long r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
-  return r;
-}
-
-/* two fp32 FMAs in one instruction (lanes of the pair independent) */
-__device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsigned long long b,
-                                                     unsigned long long c) {
-  unsigned long long d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+/* acc + a * b on the low (H = 0) or high (H = 1) bf16 halves of the words a
+ * and b, in fp32 with one rounding: a product of two bf16 values is exact in
+ * fp32, so this is the fp32 fma of the two values -- with no separate
+ * conversion of either operand. */
+template <int H>
+__device__ __forceinline__ float fma_bf16h(uint32_t a, uint32_t b, float acc) {
+  float d;
+  if (H == 0)
+    asm("{\n .reg .b16 al, ah, bl, bh;\n mov.b32 {al, ah}, %1;\n mov.b32 {bl, bh}, %2;\n"
+        " fma.rn.f32.bf16 %0, al, bl, %3;\n}"
+        : "=f"(d)
+        : "r"(a), "r"(b), "f"(acc));
+  else
+    asm("{\n .reg .b16 al, ah, bl, bh;\n mov.b32 {al, ah}, %1;\n mov.b32 {bl, bh}, %2;\n"
+        " fma.rn.f32.bf16 %0, ah, bh, %3;\n}"
+        : "=f"(d)
+        : "r"(a), "r"(b), "f"(acc));
   return d;
-}
-
-__device__ __forceinline__ float sum2(unsigned long long v) {
-  uint32_t lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(v));
-  return __uint_as_float(lo) + __uint_as_float(hi);
-}
-
-/* a bf16 pair (one 32-bit word) as an fp32 pair */
-__device__ __forceinline__ unsigned long long bf2_f2(uint32_t w) {
-  return pack2(w << 16, w & 0xFFFF0000u);
 }
 
 /* 8 bytes of shared memory at a shared-window address */
@@ -514,7 +509,10 @@ __device__ __forceinline__ uint2 lds64(uint32_t a) {
 /* NR rows (virtual n0 .. n0 + NR - 1) of one token on the CUDA cores; the
  * row count is a template parameter so that every load of the block can be
  * issued ahead of the FMAs.  st and x are shared-window addresses, read with
- * explicit shared loads.  v[r] gets this lane's partial sum of row r. */
+ * explicit shared loads.  Each 32-bit word of a row and of x holds two bf16
+ * columns; four accumulators per row (low and high halves of the two words a
+ * lane reads per chunk) keep the fma chains independent.  v[r] gets this
+ * lane's partial sum of row r. */
 template <int NR>
 __device__ __forceinline__ void cc_block(uint32_t st, int n0, int pitch, int K, uint32_t x,
                                          int lane, int pairs, float (&v)[8]) {
@@ -525,9 +523,9 @@ __device__ __forceinline__ void cc_block(uint32_t st, int n0, int pitch, int K, 
     const int row = pairs ? ((vr & 1) ? pairs + (vr >> 1) : (vr >> 1)) : vr;
     w[r] = st + (uint32_t)(row * pitch) + 8u * lane;
   }
-  unsigned long long a[NR][2];
+  float a[NR][4];
 #pragma unroll
-  for (int r = 0; r < NR; ++r) a[r][0] = a[r][1] = 0ULL;
+  for (int r = 0; r < NR; ++r) a[r][0] = a[r][1] = a[r][2] = a[r][3] = 0.0f;
   const uint32_t xl = x + 8u * lane;
   const int K128 = K & ~127; /* K is a multiple of 64: a half block may remain */
 #pragma unroll 2
@@ -536,25 +534,30 @@ __device__ __forceinline__ void cc_block(uint32_t st, int n0, int pitch, int K, 
     uint2 wv[NR];
 #pragma unroll
     for (int r = 0; r < NR; ++r) wv[r] = lds64(w[r] + 2u * c);
-    const unsigned long long x0 = bf2_f2(xv.x), x1 = bf2_f2(xv.y);
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
-      a[r][0] = ffma2(bf2_f2(wv[r].x), x0, a[r][0]);
-      a[r][1] = ffma2(bf2_f2(wv[r].y), x1, a[r][1]);
+      a[r][0] = fma_bf16h<0>(wv[r].x, xv.x, a[r][0]);
+      a[r][1] = fma_bf16h<1>(wv[r].x, xv.x, a[r][1]);
+      a[r][2] = fma_bf16h<0>(wv[r].y, xv.y, a[r][2]);
+      a[r][3] = fma_bf16h<1>(wv[r].y, xv.y, a[r][3]);
     }
   }
   if (K128 < K && lane < 16) {
     const uint2 xv = lds64(xl + 2u * K128);
-    const unsigned long long x0 = bf2_f2(xv.x), x1 = bf2_f2(xv.y);
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
       const uint2 wv = lds64(w[r] + 2u * K128);
-      a[r][0] = ffma2(bf2_f2(wv.x), x0, a[r][0]);
-      a[r][1] = ffma2(bf2_f2(wv.y), x1, a[r][1]);
+      a[r][0] = fma_bf16h<0>(wv.x, xv.x, a[r][0]);
+      a[r][1] = fma_bf16h<1>(wv.x, xv.x, a[r][1]);
+      a[r][2] = fma_bf16h<0>(wv.y, xv.y, a[r][2]);
+      a[r][3] = fma_bf16h<1>(wv.y, xv.y, a[r][3]);
     }
   }
 #pragma unroll
-  for (int r = 0; r < 8; ++r) v[r] = r < NR ? sum2(a[r < NR ? r : 0][0]) + sum2(a[r < NR ? r : 0][1]) : 0.0f;
+  for (int r = 0; r < 8; ++r) {
+    const int rr = r < NR ? r : 0;
+    v[r] = r < NR ? (a[rr][0] + a[rr][1]) + (a[rr][2] + a[rr][3]) : 0.0f;
+  }
 }
 
 /* One block of up to 8 rows of one token on the CUDA cores, out of line:
@@ -583,8 +586,8 @@ __device__ __noinline__ float cc_block_sum(uint32_t st, int n0, int nr, int pitc
 /* One token on the CUDA cores (a tensor-core tile would use 1 of its 16 M
  * rows): the rows of one ring stage (pitch bytes apart) against the bf16
  * activation x, up to eight rows per pass sharing each load of x.  Lane l
- * handles columns 4l + 128i (K a multiple of 64); each pair of products is
- * one packed fp32x2 FMA.  blk(n0, s, nr) runs on every lane with lane l
+ * handles columns 4l + 128i (K a multiple of 64); each product is one fp32
+ * FMA on the bf16 operands.  blk(n0, s, nr) runs on every lane with lane l
  * holding the sum of virtual row n0 + l / 4 (valid for l / 4 < nr). */
 template <class Blk>
 __device__ __forceinline__ void cc_rows(const uint8_t *st, int R, int pitch, int K,
@@ -2204,32 +2207,37 @@ struct Consumer {
       uint8_t *st;
       if (!stage_wait(sB + jb, st, task, OP_UP, layer)) break;
       const int kb = jb / nrb, r0 = (jb % nrb) * BR;
-      /* the block's 64 activations as fp32 pairs, the same on every lane */
-      unsigned long long a2[MK_FOLD_COLS / 2];
+      /* the block's 64 activations (bf16 values held as floats) as bf16
+       * pairs, the same on every lane */
+      uint32_t a16[MK_FOLD_COLS / 2];
       const float4 *a4 = (const float4 *)(gsm + kb * MK_FOLD_COLS);
 #pragma unroll
       for (int i = 0; i < MK_FOLD_COLS / 4; ++i) {
         const float4 v = a4[i];
-        a2[2 * i] = pack2(__float_as_uint(v.x), __float_as_uint(v.y));
-        a2[2 * i + 1] = pack2(__float_as_uint(v.z), __float_as_uint(v.w));
+        a16[2 * i] = (__float_as_uint(v.x) >> 16) | (__float_as_uint(v.y) & 0xFFFF0000u);
+        a16[2 * i + 1] = (__float_as_uint(v.z) >> 16) | (__float_as_uint(v.w) & 0xFFFF0000u);
       }
       /* box row r: 128 bytes, 16-byte chunk c stored at (c ^ (r & 7)) */
       const uint32_t sb = saddr(st);
       float *part = p.moe_part + (size_t)(layer & 1) * p.moe_part_stride + (size_t)(b0 + kb) * d + r0;
       for (int r = lane; r < BR; r += 32) {
-        unsigned long long acc0 = 0ULL, acc1 = 0ULL;
+        float m0 = 0.0f, m1 = 0.0f, m2 = 0.0f, m3 = 0.0f;
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
           uint4 w;
           asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                        : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
                        : "r"(sb + (uint32_t)(r * 128 + ((ch ^ (r & 7)) << 4))));
-          acc0 = ffma2(bf2_f2(w.x), a2[4 * ch], acc0);
-          acc1 = ffma2(bf2_f2(w.y), a2[4 * ch + 1], acc1);
-          acc0 = ffma2(bf2_f2(w.z), a2[4 * ch + 2], acc0);
-          acc1 = ffma2(bf2_f2(w.w), a2[4 * ch + 3], acc1);
+          m0 = fma_bf16h<0>(w.x, a16[4 * ch], m0);
+          m1 = fma_bf16h<1>(w.x, a16[4 * ch], m1);
+          m2 = fma_bf16h<0>(w.y, a16[4 * ch + 1], m2);
+          m3 = fma_bf16h<1>(w.y, a16[4 * ch + 1], m3);
+          m0 = fma_bf16h<0>(w.z, a16[4 * ch + 2], m0);
+          m1 = fma_bf16h<1>(w.z, a16[4 * ch + 2], m1);
+          m2 = fma_bf16h<0>(w.w, a16[4 * ch + 3], m2);
+          m3 = fma_bf16h<1>(w.w, a16[4 * ch + 3], m3);
         }
-        part[r] = sum2(acc0) + sum2(acc1);
+        part[r] = (m0 + m1) + (m2 + m3);
       }
       stage_release(sB + jb);
     }
