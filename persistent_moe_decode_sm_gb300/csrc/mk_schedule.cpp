@@ -110,6 +110,19 @@ bool mk_smem_plan(const mk_model_dims *dm, int nb, MkSmem *out) {
   return true;
 }
 
+/* Library-internal (tests): the ring geometry of the nb-token kernel --
+ * stage bytes, the rows of K bf16 one stage holds, and the total dynamic
+ * shared memory; 0 when the model does not fit. */
+extern "C" int mk_stage_geometry(const mk_model_dims *d, int nb, int K, int32_t *stage_bytes,
+                                 int32_t *rows, int64_t *dyn_bytes) {
+  MkSmem sm;
+  if (!d || !mk_smem_plan(d, nb, &sm)) return 0;
+  if (stage_bytes) *stage_bytes = sm.stage_bytes;
+  if (rows) *rows = mk_rows_per_stage(K, sm.stage_bytes, nb);
+  if (dyn_bytes) *dyn_bytes = (int64_t)sm.dyn;
+  return 1;
+}
+
 int mk_fold_rows(const mk_model_dims *d) {
   MkSmem sm;
   int lim = 64;

@@ -277,3 +277,29 @@ def test_out_tasks_fit_the_per_task_row_cap():
         for t in outs:
             cov[t[2]:t[2] + t[3]] += 1
         assert np.all(cov == 1)
+
+
+def test_stage_geometry_of_the_full_model():
+    """The ring stages the shared-memory plan leaves the full-scale model:
+    whole d-rows per stage (5 up to batch 4, 4 at batch 8, where the second
+    run of a stage sits 64 bytes out of line), Wo rows of 4096, expert down
+    rows of F, and the whole plan within the 227 KB a CTA may opt in to."""
+    import ctypes
+    d = synth.workloads()["full"].dims
+    cd = cdims(d, 8, 1024)
+    f = mk.lib().mk_stage_geometry
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.POINTER(type(cd)), ctypes.c_int, ctypes.c_int,
+                  ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
+                  ctypes.POINTER(ctypes.c_int64)]
+    want_rows = {1: 5, 2: 5, 4: 5, 8: 4}
+    for nb, rows_d in want_rows.items():
+        sb, rows, dyn = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int64()
+        assert f(ctypes.byref(cd), nb, d.d_model, ctypes.byref(sb), ctypes.byref(rows), ctypes.byref(dyn))
+        assert sb.value % 1024 == 0 and dyn.value <= 232448, (nb, sb.value, dyn.value)
+        assert rows.value == rows_d, (nb, rows.value)
+        gap = 64 if nb == 8 else 0
+        assert rows.value * 2 * d.d_model + gap <= sb.value
+        for K, least in ((d.n_q_heads * d.head_dim, 2), (d.d_ffn, 10)):
+            assert f(ctypes.byref(cd), nb, K, ctypes.byref(sb), ctypes.byref(rows), None)
+            assert rows.value >= least, (nb, K, rows.value)
