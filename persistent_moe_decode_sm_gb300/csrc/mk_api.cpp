@@ -86,6 +86,10 @@ struct mk_ctx {
   uint64_t wait_limit_ns = 1000000000ULL;
   int poison_layer = -1, poison_delta = 0;
   uint64_t steps = 0, rebuilds = 0;
+  /* the router's observed distinct experts per layer, for the role split */
+  double u_seen = 0.0;
+  int u_batch = 0;          /* batch size u_seen was observed at */
+  uint64_t u_sum_base = 0;  /* the device's sum of U when the schedule was built */
   uint32_t tag_serial = 0; /* the last step tag used (never reset) */
   mk_status sticky = MK_OK;
   bool prepared[4] = {false, false, false, false}; /* kernel attributes set per batch bucket */
@@ -138,7 +142,8 @@ mk_status upload_plan(mk_ctx *c, const MkPlan &p) {
 
 mk_status rebuild(mk_ctx *c) {
   MkPlan p;
-  mk_status st = mk_build_plan(&c->dims, c->n_sm, c->batch, c->lens.data(), &p);
+  mk_status st = mk_build_plan(&c->dims, c->n_sm, c->batch, c->lens.data(), &p,
+                               c->u_batch == c->batch ? c->u_seen : 0.0);
   if (st != MK_OK) return st;
   if (p.n_attn_slots > c->n_slots_max || p.n_lm > c->n_sm) return MK_ERR_INVALID_ARG;
   st = upload_plan(c, p);
@@ -438,6 +443,7 @@ mk_status mk_build_schedule(mk_ctx *c, int32_t batch, const int32_t *seq_lens,
       if (pg >= d.num_pages || pg < -1) return MK_ERR_PAGE_OOB;
     }
   }
+  const int prev_batch = c->scheduled ? c->batch : 0;
   c->batch = batch;
   c->lens.assign(seq_lens, seq_lens + batch);
   std::fill(c->page_table.begin(), c->page_table.end(), -1);
@@ -451,8 +457,18 @@ mk_status mk_build_schedule(mk_ctx *c, int32_t batch, const int32_t *seq_lens,
     e = cudaMemcpyAsync(c->page_table_dev, c->page_table.data(), c->page_table.size() * 4,
                         cudaMemcpyHostToDevice, c->stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
+  /* the distinct experts per layer that the previous schedule's steps saw
+   * (the stream is idle now), kept for schedules of the same batch size */
+  unsigned long long sum = 0;
+  if (e == cudaSuccess)
+    e = cudaMemcpy(&sum, &c->ctrl->sum_experts, sizeof(sum), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return MK_ERR_CUDA;
-  st = rebuild(c);
+  if (prev_batch > 0 && c->steps > 0 && sum > c->u_sum_base) {
+    c->u_seen = (double)(sum - c->u_sum_base) / ((double)c->steps * d.n_layers);
+    c->u_batch = prev_batch;
+  }
+  c->u_sum_base = sum;
+  st = rebuild(c); /* uses u_seen when it was observed at this batch size */
   if (st != MK_OK) return st;
   c->scheduled = true;
   c->steps = 0;

@@ -49,7 +49,9 @@ mk_status mk_encode_wd_maps(const mk_model_dims *d, const void *const *w_down, i
 int mk_fold_rows(const mk_model_dims *d);
 
 mk_status mk_validate_dims(const mk_model_dims *d);
+/* u_seen > 0: the distinct experts per layer observed at this batch size,
+ * used in place of the uniform-routing expectation for the role split. */
 mk_status mk_build_plan(const mk_model_dims *d, int n_cta, int batch, const int32_t *seq_lens,
-                        MkPlan *out);
+                        MkPlan *out, double u_seen = 0.0);
 
 #endif

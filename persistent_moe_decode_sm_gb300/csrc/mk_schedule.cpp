@@ -162,7 +162,7 @@ mk_status mk_validate_dims(const mk_model_dims *dm) {
 }
 
 mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int32_t *seq_lens,
-                        MkPlan *out) {
+                        MkPlan *out, double u_seen) {
   mk_status st = mk_validate_dims(dm);
   if (st != MK_OK) return st;
   if (n_cta < 1 || n_cta > 256 || !seq_lens || !out) return MK_ERR_INVALID_ARG;
@@ -257,7 +257,10 @@ mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int
     double kv = 0.0;
     for (int b = 0; b < batch; ++b) kv += (double)seq_lens[b] * Hkv * D * 2 * 2;
     const double E = d.n_experts, K = d.top_k;
-    const double u_exp = E * (1.0 - std::pow(1.0 - K / E, (double)batch));
+    /* distinct experts per layer: as observed on this batch's previous
+     * steps (a skewed router picks fewer), else the uniform expectation */
+    const double u_exp = u_seen > 0.0 ? std::min(u_seen, E)
+                                      : E * (1.0 - std::pow(1.0 - K / E, (double)batch));
     const bool fold = mk_nb_for(batch) == 1;
     const double up = u_exp * (fold ? 3.0 : 2.0) * d.d_ffn * d.d_model * 2;
     /* SM cycles of a 24 KB attention stage (48 keys x 8 query heads, both
