@@ -485,11 +485,25 @@ mk_status mk_build_plan(const mk_model_dims *dm, int n_cta, int batch, const int
   return MK_OK;
 }
 
+/* Library-internal (tests): mk_plan with the role split taken from an
+ * observed number of distinct experts per layer, as mk_build_schedule does
+ * once a schedule of the same batch size has run (u_seen <= 0: the
+ * uniform-routing expectation, i.e. mk_plan). */
+extern "C" mk_status mk_plan_observed(const mk_model_dims *dims, int32_t n_sm, int32_t batch,
+                                      const int32_t *seq_lens, double u_seen,
+                                      mk_plan_info *info, int32_t *table, int64_t cap);
+
 extern "C" mk_status mk_plan(const mk_model_dims *dims, int32_t n_sm, int32_t batch,
                              const int32_t *seq_lens, mk_plan_info *info, int32_t *table,
                              int64_t cap) {
+  return mk_plan_observed(dims, n_sm, batch, seq_lens, 0.0, info, table, cap);
+}
+
+extern "C" mk_status mk_plan_observed(const mk_model_dims *dims, int32_t n_sm, int32_t batch,
+                                      const int32_t *seq_lens, double u_seen,
+                                      mk_plan_info *info, int32_t *table, int64_t cap) {
   MkPlan p;
-  mk_status st = mk_build_plan(dims, n_sm, batch, seq_lens, &p);
+  mk_status st = mk_build_plan(dims, n_sm, batch, seq_lens, &p, u_seen > 0.0 ? u_seen : 0.0);
   if (st != MK_OK) return st;
   if (info) {
     info->n_cta = p.n_cta;

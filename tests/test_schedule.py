@@ -303,3 +303,40 @@ def test_stage_geometry_of_the_full_model():
         for K, least in ((d.n_q_heads * d.head_dim, 2), (d.d_ffn, 10)):
             assert f(ctypes.byref(cd), nb, K, ctypes.byref(sb), ctypes.byref(rows), None)
             assert rows.value >= least, (nb, K, rows.value)
+
+
+@pytest.mark.parametrize("u_seen", [8.0, 24.0, 40.0, 64.0])
+def test_schedule_from_observed_experts(u_seen):
+    """The role split from an observed number of distinct experts per layer
+    (a skewed router's batch of 8 picks fewer than the uniform 51.6): the
+    table stays complete and deadlock-free, and fewer observed experts leave
+    fewer CTAs on the expert side."""
+    import ctypes
+    d = synth.FULL
+    lens = list(synth.workloads()["full_b8"].seq_lens)
+    cd = cdims(d, 8, 17000)
+    f = mk.lib().mk_plan_observed
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.POINTER(type(cd)), ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                  ctypes.c_double, ctypes.POINTER(mk.mk_plan_info), ctypes.c_void_p,
+                  ctypes.c_int64]
+    sl = np.ascontiguousarray(lens, dtype=np.int32)
+
+    def plan(u):
+        info = mk.mk_plan_info()
+        assert f(ctypes.byref(cd), 152, len(lens), sl.ctypes.data, u, ctypes.byref(info), None, 0) == 0
+        table = np.empty((info.n_cta, info.tasks_per_cta, 32), np.int32)
+        assert f(ctypes.byref(cd), 152, len(lens), sl.ctypes.data, u, ctypes.byref(info),
+                 table.ctypes.data, table.size) == 0
+        return info, table
+
+    info, table = plan(u_seen)
+    rows = decode(table)
+    sim_d = d
+    rng = np.random.default_rng(int(u_seen))
+    simulate(sim_d, info, rows, len(lens), rng)
+    check_coverage(sim_d, info, rows, lens)
+    n_exp = sum(any(t[0] == OP_UP for t in lt) for lt, _ in rows)
+    n_exp_uniform = sum(any(t[0] == OP_UP for t in lt) for lt, _ in decode(plan(0.0)[1]))
+    if u_seen < 51.0:
+        assert n_exp < n_exp_uniform, (u_seen, n_exp, n_exp_uniform)
